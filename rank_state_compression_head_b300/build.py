@@ -1,0 +1,86 @@
+"""Build libseed.so in-tree for sm_103a with nvcc.
+
+Usage: ``python -m rank_state_compression_head_b300.build [--force] [-v]``.
+Objects go to ``_build/`` at the repository root; the library lands next to
+this file, where the Python binding loads it.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, 'csrc')
+INCLUDE = os.path.join(ROOT, 'include')
+BUILD = os.path.join(ROOT, '_build')
+LIB = os.path.join(PKG, 'libseed.so')
+SOURCES = ['api.cu', 'decode.cu', 'recompress.cu', 'dense.cu', 'synth.cu']
+ARCH = ['-gencode', 'arch=compute_103a,code=sm_103a']
+FLAGS = ['-O3', '-lineinfo', '-std=c++17', '-Xcompiler', '-fPIC', '--expt-relaxed-constexpr',
+         '-I', INCLUDE, '-I', CSRC]
+
+
+def nvcc() -> str:
+    for cand in (shutil.which('nvcc'), '/usr/local/cuda/bin/nvcc'):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError('nvcc not found')
+
+
+def _deps() -> list:
+    hdr = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(('.cuh', '.h'))]
+    hdr += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith('.h')]
+    return hdr + [os.path.abspath(__file__)]
+
+
+def _stale(target: str, deps: list) -> bool:
+    if not os.path.exists(target):
+        return True
+    t = os.path.getmtime(target)
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+    os.makedirs(BUILD, exist_ok=True)
+    common = _deps()
+    jobs = []
+    objs = []
+    for src in SOURCES:
+        s = os.path.join(CSRC, src)
+        o = os.path.join(BUILD, src.replace('.cu', '.o'))
+        objs.append(o)
+        if force or ptxas_info or _stale(o, common + [s]):
+            cmd = [nvcc()] + ARCH + FLAGS + (['-Xptxas', '-v'] if ptxas_info else []) + ['-c', s, '-o', o]
+            jobs.append(cmd)
+
+    def run(cmd):
+        if verbose:
+            print(' '.join(cmd), flush=True)
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError('nvcc failed:\n' + ' '.join(cmd) + '\n' + r.stdout + r.stderr)
+        return r.stdout + r.stderr
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        for out in ex.map(run, jobs):
+            if out.strip() and (verbose or ptxas_info):
+                print(out)
+    if force or jobs or _stale(LIB, objs):
+        cmd = [nvcc()] + ARCH + ['-shared', '-o', LIB] + objs + ['-lcudart']
+        run(cmd)
+    return LIB
+
+
+if __name__ == '__main__':
+    ap = argparse.ArgumentParser()
+    ap.add_argument('--force', action='store_true')
+    ap.add_argument('-v', '--verbose', action='store_true')
+    ap.add_argument('--ptxas-info', action='store_true')
+    a = ap.parse_args()
+    print(build(force=a.force, verbose=a.verbose, ptxas_info=a.ptxas_info))
+    sys.exit(0)

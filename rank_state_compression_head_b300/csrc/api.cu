@@ -1,0 +1,154 @@
+// C-ABI entry points of libseed.so (declared in include/seed.h).
+//
+// Every call validates its arguments on the host and launches nothing when
+// they are wrong; kernels run asynchronously on the caller's stream.  The
+// library allocates no memory and keeps no state between calls: the state
+// lives in the caller's seed_state and device buffers.
+#include "common.cuh"
+
+#include <stdint.h>
+
+using namespace seedk;
+
+namespace {
+
+inline bool misaligned(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 != 0; }
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? SEED_OK : SEED_ERR_CUDA; }
+inline int growth_of(int variant) { return variant == SEED_KDA ? 2 : 1; }
+
+// Shape, pointer and capacity checks shared by the factored-state calls.
+int check_state(const seed_state *st) {
+  if (!st) return SEED_ERR_INVALID_ARG;
+  if (st->variant < SEED_GDN || st->variant > SEED_MAMBA2) return SEED_ERR_INVALID_ARG;
+  if (st->factor_dtype != SEED_F32 && st->factor_dtype != SEED_BF16) return SEED_ERR_INVALID_ARG;
+  if (st->n_heads < 0 || st->T < 1 || st->steps_since_compress < 0) return SEED_ERR_INVALID_ARG;
+  if (st->d_k != kDK || (st->d_v != 64 && st->d_v != 128)) return SEED_ERR_UNSUPPORTED_SHAPE;
+  const int rmax = st->rank ? st->r_max : st->r;
+  if (st->r < 0 || rmax < 0) return SEED_ERR_INVALID_ARG;
+  if (!st->rank && st->r_max != st->r && st->r_max != 0) return SEED_ERR_INVALID_ARG;
+  const int dmin = st->d_k < st->d_v ? st->d_k : st->d_v;
+  if (rmax > dmin) return SEED_ERR_UNSUPPORTED_SHAPE;
+  if (rmax + growth_of(st->variant) * st->T > kMaxCols) return SEED_ERR_UNSUPPORTED_SHAPE;
+  if (st->n_heads == 0) return SEED_OK;
+  if (!st->a || !st->U || !st->W || !st->scale || !st->vbar) return SEED_ERR_INVALID_ARG;
+  if (misaligned(st->a) || misaligned(st->U) || misaligned(st->W) || misaligned(st->vbar))
+    return SEED_ERR_ALIGNMENT;
+  return SEED_OK;
+}
+
+StateView view_of(const seed_state *st) {
+  StateView v;
+  v.variant = st->variant;
+  v.n_heads = st->n_heads;
+  v.d_k = st->d_k;
+  v.d_v = st->d_v;
+  v.T = st->T;
+  v.r = st->r;
+  v.steps = st->steps_since_compress;
+  v.growth = growth_of(st->variant);
+  v.cap_uniform = (st->rank ? st->r_max : st->r) + v.growth * st->T;
+  v.rank = st->rank;
+  v.col_offset = st->col_offset;
+  v.a = st->a;
+  v.U = st->U;
+  v.W = st->W;
+  v.scale = st->scale;
+  v.vbar = st->vbar;
+  v.vbar_index = st->vbar_index;
+  v.status = st->status;
+  return v;
+}
+
+inline int rmax_of(const seed_state *st) { return st->rank ? st->r_max : st->r; }
+
+}  // namespace
+
+extern "C" int32_t seed_columns_per_head(int32_t variant, int32_t r, int32_t T) {
+  return r + growth_of(variant) * T;
+}
+
+extern "C" const char *seed_status_string(int status) {
+  switch (status) {
+    case SEED_OK: return "ok";
+    case SEED_ERR_INVALID_ARG: return "invalid argument";
+    case SEED_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case SEED_ERR_CAPACITY: return "factor capacity exceeded (recompress first)";
+    case SEED_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case SEED_ERR_CUDA: return "CUDA launch failed";
+    case SEED_ERR_NOT_CONVERGED: return "Jacobi SVD did not converge";
+    case SEED_ERR_NONFINITE: return "non-finite value";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int seed_compress_dense(const float *S, seed_state *st, float *trunc_err,
+                                   seed_stream_t stream) {
+  int c = check_state(st);
+  if (c) return c;
+  if (st->n_heads == 0) { st->steps_since_compress = 0; return SEED_OK; }
+  if (!S) return SEED_ERR_INVALID_ARG;
+  if (misaligned(S)) return SEED_ERR_ALIGNMENT;
+  seed_state tmp = *st;
+  tmp.steps_since_compress = 0;
+  c = cuda_status(launch_compress_dense(view_of(&tmp), st->factor_dtype, S, trunc_err,
+                                        (cudaStream_t)stream));
+  if (c == SEED_OK) st->steps_since_compress = 0;
+  return c;
+}
+
+extern "C" int seed_decode_step(seed_state *st, const float *q, const float *k, const float *v,
+                                const float *gate, const float *beta, const float *A, float *o,
+                                seed_stream_t stream) {
+  int c = check_state(st);
+  if (c) return c;
+  if (st->steps_since_compress >= st->T) return SEED_ERR_CAPACITY;
+  if (st->n_heads == 0) { ++st->steps_since_compress; return SEED_OK; }
+  if (!q || !k || !v || !gate || !o) return SEED_ERR_INVALID_ARG;
+  if (st->variant != SEED_MAMBA2 && !beta) return SEED_ERR_INVALID_ARG;
+  if (st->variant == SEED_MAMBA2 && !A) return SEED_ERR_INVALID_ARG;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o)) return SEED_ERR_ALIGNMENT;
+  const int cols = rmax_of(st) + growth_of(st->variant) * st->steps_since_compress;
+  c = cuda_status(launch_decode(view_of(st), st->factor_dtype, q, k, v, gate, beta, A, o, cols,
+                                (cudaStream_t)stream));
+  if (c == SEED_OK) ++st->steps_since_compress;
+  return c;
+}
+
+extern "C" int seed_recompress(seed_state *st, float *trunc_err, seed_stream_t stream) {
+  int c = check_state(st);
+  if (c) return c;
+  if (st->steps_since_compress > st->T) return SEED_ERR_CAPACITY;
+  if (st->n_heads == 0) { st->steps_since_compress = 0; return SEED_OK; }
+  const int m_max = rmax_of(st) + growth_of(st->variant) * st->steps_since_compress;
+  c = cuda_status(launch_recompress(view_of(st), st->factor_dtype, trunc_err, m_max,
+                                    (cudaStream_t)stream));
+  if (c == SEED_OK) st->steps_since_compress = 0;
+  return c;
+}
+
+extern "C" int seed_materialize(const seed_state *st, float *S_out, seed_stream_t stream) {
+  int c = check_state(st);
+  if (c) return c;
+  if (st->steps_since_compress > st->T) return SEED_ERR_CAPACITY;
+  if (st->n_heads == 0) return SEED_OK;
+  if (!S_out) return SEED_ERR_INVALID_ARG;
+  const int m_max = rmax_of(st) + growth_of(st->variant) * st->steps_since_compress;
+  return cuda_status(launch_materialize(view_of(st), st->factor_dtype, S_out, m_max > 0 ? m_max : 1,
+                                        (cudaStream_t)stream));
+}
+
+extern "C" int seed_dense_decode_step(int32_t variant, int32_t n_heads, int32_t d_k, int32_t d_v,
+                                      float *S, const float *q, const float *k, const float *v,
+                                      const float *gate, const float *beta, const float *A,
+                                      const int32_t *dir_index, float *o, seed_stream_t stream) {
+  if (variant < SEED_GDN || variant > SEED_MAMBA2 || n_heads < 0) return SEED_ERR_INVALID_ARG;
+  if (d_k != kDK || (d_v != 64 && d_v != 128)) return SEED_ERR_UNSUPPORTED_SHAPE;
+  if (n_heads == 0) return SEED_OK;
+  if (!S || !q || !k || !v || !gate || !o) return SEED_ERR_INVALID_ARG;
+  if (variant != SEED_MAMBA2 && !beta) return SEED_ERR_INVALID_ARG;
+  if (variant == SEED_MAMBA2 && !A) return SEED_ERR_INVALID_ARG;
+  if (misaligned(S) || misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o))
+    return SEED_ERR_ALIGNMENT;
+  return cuda_status(launch_dense_decode(variant, n_heads, d_v, S, q, k, v, gate, beta, A, dir_index,
+                                         o, (cudaStream_t)stream));
+}

@@ -1,0 +1,382 @@
+// Device twin of the seeded synthetic-workload generator, and the dense fp32
+// prefill whose prompt tokens are generated inside the kernel.
+//
+// Generator: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11), written from
+// its published definition, with the counter layout of the host generator:
+// key = (seed, phase << 16 | field), counter = (block, time, entity, 0).
+//
+// The prefill runs the dense recurrence over each request's prompt from S = 0
+// ("Shallow Encoding Emits Deep Memories", thelatestinai.com list view,
+// Table 1: the states that leave the prefill are then compressed), with the
+// state held in registers for the whole prompt and the tokens generated on
+// the fly, so no prompt input is ever stored.
+#include "common.cuh"
+#include "seed_synth.h"
+
+namespace seedk {
+
+constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+enum { F_Q = 1, F_K = 2, F_V = 3, F_ALPHA = 4, F_BETA = 5, F_DT = 6,
+       F_VBAR = 16, F_SINK = 17, F_A = 18, F_RANK = 19, F_CTX = 20 };
+
+__device__ __forceinline__ uint4 philox(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                        uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) { k0 += kW0; k1 += kW1; }
+    const uint32_t hi0 = __umulhi(kM0, c0), lo0 = kM0 * c0;
+    const uint32_t hi1 = __umulhi(kM1, c2), lo1 = kM1 * c2;
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+  }
+  return make_uint4(c0, c1, c2, c3);
+}
+
+__device__ __forceinline__ uint32_t fkey(int phase, int field) {
+  return ((uint32_t)(phase & 0xFFFF) << 16) | (uint32_t)(field & 0xFFFF);
+}
+
+__device__ __forceinline__ float uni(uint32_t x) {
+  return ((float)(x >> 9) + 0.5f) * 1.1920928955078125e-07f;  // 2^-23
+}
+
+// Four standard normals of block `blk` (Box-Muller on word pairs).
+__device__ __forceinline__ float4 normal4(uint32_t seed, int phase, int field, uint32_t time,
+                                          uint32_t entity, uint32_t blk) {
+  const uint4 w = philox(blk, time, entity, 0u, seed, fkey(phase, field));
+  const float r01 = sqrtf(-2.f * logf(uni(w.x)));
+  const float r23 = sqrtf(-2.f * logf(uni(w.z)));
+  float s1, c1, s3, c3;
+  sincospif(2.f * uni(w.y), &s1, &c1);
+  sincospif(2.f * uni(w.w), &s3, &c3);
+  return make_float4(r01 * c1, r01 * s1, r23 * c3, r23 * s3);
+}
+
+__device__ __forceinline__ float uniform1(uint32_t seed, int phase, int field, uint32_t time,
+                                          uint32_t entity) {
+  return uni(philox(0u, time, entity, 0u, seed, fkey(phase, field)).x);
+}
+
+__device__ __forceinline__ float softplusf(float x) { return log1pf(expf(x)); }
+
+// ---------------------------------------------------------------------------
+
+__global__ void raw_kernel(uint32_t seed, int phase, int field, uint32_t time, uint32_t entity0,
+                           int n_ent, int n_blocks, uint32_t *out) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (int64_t)n_ent * n_blocks) return;
+  const int i = (int)(idx / n_blocks), b = (int)(idx % n_blocks);
+  const uint4 w = philox((uint32_t)b, time, entity0 + (uint32_t)i, 0u, seed, fkey(phase, field));
+  reinterpret_cast<uint4 *>(out)[idx] = w;
+}
+
+// One warp per direction / head / request (grid-stride).
+__global__ void constants_kernel(const seed_synth_workload w, float *vbar, float *sink, float *A,
+                                 int32_t *rank, int32_t *plen) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int n_dir = w.n_layers * w.n_head;
+  const int64_t n_heads = (int64_t)n_dir * w.n_req;
+  for (int64_t d = wid; d < n_dir; d += nwarps) {
+    if (vbar) {
+      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lane < w.d_v / 4) z = normal4(w.seed, SEED_SYNTH_PHASE_CONST, F_VBAR, 0u, (uint32_t)d, lane);
+      const float ss = warp_sum(z.x * z.x + z.y * z.y + z.z * z.z + z.w * z.w);
+      const float nrm = sqrtf(ss);
+      if (lane < w.d_v / 4)
+        reinterpret_cast<float4 *>(vbar + d * w.d_v)[lane] =
+            make_float4(z.x / nrm, z.y / nrm, z.z / nrm, z.w / nrm);
+    }
+    if (lane == 0 && sink) {
+      const float u = uniform1(w.seed, SEED_SYNTH_PHASE_CONST, F_SINK, 0u, (uint32_t)d);
+      sink[d] = w.sink_lo + (w.sink_hi - w.sink_lo) * u;
+    }
+    if (lane == 0 && A) {
+      const float u = uniform1(w.seed, SEED_SYNTH_PHASE_CONST, F_A, 0u, (uint32_t)d);
+      A[d] = -(w.a_lo + (w.a_hi - w.a_lo) * u);
+    }
+  }
+  if (rank) {
+    for (int64_t h = wid * 32 + lane; h < n_heads; h += nwarps * 32) {
+      if (w.rank > 0) { rank[h] = w.rank; continue; }
+      const uint32_t x = philox(0u, 0u, (uint32_t)h, 0u, w.seed, fkey(SEED_SYNTH_PHASE_CONST, F_RANK)).x;
+      const uint32_t i = (uint32_t)(((uint64_t)x * (uint64_t)w.n_rank_choices) >> 32);
+      rank[h] = w.rank_choices[i];
+    }
+  }
+  if (plen) {
+    for (int64_t q = wid * 32 + lane; q < w.n_req; q += nwarps * 32) {
+      if (w.prefill_len > 0) { plen[q] = w.prefill_len; continue; }
+      const uint32_t x = philox(0u, 0u, (uint32_t)q, 0u, w.seed, fkey(SEED_SYNTH_PHASE_CONST, F_CTX)).x;
+      const uint64_t span = (uint64_t)(w.prefill_hi - w.prefill_lo + 1);
+      plen[q] = w.prefill_lo + (int32_t)(((uint64_t)x * span) >> 32);
+    }
+  }
+}
+
+// Token inputs of one head, written by warps 0..3 of the calling block.
+//   GDN/KDA: out0 = q (unit), out1 = k (unit), out2 = v, gate = alpha, beta
+//   Mamba-2: out0 = C, out1 = B, out2 = x, gate = dt
+// Returns nothing; the caller synchronises before reading.
+__device__ __forceinline__ void gen_token(const seed_synth_workload &w, int phase, uint32_t time,
+                                          uint32_t head, int dir, const float *vbar_d, float sink_d,
+                                          float *out0, float *out1, float *out2, float *gate,
+                                          float *beta, bool need_q) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool m2 = w.variant == SEED_MAMBA2;
+  if (warp == 0 || warp == 1) {
+    if (warp == 0 && !need_q) return;
+    float *out = warp == 0 ? out0 : out1;
+    float4 z = normal4(w.seed, phase, warp == 0 ? F_Q : F_K, time, head, lane);  // d_k = 128: 32 blocks
+    if (m2) {
+      const float sd = 1.f / sqrtf((float)w.d_k);
+      z = make_float4(z.x * sd, z.y * sd, z.z * sd, z.w * sd);
+    } else {
+      const float nrm = sqrtf(warp_sum(z.x * z.x + z.y * z.y + z.z * z.z + z.w * z.w));
+      z = make_float4(z.x / nrm, z.y / nrm, z.z / nrm, z.w / nrm);
+    }
+    reinterpret_cast<float4 *>(out)[lane] = z;
+  } else if (warp == 2) {
+    if (lane < w.d_v / 4) {
+      const float4 z = normal4(w.seed, phase, F_V, time, head, lane);
+      const float4 vb = reinterpret_cast<const float4 *>(vbar_d)[lane];
+      const float sd = w.noise_std;
+      reinterpret_cast<float4 *>(out2)[lane] =
+          make_float4(fmaf(sink_d, vb.x, sd * z.x), fmaf(sink_d, vb.y, sd * z.y),
+                      fmaf(sink_d, vb.z, sd * z.z), fmaf(sink_d, vb.w, sd * z.w));
+    }
+  } else if (warp == 3) {
+    if (m2) {
+      if (lane == 0) {
+        const float z = normal4(w.seed, phase, F_DT, time, head, 0u).x;
+        gate[0] = softplusf(w.dt_mu + sqrtf(w.dt_var) * z);
+      }
+    } else if (w.variant == SEED_KDA) {
+      const uint4 x = philox((uint32_t)lane, time, head, 0u, w.seed, fkey(phase, F_ALPHA));
+      const float sp = w.alpha_hi - w.alpha_lo;
+      reinterpret_cast<float4 *>(gate)[lane] =
+          make_float4(w.alpha_lo + sp * uni(x.x), w.alpha_lo + sp * uni(x.y),
+                      w.alpha_lo + sp * uni(x.z), w.alpha_lo + sp * uni(x.w));
+      if (lane == 0)
+        beta[0] = w.beta_lo + (w.beta_hi - w.beta_lo) * uniform1(w.seed, phase, F_BETA, time, head);
+    } else if (lane == 0) {
+      gate[0] = w.alpha_lo + (w.alpha_hi - w.alpha_lo) * uniform1(w.seed, phase, F_ALPHA, time, head);
+      beta[0] = w.beta_lo + (w.beta_hi - w.beta_lo) * uniform1(w.seed, phase, F_BETA, time, head);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(128) step_inputs_kernel(const seed_synth_workload w, int phase,
+                                                          int time, int64_t head0,
+                                                          const float *vbar, const float *sink,
+                                                          float *q, float *k, float *v, float *gate,
+                                                          float *beta) {
+  const int64_t i = blockIdx.x;
+  const int64_t h = head0 + i;
+  const int n_dir = w.n_layers * w.n_head;
+  const int dir = (int)(h % n_dir);
+  const bool kda = w.variant == SEED_KDA;
+  float *bptr = (beta && w.variant != SEED_MAMBA2) ? beta + i : nullptr;
+  float dummy;
+  gen_token(w, phase, (uint32_t)time, (uint32_t)h, dir, vbar + (int64_t)dir * w.d_v, sink[dir],
+            q + i * w.d_k, k + i * w.d_k, v + i * w.d_v, gate + (kda ? i * w.d_k : i),
+            bptr ? bptr : &dummy, true);
+}
+
+// Dense prefill: one CTA of 256 threads per head; state rows distributed as in
+// the dense decode step (thread holds NL float4 row pieces).
+template <int VAR, int DV>
+__global__ void __launch_bounds__(256) prefill_kernel(const seed_synth_workload w, int64_t head0,
+                                                      const int32_t *plen, const float *vbar,
+                                                      const float *sink, const float *A,
+                                                      float *S_out) {
+  constexpr int DK = kDK;
+  constexpr int NW = 8;
+  constexpr int LPR = DV / 4;
+  constexpr int RPW = 32 / LPR;
+  constexpr int NL = DK / (RPW * NW);
+  constexpr int NG = NW * RPW;
+  constexpr bool M2 = VAR == SEED_MAMBA2;
+  constexpr bool KDA = VAR == SEED_KDA;
+  __shared__ __align__(16) float kin[2][DK];
+  __shared__ __align__(16) float vin[2][DV];
+  __shared__ __align__(16) float gin[2][DK];
+  __shared__ float bin[2];
+  __shared__ __align__(16) float red[NG][DV];
+
+  const int64_t hi = blockIdx.x;
+  const int64_t h = head0 + hi;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_dir = w.n_layers * w.n_head;
+  const int dir = (int)(h % n_dir);
+  const int req = (int)(h / n_dir);
+  const int L = plen[req];
+  const float *vb = vbar + (int64_t)dir * DV;
+  const float sd = sink[dir];
+  const float Ad = M2 ? A[dir] : 0.f;
+  const int c4 = (lane % LPR) * 4;
+  const int grp = warp * RPW + lane / LPR;
+
+  float4 st[NL];
+#pragma unroll
+  for (int l = 0; l < NL; ++l) st[l] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  if (L > 0)
+    gen_token(w, SEED_SYNTH_PHASE_PREFILL, 0u, (uint32_t)h, dir, vb, sd, nullptr, kin[0], vin[0],
+              gin[0], &bin[0], false);
+  __syncthreads();
+  for (int t = 0; t < L; ++t) {
+    const int b = t & 1;
+    const float4 v4 = *reinterpret_cast<const float4 *>(&vin[b][c4]);
+    if (!M2) {
+      float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int l = 0; l < NL; ++l) {
+        const int row = (l * NW + warp) * RPW + lane / LPR;
+        const float kr = kin[b][row];
+        u.x = fmaf(kr, st[l].x, u.x); u.y = fmaf(kr, st[l].y, u.y);
+        u.z = fmaf(kr, st[l].z, u.z); u.w = fmaf(kr, st[l].w, u.w);
+      }
+      *reinterpret_cast<float4 *>(&red[grp][c4]) = u;
+    }
+    if (t + 1 < L)
+      gen_token(w, SEED_SYNTH_PHASE_PREFILL, (uint32_t)(t + 1), (uint32_t)h, dir, vb, sd, nullptr,
+                kin[b ^ 1], vin[b ^ 1], gin[b ^ 1], &bin[b ^ 1], false);
+    __syncthreads();
+    if (!M2) {
+      float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) {
+        const float4 x = *reinterpret_cast<const float4 *>(&red[gi][c4]);
+        u.x += x.x; u.y += x.y; u.z += x.z; u.w += x.w;
+      }
+      const float beta = bin[b];
+#pragma unroll
+      for (int l = 0; l < NL; ++l) {
+        const int row = (l * NW + warp) * RPW + lane / LPR;
+        const float kr = kin[b][row];
+        if (KDA) {
+          const float ar = gin[b][row];
+          const float bk = beta * kr;
+          st[l].x = fmaf(ar, fmaf(-bk, u.x, st[l].x), bk * v4.x);
+          st[l].y = fmaf(ar, fmaf(-bk, u.y, st[l].y), bk * v4.y);
+          st[l].z = fmaf(ar, fmaf(-bk, u.z, st[l].z), bk * v4.z);
+          st[l].w = fmaf(ar, fmaf(-bk, u.w, st[l].w), bk * v4.w);
+        } else {
+          const float g = gin[b][0];
+          st[l].x = fmaf(g, st[l].x, kr * beta * fmaf(-g, u.x, v4.x));
+          st[l].y = fmaf(g, st[l].y, kr * beta * fmaf(-g, u.y, v4.y));
+          st[l].z = fmaf(g, st[l].z, kr * beta * fmaf(-g, u.z, v4.z));
+          st[l].w = fmaf(g, st[l].w, kr * beta * fmaf(-g, u.w, v4.w));
+        }
+      }
+    } else {
+      const float dt = gin[b][0];
+      const float g = expf(dt * Ad);
+#pragma unroll
+      for (int l = 0; l < NL; ++l) {
+        const int row = (l * NW + warp) * RPW + lane / LPR;
+        const float bb = dt * kin[b][row];
+        st[l].x = fmaf(g, st[l].x, bb * v4.x); st[l].y = fmaf(g, st[l].y, bb * v4.y);
+        st[l].z = fmaf(g, st[l].z, bb * v4.z); st[l].w = fmaf(g, st[l].w, bb * v4.w);
+      }
+    }
+    __syncthreads();
+  }
+  float *Sh = S_out + hi * DK * DV;
+#pragma unroll
+  for (int l = 0; l < NL; ++l) {
+    const int row = (l * NW + warp) * RPW + lane / LPR;
+    *reinterpret_cast<float4 *>(Sh + row * DV + c4) = st[l];
+  }
+}
+
+static int check_workload(const seed_synth_workload *w) {
+  if (!w) return SEED_ERR_INVALID_ARG;
+  if (w->variant < SEED_GDN || w->variant > SEED_MAMBA2) return SEED_ERR_INVALID_ARG;
+  if (w->n_req < 0 || w->n_layers <= 0 || w->n_head <= 0) return SEED_ERR_INVALID_ARG;
+  if (w->d_k != kDK || (w->d_v != 64 && w->d_v != 128)) return SEED_ERR_UNSUPPORTED_SHAPE;
+  if (w->rank <= 0 && (w->n_rank_choices <= 0 || w->n_rank_choices > 4)) return SEED_ERR_INVALID_ARG;
+  if (w->prefill_len <= 0 && (w->prefill_lo < 0 || w->prefill_hi < w->prefill_lo)) return SEED_ERR_INVALID_ARG;
+  return SEED_OK;
+}
+
+}  // namespace seedk
+
+using namespace seedk;
+
+static inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? SEED_OK : SEED_ERR_CUDA; }
+
+extern "C" int seed_synth_raw(uint32_t seed, int32_t phase, int32_t field, uint32_t time,
+                              uint32_t entity0, int32_t n_entities, int32_t n_blocks, uint32_t *out,
+                              seed_stream_t stream) {
+  if (n_entities < 0 || n_blocks < 0) return SEED_ERR_INVALID_ARG;
+  if ((int64_t)n_entities * n_blocks == 0) return SEED_OK;
+  if (!out) return SEED_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(out) % 16) return SEED_ERR_ALIGNMENT;
+  const int64_t n = (int64_t)n_entities * n_blocks;
+  raw_kernel<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
+      seed, phase, field, time, entity0, n_entities, n_blocks, out);
+  return cuda_status(cudaGetLastError());
+}
+
+extern "C" int seed_synth_constants(const seed_synth_workload *w, float *vbar, float *sink_scale,
+                                    float *A, int32_t *rank, int32_t *prompt_len,
+                                    seed_stream_t stream) {
+  const int c = check_workload(w);
+  if (c) return c;
+  if (vbar && reinterpret_cast<uintptr_t>(vbar) % 16) return SEED_ERR_ALIGNMENT;
+  constants_kernel<<<1184, 256, 0, (cudaStream_t)stream>>>(*w, vbar, sink_scale, A, rank, prompt_len);
+  return cuda_status(cudaGetLastError());
+}
+
+extern "C" int seed_synth_step_inputs(const seed_synth_workload *w, int32_t phase, int32_t time,
+                                      int64_t head0, int32_t n_heads, const float *vbar,
+                                      const float *sink_scale, float *q, float *k, float *v,
+                                      float *gate, float *beta, seed_stream_t stream) {
+  const int c = check_workload(w);
+  if (c) return c;
+  if (n_heads < 0 || head0 < 0) return SEED_ERR_INVALID_ARG;
+  if (n_heads == 0) return SEED_OK;
+  if (!vbar || !sink_scale || !q || !k || !v || !gate) return SEED_ERR_INVALID_ARG;
+  if (w->variant != SEED_MAMBA2 && !beta) return SEED_ERR_INVALID_ARG;
+  for (const void *ptr : {(const void *)vbar, (const void *)q, (const void *)k, (const void *)v,
+                          (const void *)gate})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16) return SEED_ERR_ALIGNMENT;
+  step_inputs_kernel<<<n_heads, 128, 0, (cudaStream_t)stream>>>(*w, phase, time, head0, vbar,
+                                                                sink_scale, q, k, v, gate, beta);
+  return cuda_status(cudaGetLastError());
+}
+
+extern "C" int seed_synth_dense_prefill(const seed_synth_workload *w, int64_t head0, int32_t n_heads,
+                                        const int32_t *prompt_len, const float *vbar,
+                                        const float *sink_scale, const float *A, float *S_out,
+                                        seed_stream_t stream) {
+  const int c = check_workload(w);
+  if (c) return c;
+  if (n_heads < 0 || head0 < 0) return SEED_ERR_INVALID_ARG;
+  if (n_heads == 0) return SEED_OK;
+  if (!prompt_len || !vbar || !sink_scale || !S_out) return SEED_ERR_INVALID_ARG;
+  if (w->variant == SEED_MAMBA2 && !A) return SEED_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(S_out) % 16 || reinterpret_cast<uintptr_t>(vbar) % 16)
+    return SEED_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool d64 = w->d_v == 64;
+  switch (w->variant) {
+    case SEED_GDN:
+      if (d64) prefill_kernel<SEED_GDN, 64><<<n_heads, 256, 0, s>>>(*w, head0, prompt_len, vbar, sink_scale, A, S_out);
+      else prefill_kernel<SEED_GDN, 128><<<n_heads, 256, 0, s>>>(*w, head0, prompt_len, vbar, sink_scale, A, S_out);
+      break;
+    case SEED_KDA:
+      if (d64) prefill_kernel<SEED_KDA, 64><<<n_heads, 256, 0, s>>>(*w, head0, prompt_len, vbar, sink_scale, A, S_out);
+      else prefill_kernel<SEED_KDA, 128><<<n_heads, 256, 0, s>>>(*w, head0, prompt_len, vbar, sink_scale, A, S_out);
+      break;
+    default:
+      if (d64) prefill_kernel<SEED_MAMBA2, 64><<<n_heads, 256, 0, s>>>(*w, head0, prompt_len, vbar, sink_scale, A, S_out);
+      else prefill_kernel<SEED_MAMBA2, 128><<<n_heads, 256, 0, s>>>(*w, head0, prompt_len, vbar, sink_scale, A, S_out);
+      break;
+  }
+  return cuda_status(cudaGetLastError());
+}

@@ -1,0 +1,91 @@
+"""Drive one synthetic workload through the library on the GPU.
+
+Only C-ABI calls: constants, dense prefill with in-kernel prompt tokens,
+compression at the end of the prefill, then the decode loop (inputs of each
+step generated on the device, fused read-out + update, recompression every T
+steps).  PyTorch only allocates the buffers.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import (SEED_MAMBA2, VARIANTS, seed_compress_dense, seed_decode_step, seed_dense_decode_step,
+               seed_recompress, seed_synth_constants, seed_synth_dense_prefill, seed_synth_step_inputs)
+from .state import FactoredStateBuffers, synth_workload_struct
+
+PHASE_DECODE = 2
+
+
+class DeviceRun:
+    """Buffers and calls for one workload ``w`` (a ``synth.Workload``-like object)."""
+
+    def __init__(self, w, device='cuda', steps_buffered: int = 1):
+        self.w = w
+        self.dev = torch.device(device)
+        self.wst = synth_workload_struct(w)
+        H, dk, dv = w.n_heads, w.d_k, w.d_v
+        self.H = H
+        self.variant = VARIANTS[w.variant]
+        n_dir = w.n_dir
+        f32 = dict(device=self.dev, dtype=torch.float32)
+        self.vbar = torch.empty(n_dir, dv, **f32)
+        self.sink = torch.empty(n_dir, **f32)
+        self.A = torch.empty(n_dir, **f32) if w.variant == 'mamba2' else None
+        self.ranks = torch.empty(H, device=self.dev, dtype=torch.int32)
+        self.plen = torch.empty(w.n_req, device=self.dev, dtype=torch.int32)
+        seed_synth_constants(self.wst, self.vbar, self.sink, self.A, self.ranks, self.plen)
+        self.vbar_index = (torch.arange(H, device=self.dev, dtype=torch.int32) % n_dir)
+        ragged = bool(w.rank_choices)
+        self.state = FactoredStateBuffers(
+            w.variant, w.factor_dtype, H, dk, dv, w.T, self.vbar, r=w.rank if not ragged else 0,
+            ranks=self.ranks if ragged else None, vbar_index=self.vbar_index, device=self.dev)
+        nb = max(1, steps_buffered)
+        self.q = torch.empty(nb, H, dk, **f32)
+        self.k = torch.empty(nb, H, dk, **f32)
+        self.v = torch.empty(nb, H, dv, **f32)
+        self.gate = torch.empty(nb, H, dk, **f32) if w.variant == 'kda' else torch.empty(nb, H, **f32)
+        self.beta = torch.empty(nb, H, **f32)
+        self.o = torch.empty(H, dv, **f32)
+        self.trunc = torch.zeros(max(H, 1), **f32)
+        self.nb = nb
+
+    # -- setup ------------------------------------------------------------------
+    def prefill(self, head0: int = 0, n: Optional[int] = None, out: Optional[torch.Tensor] = None):
+        """Dense fp32 prefill of heads [head0, head0+n) into ``out`` (allocated if None)."""
+        n = self.H - head0 if n is None else n
+        if out is None:
+            out = torch.empty(n, self.w.d_k, self.w.d_v, device=self.dev, dtype=torch.float32)
+        seed_synth_dense_prefill(self.wst, head0, n, self.plen, self.vbar, self.sink, self.A, out)
+        return out
+
+    def compress(self, S: torch.Tensor, trunc_err: Optional[torch.Tensor] = None):
+        seed_compress_dense(S, self.state.st, trunc_err)
+
+    # -- decode loop --------------------------------------------------------------
+    def gen_inputs(self, step: int, slot: int = 0):
+        seed_synth_step_inputs(self.wst, PHASE_DECODE, step, 0, self.H, self.vbar, self.sink,
+                               self.q[slot], self.k[slot], self.v[slot], self.gate[slot],
+                               self.beta[slot])
+
+    def decode(self, slot: int = 0, stream=None):
+        seed_decode_step(self.state.st, self.q[slot], self.k[slot], self.v[slot], self.gate[slot],
+                         self.beta[slot], self.A, self.o, stream)
+
+    def recompress(self, trunc_err: Optional[torch.Tensor] = None, stream=None):
+        seed_recompress(self.state.st, trunc_err, stream)
+
+    def step(self, t: int, slot: int = 0, stream=None) -> bool:
+        """Decode step t (1-based) with inputs already in ``slot``; recompress when T divides t."""
+        self.decode(slot, stream)
+        if t % self.w.T == 0:
+            self.recompress(self.trunc, stream)
+            return True
+        return False
+
+    def dense_step(self, S: torch.Tensor, slot: int = 0, o: Optional[torch.Tensor] = None, stream=None):
+        o = self.o if o is None else o
+        seed_dense_decode_step(self.variant, self.H, self.w.d_k, self.w.d_v, S, self.q[slot],
+                               self.k[slot], self.v[slot], self.gate[slot], self.beta[slot], self.A,
+                               self.vbar_index, o, stream)

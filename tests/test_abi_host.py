@@ -1,0 +1,136 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import rank_state_compression_head_b300 as R
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000          # a 16-byte-aligned non-null address: never dereferenced on the host
+
+
+def declared_functions():
+    names = set()
+    for hdr in ('seed.h', 'seed_synth.h'):
+        with open(os.path.join(ROOT, 'include', hdr)) as f:
+            text = f.read()
+        text = re.sub(r'/\*.*?\*/', '', text, flags=re.S)
+        for m in re.finditer(r'^\s*(?:const\s+)?(?:int|int32_t|char)\s*\*?\s*(seed_\w+)\s*\(', text, re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_function():
+    names = declared_functions()
+    assert {'seed_compress_dense', 'seed_decode_step', 'seed_recompress', 'seed_materialize',
+            'seed_dense_decode_step', 'seed_status_string'} <= names
+    lib = ctypes.CDLL(R.LIB_PATH)
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+    assert names == set(R.EXPORTED_SYMBOLS)
+
+
+def test_struct_layout_matches_header():
+    # 10 int32 fields followed by 9 pointers
+    assert ctypes.sizeof(R.seed_state) == 10 * 4 + 9 * 8
+    assert R.seed_state.a.offset == 56
+
+
+def test_status_strings():
+    for code in range(8):
+        assert R.status_string(code)
+    assert 'capacity' in R.status_string(R.SEED_ERR_CAPACITY)
+    assert R.status_string(99) == 'unknown status'
+
+
+def test_columns_per_head():
+    assert R.seed_columns_per_head(R.SEED_GDN, 32, 16) == 48
+    assert R.seed_columns_per_head(R.SEED_KDA, 32, 16) == 64
+    assert R.seed_columns_per_head(R.SEED_MAMBA2, 16, 16) == 32
+
+
+def make_state(**kw):
+    st = R.seed_state(variant=R.SEED_GDN, factor_dtype=R.SEED_BF16, n_heads=4, d_k=128, d_v=128, T=16,
+                      r=32, r_max=32, steps_since_compress=0, reserved_=0, rank=None, col_offset=None,
+                      a=FAKE, U=FAKE, W=FAKE, scale=FAKE, vbar=FAKE, vbar_index=None, status=None)
+    for k, v in kw.items():
+        setattr(st, k, v)
+    return st
+
+
+def decode(st, **ptrs):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, gate=FAKE, beta=FAKE, A=None, o=FAKE)
+    p.update(ptrs)
+    return R._lib.seed_decode_step(ctypes.byref(st), p['q'], p['k'], p['v'], p['gate'], p['beta'],
+                                   p['A'], p['o'], None)
+
+
+@pytest.mark.parametrize('kw,code', [
+    (dict(d_k=64), R.SEED_ERR_UNSUPPORTED_SHAPE),
+    (dict(d_v=96), R.SEED_ERR_UNSUPPORTED_SHAPE),
+    (dict(r=129, r_max=129), R.SEED_ERR_UNSUPPORTED_SHAPE),
+    (dict(r=56, r_max=56), R.SEED_ERR_UNSUPPORTED_SHAPE),            # 56 + 16 > 64 columns
+    (dict(variant=R.SEED_KDA, r=48, r_max=48), R.SEED_ERR_UNSUPPORTED_SHAPE),  # 48 + 32 > 64
+    (dict(variant=7), R.SEED_ERR_INVALID_ARG),
+    (dict(factor_dtype=3), R.SEED_ERR_INVALID_ARG),
+    (dict(n_heads=-1), R.SEED_ERR_INVALID_ARG),
+    (dict(T=0), R.SEED_ERR_INVALID_ARG),
+    (dict(r=-1, r_max=-1), R.SEED_ERR_INVALID_ARG),
+    (dict(a=None), R.SEED_ERR_INVALID_ARG),
+    (dict(U=FAKE + 4), R.SEED_ERR_ALIGNMENT),
+    (dict(steps_since_compress=16), R.SEED_ERR_CAPACITY),
+])
+def test_decode_rejects_on_host(kw, code):
+    st = make_state(**kw)
+    before = st.steps_since_compress
+    assert decode(st) == code
+    assert st.steps_since_compress == before
+
+
+def test_decode_rejects_missing_inputs():
+    st = make_state()
+    assert decode(st, q=None) == R.SEED_ERR_INVALID_ARG
+    assert decode(st, beta=None) == R.SEED_ERR_INVALID_ARG
+    assert decode(st, o=FAKE + 8) == R.SEED_ERR_ALIGNMENT
+    m2 = make_state(variant=R.SEED_MAMBA2, d_v=64, r=16, r_max=16)
+    assert decode(m2, A=None, beta=None) == R.SEED_ERR_INVALID_ARG
+    assert R._lib.seed_decode_step(None, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None) == R.SEED_ERR_INVALID_ARG
+
+
+def test_zero_heads_is_a_no_op_that_advances_the_counter():
+    st = make_state(n_heads=0, a=None, U=None, W=None, scale=None, vbar=None)
+    for s in range(16):
+        assert decode(st, q=None, k=None, v=None, gate=None, beta=None, o=None) == R.SEED_OK
+        assert st.steps_since_compress == s + 1
+    assert decode(st) == R.SEED_ERR_CAPACITY
+    assert R._lib.seed_recompress(ctypes.byref(st), None, None) == R.SEED_OK
+    assert st.steps_since_compress == 0
+    assert R._lib.seed_materialize(ctypes.byref(st), None, None) == R.SEED_OK
+    assert R._lib.seed_compress_dense(None, ctypes.byref(st), None, None) == R.SEED_OK
+
+
+def test_other_calls_reject_on_host():
+    st = make_state()
+    assert R._lib.seed_compress_dense(None, ctypes.byref(st), None, None) == R.SEED_ERR_INVALID_ARG
+    assert R._lib.seed_compress_dense(FAKE + 4, ctypes.byref(st), None, None) == R.SEED_ERR_ALIGNMENT
+    assert R._lib.seed_materialize(ctypes.byref(st), None, None) == R.SEED_ERR_INVALID_ARG
+    st.steps_since_compress = 17
+    assert R._lib.seed_recompress(ctypes.byref(st), None, None) == R.SEED_ERR_CAPACITY
+    f = R._lib.seed_dense_decode_step
+    assert f(0, 4, 64, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None) == R.SEED_ERR_UNSUPPORTED_SHAPE
+    assert f(0, 4, 128, 128, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None) == R.SEED_ERR_INVALID_ARG
+    assert f(2, 4, 128, 64, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, None) == R.SEED_ERR_INVALID_ARG
+    assert f(0, 0, 128, 128, None, None, None, None, None, None, None, None, None, None) == R.SEED_OK
+
+
+def test_synth_calls_reject_on_host():
+    import synth
+    w = R.synth_workload_struct(synth.GDN_BATCHED)
+    bad = R.synth_workload_struct(synth.GDN_BATCHED.with_(d_k=64))
+    assert R._lib.seed_synth_constants(ctypes.byref(bad), None, None, None, None, None, None) == R.SEED_ERR_UNSUPPORTED_SHAPE
+    assert R._lib.seed_synth_step_inputs(ctypes.byref(w), 2, 0, 0, 4, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == R.SEED_ERR_INVALID_ARG
+    assert R._lib.seed_synth_dense_prefill(ctypes.byref(w), 0, 0, None, None, None, None, None, None) == R.SEED_OK
+    assert R._lib.seed_synth_raw(0, 0, 0, 0, 0, 4, 4, FAKE + 4, None) == R.SEED_ERR_ALIGNMENT
