@@ -1,0 +1,437 @@
+"""Benchmark of the sink + low-rank decode path on B300.
+
+One "step" = one decode step of every head of the workload (fused read-out +
+factored update), with the recompression back to rank r that runs after
+every T-th step included, so the figure is whole-job head-steps/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  Inputs of every step are generated on the
+device before the timed region and stay resident in HBM; L2 is flushed
+(a 256 MiB write) before every timed step, and each timed step is bracketed
+by CUDA events on the launching stream.  ``--impl reference`` times the CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = 'factored-state decode head-steps/s and HBM GB/s vs 8 TB/s; dense-state ratio'
+UNIT = 'head-steps/s'
+DEFAULT_WORKLOAD = 'gdn_batched_b64_h32_r32'
+FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument('--gpus', type=int, default=1)
+    ap.add_argument('--steps', type=int, default=256)
+    ap.add_argument('--warmup', type=int, default=16)
+    ap.add_argument('--workload', default=DEFAULT_WORKLOAD)
+    ap.add_argument('--impl', default='seed', choices=['seed', 'reference'])
+    ap.add_argument('--cpu-seconds', type=float, default=12.0, help='budget of the CPU-oracle sample')
+    ap.add_argument('--warm-seconds', type=float, default=0.5,
+                    help='keep warming up (after the W steps) until this much time has passed')
+    ap.add_argument('--no-dense', action='store_true')
+    ap.add_argument('--no-e2e', action='store_true')
+    ap.add_argument('--no-cpu', action='store_true')
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get('WORLD_SIZE', '1'))
+    rank = int(os.environ.get('RANK', '0'))
+    local = int(os.environ.get('LOCAL_RANK', '0'))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(w, seconds: float, n_sample: int = 64):
+    """Time the CPU oracle on a sample of the workload's heads: decode steps from a
+    rank-r state with recompression every T steps, until ``seconds`` have passed."""
+    import numpy as np
+    import oracle
+    import synth
+    rng = np.random.default_rng(0)
+    heads = rng.choice(w.n_heads, size=min(n_sample, w.n_heads), replace=False)
+    ranks = synth.head_ranks(w, heads)
+    growth = w.growth
+    states = []
+    for i, h in enumerate(heads):
+        d = synth.head_dir(w, h)
+        vbar = synth.sink_directions(w, [d])[0]
+        r = int(ranks[i])
+        raw = synth.random_factored_state(w.seed + 7, 1, w.d_k, w.d_v, [r], r + growth * w.T, w.variant)
+        st = oracle.FactoredState(a=raw['a'][0], U=raw['U'][0, :r].T, W=raw['W'][0, :r].T, vbar=vbar)
+        if w.variant == 'kda':
+            st.D = np.ones(w.d_k)
+        else:
+            st.scale = np.ones(r)
+        A = float(synth.mamba2_A(w, [d])[0]) if w.variant == 'mamba2' else None
+        states.append((st, A, r))
+    done = 0
+    t0 = time.perf_counter()
+    step = 0
+    while True:
+        toks = synth.decode_inputs(w, step % w.steps, heads)
+        for i in range(len(heads)):
+            st, A, r = states[i]
+            st, _ = oracle.factored_step(w.variant, st, {k: v[i] for k, v in toks.items()}, A)
+            if (step + 1) % w.T == 0:
+                st, _ = oracle.recompress(st, r)
+            states[i] = (st, A, r)
+        done += len(heads)
+        step += 1
+        el = time.perf_counter() - t0
+        if el >= seconds and step % w.T == 0:
+            break
+    return dict(value=done / el, unit=UNIT, cores=1, kind='oracle',
+                sample=f'{len(heads)} sampled heads x {step} decode steps (recompression every {w.T}), '
+                       f'float64 numpy, one thread, {el:.1f} s')
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    os.environ.setdefault('OPENBLAS_NUM_THREADS', '1')
+    steps = []
+    budget = max(0.02, min(1.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(max(0, args.warmup)):
+        oracle_sample(w, budget, n_sample=16)
+    for _ in range(args.steps):
+        steps.append(oracle_sample(w, budget, n_sample=16))
+    value = statistics.mean(s['value'] for s in steps)
+    cb = dict(steps[-1])
+    cb['value'] = value
+    out = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=ws, steps=args.steps, warmup=args.warmup,
+               ms_per_step=1e3 * w.n_heads / value, higher_is_better=True, scaling='weak',
+               vs_baseline=None, dtype='f64', data='synthetic', impl='reference',
+               config=dict(workload=w.name, heads=w.n_heads, d_k=w.d_k, d_v=w.d_v, r=w.r_max, T=w.T,
+                           factor_dtype='f64'),
+               cpu_baseline=cb, e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(out), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running (read only)."""
+    REASONS = {0x1: 'gpu_idle', 0x2: 'applications_clocks_setting', 0x4: 'sw_power_cap',
+               0x8: 'hw_slowdown', 0x10: 'sync_boost', 0x20: 'sw_thermal_slowdown',
+               0x40: 'hw_thermal_slowdown', 0x80: 'hw_power_brake_slowdown', 0x100: 'display_clock_setting'}
+
+    def __init__(self, index: int, period: float = 0.002):
+        self.samples = []
+        self.period = period
+        self._stop = threading.Event()
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.max_mhz = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+                rs = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append((time.perf_counter(), mhz, rs))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self.ok:
+            self.t.join()
+
+    def summary(self, t0: float, t1: float):
+        if not self.ok:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=['nvml unavailable'])
+        inside = [s for s in self.samples if t0 <= s[0] <= t1] or self.samples[-5:]
+        mhz = statistics.median(s[1] for s in inside) if inside else None
+        bits = 0
+        for s in inside:
+            bits |= s[2]
+        reasons = sorted(n for b, n in self.REASONS.items() if bits & b)
+        return dict(sm_mhz=mhz, sm_max_mhz=self.max_mhz, reasons=reasons, samples=len(inside))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, 'MEASURED_PEAKS.json')
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d['hbm_gbs'], src='measured')
+    return dict(hbm_gbs=6400.0, src='fallback')
+
+
+def profiled_traffic(kernel_tag: str):
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel, if its source is unchanged."""
+    path = os.path.join(ROOT, 'profiles', f'ncu_{kernel_tag}.md')
+    src = os.path.join(ROOT, 'rank_state_compression_head_b300', 'csrc', 'decode.cu')
+    if not os.path.exists(path):
+        return None
+    with open(src, 'rb') as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            if ':' in line and line.startswith('- '):
+                k, v = line[2:].split(':', 1)
+                rec[k.strip()] = v.strip()
+    if rec.get('source_sha256_16') != sha:
+        return None
+    try:
+        return float(rec['traffic_bytes_per_launch'])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_gpu(args, w):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from rank_state_compression_head_b300 import accounting as acc
+    from rank_state_compression_head_b300 import seed_recompress_ex
+    from rank_state_compression_head_b300.workload import DeviceRun
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group('nccl')
+    torch.cuda.set_device(local)
+    dev = torch.device('cuda', local)
+    stream = torch.cuda.current_stream()
+    T = w.T
+    K, W_ = args.steps, max(3, args.warmup)
+    total_steps = K + W_
+
+    # ---- setup: constants, prefill, compression, inputs of every step -----------------
+    run = DeviceRun(w, device=dev, steps_buffered=total_steps)
+    S_dense = run.prefill()
+    run.compress(S_dense)
+    for t in range(total_steps):
+        run.gen_inputs(t % w.steps, slot=t)
+    torch.cuda.synchronize()
+    ranks_host = run.ranks.cpu().numpy().astype(np.int64)
+    flush = torch.empty(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    sweeps = torch.zeros(run.H, device=dev, dtype=torch.int32)
+
+    uniq, counts = np.unique(ranks_host, return_counts=True)
+
+    def launch_bytes(s_before):  # algorithmic bytes of one decode launch at this point of the interval
+        return sum(int(c) * acc.decode_bytes(w.variant, w.d_k, w.d_v, int(r) + w.growth * s_before,
+                                              w.factor_dtype) for r, c in zip(uniq, counts))
+
+    bytes_at = [launch_bytes(s) for s in range(T)]
+    cols_at = [int(ranks_host.sum()) + run.H * w.growth * s for s in range(T)]
+
+    # ---- warm-up (brings clocks up, fills caches and code) ---------------------------
+    t_end = time.perf_counter() + args.warm_seconds
+    t = 0
+    while t < W_ or time.perf_counter() < t_end:
+        flush.zero_()
+        run.decode(slot=t % total_steps)
+        if run.state.steps_since_compress == T:
+            run.recompress()
+        t += 1
+        if t > 20000:
+            break
+    # continue the schedule from a compression boundary
+    if run.state.steps_since_compress:
+        run.recompress()
+    torch.cuda.synchronize()
+
+    # ---- timed region ------------------------------------------------------------------
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    rec_steps = []
+    bytes_decode = 0
+    m_sum = 0
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        c0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            s_before = run.state.steps_since_compress
+            m_sum += cols_at[s_before]
+            bytes_decode += bytes_at[s_before]
+            ev[i][0].record(stream)
+            run.decode(slot=W_ + i)
+            ev[i][1].record(stream)
+            if run.state.steps_since_compress == T:
+                seed_recompress_ex(run.state.st, run.trunc, sweeps)
+                rec_steps.append(i)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        c1 = time.perf_counter()
+    if ws > 1:
+        dist.barrier()
+    dec_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    rec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in rec_steps]
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = sum(step_ms)
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    heads_all = run.H * ws
+    value = heads_all * K / (total_ms / 1e3)
+    clocks = clk.summary(c0, c1)
+    sw = sweeps.cpu().numpy()
+
+    # ---- roofline of each kernel ---------------------------------------------------------
+    peaks = measured_peaks()
+    dec_avg_ms = statistics.mean(dec_ms)
+    dec_gbs = (bytes_decode / K) / (dec_avg_ms / 1e3) / 1e9
+    m_rec = ranks_host + w.growth * T
+    rec_flops = float(sum(acc.recompress_flops(w.d_k, w.d_v, int(mm), int(rr), float(max(s, 1)))
+                          for mm, rr, s in zip(m_rec, ranks_host, sw)))
+    rec_avg_ms = statistics.mean(rec_ms) if rec_ms else float('nan')
+    fp32_peak = 148 * 128 * 2 * (clocks['sm_max_mhz'] or 2032) * 1e6 / 1e12  # TFLOP/s, FFMA issue rate
+    rec_tflops = rec_flops / (rec_avg_ms / 1e3) / 1e12 if rec_ms else None
+    dec_total, rec_total = sum(dec_ms), sum(rec_ms)
+    traffic = profiled_traffic(f'decode_{w.variant}_{w.name}')
+    roof_dec = dict(kernel='decode_kernel', bound='hbm', achieved=round(dec_gbs, 1),
+                    peak=peaks['hbm_gbs'], unit='GB/s', frac=round(dec_gbs / peaks['hbm_gbs'], 4),
+                    traffic=traffic, peak_src=peaks['src'],
+                    algorithmic_bytes_per_launch=round(bytes_decode / K),
+                    avg_launch_us=round(dec_avg_ms * 1e3, 3))
+    roof_rec = dict(kernel='compress_kernel (recompress)', bound='alu', achieved=rec_tflops and round(rec_tflops, 3),
+                    peak=round(fp32_peak, 1), unit='TFLOP/s',
+                    frac=rec_tflops and round(rec_tflops / fp32_peak, 4), traffic=None,
+                    peak_src='148 SMs x 128 FP32 lanes x 2 FLOP x max SM clock',
+                    algorithmic_flops_per_launch=round(rec_flops), avg_launch_us=round(rec_avg_ms * 1e3, 1),
+                    jacobi_sweeps_mean=float(np.mean(sw)), jacobi_sweeps_max=int(np.max(sw)))
+    dominant = roof_dec if dec_total >= rec_total else roof_rec
+
+    out = dict(metric=METRIC, value=round(value), unit=UNIT, n_gpus=ws, steps=K, warmup=W_,
+               ms_per_step=round(total_ms / K, 5), higher_is_better=True, scaling='weak',
+               vs_baseline=None, dtype='f32', data='synthetic',
+               config=dict(workload=w.name, heads_per_gpu=run.H, d_k=w.d_k, d_v=w.d_v, r=w.r_max,
+                           T=w.T, factor_dtype=w.factor_dtype, variant=w.variant,
+                           l2='flushed before every timed step (256 MiB write, untimed)',
+                           parallelism=f'heads sharded, {ws} replica(s)'),
+               roofline=dominant, gpu_launches=K + len(rec_ms), clocks=clocks)
+    out['decode'] = dict(head_steps_per_s=round(heads_all * K / (dec_total / 1e3)),
+                         us_per_step=round(dec_avg_ms * 1e3, 3), gbs=round(dec_gbs, 1),
+                         frac_of_measured_hbm=round(dec_gbs / peaks['hbm_gbs'], 4),
+                         frac_of_8tbs=round(dec_gbs / 8000.0, 4),
+                         bytes_per_head_step=round(bytes_decode / K / run.H, 1),
+                         mean_columns=round(m_sum / K / run.H, 2))
+    out['recompress'] = roof_rec
+    out['time_share'] = dict(decode=round(dec_total / total_ms, 4), recompress=round(rec_total / total_ms, 4))
+
+    # ---- dense-state comparator ----------------------------------------------------------
+    if not args.no_dense:
+        o_d = torch.empty_like(run.o)
+        for t in range(W_):
+            run.dense_step(S_dense, slot=t, o=o_d)
+        dev_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            dev_ev[i][0].record(stream)
+            run.dense_step(S_dense, slot=W_ + i, o=o_d)
+            dev_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        dms = statistics.mean(dev_ev[i][0].elapsed_time(dev_ev[i][1]) for i in range(K))
+        dbytes = run.H * acc.dense_decode_bytes(w.variant, w.d_k, w.d_v)
+        out['dense'] = dict(us_per_step=round(dms * 1e3, 3), head_steps_per_s=round(run.H * ws / (dms / 1e3)),
+                            gbs=round(dbytes / (dms / 1e3) / 1e9, 1),
+                            bytes_per_head_step=acc.dense_decode_bytes(w.variant, w.d_k, w.d_v),
+                            bytes_ratio_dense_over_factored=round(dbytes / (bytes_decode / K), 3),
+                            time_ratio_dense_over_factored_decode=round(dms / dec_avg_ms, 3),
+                            time_ratio_dense_over_factored_with_recompress=round(dms / (total_ms / K), 3))
+
+    # ---- end to end through host buffers -------------------------------------------------
+    if not args.no_e2e:
+        pin = dict(pin_memory=True)
+        hq = torch.empty(K, *run.q.shape[1:], **pin)
+        hk = torch.empty(K, *run.k.shape[1:], **pin)
+        hv = torch.empty(K, *run.v.shape[1:], **pin)
+        hg = torch.empty(K, *run.gate.shape[1:], **pin)
+        hb = torch.empty(K, *run.beta.shape[1:], **pin)
+        ho = torch.empty(K, *run.o.shape, **pin)
+        for src, dst in ((run.q, hq), (run.k, hk), (run.v, hv), (run.gate, hg), (run.beta, hb)):
+            dst.copy_(src[W_:W_ + K])
+        torch.cuda.synchronize()
+        if run.state.steps_since_compress:
+            run.recompress()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h2d = sum(x[0].numel() * 4 for x in (hq, hk, hv, hg, hb))
+        d2h = ho[0].numel() * 4
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(K):
+            run.q[0].copy_(hq[i], non_blocking=True)
+            run.k[0].copy_(hk[i], non_blocking=True)
+            run.v[0].copy_(hv[i], non_blocking=True)
+            run.gate[0].copy_(hg[i], non_blocking=True)
+            run.beta[0].copy_(hb[i], non_blocking=True)
+            run.decode(slot=0)
+            if run.state.steps_since_compress == T:
+                run.recompress()
+            ho[i].copy_(run.o, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if ws > 1:
+            tt = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        out['e2e'] = dict(value=round(heads_all * K / (e2e_ms / 1e3)), unit=UNIT,
+                          h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                          ms_per_step=round(e2e_ms / K, 5))
+
+    # ---- CPU oracle baseline (rank 0, N = 1) --------------------------------------------
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        out['cpu_baseline'] = oracle_sample(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    import synth
+    if args.workload not in synth.WORKLOADS:
+        raise SystemExit(f'unknown workload {args.workload}; one of {sorted(synth.WORKLOADS)}')
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == 'reference':
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == '__main__':
+    main()

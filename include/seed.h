@@ -166,6 +166,13 @@ int seed_decode_step(seed_state *st, const float *q, const float *k, const float
 int seed_recompress(seed_state *st, float *trunc_err, seed_stream_t stream);
 
 /*
+ * seed_recompress_ex — seed_recompress that also reports, per head, the number
+ * of Jacobi sweeps it ran (sweeps [n_heads] int32, or NULL; -1 where the sweep
+ * limit was reached).  Used to count the work of a recompression.
+ */
+int seed_recompress_ex(seed_state *st, float *trunc_err, int32_t *sweeps, seed_stream_t stream);
+
+/*
  * seed_materialize — S = a vbar^T + U_eff W^T for every head (tests, export).
  *   S_out  [n_heads][d_k][d_v] fp32, row-major per head.
  */

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, 'libseed.so')
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f'{LIB_PATH} is missing: build the CUDA library first '
-        '(python -m rank_state_compression_head_b300.build). There is no CPU fallback.')
+        '(python rank_state_compression_head_b300/build.py). There is no CPU fallback.')
 
 _lib = ctypes.CDLL(LIB_PATH)
 
@@ -79,6 +79,7 @@ _PROTOS = {
     'seed_compress_dense': (ctypes.c_int, [_vp, _sp, _vp, _vp]),
     'seed_decode_step': (ctypes.c_int, [_sp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     'seed_recompress': (ctypes.c_int, [_sp, _vp, _vp]),
+    'seed_recompress_ex': (ctypes.c_int, [_sp, _vp, _vp, _vp]),
     'seed_materialize': (ctypes.c_int, [_sp, _vp, _vp]),
     'seed_dense_decode_step': (ctypes.c_int, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                               _vp, _vp, _vp, _vp, _vp]),
@@ -151,6 +152,11 @@ def seed_decode_step(st: seed_state, q, k, v, gate, beta, A, o, stream=None) -> 
 
 def seed_recompress(st: seed_state, trunc_err=None, stream=None) -> None:
     _check('seed_recompress', _lib.seed_recompress(ctypes.byref(st), _ptr(trunc_err), _stream(stream)))
+
+
+def seed_recompress_ex(st: seed_state, trunc_err=None, sweeps=None, stream=None) -> None:
+    _check('seed_recompress_ex', _lib.seed_recompress_ex(ctypes.byref(st), _ptr(trunc_err), _ptr(sweeps),
+                                                         _stream(stream)))
 
 
 def seed_materialize(st: seed_state, S_out, stream=None) -> None:

@@ -1,6 +1,7 @@
 """Build libseed.so in-tree for sm_103a with nvcc.
 
-Usage: ``python -m rank_state_compression_head_b300.build [--force] [-v]``.
+Usage: ``python rank_state_compression_head_b300/build.py [--force] [-v]`` (run as a
+script: importing the package needs the library to exist already).
 Objects go to ``_build/`` at the repository root; the library lands next to
 this file, where the Python binding loads it.
 """

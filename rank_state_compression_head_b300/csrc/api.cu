@@ -114,16 +114,21 @@ extern "C" int seed_decode_step(seed_state *st, const float *q, const float *k, 
   return c;
 }
 
-extern "C" int seed_recompress(seed_state *st, float *trunc_err, seed_stream_t stream) {
+extern "C" int seed_recompress_ex(seed_state *st, float *trunc_err, int32_t *sweeps,
+                                  seed_stream_t stream) {
   int c = check_state(st);
   if (c) return c;
   if (st->steps_since_compress > st->T) return SEED_ERR_CAPACITY;
   if (st->n_heads == 0) { st->steps_since_compress = 0; return SEED_OK; }
   const int m_max = rmax_of(st) + growth_of(st->variant) * st->steps_since_compress;
-  c = cuda_status(launch_recompress(view_of(st), st->factor_dtype, trunc_err, m_max,
+  c = cuda_status(launch_recompress(view_of(st), st->factor_dtype, trunc_err, sweeps, m_max,
                                     (cudaStream_t)stream));
   if (c == SEED_OK) st->steps_since_compress = 0;
   return c;
+}
+
+extern "C" int seed_recompress(seed_state *st, float *trunc_err, seed_stream_t stream) {
+  return seed_recompress_ex(st, trunc_err, nullptr, stream);
 }
 
 extern "C" int seed_materialize(const seed_state *st, float *S_out, seed_stream_t stream) {

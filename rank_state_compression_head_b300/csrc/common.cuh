@@ -98,8 +98,8 @@ namespace seedk {
 cudaError_t launch_decode(const StateView &sv, int factor_dtype, const float *q, const float *k,
                           const float *v, const float *gate, const float *beta, const float *A,
                           float *o, int cols_max, cudaStream_t s);
-cudaError_t launch_recompress(const StateView &sv, int factor_dtype, float *trunc_err, int m_max,
-                              cudaStream_t s);
+cudaError_t launch_recompress(const StateView &sv, int factor_dtype, float *trunc_err,
+                              int32_t *sweeps, int m_max, cudaStream_t s);
 cudaError_t launch_compress_dense(const StateView &sv, int factor_dtype, const float *S,
                                   float *trunc_err, cudaStream_t s);
 cudaError_t launch_materialize(const StateView &sv, int factor_dtype, float *S_out, int m_max,

@@ -31,6 +31,7 @@ constexpr int kMaxSweeps = 30;
 struct CompressArgs {
   StateView sv;
   float *trunc_err;
+  int32_t *sweeps;  // Jacobi sweeps per head (or -1: limit reached), optional
   const float *S;   // dense input (compress_dense) or nullptr (recompress)
   int m_max;        // smem sizing: largest column count of any head
 };
@@ -321,6 +322,7 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
     float e = 0.f;
     for (int k = r; k < m; ++k) e += sig2[order[k]];
     if (p.trunc_err) p.trunc_err[h] = sqrtf(e);
+    if (p.sweeps) p.sweeps[h] = sweeps;
     if (sv.status) sv.status[h] = sweeps < 0 ? SEED_ERR_NOT_CONVERGED : SEED_OK;
   }
 
@@ -379,16 +381,16 @@ static cudaError_t launch_compress_v(const CompressArgs &a, cudaStream_t s) {
   return launch_compress_d<SEED_GDN, TF, DENSE>(a, s);
 }
 
-cudaError_t launch_recompress(const StateView &sv, int factor_dtype, float *trunc_err, int m_max,
-                              cudaStream_t s) {
-  CompressArgs a{sv, trunc_err, nullptr, m_max};
+cudaError_t launch_recompress(const StateView &sv, int factor_dtype, float *trunc_err,
+                              int32_t *sweeps, int m_max, cudaStream_t s) {
+  CompressArgs a{sv, trunc_err, sweeps, nullptr, m_max};
   if (factor_dtype == SEED_BF16) return launch_compress_v<__nv_bfloat16, false>(a, s);
   return launch_compress_v<float, false>(a, s);
 }
 
 cudaError_t launch_compress_dense(const StateView &sv, int factor_dtype, const float *S,
                                   float *trunc_err, cudaStream_t s) {
-  CompressArgs a{sv, trunc_err, S, sv.d_v};
+  CompressArgs a{sv, trunc_err, nullptr, S, sv.d_v};
   if (factor_dtype == SEED_BF16) return launch_compress_v<__nv_bfloat16, true>(a, s);
   return launch_compress_v<float, true>(a, s);
 }
