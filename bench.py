@@ -131,34 +131,49 @@ def run_reference(args, w):
 # ----------------------------------------------------------------------------
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML while running (read only)."""
+    """Samples the SM clock and the clock-event reasons while running.
+
+    Read-only NVML queries through ctypes on libnvidia-ml (no Python NVML
+    package needed); nothing is set.
+    """
     REASONS = {0x1: 'gpu_idle', 0x2: 'applications_clocks_setting', 0x4: 'sw_power_cap',
                0x8: 'hw_slowdown', 0x10: 'sync_boost', 0x20: 'sw_thermal_slowdown',
                0x40: 'hw_thermal_slowdown', 0x80: 'hw_power_brake_slowdown', 0x100: 'display_clock_setting'}
+    NVML_CLOCK_SM = 1
 
     def __init__(self, index: int, period: float = 0.002):
+        import ctypes
         self.samples = []
         self.period = period
         self._stop = threading.Event()
         self.ok = False
+        self.why = ''
+        self.max_mhz = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            nv = ctypes.CDLL('libnvidia-ml.so.1')
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError('nvmlInit_v2 failed')
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+                raise RuntimeError('no NVML handle')
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.reason_fn = getattr(nv, 'nvmlDeviceGetCurrentClocksEventReasons', None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nv, self.h, self.ct = nv, h, ctypes
             self.ok = True
-        except Exception:
-            self.max_mhz = None
+        except Exception as e:
+            self.why = f'{type(e).__name__}: {e}'
 
     def _run(self):
+        ct = self.ct
+        mhz, rs = ct.c_uint(), ct.c_ulonglong()
         while not self._stop.is_set():
-            try:
-                mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
-                rs = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                self.samples.append((time.perf_counter(), mhz, rs))
-            except Exception:
-                pass
+            a = self.nv.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ct.byref(mhz))
+            b = self.reason_fn(self.h, ct.byref(rs))
+            if a == 0 and b == 0:
+                self.samples.append((time.perf_counter(), mhz.value, rs.value))
             time.sleep(self.period)
 
     def __enter__(self):
@@ -174,7 +189,7 @@ class ClockSampler:
 
     def summary(self, t0: float, t1: float):
         if not self.ok:
-            return dict(sm_mhz=None, sm_max_mhz=None, reasons=['nvml unavailable'])
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=['nvml unavailable: ' + self.why])
         inside = [s for s in self.samples if t0 <= s[0] <= t1] or self.samples[-5:]
         mhz = statistics.median(s[1] for s in inside) if inside else None
         bits = 0

@@ -59,6 +59,12 @@ __device__ static inline float warp_sum(float x) {
   return x;
 }
 
+__device__ static inline float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
 __device__ static inline bool finite(float x) { return isfinite(x); }
 
 // Named barrier over `nthreads` threads (a multiple of 32) with id 1..15.

@@ -27,6 +27,10 @@
 namespace seedk {
 
 constexpr int kMaxSweeps = 30;
+// After the core is scaled to a largest entry in [1/2, 1), a column whose squared
+// norm is below this is under fp32 resolution of the largest one: rotating it only
+// stirs rounding noise, so it is left alone (its singular value is negligible).
+constexpr float kNegligible = 1e-14f;
 
 struct CompressArgs {
   StateView sv;
@@ -40,6 +44,11 @@ struct CompressArgs {
 // dimension ld).  On exit the upper triangle holds R; below the diagonal of
 // column j sits the reflector's vector v_j (v_j[j] = 1 implicit), tau[j] its
 // coefficient: H_j = I - tau_j v_j v_j^T, A = H_0 H_1 ... H_{n-1} R.
+// Each reflector is formed from the column scaled by its largest magnitude,
+// so that columns far below 1 (long products of gates) do not underflow in
+// their squared norm: an inaccurate norm would give a reflector that is not
+// orthogonal, which then corrupts the larger columns it is applied to.
+// Columns below the smallest normal float are treated as zero.
 __device__ static void householder_qr(float *A, int ld, int nrows, int ncols, float *tau,
                                       int ttid, int tsize, int bar) {
   const int lane = ttid & 31;
@@ -47,17 +56,30 @@ __device__ static void householder_qr(float *A, int ld, int nrows, int ncols, fl
   for (int j = 0; j < nref; ++j) {
     float *cj = A + j * ld;
     if (ttid < 32) {
-      float ss = 0.f;
-      for (int i = j + 1 + lane; i < nrows; i += 32) ss = fmaf(cj[i], cj[i], ss);
-      ss = warp_sum(ss);
+      float amax = 0.f;
+      for (int i = j + lane; i < nrows; i += 32) amax = fmaxf(amax, fabsf(cj[i]));
+      amax = warp_max(amax);
       const float alpha = cj[j];
       float tj = 0.f, beta = alpha;
-      if (ss > 0.f) {
-        const float nrm = sqrtf(fmaf(alpha, alpha, ss));
-        beta = alpha >= 0.f ? -nrm : nrm;
-        tj = (beta - alpha) / beta;
-        const float sc = 1.f / (alpha - beta);
-        for (int i = j + 1 + lane; i < nrows; i += 32) cj[i] *= sc;
+      if (amax >= FLT_MIN) {
+        const float inv = 1.f / amax;
+        float ss = 0.f;
+        for (int i = j + 1 + lane; i < nrows; i += 32) {
+          const float x = cj[i] * inv;
+          ss = fmaf(x, x, ss);
+        }
+        ss = warp_sum(ss);
+        if (ss > 0.f) {
+          const float as = alpha * inv;
+          const float nrm = sqrtf(fmaf(as, as, ss));
+          const float bs = as >= 0.f ? -nrm : nrm;
+          tj = (bs - as) / bs;
+          const float sc = 1.f / ((as - bs) * amax);   // v_i = x_i / (alpha - beta), |v_i| <= 1
+          for (int i = j + 1 + lane; i < nrows; i += 32) cj[i] *= sc;
+          beta = bs * amax;
+        }
+      } else {
+        for (int i = j + 1 + lane; i < nrows; i += 32) cj[i] = 0.f;
       }
       __syncwarp();
       if (lane == 0) { cj[j] = beta; tau[j] = tj; }
@@ -164,7 +186,7 @@ __device__ static int jacobi_svd(float *K, float *Y, int ld, int n, float tol) {
           ga += __shfl_xor_sync(0xffffffffu, ga, o);
         }
       }
-      if (real && ga != 0.f && fabsf(ga) > tol * sqrtf(al) * sqrtf(be)) {
+      if (real && al > kNegligible && be > kNegligible && fabsf(ga) > tol * sqrtf(al) * sqrtf(be)) {
         const float zeta = (be - al) / (2.f * ga);
         const float t = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(fmaf(zeta, zeta, 1.f)));
         const float c = rsqrtf(fmaf(t, t, 1.f));
@@ -190,7 +212,7 @@ __device__ static int jacobi_svd(float *K, float *Y, int ld, int n, float tol) {
 // Dynamic shared-memory layout of the compression kernels.
 struct Smem {
   int lda, ldb, ldk;
-  int offA, offB, offK, offY, offTa, offTb, offS, offO;
+  int offA, offB, offK, offY, offTa, offTb, offS, offO, offR;
   int total_floats;
   __host__ __device__ Smem(int m, int dk, int dv, bool dense) {
     lda = dk + 1;
@@ -204,7 +226,8 @@ struct Smem {
     offTb = offTa + m;
     offS = offTb + m;
     offO = offS + m;
-    total_floats = offO + m;
+    offR = offO + m;          // 8 floats of reduction scratch
+    total_floats = offR + 8;
   }
 };
 
@@ -297,7 +320,21 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
   }
   __syncthreads();
 
-  // ---- SVD of the core ------------------------------------------------------------
+  // ---- SVD of the core, scaled by a power of two to a largest entry in [1/2, 1) ----------
+  float kmax = 0.f;
+  for (int idx = tid; idx < m * m; idx += NT) kmax = fmaxf(kmax, fabsf(K[(idx / m) * ldk + idx % m]));
+  kmax = warp_max(kmax);
+  float *red = smem + L.offR;
+  if ((tid & 31) == 0) red[tid >> 5] = kmax;
+  __syncthreads();
+  kmax = 0.f;
+  for (int w = 0; w < NT / 32; ++w) kmax = fmaxf(kmax, red[w]);
+  int kexp = 0;
+  if (kmax > 0.f) frexpf(kmax, &kexp);
+  const float kscale = ldexpf(1.f, -kexp), kunscale = ldexpf(1.f, kexp);
+  __syncthreads();
+  for (int idx = tid; idx < m * m; idx += NT) K[(idx / m) * ldk + idx % m] *= kscale;
+  __syncthreads();
   const float tol = (float)(m > 16 ? m : 16) * FLT_EPSILON;
   const int sweeps = jacobi_svd<NT>(K, Y, ldk, m, tol);
 
@@ -321,7 +358,7 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
   if (tid == 0) {
     float e = 0.f;
     for (int k = r; k < m; ++k) e += sig2[order[k]];
-    if (p.trunc_err) p.trunc_err[h] = sqrtf(e);
+    if (p.trunc_err) p.trunc_err[h] = sqrtf(e) * kunscale;
     if (p.sweeps) p.sweeps[h] = sweeps;
     if (sv.status) sv.status[h] = sweeps < 0 ? SEED_ERR_NOT_CONVERGED : SEED_OK;
   }
@@ -333,7 +370,7 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
       const float *z = K + order[k] * ldk;
       float acc = 0.f;
       for (int l = 0; l < m; ++l) acc = fmaf(A[l * lda + tid], z[l], acc);
-      Elem<TF>::store(Uh + (int64_t)k * DK + tid, acc);
+      Elem<TF>::store(Uh + (int64_t)k * DK + tid, acc * kunscale);
     }
   }
   if (tid >= NT - DV) {

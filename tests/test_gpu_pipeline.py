@@ -83,6 +83,8 @@ def run_pipeline(w, sample, steps, record):
             states[t] = gpu_head_states(run.state, sample)
         if t % w.T == 0:
             run.recompress(run.trunc)
+            bad = int((run.state.status[:run.H] != 0).sum())
+            assert bad == 0, f'recompress status after step {t}: {bad} heads'
     torch.cuda.synchronize()
     status = run.state.status[:run.H]
     assert int((status != 0).sum()) == 0, 'device status'
