@@ -8,7 +8,7 @@ every T-th step included, so the figure is whole-job head-steps/s.
 
 Prints one JSON line (rank 0).  Inputs of every step are generated on the
 device before the timed region and stay resident in HBM; L2 is flushed
-(a 256 MiB write) before every timed step, and each timed step is bracketed
+(a 256 MiB write followed by a 256 MiB read) before every timed step, and each timed step is bracketed
 by CUDA events on the launching stream.  ``--impl reference`` times the CPU
 oracle on a bounded sample of the same workload instead.
 """
@@ -235,7 +235,6 @@ def run_gpu(args, w):
     import torch
     import torch.distributed as dist
     from rank_state_compression_head_b300 import accounting as acc
-    from rank_state_compression_head_b300 import seed_recompress_ex
     from rank_state_compression_head_b300.workload import DeviceRun
 
     ws, rank, local = dist_env()
@@ -256,7 +255,17 @@ def run_gpu(args, w):
         run.gen_inputs(t % w.steps, slot=t)
     torch.cuda.synchronize()
     ranks_host = run.ranks.cpu().numpy().astype(np.int64)
-    flush = torch.empty(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    flush_w = torch.empty(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    flush_r = torch.ones(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    flush_out = torch.empty((), device=dev, dtype=torch.float32)
+
+    def l2_flush():
+        # write a buffer larger than L2, then read another one: L2 ends up holding clean,
+        # unrelated lines, so the timed step neither hits its own data nor pays for
+        # writing back the flush's dirty lines
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=flush_out)
+
     sweeps = torch.zeros(run.H, device=dev, dtype=torch.int32)
 
     uniq, counts = np.unique(ranks_host, return_counts=True)
@@ -272,7 +281,7 @@ def run_gpu(args, w):
     t_end = time.perf_counter() + args.warm_seconds
     t = 0
     while t < W_ or time.perf_counter() < t_end:
-        flush.zero_()
+        l2_flush()
         run.decode(slot=t % total_steps)
         if run.state.steps_since_compress == T:
             run.recompress()
@@ -285,6 +294,18 @@ def run_gpu(args, w):
     torch.cuda.synchronize()
 
     # ---- timed region ------------------------------------------------------------------
+    # Arguments of every call are built before timing so that the host issues each
+    # step in a few microseconds and the GPU queue never drains inside a step.
+    import ctypes
+    from rank_state_compression_head_b300 import _lib
+    sptr = stream.cuda_stream
+    st_ref = ctypes.byref(run.state.st)
+    A_ptr = run.A.data_ptr() if run.A is not None else None
+    dec_args = [(st_ref, run.q[W_ + i].data_ptr(), run.k[W_ + i].data_ptr(), run.v[W_ + i].data_ptr(),
+                 run.gate[W_ + i].data_ptr(), run.beta[W_ + i].data_ptr(), A_ptr, run.o.data_ptr(), sptr)
+                for i in range(K)]
+    rec_args = (st_ref, run.trunc.data_ptr(), sweeps.data_ptr(), sptr)
+    dec_fn, rec_fn = _lib.seed_decode_step, _lib.seed_recompress_ex
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     rec_steps = []
     bytes_decode = 0
@@ -295,17 +316,19 @@ def run_gpu(args, w):
     with ClockSampler(local) as clk:
         c0 = time.perf_counter()
         for i in range(K):
-            flush.zero_()
+            l2_flush()
             s_before = run.state.steps_since_compress
             m_sum += cols_at[s_before]
             bytes_decode += bytes_at[s_before]
             ev[i][0].record(stream)
-            run.decode(slot=W_ + i)
+            rc = dec_fn(*dec_args[i])
             ev[i][1].record(stream)
             if run.state.steps_since_compress == T:
-                seed_recompress_ex(run.state.st, run.trunc, sweeps)
+                rc |= rec_fn(*rec_args)
                 rec_steps.append(i)
             ev[i][2].record(stream)
+            if rc:
+                raise RuntimeError(f'library call failed with status {rc}')
         torch.cuda.synchronize()
         c1 = time.perf_counter()
     if ws > 1:
@@ -353,7 +376,7 @@ def run_gpu(args, w):
                vs_baseline=None, dtype='f32', data='synthetic',
                config=dict(workload=w.name, heads_per_gpu=run.H, d_k=w.d_k, d_v=w.d_v, r=w.r_max,
                            T=w.T, factor_dtype=w.factor_dtype, variant=w.variant,
-                           l2='flushed before every timed step (256 MiB write, untimed)',
+                           l2='flushed before every timed step (256 MiB write then 256 MiB read, untimed)',
                            parallelism=f'heads sharded, {ws} replica(s)'),
                roofline=dominant, gpu_launches=K + len(rec_ms), clocks=clocks)
     out['decode'] = dict(head_steps_per_s=round(heads_all * K / (dec_total / 1e3)),
@@ -372,10 +395,16 @@ def run_gpu(args, w):
             run.dense_step(S_dense, slot=t, o=o_d)
         dev_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
         torch.cuda.synchronize()
+        dn_fn = _lib.seed_dense_decode_step
+        dn_args = [(run.variant, run.H, w.d_k, w.d_v, S_dense.data_ptr(), run.q[W_ + i].data_ptr(),
+                    run.k[W_ + i].data_ptr(), run.v[W_ + i].data_ptr(), run.gate[W_ + i].data_ptr(),
+                    run.beta[W_ + i].data_ptr(), A_ptr, run.vbar_index.data_ptr(), o_d.data_ptr(), sptr)
+                   for i in range(K)]
         for i in range(K):
-            flush.zero_()
+            l2_flush()
             dev_ev[i][0].record(stream)
-            run.dense_step(S_dense, slot=W_ + i, o=o_d)
+            if dn_fn(*dn_args[i]):
+                raise RuntimeError('dense step failed')
             dev_ev[i][1].record(stream)
         torch.cuda.synchronize()
         dms = statistics.mean(dev_ev[i][0].elapsed_time(dev_ev[i][1]) for i in range(K))

@@ -28,8 +28,8 @@
  *  - Conditions found on the device (non-finite values, a Jacobi SVD that did
  *    not converge) are written per head to `status[h]` when `status` is not
  *    NULL; read it after synchronising.  0 = OK, otherwise a seed_status code.
- *  - Floating-point vectors (q, k, v, o, a, S, gates) are fp32, contiguous per
- *    head, 16-byte aligned.  Factors U and W are fp32 or bf16 (round to nearest
+ *  - Floating-point vectors (q, k, v, o, a, S, scales, the per-channel gate)
+ *    are fp32, contiguous per head, with 16-byte aligned base pointers.  Factors U and W are fp32 or bf16 (round to nearest
  *    even on store), arithmetic is fp32.
  *  - d_k must be 128; d_v must be 128 or 64.  The largest number of factor
  *    columns a head may hold is SEED_MAX_COLUMNS.
@@ -55,7 +55,8 @@ typedef enum {
   SEED_ERR_ALIGNMENT = 4,        /* a pointer is not 16-byte aligned                       */
   SEED_ERR_CUDA = 5,             /* a CUDA launch failed                                    */
   SEED_ERR_NOT_CONVERGED = 6,    /* device, per head: Jacobi SVD hit its sweep limit        */
-  SEED_ERR_NONFINITE = 7         /* device, per head: a non-finite value was produced       */
+  SEED_ERR_NONFINITE = 7,        /* device, per head: a non-finite value was produced       */
+  SEED_ERR_TIMEOUT = 8           /* device, per head: a bounded wait for a copy gave up     */
 } seed_status;
 
 typedef enum {

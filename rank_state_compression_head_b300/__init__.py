@@ -36,6 +36,7 @@ SEED_ERR_ALIGNMENT = 4
 SEED_ERR_CUDA = 5
 SEED_ERR_NOT_CONVERGED = 6
 SEED_ERR_NONFINITE = 7
+SEED_ERR_TIMEOUT = 8
 SEED_GDN, SEED_KDA, SEED_MAMBA2 = 0, 1, 2
 SEED_F32, SEED_BF16 = 0, 1
 SEED_MAX_COLUMNS = 64

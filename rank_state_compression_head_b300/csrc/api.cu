@@ -31,7 +31,8 @@ int check_state(const seed_state *st) {
   if (rmax + growth_of(st->variant) * st->T > kMaxCols) return SEED_ERR_UNSUPPORTED_SHAPE;
   if (st->n_heads == 0) return SEED_OK;
   if (!st->a || !st->U || !st->W || !st->scale || !st->vbar) return SEED_ERR_INVALID_ARG;
-  if (misaligned(st->a) || misaligned(st->U) || misaligned(st->W) || misaligned(st->vbar))
+  if (misaligned(st->a) || misaligned(st->U) || misaligned(st->W) || misaligned(st->vbar) ||
+      misaligned(st->scale))
     return SEED_ERR_ALIGNMENT;
   return SEED_OK;
 }
@@ -77,6 +78,7 @@ extern "C" const char *seed_status_string(int status) {
     case SEED_ERR_CUDA: return "CUDA launch failed";
     case SEED_ERR_NOT_CONVERGED: return "Jacobi SVD did not converge";
     case SEED_ERR_NONFINITE: return "non-finite value";
+    case SEED_ERR_TIMEOUT: return "device wait timed out";
     default: return "unknown status";
   }
 }
@@ -107,6 +109,7 @@ extern "C" int seed_decode_step(seed_state *st, const float *q, const float *k, 
   if (st->variant != SEED_MAMBA2 && !beta) return SEED_ERR_INVALID_ARG;
   if (st->variant == SEED_MAMBA2 && !A) return SEED_ERR_INVALID_ARG;
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o)) return SEED_ERR_ALIGNMENT;
+  if (st->variant == SEED_KDA && misaligned(gate)) return SEED_ERR_ALIGNMENT;
   const int cols = rmax_of(st) + growth_of(st->variant) * st->steps_since_compress;
   c = cuda_status(launch_decode(view_of(st), st->factor_dtype, q, k, v, gate, beta, A, o, cols,
                                 (cudaStream_t)stream));

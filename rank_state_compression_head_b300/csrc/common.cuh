@@ -73,6 +73,67 @@ __device__ static inline void team_sync(int id, int nthreads) {
 }
 
 // ---------------------------------------------------------------------------
+// mbarrier + bulk-copy (TMA engine, non-tensor) primitives
+// ---------------------------------------------------------------------------
+
+__device__ static inline uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ static inline void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ static inline void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ static inline void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ static inline void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ static inline void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ static inline bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false if the phase did not complete within the spin limit.
+constexpr uint32_t kSpinLimit = 1u << 26;
+__device__ static inline bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kSpinLimit; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// global -> shared bulk copy (size and both addresses multiples of 16 bytes),
+// completion counted on `bar` as transaction bytes
+__device__ static inline void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// OR of a predicate over the `nthreads` threads of named barrier `id` (also a barrier)
+__device__ static inline int team_or(int id, int nthreads, int pred) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+      " selp.s32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r;
+}
+
+// ---------------------------------------------------------------------------
 // per-head geometry shared by the factored kernels
 // ---------------------------------------------------------------------------
 
@@ -97,6 +158,40 @@ struct StateView {
   __device__ inline int dir_of(int h) const { return vbar_index ? vbar_index[h] : h; }
 };
 
+struct DecodeArgs {
+  StateView sv;
+  const float *q, *k, *v, *gate, *beta, *A;
+  float *o;
+};
+
+// Sum of eight per-lane values over the warp: after 9 shuffles lane l holds
+// the total of value ((l >> 4) & 1) * 4 + ((l >> 3) & 1) * 2 + ((l >> 2) & 1).
+__device__ inline float warp_reduce8(const float (&v)[8], int lane) {
+  float a4[4], a2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b4 ? v[i + 4] : v[i], send = b4 ? v[i] : v[i + 4];
+    a4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b3 ? a4[i + 2] : a4[i], send = b3 ? a4[i] : a4[i + 2];
+    a2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  const float keep = b2 ? a2[1] : a2[0], send = b2 ? a2[0] : a2[1];
+  float a = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  a += __shfl_xor_sync(0xffffffffu, a, 2);
+  a += __shfl_xor_sync(0xffffffffu, a, 1);
+  return a;
+}
+__device__ inline int reduce8_index(int lane) {
+  return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+}
+
+// Column scales can travel with the bulk copy when their block is 16-byte aligned.
+__device__ inline bool scales_in_stage(int64_t c0, int cap) { return ((c0 | cap) & 3) == 0; }
+
 }  // namespace seedk
 
 // Launchers implemented in the kernel files, called by the C-ABI layer.
@@ -104,6 +199,8 @@ namespace seedk {
 cudaError_t launch_decode(const StateView &sv, int factor_dtype, const float *q, const float *k,
                           const float *v, const float *gate, const float *beta, const float *A,
                           float *o, int cols_max, cudaStream_t s);
+int sm_count();
+cudaError_t launch_decode_mma(const DecodeArgs &a, int cols_max, cudaStream_t s);
 cudaError_t launch_recompress(const StateView &sv, int factor_dtype, float *trunc_err,
                               int32_t *sweeps, int m_max, cudaStream_t s);
 cudaError_t launch_compress_dense(const StateView &sv, int factor_dtype, const float *S,

@@ -1,0 +1,466 @@
+// Fused read-out + exact factored update for bf16 factors, with the two
+// contractions of a step on the tensor cores.
+//
+// "Shallow Encoding Emits Deep Memories", picx.dev summary, Methodology >
+// Exact Update (Lemma 2); thelatestinai.com list view, Table 1 (decode
+// column: read-out and update of each recurrent state).
+//
+// CTAs of 256 threads walk the heads blockIdx.x, blockIdx.x + gridDim.x, ...
+// through a ring of NS shared-memory stages (NS - 1 heads in flight while one
+// is computed); launched with one stage and one head per CTA, as many CTAs per
+// SM as fit keep several heads' loads in flight.  The threads copy the factor columns
+// (contiguous in HBM) with asynchronous 16-byte copies into rows padded to
+// 272 bytes, so that the ldmatrix reads below hit 32 distinct banks.  Per
+// head the CTA does
+//
+//   U pass   X[4][m] = [k_hi; k_lo; q_hi; q_lo] U_stored          (mma m16n8k16)
+//   scale    x_k = c * (X0 + X1),  x_q = c * (X2 + X3)              (column scales)
+//   W pass   [Wx_k Wx_q] = W [x_k_hi x_k_lo x_q_hi x_q_lo]           (mma m16n8k16)
+//
+// Products of bf16 values are exact in fp32 and the accumulation is fp32.  The
+// fp32 operands (k, q, x) enter as a bf16 pair hi + lo, so they carry 16
+// significant bits; the result differs from fp32 dot products by less than
+// fp32 summation-order noise times ~2^-8.  The read-out and the appended
+// columns then follow Lemma 2 exactly as in the CUDA-core kernel (decode.cu).
+#include "common.cuh"
+
+namespace seedk {
+
+constexpr int kMmaThreads = 128;
+
+template <int VAR, int DV, int MAXC>
+struct MmaStage {
+  static constexpr int DK = kDK;
+  static constexpr bool KDA = VAR == SEED_KDA;
+  static constexpr int USTR = DK * 2 + 16;  // padded bytes per U column
+  static constexpr int WSTR = DV * 2 + 16;  // padded bytes per W column
+  static constexpr int U_OFF = 0;
+  static constexpr int W_OFF = U_OFF + MAXC * USTR;
+  static constexpr int Q_OFF = W_OFF + MAXC * WSTR;
+  static constexpr int K_OFF = Q_OFF + DK * 4;
+  static constexpr int A_OFF = K_OFF + DK * 4;
+  static constexpr int V_OFF = A_OFF + DK * 4;
+  static constexpr int VB_OFF = V_OFF + DV * 4;
+  static constexpr int SC_OFF = VB_OFF + DV * 4;                 // column scales [MAXC], or D [DK] (KDA)
+  static constexpr int AL_OFF = SC_OFF + (KDA ? DK : MAXC) * 4;  // KDA: alpha [DK]
+  static constexpr int G_OFF = AL_OFF + (KDA ? DK * 4 : 0);      // gate, beta, A (scalars)
+  static constexpr int BYTES = G_OFF + 16;
+  static_assert(W_OFF % 16 == 0 && Q_OFF % 16 == 0 && SC_OFF % 16 == 0 && BYTES % 16 == 0,
+                "16-byte copies");
+};
+
+template <int VAR, int DV, int MAXC, int NS>
+struct MmaSmem {
+  using S = MmaStage<VAR, DV, MAXC>;
+  static constexpr int NX = VAR == SEED_MAMBA2 ? 1 : 2;
+  static constexpr int XLD = MAXC + 16;                                    // bf16 per x row
+  static constexpr int XS_OFF = NS * S::BYTES;                             // bf16 [2 NX][XLD]
+  static constexpr int WX_OFF = XS_OFF + ((2 * NX * XLD * 2 + 15) & ~15);  // f32 [NX][DV]
+  static constexpr int SCAL_OFF = WX_OFF + NX * DV * 4;                    // f32 [NW][8]
+  static constexpr int BYTES = SCAL_OFF + (kMmaThreads / 32) * 8 * 4;
+};
+
+__device__ static inline void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ static inline void cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ static inline void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ static inline void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ static inline void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ static inline void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// D += A B, m16n8k16, bf16 inputs, fp32 accumulate
+__device__ static inline void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                       uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// High (part = 0) or low (part = 1) bf16 of the split x = hi + lo.
+__device__ static inline __nv_bfloat16 bf16_part(float x, int part) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  return part ? __float2bfloat16_rn(x - __bfloat162float(hi)) : hi;
+}
+__device__ static inline uint32_t pack_bf16(__nv_bfloat16 lo_elem, __nv_bfloat16 hi_elem) {
+  return (uint32_t)__bfloat16_as_ushort(lo_elem) | ((uint32_t)__bfloat16_as_ushort(hi_elem) << 16);
+}
+
+template <int VAR, int DV, int MAXC, int NS>
+__global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArgs p) {
+  using TF = __nv_bfloat16;
+  constexpr int DK = kDK;
+  constexpr int NT = kMmaThreads;
+  using S = MmaStage<VAR, DV, MAXC>;
+  using L = MmaSmem<VAR, DV, MAXC, NS>;
+  constexpr int NX = L::NX;
+  constexpr int NA = 2 * NX;  // rows of the U-pass operand: hi/lo of k (and q)
+  constexpr bool KDA = VAR == SEED_KDA;
+  constexpr bool M2 = VAR == SEED_MAMBA2;
+  constexpr int NSW = (DK > DV ? DK : DV) / 32;  // warps holding scalar partials
+  static_assert(MAXC % 16 == 0 && MAXC <= 64, "column tiles");
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem + L::XS_OFF);
+  float *wxs = reinterpret_cast<float *>(smem + L::WX_OFF);
+  float *scal = reinterpret_cast<float *>(smem + L::SCAL_OFF);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
+  const StateView &sv = p.sv;
+  const int growth = sv.growth;
+  const int G = gridDim.x;
+  const int first = blockIdx.x;
+  const int nmine = first < sv.n_heads ? (sv.n_heads - first + G - 1) / G : 0;
+
+  // Copy head number i of this CTA into stage i % NS (one commit group per head,
+  // empty when i is past the end, so that group counting stays uniform).
+  auto issue = [&](int i) {
+    if (i < nmine) {
+      const int h = first + i * G;
+      const int r_h = sv.rank_of(h);
+      const int m = r_h + growth * sv.steps;
+      if (r_h >= 0 && m <= MAXC) {
+        unsigned char *st = smem + (i % NS) * S::BYTES;
+        const int64_t c0 = sv.col0(h);
+        const int dir = sv.dir_of(h);
+        const TF *Ug = reinterpret_cast<const TF *>(sv.U) + c0 * DK;
+        const TF *Wg = reinterpret_cast<const TF *>(sv.W) + c0 * DV;
+        constexpr int UCH = DK * 2 / 16, WCH = DV * 2 / 16;  // 16-byte chunks per column
+        for (int idx = tid; idx < m * UCH; idx += NT) {
+          const int j = idx / UCH, c = idx % UCH;
+          cp_async16(st + S::U_OFF + j * S::USTR + c * 16, Ug + (int64_t)j * DK + c * 8);
+        }
+        for (int idx = tid; idx < m * WCH; idx += NT) {
+          const int j = idx / WCH, c = idx % WCH;
+          cp_async16(st + S::W_OFF + j * S::WSTR + c * 16, Wg + (int64_t)j * DV + c * 8);
+        }
+        if (tid < DK / 4) {
+          cp_async16(st + S::Q_OFF + tid * 16, p.q + (int64_t)h * DK + tid * 4);
+          cp_async16(st + S::K_OFF + tid * 16, p.k + (int64_t)h * DK + tid * 4);
+          cp_async16(st + S::A_OFF + tid * 16, sv.a + (int64_t)h * DK + tid * 4);
+          if (KDA) {
+            cp_async16(st + S::SC_OFF + tid * 16, sv.scale + (int64_t)h * DK + tid * 4);
+            cp_async16(st + S::AL_OFF + tid * 16, p.gate + (int64_t)h * DK + tid * 4);
+          }
+        } else if (tid < DK / 4 + DV / 4) {
+          const int c = tid - DK / 4;
+          cp_async16(st + S::V_OFF + c * 16, p.v + (int64_t)h * DV + c * 4);
+          cp_async16(st + S::VB_OFF + c * 16, sv.vbar + (int64_t)dir * DV + c * 4);
+        } else if (tid == DK / 4 + DV / 4) {
+          float *gates = reinterpret_cast<float *>(st + S::G_OFF);
+          if (!KDA) cp_async4(gates + 0, p.gate + h);
+          if (!M2) cp_async4(gates + 1, p.beta + h);
+          if (M2) cp_async4(gates + 2, p.A + dir);
+        } else if (!KDA && scales_in_stage(c0, r_h + growth * sv.T)) {
+          const int c = tid - DK / 4 - DV / 4 - 1;
+          for (int cc = c; cc * 4 < m; cc += NT - DK / 4 - DV / 4 - 1)
+            cp_async16(st + S::SC_OFF + cc * 16, sv.scale + c0 + cc * 4);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  for (int i = 0; i < NS - 1; ++i) issue(i);
+
+  for (int i = 0; i < nmine; ++i) {
+    // The stage of head i-1 is free: its last readers passed barrier C of that head.
+    issue(i + NS - 1);
+    cp_async_wait<NS - 1>();  // this thread's copies of head i have landed
+
+    const int h = first + i * G;
+    const int r_h = sv.rank_of(h);
+    const int m = r_h + growth * sv.steps;
+    const bool bad_rank = r_h < 0 || m > MAXC;
+    const int64_t c0 = bad_rank ? 0 : sv.col0(h);
+    unsigned char *st = smem + (i % NS) * S::BYTES;
+    float *scw = reinterpret_cast<float *>(st + S::SC_OFF);
+    if (!bad_rank && !KDA && !scales_in_stage(c0, r_h + growth * sv.T))
+      for (int j = tid; j < m; j += NT) scw[j] = sv.scale[c0 + j];  // unaligned column scales
+    __syncthreads();  // barrier A: head i is in shared memory
+    if (bad_rank) {
+      if (tid == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
+      continue;
+    }
+    if (tid == 0 && sv.status) sv.status[h] = SEED_OK;
+
+    const uint32_t u_base = smem_u32(st + S::U_OFF), w_base = smem_u32(st + S::W_OFF);
+    const float *qs = reinterpret_cast<const float *>(st + S::Q_OFF);
+    const float *ks = reinterpret_cast<const float *>(st + S::K_OFF);
+    const float *as = reinterpret_cast<const float *>(st + S::A_OFF);
+    const float *vs = reinterpret_cast<const float *>(st + S::V_OFF);
+    const float *vbs = reinterpret_cast<const float *>(st + S::VB_OFF);
+    const float *scs = scw;
+    const float *als = reinterpret_cast<const float *>(st + S::AL_OFF);
+    const float *gts = reinterpret_cast<const float *>(st + S::G_OFF);
+    float g = 0.f, beta = 0.f, dt = 0.f;
+    if (VAR == SEED_GDN) { g = gts[0]; beta = gts[1]; }
+    if (KDA) beta = gts[1];
+    if (M2) { dt = gts[0]; g = expf(dt * gts[2]); }
+    const int m16 = (m + 15) & ~15;
+
+    // padding: x rows and W columns [m, m16) must be zero for the W pass
+    for (int idx = tid; idx < NA * (L::XLD - m); idx += NT) {
+      const int row = idx / (L::XLD - m), j = m + idx % (L::XLD - m);
+      xs[row * L::XLD + j] = __float2bfloat16_rn(0.f);
+    }
+    {
+      constexpr int CH = S::WSTR / 16;
+      for (int idx = tid; idx < (m16 - m) * CH; idx += NT) {
+        const int j = m + idx / CH, c = idx % CH;
+        *reinterpret_cast<uint4 *>(st + S::W_OFF + j * S::WSTR + c * 16) = make_uint4(0, 0, 0, 0);
+      }
+    }
+
+    // ---- U pass: column tiles of 8, round robin over the warps -----------------------
+    if (warp * 8 < m) {
+      uint32_t a0[8], a2[8];
+#pragma unroll
+      for (int ks_ = 0; ks_ < 8; ++ks_) {
+        a0[ks_] = 0u;
+        a2[ks_] = 0u;
+        if (gq < NA) {
+          const int k0 = ks_ * 16 + 2 * tq;
+          const float *vec = (gq < 2) ? (M2 ? qs : ks) : qs;
+          float2 lo2 = *reinterpret_cast<const float2 *>(vec + k0);
+          float2 hi2 = *reinterpret_cast<const float2 *>(vec + k0 + 8);
+          if (KDA) {  // D k for the k rows, alpha D q for the q rows
+            const float2 d_lo = *reinterpret_cast<const float2 *>(scs + k0);
+            const float2 d_hi = *reinterpret_cast<const float2 *>(scs + k0 + 8);
+            lo2.x *= d_lo.x; lo2.y *= d_lo.y; hi2.x *= d_hi.x; hi2.y *= d_hi.y;
+            if (gq >= 2) {
+              const float2 l_lo = *reinterpret_cast<const float2 *>(als + k0);
+              const float2 l_hi = *reinterpret_cast<const float2 *>(als + k0 + 8);
+              lo2.x *= l_lo.x; lo2.y *= l_lo.y; hi2.x *= l_hi.x; hi2.y *= l_hi.y;
+            }
+          }
+          const int part = gq & 1;
+          a0[ks_] = pack_bf16(bf16_part(lo2.x, part), bf16_part(lo2.y, part));
+          a2[ks_] = pack_bf16(bf16_part(hi2.x, part), bf16_part(hi2.y, part));
+        }
+      }
+      for (int n0 = warp * 8; n0 < m; n0 += NT / 4) {
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t row_addr = u_base + (uint32_t)((n0 + (lane & 7)) * S::USTR + (lane >> 3) * 16);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t b[4];
+        ldsm_x4(row_addr + kk * 64, b);
+        mma_bf16(d, a0[2 * kk], 0u, a2[2 * kk], 0u, b[0], b[1]);
+        mma_bf16(d, a0[2 * kk + 1], 0u, a2[2 * kk + 1], 0u, b[2], b[3]);
+      }
+      // rows 2r and 2r+1 (hi, lo) of the same vector: lane 4g+t and lane 4(g+1)+t
+      const float o0 = __shfl_down_sync(0xffffffffu, d[0], 4);
+      const float o1 = __shfl_down_sync(0xffffffffu, d[1], 4);
+      if (gq < NA && (gq & 1) == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = n0 + 2 * tq + e;
+          if (j < m) {
+            const float c = KDA ? 1.f : scs[j];
+            const float x = c * (e ? d[1] + o1 : d[0] + o0);
+            const __nv_bfloat16 xh = __float2bfloat16_rn(x);
+            xs[gq * L::XLD + j] = xh;
+            xs[(gq + 1) * L::XLD + j] = __float2bfloat16_rn(x - __bfloat162float(xh));
+          }
+        }
+      }
+      }
+    }
+
+    // ---- block scalars: thread t owns row t (< DK) and value column t (< DV) ----------
+    float S_loc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) S_loc[j] = 0.f;
+    float kt = 0.f, qt = 0.f, at = 0.f, vt = 0.f, vbt = 0.f, alt = 0.f, Dt = 0.f, ct = 0.f;
+    float unew0 = 0.f, unew1 = 0.f;
+    if (tid < DK) {
+      kt = ks[tid]; qt = qs[tid]; at = as[tid];
+      if (VAR == SEED_GDN) {
+        unew0 = Elem<TF>::round(kt);
+        S_loc[0] = kt * at; S_loc[1] = qt * at; S_loc[2] = kt * qt; S_loc[3] = unew0 * qt;
+      } else if (KDA) {
+        alt = als[tid];
+        Dt = scs[tid];
+        const float Dn = alt * Dt;
+        unew0 = Elem<TF>::round(kt / Dt);
+        unew1 = Elem<TF>::round(kt / Dn);
+        S_loc[0] = kt * at; S_loc[1] = alt * at * qt; S_loc[2] = alt * kt * qt; S_loc[3] = kt * qt;
+        S_loc[6] = unew0 * Dn * qt; S_loc[7] = unew1 * Dn * qt;
+      } else {
+        unew0 = Elem<TF>::round(dt * kt);
+        S_loc[0] = at * qt; S_loc[1] = kt * qt; S_loc[2] = unew0 * qt;
+      }
+    }
+    if (tid < DV) {
+      vt = vs[tid]; vbt = vbs[tid];
+      S_loc[4] = vt * vbt; S_loc[5] = vbt * vbt;
+    }
+    if (!KDA && tid < m) ct = scs[tid];
+    if (warp < NSW) {
+      const float r = warp_reduce8(S_loc, lane);
+      if ((lane & 3) == 0) scal[warp * 8 + reduce8_index(lane)] = r;
+    }
+    __syncthreads();  // barrier B: x, the padding and the scalar partials are visible
+
+    // ---- W pass: row tiles of 16 of W x, round robin over the warps -------------------
+    for (int i0 = warp * 16; i0 < DV; i0 += NT / 2) {
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      const int rsel = (lane & 7) + ((lane >> 4) << 3);
+      const int csel = i0 + ((lane >> 3) & 1) * 8;
+      for (int j0 = 0; j0 < m16; j0 += 16) {
+        uint32_t a[4];
+        ldsm_x4_t(w_base + (uint32_t)((j0 + rsel) * S::WSTR + csel * 2), a);
+        uint32_t b0 = 0u, b1 = 0u;
+        if (gq < NA) {
+          b0 = *reinterpret_cast<const uint32_t *>(xs + gq * L::XLD + j0 + 2 * tq);
+          b1 = *reinterpret_cast<const uint32_t *>(xs + gq * L::XLD + j0 + 2 * tq + 8);
+        }
+        mma_bf16(d, a[0], a[1], a[2], a[3], b0, b1);
+      }
+      if (tq < NX) {
+        wxs[tq * DV + i0 + gq] = d[0] + d[1];
+        wxs[tq * DV + i0 + gq + 8] = d[2] + d[3];
+      }
+    }
+    __syncthreads();  // barrier C: W x complete; the stage is no longer read
+
+    // ---- update and read-out (registers, scal, wxs only) -------------------------------
+    float Sg[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < NSW; ++w) a += scal[w * 8 + j];
+      Sg[j] = a;
+    }
+    const float omega = Sg[4] / Sg[5];
+    int bad = 0;
+    TF *Uo = reinterpret_cast<TF *>(sv.U) + (c0 + m) * DK;
+    TF *Wo = reinterpret_cast<TF *>(sv.W) + (c0 + m) * DV;
+    float wx[NX];
+#pragma unroll
+    for (int j = 0; j < NX; ++j) wx[j] = tid < DV ? wxs[j * DV + tid] : 0.f;
+    if (VAR == SEED_GDN) {
+      const float coef = beta * (omega - g * Sg[0]);
+      const float aq = fmaf(g, Sg[1], coef * Sg[2]);
+      if (tid < DK) {
+        const float an = fmaf(g, at, coef * kt);
+        sv.a[(int64_t)h * DK + tid] = an;
+        Elem<TF>::store(Uo + tid, kt);
+        bad |= !finite(an);
+      }
+      if (tid < DV) {
+        const float eps = fmaf(-omega, vbt, vt);
+        const float wn = Elem<TF>::round(beta * fmaf(-g, wx[0], eps));
+        Elem<TF>::store(Wo + tid, wn);
+        const float o = fmaf(vbt, aq, fmaf(g, wx[NX - 1], Sg[3] * wn));
+        p.o[(int64_t)h * DV + tid] = o;
+        bad |= !finite(o);
+      }
+      if (tid < m) sv.scale[c0 + tid] = g * ct;
+      if (tid == m) sv.scale[c0 + m] = 1.f;
+    } else if (KDA) {
+      const float aq = Sg[1] - beta * Sg[0] * Sg[2] + beta * omega * Sg[3];
+      if (tid < DK) {
+        const float an = alt * fmaf(-beta * kt, Sg[0], at) + beta * omega * kt;
+        sv.a[(int64_t)h * DK + tid] = an;
+        sv.scale[(int64_t)h * DK + tid] = alt * Dt;
+        Elem<TF>::store(Uo + tid, unew0);
+        Elem<TF>::store(Uo + DK + tid, unew1);
+        bad |= !finite(an);
+      }
+      if (tid < DV) {
+        const float eps = fmaf(-omega, vbt, vt);
+        const float w1 = Elem<TF>::round(-beta * wx[0]);
+        const float w2 = Elem<TF>::round(beta * eps);
+        Elem<TF>::store(Wo + tid, w1);
+        Elem<TF>::store(Wo + DV + tid, w2);
+        const float o = fmaf(vbt, aq, wx[NX - 1] + w1 * Sg[6] + w2 * Sg[7]);
+        p.o[(int64_t)h * DV + tid] = o;
+        bad |= !finite(o);
+      }
+    } else {
+      const float coef = dt * omega;
+      const float aC = fmaf(g, Sg[0], coef * Sg[1]);
+      if (tid < DK) {
+        const float an = fmaf(g, at, coef * kt);
+        sv.a[(int64_t)h * DK + tid] = an;
+        Elem<TF>::store(Uo + tid, unew0);
+        bad |= !finite(an);
+      }
+      if (tid < DV) {
+        const float wn = Elem<TF>::round(fmaf(-omega, vbt, vt));
+        Elem<TF>::store(Wo + tid, wn);
+        const float o = fmaf(vbt, aC, fmaf(g, wx[0], Sg[2] * wn));
+        p.o[(int64_t)h * DV + tid] = o;
+        bad |= !finite(o);
+      }
+      if (tid < m) sv.scale[c0 + tid] = g * ct;
+      if (tid == m) sv.scale[c0 + m] = 1.f;
+    }
+    // thread 0 wrote OK before barriers B and C, so this write lands after it
+    if (bad && sv.status) sv.status[h] = SEED_ERR_NONFINITE;
+  }
+  cp_async_wait<0>();
+}
+
+// One stage and one head per CTA (grid = heads): several CTAs per SM keep
+// several heads' loads in flight.  With NS > 1 the same kernel runs
+// persistently over a ring of NS stages.
+template <int VAR, int DV, int MAXC>
+static cudaError_t launch_mma_t(const DecodeArgs &a, cudaStream_t s) {
+  constexpr int NS = 1;
+  using L = MmaSmem<VAR, DV, MAXC, NS>;
+  auto kern = decode_mma_kernel<VAR, DV, MAXC, NS>;
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMmaThreads, L::BYTES);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+  }
+  int grid = NS == 1 ? a.sv.n_heads : sm_count() * per_sm;
+  if (grid > a.sv.n_heads) grid = a.sv.n_heads;
+  kern<<<grid, kMmaThreads, L::BYTES, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int VAR, int DV>
+static cudaError_t launch_mma_c(const DecodeArgs &a, int cols_max, cudaStream_t s) {
+  if (cols_max <= 16) return launch_mma_t<VAR, DV, 16>(a, s);
+  if (cols_max <= 32) return launch_mma_t<VAR, DV, 32>(a, s);
+  if (cols_max <= 48) return launch_mma_t<VAR, DV, 48>(a, s);
+  return launch_mma_t<VAR, DV, 64>(a, s);
+}
+
+template <int VAR>
+static cudaError_t launch_mma_d(const DecodeArgs &a, int cols_max, cudaStream_t s) {
+  if (a.sv.d_v == 64) return launch_mma_c<VAR, 64>(a, cols_max, s);
+  return launch_mma_c<VAR, 128>(a, cols_max, s);
+}
+
+cudaError_t launch_decode_mma(const DecodeArgs &a, int cols_max, cudaStream_t s) {
+  switch (a.sv.variant) {
+    case SEED_GDN: return launch_mma_d<SEED_GDN>(a, cols_max, s);
+    case SEED_KDA: return launch_mma_d<SEED_KDA>(a, cols_max, s);
+    default: return launch_mma_d<SEED_MAMBA2>(a, cols_max, s);
+  }
+}
+
+}  // namespace seedk

@@ -40,7 +40,7 @@ def test_struct_layout_matches_header():
 
 
 def test_status_strings():
-    for code in range(8):
+    for code in range(9):
         assert R.status_string(code)
     assert 'capacity' in R.status_string(R.SEED_ERR_CAPACITY)
     assert R.status_string(99) == 'unknown status'
@@ -81,6 +81,7 @@ def decode(st, **ptrs):
     (dict(r=-1, r_max=-1), R.SEED_ERR_INVALID_ARG),
     (dict(a=None), R.SEED_ERR_INVALID_ARG),
     (dict(U=FAKE + 4), R.SEED_ERR_ALIGNMENT),
+    (dict(scale=FAKE + 4), R.SEED_ERR_ALIGNMENT),
     (dict(steps_since_compress=16), R.SEED_ERR_CAPACITY),
 ])
 def test_decode_rejects_on_host(kw, code):
@@ -95,6 +96,8 @@ def test_decode_rejects_missing_inputs():
     assert decode(st, q=None) == R.SEED_ERR_INVALID_ARG
     assert decode(st, beta=None) == R.SEED_ERR_INVALID_ARG
     assert decode(st, o=FAKE + 8) == R.SEED_ERR_ALIGNMENT
+    kda = make_state(variant=R.SEED_KDA, r=16, r_max=16)
+    assert decode(kda, gate=FAKE + 4) == R.SEED_ERR_ALIGNMENT
     m2 = make_state(variant=R.SEED_MAMBA2, d_v=64, r=16, r_max=16)
     assert decode(m2, A=None, beta=None) == R.SEED_ERR_INVALID_ARG
     assert R._lib.seed_decode_step(None, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None) == R.SEED_ERR_INVALID_ARG
