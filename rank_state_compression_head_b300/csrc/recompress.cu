@@ -10,13 +10,15 @@
 //   A = U_eff, B = W (fp32 in shared memory, column-major, padded columns)
 //   Householder QR of A and of B, concurrently in two 64-thread teams
 //   K = R_a R_b^T (m x m)
-//   one-sided Jacobi SVD of K: rotate pairs of columns of K (and of Y = I)
-//     until every pair is orthogonal; then K Y = X Sigma, K = X Sigma Y^T
+//   one-sided Jacobi SVD of K: rotate pairs of columns of K until every pair
+//     is orthogonal; then K J = X Sigma, K = X Sigma J^T
 //   order columns by |K_j| (= sigma_j), keep the rank(h) largest
 //   Q_a, Q_b formed in place from the reflectors
-//   U_new = Q_a (K)[:, kept] = Q_a X_r Sigma_r,  W_new = Q_b Y[:, kept]
+//   U_new = Q_a X_r,  W_new = Q_b K^T X_r = Q_b Y_r Sigma_r   (X_r: normalised
+//   kept columns of K J; the singular values go with W, and K^T X_r is the
+//   projection of the core onto the kept directions, so no rotation is kept)
 // compress_dense (one CTA of 256 threads per head): the same with A = C and
-// B = I (so K = R_a and W_new = Y[:, kept]).
+// B = I (so K = R_a and W_new = R_a^T X_r).
 //
 // The arithmetic is fp32 FMA: the QR and Jacobi steps are sequences of small
 // dependent reductions that do not map onto tensor-core tiles.
@@ -38,17 +40,45 @@ struct CompressArgs {
   int32_t *sweeps;  // Jacobi sweeps per head (or -1: limit reached), optional
   const float *S;   // dense input (compress_dense) or nullptr (recompress)
   int m_max;        // smem sizing: largest column count of any head
+  int cs_alloc;     // column stride of the core buffers in the allocation
 };
 
+// x . y over rows [i0, nrows) of two columns (16-byte aligned column starts,
+// nrows a multiple of 4): scalar head up to a multiple of 4, then float4 body.
+__device__ static inline float col_dot(const float *__restrict__ x, const float *__restrict__ y, int i0,
+                                       int nrows) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  int i = i0;
+  for (; (i & 3) && i < nrows; ++i) s0 = fmaf(x[i], y[i], s0);
+  for (; i < nrows; i += 4) {
+    const float4 a = *reinterpret_cast<const float4 *>(x + i);
+    const float4 b = *reinterpret_cast<const float4 *>(y + i);
+    s0 = fmaf(a.x, b.x, s0); s1 = fmaf(a.y, b.y, s1); s2 = fmaf(a.z, b.z, s2); s3 = fmaf(a.w, b.w, s3);
+  }
+  return (s0 + s1) + (s2 + s3);
+}
+// y[i] -= a x[i] over rows [i0, nrows), same layout rules.
+__device__ static inline void col_axpy(float a, const float *__restrict__ x, float *__restrict__ y, int i0,
+                                       int nrows) {
+  int i = i0;
+  for (; (i & 3) && i < nrows; ++i) y[i] = fmaf(-a, x[i], y[i]);
+  for (; i < nrows; i += 4) {
+    const float4 b = *reinterpret_cast<const float4 *>(x + i);
+    float4 c = *reinterpret_cast<const float4 *>(y + i);
+    c.x = fmaf(-a, b.x, c.x); c.y = fmaf(-a, b.y, c.y); c.z = fmaf(-a, b.z, c.z); c.w = fmaf(-a, b.w, c.w);
+    *reinterpret_cast<float4 *>(y + i) = c;
+  }
+}
+
 // Householder QR in place on a column-major nrows x ncols panel (leading
-// dimension ld).  On exit the upper triangle holds R; below the diagonal of
-// column j sits the reflector's vector v_j (v_j[j] = 1 implicit), tau[j] its
-// coefficient: H_j = I - tau_j v_j v_j^T, A = H_0 H_1 ... H_{n-1} R.
-// Each reflector is formed from the column scaled by its largest magnitude,
-// so that columns far below 1 (long products of gates) do not underflow in
-// their squared norm: an inaccurate norm would give a reflector that is not
-// orthogonal, which then corrupts the larger columns it is applied to.
-// Columns below the smallest normal float are treated as zero.
+// dimension ld, a multiple of 4; nrows a multiple of 4).  On exit the upper
+// triangle holds R; below the diagonal of column j sits the reflector's vector
+// v_j (v_j[j] = 1 implicit), tau[j] its coefficient: H_j = I - tau_j v_j v_j^T,
+// A = H_0 H_1 ... H_{n-1} R.  Each reflector is formed from the column scaled
+// by its largest magnitude, so that columns far below 1 (long products of
+// gates) do not underflow in their squared norm: an inaccurate norm would give
+// a reflector that is not orthogonal, which then corrupts the larger columns
+// it is applied to.  Columns below the smallest normal float are treated as zero.
 __device__ static void householder_qr(float *A, int ld, int nrows, int ncols, float *tau,
                                       int ttid, int tsize, int bar) {
   const int lane = ttid & 31;
@@ -74,7 +104,7 @@ __device__ static void householder_qr(float *A, int ld, int nrows, int ncols, fl
           const float nrm = sqrtf(fmaf(as, as, ss));
           const float bs = as >= 0.f ? -nrm : nrm;
           tj = (bs - as) / bs;
-          const float sc = 1.f / ((as - bs) * amax);   // v_i = x_i / (alpha - beta), |v_i| <= 1
+          const float sc = 1.f / ((as - bs) * amax);  // v_i = x_i / (alpha - beta), |v_i| <= 1
           for (int i = j + 1 + lane; i < nrows; i += 32) cj[i] *= sc;
           beta = bs * amax;
         }
@@ -89,18 +119,9 @@ __device__ static void householder_qr(float *A, int ld, int nrows, int ncols, fl
     if (tj != 0.f) {
       for (int l = j + 1 + ttid; l < ncols; l += tsize) {
         float *cl = A + l * ld;
-        float s0 = cl[j], s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        int i = j + 1;
-        for (; i + 3 < nrows; i += 4) {
-          s0 = fmaf(cj[i], cl[i], s0);
-          s1 = fmaf(cj[i + 1], cl[i + 1], s1);
-          s2 = fmaf(cj[i + 2], cl[i + 2], s2);
-          s3 = fmaf(cj[i + 3], cl[i + 3], s3);
-        }
-        for (; i < nrows; ++i) s0 = fmaf(cj[i], cl[i], s0);
-        const float sv = tj * ((s0 + s1) + (s2 + s3));
+        const float sv = tj * (cl[j] + col_dot(cj, cl, j + 1, nrows));
         cl[j] -= sv;
-        for (i = j + 1; i < nrows; ++i) cl[i] = fmaf(-sv, cj[i], cl[i]);
+        col_axpy(sv, cj, cl, j + 1, nrows);
       }
     }
     team_sync(bar, tsize);
@@ -115,17 +136,10 @@ __device__ static void form_q(float *A, int ld, int nrows, int ncols, const floa
     const float tj = tau[j];
     if (tj != 0.f) {
       for (int l = j + 1 + ttid; l < ncols; l += tsize) {
-        float *cl = A + l * ld;  // rows < l of a finished column are zero
-        float s0 = 0.f, s1 = 0.f;
-        int i = j + 1;
-        for (; i + 1 < nrows; i += 2) {
-          s0 = fmaf(cj[i], cl[i], s0);
-          s1 = fmaf(cj[i + 1], cl[i + 1], s1);
-        }
-        for (; i < nrows; ++i) s0 = fmaf(cj[i], cl[i], s0);
-        const float sv = tj * (s0 + s1);   // cl[j] == 0 here
+        float *cl = A + l * ld;  // rows < l of a finished column are zero, so cl[j] == 0
+        const float sv = tj * col_dot(cj, cl, j + 1, nrows);
         cl[j] = -sv;
-        for (i = j + 1; i < nrows; ++i) cl[i] = fmaf(-sv, cj[i], cl[i]);
+        col_axpy(sv, cj, cl, j + 1, nrows);
       }
     }
     team_sync(bar, tsize);
@@ -139,43 +153,73 @@ __device__ static void form_q(float *A, int ld, int nrows, int ncols, const floa
   }
 }
 
-// One-sided (Hestenes) Jacobi on the n columns of K (ld x n, rows 0..n-1),
-// accumulating the rotations in Y (starts as I).  Round-robin pair order: n'
-// = n rounded up to even seats, seat 0 fixed, the others rotate each round;
-// pair i joins seats i and n'-1-i.  A pair is rotated when
-// |k_p . k_q| > tol |k_p| |k_q|.  Whole block (NT threads).  Returns the
-// number of sweeps, or -1 if the sweep limit was reached while still rotating.
-template <int NT>
-__device__ static int jacobi_svd(float *K, float *Y, int ld, int n, float tol) {
-  const int tid = threadIdx.x;
-  for (int idx = tid; idx < n * ld; idx += NT) {
-    const int c = idx / ld, r = idx % ld;
-    Y[idx] = (r == c) ? 1.f : 0.f;
+// Geometry of the core K (n x n) in shared memory for the Jacobi rounds: the
+// threads of a column pair own contiguous chunks of R = ld / tpp rows (R a
+// multiple of 4, rows n..ld-1 are zero), columns are cs = ld + 4 floats apart
+// so that 16-byte accesses of different columns spread over the banks.
+struct JacobiGeom {
+  int tpp, ld, cs;
+};
+__host__ __device__ inline JacobiGeom jacobi_geom(int n, int nthreads) {
+  const int P = (n + 1) / 2 > 0 ? (n + 1) / 2 : 1;
+  const int n4 = (n + 3) & ~3;
+  int tpp = 1;
+  while (tpp * 2 * P <= nthreads && tpp < 32 && 8 * tpp <= n4) tpp *= 2;
+  const int ld = (n + 4 * tpp - 1) / (4 * tpp) * (4 * tpp);
+  return JacobiGeom{tpp, ld, ld + 4};
+}
+__host__ inline int jacobi_cs_alloc(int m_max, int nthreads) {
+  int cs = 4;
+  for (int n = 0; n <= m_max; ++n) {
+    const int c = jacobi_geom(n, nthreads).cs;
+    cs = c > cs ? c : cs;
   }
-  if (n < 2) { __syncthreads(); return 0; }
+  return cs;
+}
+
+// One-sided (Hestenes) Jacobi on the n columns of K: rotate pairs of columns
+// until every pair is orthogonal, K <- K J, so that the columns of K J are
+// X Sigma.  The rotations J are not kept: the rebuild uses the original core.
+// Round-robin pair order: n' = n rounded up to even seats, seat 0 fixed, the
+// others move one seat each round; pair i joins seats i and n'-1-i.  A pair is
+// rotated when |k_p . k_q| > tol |k_p| |k_q| and both columns are above fp32
+// resolution of the core (scaled to a largest entry in [1/2, 1)).  Each thread
+// keeps its chunk of both columns in registers through a round.  Whole block.
+// Returns the number of sweeps, or -1 if the sweep limit was reached.
+template <int NT, int RMAX>
+__device__ static int jacobi_svd(float *K, int n, const JacobiGeom &g, float tol) {
+  if (n < 2) return 0;
+  const int tid = threadIdx.x;
   const int nn = n + (n & 1);
   const int P = nn / 2;
-  int tpp = 1;
-  while (tpp * 2 * P <= NT && tpp < 32) tpp *= 2;
+  const int tpp = g.tpp, cs = g.cs;
+  const int R = g.ld / tpp, R4 = R / 4;
   const int pair = tid / tpp, sub = tid % tpp;
   const bool active = pair < P;
-  __syncthreads();
   for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
     int rotated = 0;
     for (int round = 0; round < nn - 1; ++round) {
-      int p = -1, q = -1;
+      int p = 0, q = 0;
       if (active) {
         const int sp = pair, sq = nn - 1 - pair;
         p = sp == 0 ? 0 : 1 + (sp - 1 + round) % (nn - 1);
         q = 1 + (sq - 1 + round) % (nn - 1);
       }
       const bool real = active && p < n && q < n;
+      float4 xp[RMAX / 4], xq[RMAX / 4];
       float al = 0.f, be = 0.f, ga = 0.f;
+      float4 *kp = reinterpret_cast<float4 *>(K + p * cs + sub * R);
+      float4 *kq = reinterpret_cast<float4 *>(K + q * cs + sub * R);
       if (real) {
-        const float *kp = K + p * ld, *kq = K + q * ld;
-        for (int r = sub; r < n; r += tpp) {
-          const float x = kp[r], y = kq[r];
-          al = fmaf(x, x, al); be = fmaf(y, y, be); ga = fmaf(x, y, ga);
+#pragma unroll
+        for (int v = 0; v < RMAX / 4; ++v) {
+          if (v < R4) {
+            xp[v] = kp[v];
+            xq[v] = kq[v];
+            al = fmaf(xp[v].x, xp[v].x, fmaf(xp[v].y, xp[v].y, fmaf(xp[v].z, xp[v].z, fmaf(xp[v].w, xp[v].w, al))));
+            be = fmaf(xq[v].x, xq[v].x, fmaf(xq[v].y, xq[v].y, fmaf(xq[v].z, xq[v].z, fmaf(xq[v].w, xq[v].w, be))));
+            ga = fmaf(xp[v].x, xq[v].x, fmaf(xp[v].y, xq[v].y, fmaf(xp[v].z, xq[v].z, fmaf(xp[v].w, xq[v].w, ga))));
+          }
         }
       }
 #pragma unroll
@@ -191,14 +235,15 @@ __device__ static int jacobi_svd(float *K, float *Y, int ld, int n, float tol) {
         const float t = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(fmaf(zeta, zeta, 1.f)));
         const float c = rsqrtf(fmaf(t, t, 1.f));
         const float s = c * t;
-        float *kp = K + p * ld, *kq = K + q * ld, *yp = Y + p * ld, *yq = Y + q * ld;
-        for (int r = sub; r < n; r += tpp) {
-          const float x = kp[r], y = kq[r];
-          kp[r] = fmaf(c, x, -s * y);
-          kq[r] = fmaf(s, x, c * y);
-          const float u = yp[r], w = yq[r];
-          yp[r] = fmaf(c, u, -s * w);
-          yq[r] = fmaf(s, u, c * w);
+#pragma unroll
+        for (int v = 0; v < RMAX / 4; ++v) {
+          if (v < R4) {
+            const float4 a = xp[v], b = xq[v];
+            kp[v] = make_float4(fmaf(c, a.x, -s * b.x), fmaf(c, a.y, -s * b.y), fmaf(c, a.z, -s * b.z),
+                                fmaf(c, a.w, -s * b.w));
+            kq[v] = make_float4(fmaf(s, a.x, c * b.x), fmaf(s, a.y, c * b.y), fmaf(s, a.z, c * b.z),
+                                fmaf(s, a.w, c * b.w));
+          }
         }
         rotated = 1;
       }
@@ -209,24 +254,26 @@ __device__ static int jacobi_svd(float *K, float *Y, int ld, int n, float tol) {
   return -1;
 }
 
-// Dynamic shared-memory layout of the compression kernels.
+// Dynamic shared-memory layout of the compression kernels (offsets in floats,
+// multiples of 4).
 struct Smem {
-  int lda, ldb, ldk;
-  int offA, offB, offK, offY, offTa, offTb, offS, offO, offR;
+  int lda, ldb;
+  int offA, offB, offK, offK0, offTa, offTb, offS, offI, offO, offR;
   int total_floats;
-  __host__ __device__ Smem(int m, int dk, int dv, bool dense) {
-    lda = dk + 1;
-    ldb = dv + 1;
-    ldk = m + 1;
+  __host__ __device__ Smem(int m, int dk, int dv, bool dense, int cs) {
+    lda = dk + 4;  // 16-byte aligned columns, 4 banks apart
+    ldb = dv + 4;
+    auto up4 = [](int x) { return (x + 3) & ~3; };
     offA = 0;
-    offB = offA + m * lda;
-    offK = offB + (dense ? 0 : m * ldb);
-    offY = offK + m * ldk;
-    offTa = offY + m * ldk;
-    offTb = offTa + m;
-    offS = offTb + m;
-    offO = offS + m;
-    offR = offO + m;          // 8 floats of reduction scratch
+    offB = up4(offA + m * lda);
+    offK = up4(offB + (dense ? 0 : m * ldb));
+    offK0 = up4(offK + m * cs);
+    offTa = up4(offK0 + m * cs);
+    offTb = offTa + up4(m);
+    offS = offTb + up4(m);
+    offI = offS + up4(m);
+    offO = offI + up4(m);
+    offR = offO + up4(m);     // 8 floats of reduction scratch
     total_floats = offR + 8;
   }
 };
@@ -235,6 +282,7 @@ template <int VAR, typename TF, int DV, bool DENSE>
 __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const CompressArgs p) {
   constexpr int DK = kDK;
   constexpr int NT = DENSE ? 256 : 128;
+  constexpr int RMAX = DENSE ? 32 : 16;
   extern __shared__ __align__(16) float smem[];
   const int h = blockIdx.x;
   const int tid = threadIdx.x;
@@ -246,11 +294,14 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
     return;
   }
   const int64_t c0 = sv.col0(h);
-  const Smem L(DENSE ? DV : p.m_max, DK, DV, DENSE);
-  float *A = smem + L.offA, *B = smem + L.offB, *K = smem + L.offK, *Y = smem + L.offY;
-  float *tauA = smem + L.offTa, *tauB = smem + L.offTb, *sig2 = smem + L.offS;
+  const Smem L(DENSE ? DV : p.m_max, DK, DV, DENSE, p.cs_alloc);
+  const JacobiGeom jg = jacobi_geom(m, NT);
+  const int cs = jg.cs, ldr = jg.ld;
+  float *A = smem + L.offA, *B = smem + L.offB, *K = smem + L.offK, *K0 = smem + L.offK0;
+  float *tauA = smem + L.offTa, *tauB = smem + L.offTb, *sig2 = smem + L.offS, *inv = smem + L.offI;
   int *order = reinterpret_cast<int *>(smem + L.offO);
-  const int lda = L.lda, ldb = L.ldb, ldk = L.ldk;
+  float *red = smem + L.offR;
+  const int lda = L.lda, ldb = L.ldb;
   TF *Uh = reinterpret_cast<TF *>(sv.U) + c0 * DK;
   TF *Wh = reinterpret_cast<TF *>(sv.W) + c0 * DV;
 
@@ -297,16 +348,19 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
   }
   __syncthreads();
 
-  // ---- core K = R_a R_b^T (or R_a) ----------------------------------------------
-  for (int idx = tid; idx < m * m; idx += NT) {
-    const int j = idx / m, i = idx % m;  // K[j][i]: column j, row i
+  // ---- core K = R_a R_b^T (or R_a), rows padded with zeros to ld; K0 keeps a copy --------
+  for (int idx = tid; idx < m * ldr; idx += NT) {
+    const int j = idx / ldr, i = idx % ldr;  // K[j][i]: column j, row i
     float acc = 0.f;
-    if (DENSE) {
-      acc = i <= j ? A[j * lda + i] : 0.f;
-    } else {
-      for (int l = max(i, j); l < m; ++l) acc = fmaf(A[l * lda + i], B[l * ldb + j], acc);
+    if (i < m) {
+      if (DENSE) {
+        acc = i <= j ? A[j * lda + i] : 0.f;
+      } else {
+        for (int l = max(i, j); l < m; ++l) acc = fmaf(A[l * lda + i], B[l * ldb + j], acc);
+      }
     }
-    K[j * ldk + i] = acc;
+    K[j * cs + i] = acc;
+    K0[j * cs + i] = acc;
   }
   __syncthreads();
 
@@ -318,13 +372,11 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
     if (team == 0) form_q(A, lda, DK, m, tauA, ttid, 64, 1);
     else form_q(B, ldb, DV, m, tauB, ttid, 64, 2);
   }
-  __syncthreads();
 
   // ---- SVD of the core, scaled by a power of two to a largest entry in [1/2, 1) ----------
   float kmax = 0.f;
-  for (int idx = tid; idx < m * m; idx += NT) kmax = fmaxf(kmax, fabsf(K[(idx / m) * ldk + idx % m]));
+  for (int idx = tid; idx < m * ldr; idx += NT) kmax = fmaxf(kmax, fabsf(K[(idx / ldr) * cs + idx % ldr]));
   kmax = warp_max(kmax);
-  float *red = smem + L.offR;
   if ((tid & 31) == 0) red[tid >> 5] = kmax;
   __syncthreads();
   kmax = 0.f;
@@ -332,17 +384,17 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
   int kexp = 0;
   if (kmax > 0.f) frexpf(kmax, &kexp);
   const float kscale = ldexpf(1.f, -kexp), kunscale = ldexpf(1.f, kexp);
+  for (int idx = tid; idx < m * ldr; idx += NT) K[(idx / ldr) * cs + idx % ldr] *= kscale;
   __syncthreads();
-  for (int idx = tid; idx < m * m; idx += NT) K[(idx / m) * ldk + idx % m] *= kscale;
-  __syncthreads();
-  const float tol = (float)(m > 16 ? m : 16) * FLT_EPSILON;
-  const int sweeps = jacobi_svd<NT>(K, Y, ldk, m, tol);
+  const float tol = sizeof(TF) == 2 ? 1e-5f : (float)(m > 16 ? m : 16) * FLT_EPSILON;
+  const int sweeps = jacobi_svd<NT, RMAX>(K, m, jg, tol);
 
   // ---- order by sigma, truncation error -----------------------------------------------
   for (int j = tid; j < m; j += NT) {
     float acc = 0.f;
-    for (int i = 0; i < m; ++i) acc = fmaf(K[j * ldk + i], K[j * ldk + i], acc);
+    for (int i = 0; i < m; ++i) acc = fmaf(K[j * cs + i], K[j * cs + i], acc);
     sig2[j] = acc;
+    inv[j] = acc > kNegligible ? rsqrtf(acc) : 0.f;  // x_j = (K J)_j / sigma_j
   }
   __syncthreads();
   for (int j = tid; j < m; j += NT) {
@@ -363,28 +415,46 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
     if (sv.status) sv.status[h] = sweeps < 0 ? SEED_ERR_NOT_CONVERGED : SEED_OK;
   }
 
-  // ---- rebuild the kept columns -----------------------------------------------------
+  // ---- rebuild the kept columns: U = Q_a X_r,  W = Q_b K0^T X_r ----------------------------
   const int rk = r < m ? r : m;
   if (tid < DK) {
     for (int k = 0; k < rk; ++k) {
-      const float *z = K + order[k] * ldk;
+      const int col = order[k];
+      const float *z = K + col * cs;
       float acc = 0.f;
       for (int l = 0; l < m; ++l) acc = fmaf(A[l * lda + tid], z[l], acc);
-      Elem<TF>::store(Uh + (int64_t)k * DK + tid, acc * kunscale);
+      Elem<TF>::store(Uh + (int64_t)k * DK + tid, acc * inv[col]);
     }
   }
-  if (tid >= NT - DV) {
-    const int i = tid - (NT - DV);
-    for (int k = 0; k < rk; ++k) {
-      const float *y = Y + order[k] * ldk;
-      float acc;
-      if (DENSE) {
-        acc = y[i];
-      } else {
-        acc = 0.f;
-        for (int l = 0; l < m; ++l) acc = fmaf(B[l * ldb + i], y[l], acc);
+  if (DENSE) {
+    // Q_b = I: W[:, k] = K0^T x_k
+    for (int i = tid; i < DV; i += NT) {
+      for (int k = 0; k < rk; ++k) {
+        const int col = order[k];
+        const float *z = K + col * cs;
+        float acc = 0.f;
+        for (int l = 0; l < m; ++l) acc = fmaf(K0[i * cs + l], z[l], acc);
+        Elem<TF>::store(Wh + (int64_t)k * DV + i, acc * inv[col]);
       }
-      Elem<TF>::store(Wh + (int64_t)k * DV + i, acc);
+    }
+  } else {
+    __syncthreads();  // A (Q_a) is no longer needed: Y = K0^T X_r goes there
+    float *Y = A;
+    for (int idx = tid; idx < rk * m; idx += NT) {
+      const int k = idx / m, l = idx % m;
+      const int col = order[k];
+      const float *z = K + col * cs;
+      float acc = 0.f;
+      for (int i = 0; i < m; ++i) acc = fmaf(K0[l * cs + i], z[i], acc);
+      Y[k * cs + l] = acc * inv[col];
+    }
+    __syncthreads();
+    if (tid < DV) {
+      for (int k = 0; k < rk; ++k) {
+        float acc = 0.f;
+        for (int l = 0; l < m; ++l) acc = fmaf(B[l * ldb + tid], Y[k * cs + l], acc);
+        Elem<TF>::store(Wh + (int64_t)k * DV + tid, acc);
+      }
     }
   }
   if (VAR == SEED_KDA) {
@@ -396,12 +466,15 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
 
 template <int VAR, typename TF, int DV, bool DENSE>
 static cudaError_t launch_compress_t(const CompressArgs &a, cudaStream_t s) {
-  const Smem L(DENSE ? DV : a.m_max, kDK, DV, DENSE);
+  CompressArgs args = a;
+  const int m_alloc = DENSE ? DV : a.m_max;
+  args.cs_alloc = jacobi_cs_alloc(m_alloc, DENSE ? 256 : 128);
+  const Smem L(m_alloc, kDK, DV, DENSE, args.cs_alloc);
   const size_t bytes = (size_t)L.total_floats * sizeof(float);
   auto kern = compress_kernel<VAR, TF, DV, DENSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  kern<<<a.sv.n_heads, DENSE ? 256 : 128, bytes, s>>>(a);
+  kern<<<a.sv.n_heads, DENSE ? 256 : 128, bytes, s>>>(args);
   return cudaGetLastError();
 }
 
@@ -420,14 +493,14 @@ static cudaError_t launch_compress_v(const CompressArgs &a, cudaStream_t s) {
 
 cudaError_t launch_recompress(const StateView &sv, int factor_dtype, float *trunc_err,
                               int32_t *sweeps, int m_max, cudaStream_t s) {
-  CompressArgs a{sv, trunc_err, sweeps, nullptr, m_max};
+  CompressArgs a{sv, trunc_err, sweeps, nullptr, m_max, 0};
   if (factor_dtype == SEED_BF16) return launch_compress_v<__nv_bfloat16, false>(a, s);
   return launch_compress_v<float, false>(a, s);
 }
 
 cudaError_t launch_compress_dense(const StateView &sv, int factor_dtype, const float *S,
                                   float *trunc_err, cudaStream_t s) {
-  CompressArgs a{sv, trunc_err, nullptr, S, sv.d_v};
+  CompressArgs a{sv, trunc_err, nullptr, S, sv.d_v, 0};
   if (factor_dtype == SEED_BF16) return launch_compress_v<__nv_bfloat16, true>(a, s);
   return launch_compress_v<float, true>(a, s);
 }
