@@ -231,8 +231,12 @@ __device__ static int jacobi_svd(float *K, int n, const JacobiGeom &g, float tol
         }
       }
       if (real && al > kNegligible && be > kNegligible && fabsf(ga) > tol * sqrtf(al) * sqrtf(be)) {
-        const float zeta = (be - al) / (2.f * ga);
-        const float t = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(fmaf(zeta, zeta, 1.f)));
+        // Any t gives an exact rotation (c^2 + s^2 = 1 to rounding), so the angle
+        // may use fast reciprocals; |zeta| large (tiny ga) gives t ~ 1/(2 zeta).
+        const float zeta = (be - al) * __frcp_rn(2.f * ga);
+        const float az = fabsf(zeta);
+        const float root = az < 1e18f ? az + fmaf(az, az, 1.f) * rsqrtf(fmaf(az, az, 1.f)) : 2.f * az;
+        const float t = copysignf(__frcp_rn(root), zeta);
         const float c = rsqrtf(fmaf(t, t, 1.f));
         const float s = c * t;
 #pragma unroll
