@@ -90,13 +90,15 @@ __device__ static inline void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// High (part = 0) or low (part = 1) bf16 of the split x = hi + lo.
-__device__ static inline __nv_bfloat16 bf16_part(float x, int part) {
-  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-  return part ? __float2bfloat16_rn(x - __bfloat162float(hi)) : hi;
-}
-__device__ static inline uint32_t pack_bf16(__nv_bfloat16 lo_elem, __nv_bfloat16 hi_elem) {
-  return (uint32_t)__bfloat16_as_ushort(lo_elem) | ((uint32_t)__bfloat16_as_ushort(hi_elem) << 16);
+// Two fp32 values as packed bf16: their high parts (part = 0) or the
+// remainders x - hi (part = 1); element .x goes to the low half.
+__device__ static inline uint32_t split_bf16x2(float2 v, int part) {
+  __nv_bfloat162 hi = __float22bfloat162_rn(v);
+  if (part) {
+    const float2 h = __bfloat1622float2(hi);
+    hi = __float22bfloat162_rn(make_float2(v.x - h.x, v.y - h.y));
+  }
+  return *reinterpret_cast<uint32_t *>(&hi);
 }
 
 template <int VAR, int DV, int MAXC, int NS>
@@ -248,21 +250,22 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
               lo2.x *= l_lo.x; lo2.y *= l_lo.y; hi2.x *= l_hi.x; hi2.y *= l_hi.y;
             }
           }
-          const int part = gq & 1;
-          a0[ks_] = pack_bf16(bf16_part(lo2.x, part), bf16_part(lo2.y, part));
-          a2[ks_] = pack_bf16(bf16_part(hi2.x, part), bf16_part(hi2.y, part));
+          a0[ks_] = split_bf16x2(lo2, gq & 1);
+          a2[ks_] = split_bf16x2(hi2, gq & 1);
         }
       }
       for (int n0 = warp * 8; n0 < m; n0 += NT / 4) {
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};  // two chains of k-steps
       const uint32_t row_addr = u_base + (uint32_t)((n0 + (lane & 7)) * S::USTR + (lane >> 3) * 16);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         uint32_t b[4];
         ldsm_x4(row_addr + kk * 64, b);
         mma_bf16(d, a0[2 * kk], 0u, a2[2 * kk], 0u, b[0], b[1]);
-        mma_bf16(d, a0[2 * kk + 1], 0u, a2[2 * kk + 1], 0u, b[2], b[3]);
+        mma_bf16(e, a0[2 * kk + 1], 0u, a2[2 * kk + 1], 0u, b[2], b[3]);
       }
+      d[0] += e[0];
+      d[1] += e[1];
       // rows 2r and 2r+1 (hi, lo) of the same vector: lane 4g+t and lane 4(g+1)+t
       const float o0 = __shfl_down_sync(0xffffffffu, d[0], 4);
       const float o1 = __shfl_down_sync(0xffffffffu, d[1], 4);
@@ -316,6 +319,14 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
       if ((lane & 3) == 0) scal[warp * 8 + reduce8_index(lane)] = r;
     }
     __syncthreads();  // barrier B: x, the padding and the scalar partials are visible
+    float Sg[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < NSW; ++w) a += scal[w * 8 + j];
+      Sg[j] = a;
+    }
 
     // ---- W pass: row tiles of 16 of W x, round robin over the warps -------------------
     for (int i0 = warp * 16; i0 < DV; i0 += NT / 2) {
@@ -340,14 +351,6 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
     __syncthreads();  // barrier C: W x complete; the stage is no longer read
 
     // ---- update and read-out (registers, scal, wxs only) -------------------------------
-    float Sg[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float a = 0.f;
-#pragma unroll
-      for (int w = 0; w < NSW; ++w) a += scal[w * 8 + j];
-      Sg[j] = a;
-    }
     const float omega = Sg[4] / Sg[5];
     int bad = 0;
     TF *Uo = reinterpret_cast<TF *>(sv.U) + (c0 + m) * DK;
