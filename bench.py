@@ -45,6 +45,8 @@ def parse():
     ap.add_argument('--no-dense', action='store_true')
     ap.add_argument('--no-e2e', action='store_true')
     ap.add_argument('--no-cpu', action='store_true')
+    ap.add_argument('--recompress', default='phases', choices=['phases', 'single'],
+                    help='three-phase recompression over a workspace, or the single kernel')
     return ap.parse_args()
 
 
@@ -235,7 +237,7 @@ def run_gpu(args, w):
     import torch
     import torch.distributed as dist
     from rank_state_compression_head_b300 import accounting as acc
-    from rank_state_compression_head_b300.workload import DeviceRun
+    from rank_state_compression_head_b300.workload import DEFAULT_WS_HEADS, DeviceRun
 
     ws, rank, local = dist_env()
     if ws > 1:
@@ -248,7 +250,10 @@ def run_gpu(args, w):
     total_steps = K + W_
 
     # ---- setup: constants, prefill, compression, inputs of every step -----------------
-    run = DeviceRun(w, device=dev, steps_buffered=total_steps)
+    ws_heads = DEFAULT_WS_HEADS if args.recompress == 'phases' else 0
+    run = DeviceRun(w, device=dev, steps_buffered=total_steps, ws_heads=ws_heads)
+    rec_groups = -(-run.H // min(run.H, ws_heads)) if ws_heads else 1
+    rec_launches = 3 * rec_groups if ws_heads else 1
     S_dense = run.prefill()
     run.compress(S_dense)
     for t in range(total_steps):
@@ -304,8 +309,13 @@ def run_gpu(args, w):
     dec_args = [(st_ref, run.q[W_ + i].data_ptr(), run.k[W_ + i].data_ptr(), run.v[W_ + i].data_ptr(),
                  run.gate[W_ + i].data_ptr(), run.beta[W_ + i].data_ptr(), A_ptr, run.o.data_ptr(), sptr)
                 for i in range(K)]
-    rec_args = (st_ref, run.trunc.data_ptr(), sweeps.data_ptr(), sptr)
-    dec_fn, rec_fn = _lib.seed_decode_step, _lib.seed_recompress_ex
+    if run.ws is not None:
+        rec_fn = _lib.seed_recompress_ws
+        rec_args = (st_ref, run.trunc.data_ptr(), sweeps.data_ptr(), run.ws.data_ptr(), run.ws_bytes, sptr)
+    else:
+        rec_fn = _lib.seed_recompress_ex
+        rec_args = (st_ref, run.trunc.data_ptr(), sweeps.data_ptr(), sptr)
+    dec_fn = _lib.seed_decode_step
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     rec_steps = []
     bytes_decode = 0
@@ -363,7 +373,8 @@ def run_gpu(args, w):
                     traffic=traffic, peak_src=peaks['src'],
                     algorithmic_bytes_per_launch=round(bytes_decode / K),
                     avg_launch_us=round(dec_avg_ms * 1e3, 3))
-    roof_rec = dict(kernel='compress_kernel (recompress)', bound='alu', achieved=rec_tflops and round(rec_tflops, 3),
+    rec_kernels = 'qr_phase + svd_phase + rebuild_phase' if run.ws is not None else 'compress_kernel'
+    roof_rec = dict(kernel=f'{rec_kernels} (recompress)', bound='alu', achieved=rec_tflops and round(rec_tflops, 3),
                     peak=round(fp32_peak, 1), unit='TFLOP/s',
                     frac=rec_tflops and round(rec_tflops / fp32_peak, 4), traffic=None,
                     peak_src='148 SMs x 128 FP32 lanes x 2 FLOP x max SM clock',
@@ -378,7 +389,7 @@ def run_gpu(args, w):
                            T=w.T, factor_dtype=w.factor_dtype, variant=w.variant,
                            l2='flushed before every timed step (256 MiB write then 256 MiB read, untimed)',
                            parallelism=f'heads sharded, {ws} replica(s)'),
-               roofline=dominant, gpu_launches=K + len(rec_ms), clocks=clocks)
+               roofline=dominant, gpu_launches=K + rec_launches * len(rec_ms), clocks=clocks)
     out['decode'] = dict(head_steps_per_s=round(heads_all * K / (dec_total / 1e3)),
                          us_per_step=round(dec_avg_ms * 1e3, 3), gbs=round(dec_gbs, 1),
                          frac_of_measured_hbm=round(dec_gbs / peaks['hbm_gbs'], 4),

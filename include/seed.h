@@ -160,7 +160,8 @@ int seed_decode_step(seed_state *st, const float *q, const float *k, const float
  * error bound: summary, Open-Loop Error Bound (Corollary 4)).
  * A = U_eff, B = W (m columns each); Householder QR A = Q_a R_a, B = Q_b R_b;
  * core K = R_a R_b^T; one-sided Jacobi SVD K = X Sigma Y^T; keep the rank(h)
- * largest: U = Q_a X_r Sigma_r, W = Q_b Y_r; scales (or D) = 1; a unchanged.
+ * largest: U = Q_a X_r, W = Q_b K^T X_r (= Q_b Y_r Sigma_r); scales (or D) = 1;
+ * a unchanged.
  *   trunc_err  [n_heads] sqrt(sum of the discarded sigma^2), or NULL.
  * Sets st->steps_since_compress = 0.  Per-head status 6 if the sweep limit is hit.
  */
@@ -172,6 +173,34 @@ int seed_recompress(seed_state *st, float *trunc_err, seed_stream_t stream);
  * limit was reached).  Used to count the work of a recompression.
  */
 int seed_recompress_ex(seed_state *st, float *trunc_err, int32_t *sweeps, seed_stream_t stream);
+
+/*
+ * seed_recompress_workspace_bytes — size of the device workspace that
+ * seed_recompress_ws needs to recompress `heads` heads per group, at the
+ * state's full capacity (r_max + growth*T columns per head), so that one
+ * allocation serves every call on this state.  Written to *bytes.
+ * Returns a seed_status code (SEED_ERR_INVALID_ARG for heads < 1 or bytes NULL).
+ */
+int seed_recompress_workspace_bytes(const seed_state *st, int32_t heads, int64_t *bytes);
+
+/*
+ * seed_recompress_ws — seed_recompress_ex in three phases that pass their
+ * intermediates through a caller-provided workspace: (1) per head, Householder
+ * QR of U_eff and of W, the core K, the explicit Q_a and Q_b; (2) per head, the
+ * Jacobi SVD of K, ordering and truncation error; (3) per head and factor, the
+ * rebuild.  Each phase holds only its own operands in shared memory, so more
+ * heads are resident per SM than in the single kernel of seed_recompress.
+ * Results (factors, trunc_err, sweeps, status) are bit-identical to
+ * seed_recompress_ex.
+ *   workspace        DEVICE memory owned by the caller, 16-byte aligned
+ *   workspace_bytes  its size; heads are processed in groups of as many as it
+ *                    holds (SEED_ERR_INVALID_ARG if not even one); groups of at
+ *                    least 8 x the SM count keep every SM busy
+ * The workspace may not be used by any other call until this one has finished
+ * on `stream`.  Sets st->steps_since_compress = 0.
+ */
+int seed_recompress_ws(seed_state *st, float *trunc_err, int32_t *sweeps, void *workspace,
+                       int64_t workspace_bytes, seed_stream_t stream);
 
 /*
  * seed_materialize — S = a vbar^T + U_eff W^T for every head (tests, export).

@@ -81,6 +81,8 @@ _PROTOS = {
     'seed_decode_step': (ctypes.c_int, [_sp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     'seed_recompress': (ctypes.c_int, [_sp, _vp, _vp]),
     'seed_recompress_ex': (ctypes.c_int, [_sp, _vp, _vp, _vp]),
+    'seed_recompress_workspace_bytes': (ctypes.c_int, [_sp, _i32, _vp]),
+    'seed_recompress_ws': (ctypes.c_int, [_sp, _vp, _vp, _vp, _i64, _vp]),
     'seed_materialize': (ctypes.c_int, [_sp, _vp, _vp]),
     'seed_dense_decode_step': (ctypes.c_int, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                               _vp, _vp, _vp, _vp, _vp]),
@@ -158,6 +160,20 @@ def seed_recompress(st: seed_state, trunc_err=None, stream=None) -> None:
 def seed_recompress_ex(st: seed_state, trunc_err=None, sweeps=None, stream=None) -> None:
     _check('seed_recompress_ex', _lib.seed_recompress_ex(ctypes.byref(st), _ptr(trunc_err), _ptr(sweeps),
                                                          _stream(stream)))
+
+
+def seed_recompress_workspace_bytes(st: seed_state, heads: int) -> int:
+    out = ctypes.c_int64(0)
+    _check('seed_recompress_workspace_bytes',
+           _lib.seed_recompress_workspace_bytes(ctypes.byref(st), int(heads), ctypes.addressof(out)))
+    return int(out.value)
+
+
+def seed_recompress_ws(st: seed_state, trunc_err=None, sweeps=None, workspace=None, workspace_bytes: int = 0,
+                       stream=None) -> None:
+    _check('seed_recompress_ws',
+           _lib.seed_recompress_ws(ctypes.byref(st), _ptr(trunc_err), _ptr(sweeps), _ptr(workspace),
+                                   int(workspace_bytes), _stream(stream)))
 
 
 def seed_materialize(st: seed_state, S_out, stream=None) -> None:

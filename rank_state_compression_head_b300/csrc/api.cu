@@ -130,6 +130,35 @@ extern "C" int seed_recompress_ex(seed_state *st, float *trunc_err, int32_t *swe
   return c;
 }
 
+extern "C" int seed_recompress_workspace_bytes(const seed_state *st, int32_t heads, int64_t *bytes) {
+  const int c = check_state(st);
+  if (c) return c;
+  if (heads < 1 || !bytes) return SEED_ERR_INVALID_ARG;
+  const int rmax = rmax_of(st);
+  const int m_cap = rmax + growth_of(st->variant) * st->T;
+  *bytes = (int64_t)heads * split_floats_per_head(m_cap, rmax, st->d_v) * (int64_t)sizeof(float);
+  return SEED_OK;
+}
+
+extern "C" int seed_recompress_ws(seed_state *st, float *trunc_err, int32_t *sweeps, void *workspace,
+                                  int64_t workspace_bytes, seed_stream_t stream) {
+  int c = check_state(st);
+  if (c) return c;
+  if (st->steps_since_compress > st->T) return SEED_ERR_CAPACITY;
+  if (st->n_heads == 0) { st->steps_since_compress = 0; return SEED_OK; }
+  if (!workspace || workspace_bytes < 0) return SEED_ERR_INVALID_ARG;
+  if (misaligned(workspace)) return SEED_ERR_ALIGNMENT;
+  const int rmax = rmax_of(st);
+  const int m_max = rmax + growth_of(st->variant) * st->steps_since_compress;
+  const int64_t per_head = split_floats_per_head(m_max, rmax, st->d_v) * (int64_t)sizeof(float);
+  const int64_t chunk = workspace_bytes / per_head;
+  if (chunk < 1) return SEED_ERR_INVALID_ARG;
+  c = cuda_status(launch_recompress_split(view_of(st), st->factor_dtype, trunc_err, sweeps, m_max, rmax,
+                                          static_cast<float *>(workspace), chunk, (cudaStream_t)stream));
+  if (c == SEED_OK) st->steps_since_compress = 0;
+  return c;
+}
+
 extern "C" int seed_recompress(seed_state *st, float *trunc_err, seed_stream_t stream) {
   return seed_recompress_ex(st, trunc_err, nullptr, stream);
 }

@@ -203,6 +203,10 @@ int sm_count();
 cudaError_t launch_decode_mma(const DecodeArgs &a, int cols_max, cudaStream_t s);
 cudaError_t launch_recompress(const StateView &sv, int factor_dtype, float *trunc_err,
                               int32_t *sweeps, int m_max, cudaStream_t s);
+cudaError_t launch_recompress_split(const StateView &sv, int factor_dtype, float *trunc_err,
+                                    int32_t *sweeps, int m_max, int r_max, float *ws,
+                                    int64_t chunk, cudaStream_t s);
+int64_t split_floats_per_head(int m_max, int r_max, int d_v);
 cudaError_t launch_compress_dense(const StateView &sv, int factor_dtype, const float *S,
                                   float *trunc_err, cudaStream_t s);
 cudaError_t launch_materialize(const StateView &sv, int factor_dtype, float *S_out, int m_max,

@@ -1,0 +1,236 @@
+// Device building blocks of the compression kernels: Householder QR of a
+// factor panel, the explicit Q, and the one-sided Jacobi SVD of the core.
+// Used by the single-kernel compression (recompress.cu) and by the
+// three-phase recompression over a workspace (recompress_split.cu), which
+// therefore perform the same arithmetic.
+#pragma once
+
+#include "common.cuh"
+
+#include <float.h>
+
+namespace seedk {
+
+constexpr int kMaxSweeps = 30;
+// After the core is scaled to a largest entry in [1/2, 1), a column whose squared
+// norm is below this is under fp32 resolution of the largest one: rotating it only
+// stirs rounding noise, so it is left alone (its singular value is negligible).
+constexpr float kNegligible = 1e-14f;
+
+// x . y over rows [i0, nrows) of two columns (16-byte aligned column starts,
+// nrows a multiple of 4): scalar head up to a multiple of 4, then float4 body.
+__device__ static inline float col_dot(const float *__restrict__ x, const float *__restrict__ y, int i0,
+                                       int nrows) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  int i = i0;
+  for (; (i & 3) && i < nrows; ++i) s0 = fmaf(x[i], y[i], s0);
+  for (; i < nrows; i += 4) {
+    const float4 a = *reinterpret_cast<const float4 *>(x + i);
+    const float4 b = *reinterpret_cast<const float4 *>(y + i);
+    s0 = fmaf(a.x, b.x, s0); s1 = fmaf(a.y, b.y, s1); s2 = fmaf(a.z, b.z, s2); s3 = fmaf(a.w, b.w, s3);
+  }
+  return (s0 + s1) + (s2 + s3);
+}
+// y[i] -= a x[i] over rows [i0, nrows), same layout rules.
+__device__ static inline void col_axpy(float a, const float *__restrict__ x, float *__restrict__ y, int i0,
+                                       int nrows) {
+  int i = i0;
+  for (; (i & 3) && i < nrows; ++i) y[i] = fmaf(-a, x[i], y[i]);
+  for (; i < nrows; i += 4) {
+    const float4 b = *reinterpret_cast<const float4 *>(x + i);
+    float4 c = *reinterpret_cast<const float4 *>(y + i);
+    c.x = fmaf(-a, b.x, c.x); c.y = fmaf(-a, b.y, c.y); c.z = fmaf(-a, b.z, c.z); c.w = fmaf(-a, b.w, c.w);
+    *reinterpret_cast<float4 *>(y + i) = c;
+  }
+}
+
+// Householder QR in place on a column-major nrows x ncols panel (leading
+// dimension ld, a multiple of 4; nrows a multiple of 4).  On exit the upper
+// triangle holds R; below the diagonal of column j sits the reflector's vector
+// v_j (v_j[j] = 1 implicit), tau[j] its coefficient: H_j = I - tau_j v_j v_j^T,
+// A = H_0 H_1 ... H_{n-1} R.  Each reflector is formed from the column scaled
+// by its largest magnitude, so that columns far below 1 (long products of
+// gates) do not underflow in their squared norm: an inaccurate norm would give
+// a reflector that is not orthogonal, which then corrupts the larger columns
+// it is applied to.  Columns below the smallest normal float are treated as zero.
+// Run by a team of tsize threads (ttid its index) synchronised on named barrier bar.
+__device__ static void householder_qr(float *A, int ld, int nrows, int ncols, float *tau,
+                                      int ttid, int tsize, int bar) {
+  const int lane = ttid & 31;
+  const int nref = ncols < nrows ? ncols : nrows;
+  for (int j = 0; j < nref; ++j) {
+    float *cj = A + j * ld;
+    if (ttid < 32) {
+      float amax = 0.f;
+      for (int i = j + lane; i < nrows; i += 32) amax = fmaxf(amax, fabsf(cj[i]));
+      amax = warp_max(amax);
+      const float alpha = cj[j];
+      float tj = 0.f, beta = alpha;
+      if (amax >= FLT_MIN) {
+        const float inv = 1.f / amax;
+        float ss = 0.f;
+        for (int i = j + 1 + lane; i < nrows; i += 32) {
+          const float x = cj[i] * inv;
+          ss = fmaf(x, x, ss);
+        }
+        ss = warp_sum(ss);
+        if (ss > 0.f) {
+          const float as = alpha * inv;
+          const float nrm = sqrtf(fmaf(as, as, ss));
+          const float bs = as >= 0.f ? -nrm : nrm;
+          tj = (bs - as) / bs;
+          const float sc = 1.f / ((as - bs) * amax);  // v_i = x_i / (alpha - beta), |v_i| <= 1
+          for (int i = j + 1 + lane; i < nrows; i += 32) cj[i] *= sc;
+          beta = bs * amax;
+        }
+      } else {
+        for (int i = j + 1 + lane; i < nrows; i += 32) cj[i] = 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) { cj[j] = beta; tau[j] = tj; }
+    }
+    team_sync(bar, tsize);
+    const float tj = tau[j];
+    if (tj != 0.f) {
+      for (int l = j + 1 + ttid; l < ncols; l += tsize) {
+        float *cl = A + l * ld;
+        const float sv = tj * (cl[j] + col_dot(cj, cl, j + 1, nrows));
+        cl[j] -= sv;
+        col_axpy(sv, cj, cl, j + 1, nrows);
+      }
+    }
+    team_sync(bar, tsize);
+  }
+}
+
+// Overwrite the reflectors with the first ncols columns of Q = H_0 ... H_{n-1}.
+__device__ static void form_q(float *A, int ld, int nrows, int ncols, const float *tau, int ttid,
+                              int tsize, int bar) {
+  for (int j = ncols - 1; j >= 0; --j) {
+    const float *cj = A + j * ld;
+    const float tj = tau[j];
+    if (tj != 0.f) {
+      for (int l = j + 1 + ttid; l < ncols; l += tsize) {
+        float *cl = A + l * ld;  // rows < l of a finished column are zero, so cl[j] == 0
+        const float sv = tj * col_dot(cj, cl, j + 1, nrows);
+        cl[j] = -sv;
+        col_axpy(sv, cj, cl, j + 1, nrows);
+      }
+    }
+    team_sync(bar, tsize);
+    float *cw = A + j * ld;
+    for (int i = ttid; i < nrows; i += tsize) {
+      if (i < j) cw[i] = 0.f;
+      else if (i == j) cw[i] = 1.f - tj;
+      else cw[i] = -tj * cw[i];
+    }
+    team_sync(bar, tsize);
+  }
+}
+
+// Geometry of the core K (n x n) in shared memory for the Jacobi rounds: the
+// threads of a column pair own contiguous chunks of R = ld / tpp rows (R a
+// multiple of 4, rows n..ld-1 are zero), columns are cs = ld + 4 floats apart
+// so that 16-byte accesses of different columns spread over the banks.
+struct JacobiGeom {
+  int tpp, ld, cs;
+};
+__host__ __device__ inline JacobiGeom jacobi_geom(int n, int nthreads) {
+  const int P = (n + 1) / 2 > 0 ? (n + 1) / 2 : 1;
+  const int n4 = (n + 3) & ~3;
+  int tpp = 1;
+  while (tpp * 2 * P <= nthreads && tpp < 32 && 8 * tpp <= n4) tpp *= 2;
+  const int ld = (n + 4 * tpp - 1) / (4 * tpp) * (4 * tpp);
+  return JacobiGeom{tpp, ld, ld + 4};
+}
+__host__ inline int jacobi_cs_alloc(int m_max, int nthreads) {
+  int cs = 4;
+  for (int n = 0; n <= m_max; ++n) {
+    const int c = jacobi_geom(n, nthreads).cs;
+    cs = c > cs ? c : cs;
+  }
+  return cs;
+}
+
+// One-sided (Hestenes) Jacobi on the n columns of K: rotate pairs of columns
+// until every pair is orthogonal, K <- K J, so that the columns of K J are
+// X Sigma.  The rotations J are not kept: the rebuild uses the original core.
+// Round-robin pair order: n' = n rounded up to even seats, seat 0 fixed, the
+// others move one seat each round; pair i joins seats i and n'-1-i.  A pair is
+// rotated when (k_p . k_q)^2 > tol^2 |k_p|^2 |k_q|^2 and both columns are above
+// fp32 resolution of the core (scaled to a largest entry in [1/2, 1)).  Each
+// thread keeps its chunk of both columns in registers through a round.  Whole
+// block of NT threads.  Returns the number of sweeps, or -1 if the sweep limit
+// was reached.
+template <int NT, int RMAX>
+__device__ static int jacobi_svd(float *K, int n, const JacobiGeom &g, float tol) {
+  if (n < 2) return 0;
+  const int tid = threadIdx.x;
+  const int nn = n + (n & 1);
+  const int P = nn / 2;
+  const int tpp = g.tpp, cs = g.cs;
+  const int R = g.ld / tpp, R4 = R / 4;
+  const int pair = tid / tpp, sub = tid % tpp;
+  const bool active = pair < P;
+  const float tol2 = tol * tol;
+  // seat s >= 1 holds column 1 + (s - 1 + round) mod (n' - 1): advance by one per round
+  int p = active ? pair : 0, q = active ? nn - 1 - pair : 0;
+  for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
+    int rotated = 0;
+    for (int round = 0; round < nn - 1; ++round) {
+      const bool real = active && p < n && q < n;
+      float4 xp[RMAX / 4], xq[RMAX / 4];
+      float al = 0.f, be = 0.f, ga = 0.f;
+      float4 *kp = reinterpret_cast<float4 *>(K + p * cs + sub * R);
+      float4 *kq = reinterpret_cast<float4 *>(K + q * cs + sub * R);
+      if (real) {
+#pragma unroll
+        for (int v = 0; v < RMAX / 4; ++v) {
+          if (v < R4) {
+            xp[v] = kp[v];
+            xq[v] = kq[v];
+            al = fmaf(xp[v].x, xp[v].x, fmaf(xp[v].y, xp[v].y, fmaf(xp[v].z, xp[v].z, fmaf(xp[v].w, xp[v].w, al))));
+            be = fmaf(xq[v].x, xq[v].x, fmaf(xq[v].y, xq[v].y, fmaf(xq[v].z, xq[v].z, fmaf(xq[v].w, xq[v].w, be))));
+            ga = fmaf(xp[v].x, xq[v].x, fmaf(xp[v].y, xq[v].y, fmaf(xp[v].z, xq[v].z, fmaf(xp[v].w, xq[v].w, ga))));
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        if (o < tpp) {
+          al += __shfl_xor_sync(0xffffffffu, al, o);
+          be += __shfl_xor_sync(0xffffffffu, be, o);
+          ga += __shfl_xor_sync(0xffffffffu, ga, o);
+        }
+      }
+      if (real && al > kNegligible && be > kNegligible && ga * ga > tol2 * al * be) {
+        // Any t gives an exact rotation (c^2 + s^2 = 1 to rounding), so the angle
+        // may use fast reciprocals; |zeta| large (tiny ga) gives t ~ 1/(2 zeta).
+        const float zeta = (be - al) * __frcp_rn(2.f * ga);
+        const float az = fabsf(zeta);
+        const float root = az < 1e18f ? az + fmaf(az, az, 1.f) * rsqrtf(fmaf(az, az, 1.f)) : 2.f * az;
+        const float t = copysignf(__frcp_rn(root), zeta);
+        const float c = rsqrtf(fmaf(t, t, 1.f));
+        const float s = c * t;
+#pragma unroll
+        for (int v = 0; v < RMAX / 4; ++v) {
+          if (v < R4) {
+            const float4 a = xp[v], b = xq[v];
+            kp[v] = make_float4(fmaf(c, a.x, -s * b.x), fmaf(c, a.y, -s * b.y), fmaf(c, a.z, -s * b.z),
+                                fmaf(c, a.w, -s * b.w));
+            kq[v] = make_float4(fmaf(s, a.x, c * b.x), fmaf(s, a.y, c * b.y), fmaf(s, a.z, c * b.z),
+                                fmaf(s, a.w, c * b.w));
+          }
+        }
+        rotated = 1;
+      }
+      if (p != 0) p = p == nn - 1 ? 1 : p + 1;
+      q = q == nn - 1 ? 1 : q + 1;
+      __syncthreads();
+    }
+    if (!__syncthreads_or(rotated)) return sweep + 1;
+  }
+  return -1;
+}
+
+}  // namespace seedk

@@ -1,0 +1,292 @@
+// Recompression in three phases over a caller-provided device workspace.
+//
+// Same arithmetic, in the same order, as the single-kernel recompression in
+// recompress.cu ("Shallow Encoding Emits Deep Memories", thelatestinai.com list
+// view, Table 1: the decode compresses back to rank R every W steps), so both
+// give bit-identical factors.  Splitting it lets each phase hold only what it
+// needs in shared memory: the Jacobi rounds (the longest, latency-bound phase)
+// then run with about three times as many heads resident per SM.
+//
+//   qr_phase      one CTA of 128 threads per head: Householder QR of U_eff and
+//                 of W in two 64-thread teams, core K = R_a R_b^T, explicit Q_a
+//                 and Q_b; writes K, Q_a, Q_b to the workspace
+//   svd_phase     one CTA of 128 threads per head: one-sided Jacobi on the core,
+//                 ordering, truncation error; writes the kept columns Z of K J
+//                 (unnormalised) with their 1/sigma, and Y = K^T X_r
+//   rebuild_phase one CTA per (head, factor): U = Q_a Z diag(1/sigma), W = Q_b Y;
+//                 resets the lazy scales
+//
+// Workspace per head (fp32, column-major panels): Q_a [m][d_k], Q_b [m][d_v],
+// K [m][m], Z [r][m], Y [r][m], 1/sigma [r], rounded up to 256 bytes, with m the
+// largest column count of any head at this call and r the largest rank.
+#include "recompress_core.cuh"
+
+namespace seedk {
+
+struct SplitLayout {
+  int64_t qa, qb, k, z, y, zinv, per_head;  // offsets and stride in floats
+  __host__ __device__ SplitLayout(int m, int r, int dk, int dv) {
+    qa = 0;
+    qb = qa + (int64_t)m * dk;
+    k = qb + (int64_t)m * dv;
+    z = k + (int64_t)m * m;
+    y = z + (int64_t)r * m;
+    zinv = y + (int64_t)r * m;
+    per_head = (zinv + r + 63) & ~(int64_t)63;
+    if (per_head == 0) per_head = 64;  // no columns: keep a nonzero stride
+  }
+};
+
+struct SplitArgs {
+  StateView sv;
+  float *ws;
+  int head0;     // first head of this chunk; workspace slot b serves head head0 + b
+  int m_max, r_max;
+  float *trunc_err;
+  int32_t *sweeps;
+  int cs_alloc;
+};
+
+constexpr int kSplitThreads = 128;
+
+__device__ inline bool split_head_ok(const StateView &sv, int h, int m_max, int &r, int &m) {
+  r = sv.rank_of(h);
+  m = r + sv.growth * sv.steps;
+  return r >= 0 && m <= m_max;
+}
+
+// ---- phase 1: QR of both factors, core, explicit Q --------------------------------------
+template <int VAR, typename TF, int DV>
+__global__ void __launch_bounds__(kSplitThreads) qr_phase(const SplitArgs p) {
+  constexpr int DK = kDK;
+  extern __shared__ __align__(16) float smem[];
+  const int h = p.head0 + blockIdx.x;
+  const int tid = threadIdx.x;
+  const StateView &sv = p.sv;
+  int r, m;
+  if (!split_head_ok(sv, h, p.m_max, r, m)) return;  // reported by the SVD phase
+  constexpr int lda = DK + 4, ldb = DV + 4;
+  float *A = smem;
+  float *B = A + ((p.m_max * lda + 3) & ~3);
+  float *tauA = B + ((p.m_max * ldb + 3) & ~3);
+  float *tauB = tauA + ((p.m_max + 3) & ~3);
+  const int64_t c0 = sv.col0(h);
+  const TF *Uh = reinterpret_cast<const TF *>(sv.U) + c0 * DK;
+  const TF *Wh = reinterpret_cast<const TF *>(sv.W) + c0 * DV;
+  for (int idx = tid; idx < m * DK; idx += kSplitThreads) {
+    const int j = idx / DK, i = idx % DK;
+    const float u = Elem<TF>::load(Uh + idx);
+    const float f = VAR == SEED_KDA ? sv.scale[(int64_t)h * DK + i] : sv.scale[c0 + j];
+    A[j * lda + i] = u * f;
+  }
+  for (int idx = tid; idx < m * DV; idx += kSplitThreads) {
+    const int j = idx / DV, i = idx % DV;
+    B[j * ldb + i] = Elem<TF>::load(Wh + idx);
+  }
+  __syncthreads();
+  const int team = tid / 64, ttid = tid % 64;
+  if (team == 0) householder_qr(A, lda, DK, m, tauA, ttid, 64, 1);
+  else householder_qr(B, ldb, DV, m, tauB, ttid, 64, 2);
+  __syncthreads();
+
+  const SplitLayout L(p.m_max, p.r_max, DK, DV);
+  float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
+  float *Kw = ws + L.k;
+  for (int idx = tid; idx < m * m; idx += kSplitThreads) {
+    const int j = idx / m, i = idx % m;  // K[j][i]: column j, row i
+    float acc = 0.f;
+    for (int l = max(i, j); l < m; ++l) acc = fmaf(A[l * lda + i], B[l * ldb + j], acc);
+    Kw[idx] = acc;
+  }
+  __syncthreads();
+  if (team == 0) form_q(A, lda, DK, m, tauA, ttid, 64, 1);
+  else form_q(B, ldb, DV, m, tauB, ttid, 64, 2);
+  __syncthreads();
+  float *Qa = ws + L.qa, *Qb = ws + L.qb;
+  for (int idx = tid; idx < m * DK; idx += kSplitThreads) Qa[idx] = A[(idx / DK) * lda + idx % DK];
+  for (int idx = tid; idx < m * DV; idx += kSplitThreads) Qb[idx] = B[(idx / DV) * ldb + idx % DV];
+}
+
+// ---- phase 2: SVD of the core ------------------------------------------------------------
+template <typename TF, int DV>
+__global__ void __launch_bounds__(kSplitThreads) svd_phase(const SplitArgs p) {
+  constexpr int DK = kDK;
+  constexpr int NT = kSplitThreads;
+  extern __shared__ __align__(16) float smem[];
+  const int h = p.head0 + blockIdx.x;
+  const int tid = threadIdx.x;
+  const StateView &sv = p.sv;
+  int r, m;
+  if (!split_head_ok(sv, h, p.m_max, r, m)) {  // rank table disagrees with r_max: touch nothing
+    if (tid == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
+    return;
+  }
+  const SplitLayout L(p.m_max, p.r_max, DK, DV);
+  float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
+  const JacobiGeom jg = jacobi_geom(m, NT);
+  const int cs = jg.cs, ldr = jg.ld;
+  const int up = (p.m_max + 3) & ~3;
+  float *K = smem;
+  float *K0 = K + p.m_max * p.cs_alloc;
+  float *sig2 = K0 + p.m_max * p.cs_alloc;
+  float *inv = sig2 + up;
+  int *order = reinterpret_cast<int *>(inv + up);
+  float *red = reinterpret_cast<float *>(order + up);
+
+  // core, rows padded with zeros to ld; K0 keeps a copy
+  const float *Kw = ws + L.k;
+  float kmax = 0.f;
+  for (int idx = tid; idx < m * ldr; idx += NT) {
+    const int j = idx / ldr, i = idx % ldr;
+    const float x = i < m ? Kw[j * m + i] : 0.f;
+    K[j * cs + i] = x;
+    K0[j * cs + i] = x;
+    kmax = fmaxf(kmax, fabsf(x));
+  }
+  // scale by a power of two to a largest entry in [1/2, 1)
+  kmax = warp_max(kmax);
+  if ((tid & 31) == 0) red[tid >> 5] = kmax;
+  __syncthreads();
+  kmax = 0.f;
+  for (int w = 0; w < NT / 32; ++w) kmax = fmaxf(kmax, red[w]);
+  int kexp = 0;
+  if (kmax > 0.f) frexpf(kmax, &kexp);
+  const float kscale = ldexpf(1.f, -kexp), kunscale = ldexpf(1.f, kexp);
+  for (int idx = tid; idx < m * ldr; idx += NT) K[(idx / ldr) * cs + idx % ldr] *= kscale;
+  __syncthreads();
+  const float tol = sizeof(TF) == 2 ? 1e-5f : (float)(m > 16 ? m : 16) * FLT_EPSILON;
+  const int sweeps = jacobi_svd<NT, 16>(K, m, jg, tol);
+
+  for (int j = tid; j < m; j += NT) {
+    float acc = 0.f;
+    for (int i = 0; i < m; ++i) acc = fmaf(K[j * cs + i], K[j * cs + i], acc);
+    sig2[j] = acc;
+    inv[j] = acc > kNegligible ? rsqrtf(acc) : 0.f;
+  }
+  __syncthreads();
+  for (int j = tid; j < m; j += NT) {
+    int rank = 0;
+    const float sj = sig2[j];
+    for (int i = 0; i < m; ++i) {
+      const float si = sig2[i];
+      rank += (si > sj) || (si == sj && i < j);
+    }
+    order[rank] = j;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float e = 0.f;
+    for (int k = r; k < m; ++k) e += sig2[order[k]];
+    if (p.trunc_err) p.trunc_err[h] = sqrtf(e) * kunscale;
+    if (p.sweeps) p.sweeps[h] = sweeps;
+    if (sv.status) sv.status[h] = sweeps < 0 ? SEED_ERR_NOT_CONVERGED : SEED_OK;
+  }
+  // kept columns z_k = (K J)_{order[k]}, 1/sigma_k, and Y[k] = K0^T z_k / sigma_k
+  const int rk = r < m ? r : m;
+  float *Z = ws + L.z, *Y = ws + L.y, *Zinv = ws + L.zinv;
+  for (int idx = tid; idx < rk * m; idx += NT) {
+    const int k = idx / m, l = idx % m;
+    const int col = order[k];
+    const float *z = K + col * cs;
+    float acc = 0.f;
+    for (int i = 0; i < m; ++i) acc = fmaf(K0[l * cs + i], z[i], acc);
+    Y[idx] = acc * inv[col];
+    Z[idx] = z[l];
+  }
+  for (int k = tid; k < rk; k += NT) Zinv[k] = inv[order[k]];
+}
+
+// ---- phase 3: rebuild the factors ---------------------------------------------------------
+template <int VAR, typename TF, int DV>
+__global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p) {
+  constexpr int DK = kDK;
+  extern __shared__ __align__(16) float smem[];
+  const int h = p.head0 + blockIdx.x;
+  const int panel = blockIdx.y;  // 0: U from Q_a and Z, 1: W from Q_b and Y
+  const int tid = threadIdx.x;
+  const StateView &sv = p.sv;
+  int r, m;
+  if (!split_head_ok(sv, h, p.m_max, r, m)) return;
+  const SplitLayout L(p.m_max, p.r_max, DK, DV);
+  const float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
+  const int rows = panel == 0 ? DK : DV;
+  const int rk = r < m ? r : m;
+  float *zs = smem;  // [rk][m]
+  const float *src = ws + (panel == 0 ? L.z : L.y);
+  for (int idx = tid; idx < rk * m; idx += kSplitThreads) zs[idx] = src[idx];
+  __syncthreads();
+  const int64_t c0 = sv.col0(h);
+  if (tid < rows) {
+    const float *Q = ws + (panel == 0 ? L.qa : L.qb);
+    float q[kMaxCols];
+#pragma unroll
+    for (int l = 0; l < kMaxCols; ++l) q[l] = l < m ? Q[l * rows + tid] : 0.f;
+    TF *out = reinterpret_cast<TF *>(panel == 0 ? sv.U : sv.W) + c0 * rows;
+    const float *zinv = ws + L.zinv;
+    for (int k = 0; k < rk; ++k) {
+      const float *z = zs + k * m;
+      float acc = 0.f;
+#pragma unroll
+      for (int l = 0; l < kMaxCols; ++l)
+        if (l < m) acc = fmaf(q[l], z[l], acc);
+      Elem<TF>::store(out + (int64_t)k * rows + tid, panel == 0 ? acc * zinv[k] : acc);
+    }
+  }
+  if (panel == 0) {
+    if (VAR == SEED_KDA) {
+      for (int i = tid; i < DK; i += kSplitThreads) sv.scale[(int64_t)h * DK + i] = 1.f;
+    } else {
+      for (int k = tid; k < rk; k += kSplitThreads) sv.scale[c0 + k] = 1.f;
+    }
+  }
+}
+
+int64_t split_floats_per_head(int m_max, int r_max, int d_v) {
+  return SplitLayout(m_max, r_max, kDK, d_v).per_head;
+}
+
+template <int VAR, typename TF, int DV>
+static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaStream_t s) {
+  const int up = (a.m_max + 3) & ~3;
+  const int qr_bytes = (((a.m_max * (kDK + 4) + 3) & ~3) + ((a.m_max * (DV + 4) + 3) & ~3) + 2 * up) * 4;
+  a.cs_alloc = jacobi_cs_alloc(a.m_max, kSplitThreads);
+  const int svd_bytes = (2 * a.m_max * a.cs_alloc + 3 * up + 8) * 4;
+  const int rb_bytes = (a.r_max * a.m_max > 0 ? a.r_max * a.m_max : 1) * 4;
+  auto k1 = qr_phase<VAR, TF, DV>;
+  auto k2 = svd_phase<TF, DV>;
+  auto k3 = rebuild_phase<VAR, TF, DV>;
+  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, qr_bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, svd_bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, rb_bytes);
+  if (e != cudaSuccess) return e;
+  for (int64_t h0 = 0; h0 < n_heads; h0 += chunk) {
+    const int n = (int)(n_heads - h0 < chunk ? n_heads - h0 : chunk);
+    a.head0 = (int)h0;
+    k1<<<n, kSplitThreads, qr_bytes, s>>>(a);
+    k2<<<n, kSplitThreads, svd_bytes, s>>>(a);
+    k3<<<dim3(n, 2), kSplitThreads, rb_bytes, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <typename TF, int DV>
+static cudaError_t launch_split_v(const SplitArgs &a, int n, int64_t chunk, cudaStream_t s) {
+  // Only the scale layout differs between variants here.
+  if (a.sv.variant == SEED_KDA) return launch_split_t<SEED_KDA, TF, DV>(a, n, chunk, s);
+  return launch_split_t<SEED_GDN, TF, DV>(a, n, chunk, s);
+}
+
+cudaError_t launch_recompress_split(const StateView &sv, int factor_dtype, float *trunc_err,
+                                    int32_t *sweeps, int m_max, int r_max, float *ws,
+                                    int64_t chunk, cudaStream_t s) {
+  SplitArgs a{sv, ws, 0, m_max, r_max, trunc_err, sweeps, 0};
+  const int n = sv.n_heads;
+  if (factor_dtype == SEED_BF16)
+    return sv.d_v == 64 ? launch_split_v<__nv_bfloat16, 64>(a, n, chunk, s)
+                        : launch_split_v<__nv_bfloat16, 128>(a, n, chunk, s);
+  return sv.d_v == 64 ? launch_split_v<float, 64>(a, n, chunk, s) : launch_split_v<float, 128>(a, n, chunk, s);
+}
+
+}  // namespace seedk

@@ -12,16 +12,24 @@ from typing import Optional
 import torch
 
 from . import (SEED_MAMBA2, VARIANTS, seed_compress_dense, seed_decode_step, seed_dense_decode_step,
-               seed_recompress, seed_synth_constants, seed_synth_dense_prefill, seed_synth_step_inputs)
+               seed_recompress_ex, seed_recompress_workspace_bytes, seed_recompress_ws, seed_synth_constants,
+               seed_synth_dense_prefill, seed_synth_step_inputs)
 from .state import FactoredStateBuffers, synth_workload_struct
 
 PHASE_DECODE = 2
 
 
-class DeviceRun:
-    """Buffers and calls for one workload ``w`` (a ``synth.Workload``-like object)."""
+# Heads per recompression group: enough to keep every SM busy, a few GB of workspace.
+DEFAULT_WS_HEADS = 65536
 
-    def __init__(self, w, device='cuda', steps_buffered: int = 1):
+
+class DeviceRun:
+    """Buffers and calls for one workload ``w`` (a ``synth.Workload``-like object).
+
+    ``ws_heads`` > 0 recompresses through the three-phase path with a workspace
+    for that many heads per group; 0 uses the single-kernel recompression."""
+
+    def __init__(self, w, device='cuda', steps_buffered: int = 1, ws_heads: int = DEFAULT_WS_HEADS):
         self.w = w
         self.dev = torch.device(device)
         self.wst = synth_workload_struct(w)
@@ -50,6 +58,10 @@ class DeviceRun:
         self.o = torch.empty(H, dv, **f32)
         self.trunc = torch.zeros(max(H, 1), **f32)
         self.nb = nb
+        self.ws, self.ws_bytes = None, 0
+        if ws_heads > 0 and H > 0:
+            self.ws_bytes = seed_recompress_workspace_bytes(self.state.st, min(H, ws_heads))
+            self.ws = torch.empty(self.ws_bytes, device=self.dev, dtype=torch.uint8)
 
     # -- setup ------------------------------------------------------------------
     def prefill(self, head0: int = 0, n: Optional[int] = None, out: Optional[torch.Tensor] = None):
@@ -73,8 +85,11 @@ class DeviceRun:
         seed_decode_step(self.state.st, self.q[slot], self.k[slot], self.v[slot], self.gate[slot],
                          self.beta[slot], self.A, self.o, stream)
 
-    def recompress(self, trunc_err: Optional[torch.Tensor] = None, stream=None):
-        seed_recompress(self.state.st, trunc_err, stream)
+    def recompress(self, trunc_err: Optional[torch.Tensor] = None, stream=None, sweeps=None):
+        if self.ws is not None:
+            seed_recompress_ws(self.state.st, trunc_err, sweeps, self.ws, self.ws_bytes, stream)
+        else:
+            seed_recompress_ex(self.state.st, trunc_err, sweeps, stream)
 
     def step(self, t: int, slot: int = 0, stream=None) -> bool:
         """Decode step t (1-based) with inputs already in ``slot``; recompress when T divides t."""

@@ -137,3 +137,40 @@ def test_synth_calls_reject_on_host():
     assert R._lib.seed_synth_step_inputs(ctypes.byref(w), 2, 0, 0, 4, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == R.SEED_ERR_INVALID_ARG
     assert R._lib.seed_synth_dense_prefill(ctypes.byref(w), 0, 0, None, None, None, None, None, None) == R.SEED_OK
     assert R._lib.seed_synth_raw(0, 0, 0, 0, 0, 4, 4, FAKE + 4, None) == R.SEED_ERR_ALIGNMENT
+
+
+def _ws_floats(m, r, dk, dv):
+    n = m * dk + m * dv + m * m + 2 * r * m + r
+    n = (n + 63) // 64 * 64
+    return max(n, 64)
+
+
+def test_recompress_workspace_bytes():
+    st = make_state()                                   # gdn, r = 32, T = 16, d_v = 128
+    assert R.seed_recompress_workspace_bytes(st, 1) == 4 * _ws_floats(48, 32, 128, 128)
+    assert R.seed_recompress_workspace_bytes(st, 1000) == 1000 * 4 * _ws_floats(48, 32, 128, 128)
+    kda = make_state(variant=R.SEED_KDA, r=16, r_max=16, T=8)
+    assert R.seed_recompress_workspace_bytes(kda, 3) == 3 * 4 * _ws_floats(32, 16, 128, 128)
+    m2 = make_state(variant=R.SEED_MAMBA2, d_v=64, r=16, r_max=16)
+    assert R.seed_recompress_workspace_bytes(m2, 2) == 2 * 4 * _ws_floats(32, 16, 128, 64)
+    out = ctypes.c_int64(0)
+    f = R._lib.seed_recompress_workspace_bytes
+    assert f(ctypes.byref(st), 0, ctypes.addressof(out)) == R.SEED_ERR_INVALID_ARG
+    assert f(ctypes.byref(st), 4, None) == R.SEED_ERR_INVALID_ARG
+    assert f(ctypes.byref(make_state(d_k=64)), 4, ctypes.addressof(out)) == R.SEED_ERR_UNSUPPORTED_SHAPE
+
+
+def test_recompress_ws_rejects_on_host():
+    f = R._lib.seed_recompress_ws
+    st = make_state(steps_since_compress=16)
+    one_head = 4 * _ws_floats(48, 32, 128, 128)
+    assert f(ctypes.byref(st), None, None, None, one_head, None) == R.SEED_ERR_INVALID_ARG
+    assert f(ctypes.byref(st), None, None, FAKE + 4, one_head, None) == R.SEED_ERR_ALIGNMENT
+    assert f(ctypes.byref(st), None, None, FAKE, one_head - 4, None) == R.SEED_ERR_INVALID_ARG
+    assert f(ctypes.byref(st), None, None, FAKE, -1, None) == R.SEED_ERR_INVALID_ARG
+    st.steps_since_compress = 17
+    assert f(ctypes.byref(st), None, None, FAKE, one_head, None) == R.SEED_ERR_CAPACITY
+    assert st.steps_since_compress == 17
+    empty = make_state(n_heads=0, a=None, U=None, W=None, scale=None, vbar=None, steps_since_compress=5)
+    assert f(ctypes.byref(empty), None, None, None, 0, None) == R.SEED_OK
+    assert empty.steps_since_compress == 0
