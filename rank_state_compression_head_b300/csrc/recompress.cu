@@ -9,16 +9,15 @@
 // recompress (one CTA of 128 threads per head):
 //   A = U_eff, B = W (fp32 in shared memory, column-major, padded columns)
 //   Householder QR of A and of B, concurrently in two 64-thread teams
-//   K = R_a R_b^T (m x m)
-//   one-sided Jacobi SVD of K: rotate pairs of columns of K until every pair
-//     is orthogonal; then K J = X Sigma, K = X Sigma J^T
-//   order columns by |K_j| (= sigma_j), keep the rank(h) largest
-//   Q_a, Q_b formed in place from the reflectors
-//   U_new = Q_a X_r,  W_new = Q_b K^T X_r = Q_b Y_r Sigma_r   (X_r: normalised
-//   kept columns of K J; the singular values go with W, and K^T X_r is the
-//   projection of the core onto the kept directions, so no rotation is kept)
-// compress_dense (one CTA of 256 threads per head): the same with A = C and
-// B = I (so K = R_a and W_new = R_a^T X_r).
+//   core K = R_a R_b^T (m x m); Q_a, Q_b formed in place from the reflectors
+//   K P = Q R (pivoted QR), one-sided Jacobi on R^T: R^T J = V Sigma
+//   keep the rank(h) largest sigma; y_k = P v_k (right singular vectors of K)
+//   U_new = Q_a K y_k (= sigma_k Q_a x_k),  W_new = Q_b y_k
+//   (no rotation is kept: the kept directions are read off R^T J and applied
+//   to the original core)
+// compress_dense (one CTA of 256 threads per head): A = C and B = I, so
+// K = R_a; plain one-sided Jacobi on K: K J = X Sigma, U_new = Q_a X_r,
+// W_new = R_a^T X_r.
 //
 // The arithmetic is fp32 FMA: the QR and Jacobi steps are sequences of small
 // dependent reductions that do not map onto tensor-core tiles.
@@ -35,23 +34,19 @@ struct CompressArgs {
   int cs_alloc;     // column stride of the core buffers in the allocation
 };
 
-// Dynamic shared-memory layout of the compression kernels (offsets in floats,
-// multiples of 4).
-struct Smem {
-  int lda, ldb;
-  int offA, offB, offK, offK0, offTa, offTb, offS, offI, offO, offR;
+// Dynamic shared-memory layout of compress_dense (offsets in floats, multiples of 4).
+struct DenseSmem {
+  int lda;
+  int offA, offK, offK0, offTa, offS, offI, offO, offR;
   int total_floats;
-  __host__ __device__ Smem(int m, int dk, int dv, bool dense, int cs) {
+  __host__ __device__ DenseSmem(int m, int dk, int cs) {
     lda = dk + 4;  // 16-byte aligned columns, 4 banks apart
-    ldb = dv + 4;
     auto up4 = [](int x) { return (x + 3) & ~3; };
     offA = 0;
-    offB = up4(offA + m * lda);
-    offK = up4(offB + (dense ? 0 : m * ldb));
+    offK = up4(offA + m * lda);
     offK0 = up4(offK + m * cs);
     offTa = up4(offK0 + m * cs);
-    offTb = offTa + up4(m);
-    offS = offTb + up4(m);
+    offS = offTa + up4(m);
     offI = offS + up4(m);
     offO = offI + up4(m);
     offR = offO + up4(m);     // 8 floats of reduction scratch
@@ -59,100 +54,62 @@ struct Smem {
   }
 };
 
-template <int VAR, typename TF, int DV, bool DENSE>
-__global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const CompressArgs p) {
+template <int VAR, typename TF, int DV>
+__global__ void __launch_bounds__(256) compress_dense_kernel(const CompressArgs p) {
   constexpr int DK = kDK;
-  constexpr int NT = DENSE ? 256 : 128;
-  constexpr int RMAX = DENSE ? 32 : 16;
+  constexpr int NT = 256;
   extern __shared__ __align__(16) float smem[];
   const int h = blockIdx.x;
   const int tid = threadIdx.x;
   const StateView &sv = p.sv;
   const int r = sv.rank_of(h);
-  const int m = DENSE ? DV : r + sv.growth * sv.steps;
-  if (r < 0 || (!DENSE && m > p.m_max)) {  // rank table disagrees with r_max: touch nothing
+  const int m = DV;
+  if (r < 0) {  // rank table disagrees with r_max: touch nothing
     if (tid == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
     return;
   }
   const int64_t c0 = sv.col0(h);
-  const Smem L(DENSE ? DV : p.m_max, DK, DV, DENSE, p.cs_alloc);
+  const DenseSmem L(DV, DK, p.cs_alloc);
   const JacobiGeom jg = jacobi_geom(m, NT);
   const int cs = jg.cs, ldr = jg.ld;
-  float *A = smem + L.offA, *B = smem + L.offB, *K = smem + L.offK, *K0 = smem + L.offK0;
-  float *tauA = smem + L.offTa, *tauB = smem + L.offTb, *sig2 = smem + L.offS, *inv = smem + L.offI;
+  float *A = smem + L.offA, *K = smem + L.offK, *K0 = smem + L.offK0;
+  float *tauA = smem + L.offTa, *sig2 = smem + L.offS, *inv = smem + L.offI;
   int *order = reinterpret_cast<int *>(smem + L.offO);
   float *red = smem + L.offR;
-  const int lda = L.lda, ldb = L.ldb;
+  const int lda = L.lda;
   TF *Uh = reinterpret_cast<TF *>(sv.U) + c0 * DK;
   TF *Wh = reinterpret_cast<TF *>(sv.W) + c0 * DV;
 
-  // ---- load -------------------------------------------------------------------
-  if (DENSE) {
-    // A[j][i] = S[i][j]; then a = S vbar / |vbar|^2 and C = S - a vbar^T in place
-    const float *Sh = p.S + (int64_t)h * DK * DV;
-    for (int idx = tid; idx < DK * DV; idx += NT) {
-      const int i = idx / DV, j = idx % DV;
-      A[j * lda + i] = Sh[idx];
-    }
-    __syncthreads();
-    const float *vb = sv.vbar + (int64_t)sv.dir_of(h) * DV;
-    float vv = 0.f;
-    for (int j = 0; j < DV; ++j) vv = fmaf(vb[j], vb[j], vv);
-    if (tid < DK) {
-      float acc = 0.f;
-      for (int j = 0; j < DV; ++j) acc = fmaf(A[j * lda + tid], vb[j], acc);
-      const float ai = acc / vv;
-      sv.a[(int64_t)h * DK + tid] = ai;
-      for (int j = 0; j < DV; ++j) A[j * lda + tid] = fmaf(-ai, vb[j], A[j * lda + tid]);
-    }
-  } else {
-    for (int idx = tid; idx < m * DK; idx += NT) {
-      const int j = idx / DK, i = idx % DK;
-      const float u = Elem<TF>::load(Uh + idx);
-      const float f = VAR == SEED_KDA ? sv.scale[(int64_t)h * DK + i] : sv.scale[c0 + j];
-      A[j * lda + i] = u * f;
-    }
-    for (int idx = tid; idx < m * DV; idx += NT) {
-      const int j = idx / DV, i = idx % DV;
-      B[j * ldb + i] = Elem<TF>::load(Wh + idx);
-    }
+  // ---- A[j][i] = S[i][j]; then a = S vbar / |vbar|^2 and C = S - a vbar^T in place -------
+  const float *Sh = p.S + (int64_t)h * DK * DV;
+  for (int idx = tid; idx < DK * DV; idx += NT) {
+    const int i = idx / DV, j = idx % DV;
+    A[j * lda + i] = Sh[idx];
+  }
+  __syncthreads();
+  const float *vb = sv.vbar + (int64_t)sv.dir_of(h) * DV;
+  float vv = 0.f;
+  for (int j = 0; j < DV; ++j) vv = fmaf(vb[j], vb[j], vv);
+  if (tid < DK) {
+    float acc = 0.f;
+    for (int j = 0; j < DV; ++j) acc = fmaf(A[j * lda + tid], vb[j], acc);
+    const float ai = acc / vv;
+    sv.a[(int64_t)h * DK + tid] = ai;
+    for (int j = 0; j < DV; ++j) A[j * lda + tid] = fmaf(-ai, vb[j], A[j * lda + tid]);
   }
   __syncthreads();
 
-  // ---- QR ---------------------------------------------------------------------
-  if (DENSE) {
-    householder_qr(A, lda, DK, m, tauA, tid, NT, 1);
-  } else {
-    const int team = tid / 64, ttid = tid % 64;
-    if (team == 0) householder_qr(A, lda, DK, m, tauA, ttid, 64, 1);
-    else householder_qr(B, ldb, DV, m, tauB, ttid, 64, 2);
-  }
+  // ---- QR of C; K = R_a (rows padded with zeros to ld), K0 keeps a copy -------------------
+  householder_qr(A, lda, DK, m, tauA, tid, NT, 1);
   __syncthreads();
-
-  // ---- core K = R_a R_b^T (or R_a), rows padded with zeros to ld; K0 keeps a copy --------
   for (int idx = tid; idx < m * ldr; idx += NT) {
     const int j = idx / ldr, i = idx % ldr;  // K[j][i]: column j, row i
-    float acc = 0.f;
-    if (i < m) {
-      if (DENSE) {
-        acc = i <= j ? A[j * lda + i] : 0.f;
-      } else {
-        for (int l = max(i, j); l < m; ++l) acc = fmaf(A[l * lda + i], B[l * ldb + j], acc);
-      }
-    }
-    K[j * cs + i] = acc;
-    K0[j * cs + i] = acc;
+    const float x = (i < m && i <= j) ? A[j * lda + i] : 0.f;
+    K[j * cs + i] = x;
+    K0[j * cs + i] = x;
   }
   __syncthreads();
-
-  // ---- Q factors in place -----------------------------------------------------------
-  if (DENSE) {
-    form_q(A, lda, DK, m, tauA, tid, NT, 1);
-  } else {
-    const int team = tid / 64, ttid = tid % 64;
-    if (team == 0) form_q(A, lda, DK, m, tauA, ttid, 64, 1);
-    else form_q(B, ldb, DV, m, tauB, ttid, 64, 2);
-  }
+  form_q(A, lda, DK, m, tauA, tid, NT, 1);
 
   // ---- SVD of the core, scaled by a power of two to a largest entry in [1/2, 1) ----------
   float kmax = 0.f;
@@ -167,8 +124,8 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
   const float kscale = ldexpf(1.f, -kexp), kunscale = ldexpf(1.f, kexp);
   for (int idx = tid; idx < m * ldr; idx += NT) K[(idx / ldr) * cs + idx % ldr] *= kscale;
   __syncthreads();
-  const float tol = sizeof(TF) == 2 ? 1e-5f : (float)(m > 16 ? m : 16) * FLT_EPSILON;
-  const int sweeps = jacobi_svd<NT, RMAX>(K, m, jg, tol);
+  const float tol = sizeof(TF) == 2 ? 1e-5f : (float)m * FLT_EPSILON;
+  const int sweeps = jacobi_svd<NT, 32>(K, m, jg, tol);
 
   // ---- order by sigma, truncation error -----------------------------------------------
   for (int j = tid; j < m; j += NT) {
@@ -192,11 +149,10 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
     float e = 0.f;
     for (int k = r; k < m; ++k) e += sig2[order[k]];
     if (p.trunc_err) p.trunc_err[h] = sqrtf(e) * kunscale;
-    if (p.sweeps) p.sweeps[h] = sweeps;
     if (sv.status) sv.status[h] = sweeps < 0 ? SEED_ERR_NOT_CONVERGED : SEED_OK;
   }
 
-  // ---- rebuild the kept columns: U = Q_a X_r,  W = Q_b K0^T X_r ----------------------------
+  // ---- U = Q_a X_r,  W = R_a^T X_r ------------------------------------------------------------
   const int rk = r < m ? r : m;
   if (tid < DK) {
     for (int k = 0; k < rk; ++k) {
@@ -207,35 +163,13 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
       Elem<TF>::store(Uh + (int64_t)k * DK + tid, acc * inv[col]);
     }
   }
-  if (DENSE) {
-    // Q_b = I: W[:, k] = K0^T x_k
-    for (int i = tid; i < DV; i += NT) {
-      for (int k = 0; k < rk; ++k) {
-        const int col = order[k];
-        const float *z = K + col * cs;
-        float acc = 0.f;
-        for (int l = 0; l < m; ++l) acc = fmaf(K0[i * cs + l], z[l], acc);
-        Elem<TF>::store(Wh + (int64_t)k * DV + i, acc * inv[col]);
-      }
-    }
-  } else {
-    __syncthreads();  // A (Q_a) is no longer needed: Y = K0^T X_r goes there
-    float *Y = A;
-    for (int idx = tid; idx < rk * m; idx += NT) {
-      const int k = idx / m, l = idx % m;
+  for (int i = tid; i < DV; i += NT) {
+    for (int k = 0; k < rk; ++k) {
       const int col = order[k];
       const float *z = K + col * cs;
       float acc = 0.f;
-      for (int i = 0; i < m; ++i) acc = fmaf(K0[l * cs + i], z[i], acc);
-      Y[k * cs + l] = acc * inv[col];
-    }
-    __syncthreads();
-    if (tid < DV) {
-      for (int k = 0; k < rk; ++k) {
-        float acc = 0.f;
-        for (int l = 0; l < m; ++l) acc = fmaf(B[l * ldb + tid], Y[k * cs + l], acc);
-        Elem<TF>::store(Wh + (int64_t)k * DV + tid, acc);
-      }
+      for (int l = 0; l < m; ++l) acc = fmaf(K0[i * cs + l], z[l], acc);
+      Elem<TF>::store(Wh + (int64_t)k * DV + i, acc * inv[col]);
     }
   }
   if (VAR == SEED_KDA) {
@@ -245,31 +179,194 @@ __global__ void __launch_bounds__(DENSE ? 256 : 128) compress_kernel(const Compr
   }
 }
 
-template <int VAR, typename TF, int DV, bool DENSE>
-static cudaError_t launch_compress_t(const CompressArgs &a, cudaStream_t s) {
+// Dynamic shared-memory layout of the single-kernel recompression (offsets in
+// floats, multiples of 4): the two factor panels, the two core buffers of the
+// pivoted QR and Jacobi (m + 1 seats for an odd m), the unscaled core, vectors.
+struct RecSmem {
+  int lda, ldb;
+  int offA, offB, offK, offT, offK0, offTa, offTb, offS, offI, offV, offO, offP, offQ, offR;
+  int total_floats;
+  __host__ __device__ RecSmem(int m, int dk, int dv, int cs) {
+    lda = dk + 4;
+    ldb = dv + 4;
+    auto up4 = [](int x) { return (x + 3) & ~3; };
+    const int seats = m + 1;
+    offA = 0;
+    offB = up4(offA + m * lda);
+    offK = up4(offB + m * ldb);
+    offT = offK + seats * cs;
+    offK0 = offT + seats * cs;
+    offTa = offK0 + m * cs;
+    offTb = offTa + up4(m);
+    offS = offTb + up4(m);
+    offI = offS + up4(m);
+    offV = offI + up4(m);
+    offO = offV + up4(m);
+    offP = offO + up4(m);
+    offQ = offP + up4(m);
+    offR = offQ + up4(m);
+    total_floats = offR + 8;
+  }
+};
+
+template <int VAR, typename TF, int DV>
+__global__ void __launch_bounds__(128) recompress_kernel(const CompressArgs p) {
+  constexpr int DK = kDK;
+  constexpr int NT = 128;
+  extern __shared__ __align__(16) float smem[];
+  const int h = blockIdx.x;
+  const int tid = threadIdx.x;
+  const StateView &sv = p.sv;
+  const int r = sv.rank_of(h);
+  const int m = r + sv.growth * sv.steps;
+  if (r < 0 || m > p.m_max) {  // rank table disagrees with r_max: touch nothing
+    if (tid == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
+    return;
+  }
+  const int64_t c0 = sv.col0(h);
+  const RecSmem L(p.m_max, DK, DV, p.cs_alloc);
+  const JacobiGeom g = seat_geom(m, NT);
+  const int cs = g.cs;
+  const int m4 = (m + 3) & ~3;
+  float *A = smem + L.offA, *B = smem + L.offB, *Kb = smem + L.offK, *Tb = smem + L.offT;
+  float *K0 = smem + L.offK0, *tauA = smem + L.offTa, *tauB = smem + L.offTb;
+  float *sig2 = smem + L.offS, *inv = smem + L.offI, *vn = smem + L.offV, *red = smem + L.offR;
+  int *order = reinterpret_cast<int *>(smem + L.offO);
+  int *piv = reinterpret_cast<int *>(smem + L.offP);
+  int *pinv = reinterpret_cast<int *>(smem + L.offQ);
+  const int lda = L.lda, ldb = L.ldb;
+  TF *Uh = reinterpret_cast<TF *>(sv.U) + c0 * DK;
+  TF *Wh = reinterpret_cast<TF *>(sv.W) + c0 * DV;
+
+  // ---- load -------------------------------------------------------------------
+  for (int idx = tid; idx < m * DK; idx += NT) {
+    const int j = idx / DK, i = idx % DK;
+    const float u = Elem<TF>::load(Uh + idx);
+    const float f = VAR == SEED_KDA ? sv.scale[(int64_t)h * DK + i] : sv.scale[c0 + j];
+    A[j * lda + i] = u * f;
+  }
+  for (int idx = tid; idx < m * DV; idx += NT) {
+    const int j = idx / DV, i = idx % DV;
+    B[j * ldb + i] = Elem<TF>::load(Wh + idx);
+  }
+  __syncthreads();
+
+  // ---- QR of both factors, core K = R_a R_b^T, Q factors in place ----------------------
+  const int team = tid / 64, ttid = tid % 64;
+  if (team == 0) householder_qr(A, lda, DK, m, tauA, ttid, 64, 1);
+  else householder_qr(B, ldb, DV, m, tauB, ttid, 64, 2);
+  __syncthreads();
+  for (int idx = tid; idx < m * m4; idx += NT) {
+    const int j = idx / m4, i = idx % m4;  // K[j][i]: column j, row i
+    float acc = 0.f;
+    if (i < m)
+      for (int l = max(i, j); l < m; ++l) acc = fmaf(A[l * lda + i], B[l * ldb + j], acc);
+    Kb[j * cs + i] = acc;
+    K0[j * cs + i] = acc;
+  }
+  __syncthreads();
+  if (team == 0) form_q(A, lda, DK, m, tauA, ttid, 64, 1);
+  else form_q(B, ldb, DV, m, tauB, ttid, 64, 2);
+
+  // ---- core scaled by a power of two to a largest entry in [1/2, 1), then factored ---------
+  float kmax = 0.f;
+  for (int idx = tid; idx < m * m4; idx += NT) kmax = fmaxf(kmax, fabsf(Kb[(idx / m4) * cs + idx % m4]));
+  kmax = warp_max(kmax);
+  if ((tid & 31) == 0) red[tid >> 5] = kmax;
+  __syncthreads();
+  kmax = 0.f;
+  for (int w = 0; w < NT / 32; ++w) kmax = fmaxf(kmax, red[w]);
+  int kexp = 0;
+  if (kmax > 0.f) frexpf(kmax, &kexp);
+  const float kscale = ldexpf(1.f, -kexp), kunscale = ldexpf(1.f, kexp);
+  for (int idx = tid; idx < m * m4; idx += NT) Kb[(idx / m4) * cs + idx % m4] *= kscale;
+  __syncthreads();
+  const float tol = sizeof(TF) == 2 ? 1e-5f : (float)(m > 16 ? m : 16) * FLT_EPSILON;
+  float *F;
+  const int sweeps = core_factor<NT>(Kb, Tb, m, g, tol, piv, vn, sig2, inv, order, red, &F);
+  if (tid == 0) {
+    float e = 0.f;
+    for (int k = r; k < m; ++k) e += sig2[order[k]];
+    if (p.trunc_err) p.trunc_err[h] = sqrtf(e) * kunscale;
+    if (p.sweeps) p.sweeps[h] = sweeps;
+    if (sv.status) sv.status[h] = sweeps < 0 ? SEED_ERR_NOT_CONVERGED : SEED_OK;
+  }
+
+  // ---- z_k = K y_k into the free core buffer; y_k[piv[i]] = (R^T J)_{i,order[k]} / sigma_k ----
+  const int rk = r < m ? r : m;
+  float *Z = F == Kb ? Tb : Kb;  // [rk][m]
+  for (int i = tid; i < m; i += NT) pinv[piv[i]] = i;
+  for (int idx = tid; idx < rk * m; idx += NT) {
+    const int k = idx / m, l = idx % m;
+    const int col = order[k];
+    const float *f = F + col * cs;
+    float acc = 0.f;
+    for (int i = 0; i < m; ++i) acc = fmaf(K0[piv[i] * cs + l], f[i], acc);
+    Z[idx] = acc * inv[col];
+  }
+  __syncthreads();
+
+  // ---- U = Q_a Z,  W = Q_b Y -------------------------------------------------------------------
+  if (tid < DK) {
+    for (int k = 0; k < rk; ++k) {
+      float acc = 0.f;
+      for (int l = 0; l < m; ++l) acc = fmaf(A[l * lda + tid], Z[k * m + l], acc);
+      Elem<TF>::store(Uh + (int64_t)k * DK + tid, acc);
+    }
+  }
+  if (tid < DV) {
+    for (int k = 0; k < rk; ++k) {
+      const int col = order[k];
+      const float *f = F + col * cs;
+      const float ik = inv[col];
+      float acc = 0.f;
+      for (int l = 0; l < m; ++l) acc = fmaf(B[l * ldb + tid], f[pinv[l]] * ik, acc);
+      Elem<TF>::store(Wh + (int64_t)k * DV + tid, acc);
+    }
+  }
+  if (VAR == SEED_KDA) {
+    for (int i = tid; i < DK; i += NT) sv.scale[(int64_t)h * DK + i] = 1.f;
+  } else {
+    for (int k = tid; k < rk; k += NT) sv.scale[c0 + k] = 1.f;
+  }
+}
+
+template <int VAR, typename TF, int DV>
+static cudaError_t launch_recompress_t(const CompressArgs &a, cudaStream_t s) {
   CompressArgs args = a;
-  const int m_alloc = DENSE ? DV : a.m_max;
-  args.cs_alloc = jacobi_cs_alloc(m_alloc, DENSE ? 256 : 128);
-  const Smem L(m_alloc, kDK, DV, DENSE, args.cs_alloc);
+  args.cs_alloc = seat_cs_alloc(a.m_max, 128);
+  const RecSmem L(a.m_max, kDK, DV, args.cs_alloc);
   const size_t bytes = (size_t)L.total_floats * sizeof(float);
-  auto kern = compress_kernel<VAR, TF, DV, DENSE>;
+  auto kern = recompress_kernel<VAR, TF, DV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  kern<<<a.sv.n_heads, DENSE ? 256 : 128, bytes, s>>>(args);
+  kern<<<a.sv.n_heads, 128, bytes, s>>>(args);
   return cudaGetLastError();
 }
 
-template <int VAR, typename TF, bool DENSE>
-static cudaError_t launch_compress_d(const CompressArgs &a, cudaStream_t s) {
-  if (a.sv.d_v == 64) return launch_compress_t<VAR, TF, 64, DENSE>(a, s);
-  return launch_compress_t<VAR, TF, 128, DENSE>(a, s);
+template <int VAR, typename TF, int DV>
+static cudaError_t launch_dense_t(const CompressArgs &a, cudaStream_t s) {
+  CompressArgs args = a;
+  args.cs_alloc = jacobi_cs_alloc(DV, 256);
+  const DenseSmem L(DV, kDK, args.cs_alloc);
+  const size_t bytes = (size_t)L.total_floats * sizeof(float);
+  auto kern = compress_dense_kernel<VAR, TF, DV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  kern<<<a.sv.n_heads, 256, bytes, s>>>(args);
+  return cudaGetLastError();
 }
 
 template <typename TF, bool DENSE>
 static cudaError_t launch_compress_v(const CompressArgs &a, cudaStream_t s) {
   // Only the scale layout differs between variants here.
-  if (a.sv.variant == SEED_KDA) return launch_compress_d<SEED_KDA, TF, DENSE>(a, s);
-  return launch_compress_d<SEED_GDN, TF, DENSE>(a, s);
+  const bool kda = a.sv.variant == SEED_KDA, dv64 = a.sv.d_v == 64;
+  if (DENSE) {
+    if (kda) return dv64 ? launch_dense_t<SEED_KDA, TF, 64>(a, s) : launch_dense_t<SEED_KDA, TF, 128>(a, s);
+    return dv64 ? launch_dense_t<SEED_GDN, TF, 64>(a, s) : launch_dense_t<SEED_GDN, TF, 128>(a, s);
+  }
+  if (kda) return dv64 ? launch_recompress_t<SEED_KDA, TF, 64>(a, s) : launch_recompress_t<SEED_KDA, TF, 128>(a, s);
+  return dv64 ? launch_recompress_t<SEED_GDN, TF, 64>(a, s) : launch_recompress_t<SEED_GDN, TF, 128>(a, s);
 }
 
 cudaError_t launch_recompress(const StateView &sv, int factor_dtype, float *trunc_err,

@@ -10,29 +10,31 @@
 //   qr_phase      one CTA of 128 threads per head: Householder QR of U_eff and
 //                 of W in two 64-thread teams, core K = R_a R_b^T, explicit Q_a
 //                 and Q_b; writes K, Q_a, Q_b to the workspace
-//   svd_phase     one CTA of 128 threads per head: one-sided Jacobi on the core,
-//                 ordering, truncation error; writes the kept columns Z of K J
-//                 (unnormalised) with their 1/sigma, and Y = K^T X_r
-//   rebuild_phase one CTA per (head, factor): U = Q_a Z diag(1/sigma), W = Q_b Y;
-//                 resets the lazy scales
+//   svd_phase     one CTA of 128 threads per head: pivoted QR of the core and
+//                 one-sided Jacobi on R^T, ordering, truncation error; writes
+//                 the kept right singular vectors Y (y_k) and Z (z_k = K y_k)
+//   rebuild_phase one CTA per (head, factor): U = Q_a Z, W = Q_b Y; resets the
+//                 lazy scales
 //
 // Workspace per head (fp32, column-major panels): Q_a [m][d_k], Q_b [m][d_v],
-// K [m][m], Z [r][m], Y [r][m], 1/sigma [r], rounded up to 256 bytes, with m the
-// largest column count of any head at this call and r the largest rank.
+// K [m][m], Z [r][m4], Y [r][m4] (m4 = m rounded up to 4, zero padded), rounded
+// up to 256 bytes, with m the largest column count of any head at this call and
+// r the largest rank.
 #include "recompress_core.cuh"
 
 namespace seedk {
 
 struct SplitLayout {
-  int64_t qa, qb, k, z, y, zinv, per_head;  // offsets and stride in floats
+  int64_t qa, qb, k, z, y, per_head;  // offsets and stride in floats
+  int m4;                             // row stride of Z and Y
   __host__ __device__ SplitLayout(int m, int r, int dk, int dv) {
+    m4 = (m + 3) & ~3;
     qa = 0;
     qb = qa + (int64_t)m * dk;
     k = qb + (int64_t)m * dv;
     z = k + (int64_t)m * m;
-    y = z + (int64_t)r * m;
-    zinv = y + (int64_t)r * m;
-    per_head = (zinv + r + 63) & ~(int64_t)63;
+    y = z + (int64_t)r * m4;
+    per_head = (y + (int64_t)r * m4 + 63) & ~(int64_t)63;
     if (per_head == 0) per_head = 64;  // no columns: keep a nonzero stride
   }
 };
@@ -109,7 +111,7 @@ __global__ void __launch_bounds__(kSplitThreads) qr_phase(const SplitArgs p) {
 
 // ---- phase 2: SVD of the core ------------------------------------------------------------
 template <typename TF, int DV>
-__global__ void __launch_bounds__(kSplitThreads) svd_phase(const SplitArgs p) {
+__global__ void __launch_bounds__(kSplitThreads, 8) svd_phase(const SplitArgs p) {
   constexpr int DK = kDK;
   constexpr int NT = kSplitThreads;
   extern __shared__ __align__(16) float smem[];
@@ -123,27 +125,26 @@ __global__ void __launch_bounds__(kSplitThreads) svd_phase(const SplitArgs p) {
   }
   const SplitLayout L(p.m_max, p.r_max, DK, DV);
   float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
-  const JacobiGeom jg = jacobi_geom(m, NT);
-  const int cs = jg.cs, ldr = jg.ld;
+  const JacobiGeom g = seat_geom(m, NT);
+  const int cs = g.cs;
+  const int m4 = (m + 3) & ~3;
   const int up = (p.m_max + 3) & ~3;
-  float *K = smem;
-  float *K0 = K + p.m_max * p.cs_alloc;
-  float *sig2 = K0 + p.m_max * p.cs_alloc;
-  float *inv = sig2 + up;
-  int *order = reinterpret_cast<int *>(inv + up);
-  float *red = reinterpret_cast<float *>(order + up);
+  const int buf = (p.m_max + 1) * p.cs_alloc;
+  float *Kb = smem, *Tb = smem + buf;
+  float *sig2 = Tb + buf, *inv = sig2 + up, *vn = inv + up;
+  int *order = reinterpret_cast<int *>(vn + up);
+  int *piv = order + up;
+  float *red = reinterpret_cast<float *>(piv + up);
 
-  // core, rows padded with zeros to ld; K0 keeps a copy
+  // core, rows m..m4-1 zero, scaled by a power of two to a largest entry in [1/2, 1)
   const float *Kw = ws + L.k;
-  float kmax = 0.f;
-  for (int idx = tid; idx < m * ldr; idx += NT) {
-    const int j = idx / ldr, i = idx % ldr;
-    const float x = i < m ? Kw[j * m + i] : 0.f;
-    K[j * cs + i] = x;
-    K0[j * cs + i] = x;
-    kmax = fmaxf(kmax, fabsf(x));
+  for (int idx = tid; idx < m * m4; idx += NT) {
+    const int j = idx / m4, i = idx % m4;
+    Kb[j * cs + i] = i < m ? Kw[j * m + i] : 0.f;
   }
-  // scale by a power of two to a largest entry in [1/2, 1)
+  __syncthreads();
+  float kmax = 0.f;
+  for (int idx = tid; idx < m * m4; idx += NT) kmax = fmaxf(kmax, fabsf(Kb[(idx / m4) * cs + idx % m4]));
   kmax = warp_max(kmax);
   if ((tid & 31) == 0) red[tid >> 5] = kmax;
   __syncthreads();
@@ -152,28 +153,11 @@ __global__ void __launch_bounds__(kSplitThreads) svd_phase(const SplitArgs p) {
   int kexp = 0;
   if (kmax > 0.f) frexpf(kmax, &kexp);
   const float kscale = ldexpf(1.f, -kexp), kunscale = ldexpf(1.f, kexp);
-  for (int idx = tid; idx < m * ldr; idx += NT) K[(idx / ldr) * cs + idx % ldr] *= kscale;
+  for (int idx = tid; idx < m * m4; idx += NT) Kb[(idx / m4) * cs + idx % m4] *= kscale;
   __syncthreads();
   const float tol = sizeof(TF) == 2 ? 1e-5f : (float)(m > 16 ? m : 16) * FLT_EPSILON;
-  const int sweeps = jacobi_svd<NT, 16>(K, m, jg, tol);
-
-  for (int j = tid; j < m; j += NT) {
-    float acc = 0.f;
-    for (int i = 0; i < m; ++i) acc = fmaf(K[j * cs + i], K[j * cs + i], acc);
-    sig2[j] = acc;
-    inv[j] = acc > kNegligible ? rsqrtf(acc) : 0.f;
-  }
-  __syncthreads();
-  for (int j = tid; j < m; j += NT) {
-    int rank = 0;
-    const float sj = sig2[j];
-    for (int i = 0; i < m; ++i) {
-      const float si = sig2[i];
-      rank += (si > sj) || (si == sj && i < j);
-    }
-    order[rank] = j;
-  }
-  __syncthreads();
+  float *F;
+  const int sweeps = core_factor<NT>(Kb, Tb, m, g, tol, piv, vn, sig2, inv, order, red, &F);
   if (tid == 0) {
     float e = 0.f;
     for (int k = r; k < m; ++k) e += sig2[order[k]];
@@ -181,22 +165,33 @@ __global__ void __launch_bounds__(kSplitThreads) svd_phase(const SplitArgs p) {
     if (p.sweeps) p.sweeps[h] = sweeps;
     if (sv.status) sv.status[h] = sweeps < 0 ? SEED_ERR_NOT_CONVERGED : SEED_OK;
   }
-  // kept columns z_k = (K J)_{order[k]}, 1/sigma_k, and Y[k] = K0^T z_k / sigma_k
+  // the unscaled core into the free buffer; y_k[piv[i]] = (R^T J)_{i,order[k]} / sigma_k
+  // and z_k = K y_k, rows m..m4-1 zero
+  float *K0 = F == Kb ? Tb : Kb;
+  for (int idx = tid; idx < m * m; idx += NT) K0[(idx / m) * cs + idx % m] = Kw[idx];
+  __syncthreads();
   const int rk = r < m ? r : m;
-  float *Z = ws + L.z, *Y = ws + L.y, *Zinv = ws + L.zinv;
-  for (int idx = tid; idx < rk * m; idx += NT) {
-    const int k = idx / m, l = idx % m;
+  float *Z = ws + L.z, *Y = ws + L.y;
+  for (int idx = tid; idx < rk * m4; idx += NT) {
+    const int k = idx / m4, l = idx % m4;
     const int col = order[k];
-    const float *z = K + col * cs;
-    float acc = 0.f;
-    for (int i = 0; i < m; ++i) acc = fmaf(K0[l * cs + i], z[i], acc);
-    Y[idx] = acc * inv[col];
-    Z[idx] = z[l];
+    const float *f = F + col * cs;
+    float z = 0.f;
+    if (l < m) {
+      float acc = 0.f;
+      for (int i = 0; i < m; ++i) acc = fmaf(K0[piv[i] * cs + l], f[i], acc);
+      z = acc * inv[col];
+      Y[k * L.m4 + piv[l]] = f[l] * inv[col];
+    } else {
+      Y[k * L.m4 + l] = 0.f;
+    }
+    Z[k * L.m4 + l] = z;
   }
-  for (int k = tid; k < rk; k += NT) Zinv[k] = inv[order[k]];
 }
 
 // ---- phase 3: rebuild the factors ---------------------------------------------------------
+// One row of the factor per thread: Q row in registers, the kept coefficient
+// vectors from shared memory as broadcast 16-byte loads, two outputs at a time.
 template <int VAR, typename TF, int DV>
 __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p) {
   constexpr int DK = kDK;
@@ -211,9 +206,10 @@ __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p
   const float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
   const int rows = panel == 0 ? DK : DV;
   const int rk = r < m ? r : m;
-  float *zs = smem;  // [rk][m]
+  const int m4 = (m + 3) & ~3;
+  float *zs = smem;  // [rk][m4]
   const float *src = ws + (panel == 0 ? L.z : L.y);
-  for (int idx = tid; idx < rk * m; idx += kSplitThreads) zs[idx] = src[idx];
+  for (int idx = tid; idx < rk * m4; idx += kSplitThreads) zs[idx] = src[(idx / m4) * L.m4 + idx % m4];
   __syncthreads();
   const int64_t c0 = sv.col0(h);
   if (tid < rows) {
@@ -222,14 +218,38 @@ __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p
 #pragma unroll
     for (int l = 0; l < kMaxCols; ++l) q[l] = l < m ? Q[l * rows + tid] : 0.f;
     TF *out = reinterpret_cast<TF *>(panel == 0 ? sv.U : sv.W) + c0 * rows;
-    const float *zinv = ws + L.zinv;
-    for (int k = 0; k < rk; ++k) {
-      const float *z = zs + k * m;
-      float acc = 0.f;
+    int k = 0;
+    for (; k + 1 < rk; k += 2) {
+      const float4 *z0 = reinterpret_cast<const float4 *>(zs + k * m4);
+      const float4 *z1 = reinterpret_cast<const float4 *>(zs + (k + 1) * m4);
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int l = 0; l < kMaxCols; ++l)
-        if (l < m) acc = fmaf(q[l], z[l], acc);
-      Elem<TF>::store(out + (int64_t)k * rows + tid, panel == 0 ? acc * zinv[k] : acc);
+      for (int l4 = 0; l4 < kMaxCols / 4; ++l4) {
+        if (4 * l4 < m) {
+          const float4 u = z0[l4], w = z1[l4];
+          a0 = fmaf(q[4 * l4], u.x, a0); a1 = fmaf(q[4 * l4], w.x, a1);
+          if (4 * l4 + 1 < m) { a0 = fmaf(q[4 * l4 + 1], u.y, a0); a1 = fmaf(q[4 * l4 + 1], w.y, a1); }
+          if (4 * l4 + 2 < m) { a0 = fmaf(q[4 * l4 + 2], u.z, a0); a1 = fmaf(q[4 * l4 + 2], w.z, a1); }
+          if (4 * l4 + 3 < m) { a0 = fmaf(q[4 * l4 + 3], u.w, a0); a1 = fmaf(q[4 * l4 + 3], w.w, a1); }
+        }
+      }
+      Elem<TF>::store(out + (int64_t)k * rows + tid, a0);
+      Elem<TF>::store(out + (int64_t)(k + 1) * rows + tid, a1);
+    }
+    if (k < rk) {
+      const float4 *z0 = reinterpret_cast<const float4 *>(zs + k * m4);
+      float a0 = 0.f;
+#pragma unroll
+      for (int l4 = 0; l4 < kMaxCols / 4; ++l4) {
+        if (4 * l4 < m) {
+          const float4 u = z0[l4];
+          a0 = fmaf(q[4 * l4], u.x, a0);
+          if (4 * l4 + 1 < m) a0 = fmaf(q[4 * l4 + 1], u.y, a0);
+          if (4 * l4 + 2 < m) a0 = fmaf(q[4 * l4 + 2], u.z, a0);
+          if (4 * l4 + 3 < m) a0 = fmaf(q[4 * l4 + 3], u.w, a0);
+        }
+      }
+      Elem<TF>::store(out + (int64_t)k * rows + tid, a0);
     }
   }
   if (panel == 0) {
@@ -249,9 +269,9 @@ template <int VAR, typename TF, int DV>
 static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaStream_t s) {
   const int up = (a.m_max + 3) & ~3;
   const int qr_bytes = (((a.m_max * (kDK + 4) + 3) & ~3) + ((a.m_max * (DV + 4) + 3) & ~3) + 2 * up) * 4;
-  a.cs_alloc = jacobi_cs_alloc(a.m_max, kSplitThreads);
-  const int svd_bytes = (2 * a.m_max * a.cs_alloc + 3 * up + 8) * 4;
-  const int rb_bytes = (a.r_max * a.m_max > 0 ? a.r_max * a.m_max : 1) * 4;
+  a.cs_alloc = seat_cs_alloc(a.m_max, kSplitThreads);
+  const int svd_bytes = (2 * (a.m_max + 1) * a.cs_alloc + 5 * up + 8) * 4;
+  const int rb_bytes = (a.r_max * up > 0 ? a.r_max * up : 4) * 4;
   auto k1 = qr_phase<VAR, TF, DV>;
   auto k2 = svd_phase<TF, DV>;
   auto k3 = rebuild_phase<VAR, TF, DV>;

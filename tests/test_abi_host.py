@@ -140,7 +140,8 @@ def test_synth_calls_reject_on_host():
 
 
 def _ws_floats(m, r, dk, dv):
-    n = m * dk + m * dv + m * m + 2 * r * m + r
+    m4 = (m + 3) // 4 * 4
+    n = m * dk + m * dv + m * m + 2 * r * m4
     n = (n + 63) // 64 * 64
     return max(n, 64)
 
