@@ -1,0 +1,157 @@
+// Householder QR of a factor panel with the panel held in registers.
+//
+// TPC threads per column (TPC = 4 here): thread part p < TPC of column l holds
+// rows 4c..4c+3 of the column for the chunks c = p + TPC i, i < rows / (4 TPC).
+//
+// Factorization (one barrier per step j): the warp that holds column j turns
+// it into the reflector together - the two owners lay the column out in V[j]
+// (shared), the 32 lanes form amax, the scaled norm and v_j (v_j[j] = 1, zeros
+// above) in place, the owners read back beta (row j) and v_j (rows below).
+// After the barrier every later column takes v_j . a_l over its rows (two
+// shuffles join the parts) and subtracts tau_j (v_j . a_l) v_j in its
+// registers.  The panel itself never goes through shared memory; V keeps all
+// reflectors for the explicit Q.
+//
+// Explicit Q: column l of Q = H_0 H_1 ... H_{m-1} [I; 0] is H_0 ... H_l e_l
+// (H_j e_l = e_l for j > l), so every column starts from e_l and applies its
+// reflectors from H_l down to H_0 on its own, with no barrier.
+//
+// The reflector is the one of householder_qr (formed from the column scaled by
+// its largest magnitude; zero below the smallest normal float), so the result
+// differs from householder_qr / form_q only in summation order.
+#pragma once
+
+#include "common.cuh"
+
+#include <float.h>
+
+namespace seedk {
+
+constexpr int kTPC = 4;                   // threads per column
+constexpr int kRRChunks = 128 / (4 * kTPC);  // float4 chunks per thread for a 128-row panel
+
+// My part of a column: chunks i < nch (nch = rows / (4 TPC)) are in use.
+struct RRCol {
+  float4 x[kRRChunks];
+  int nch;
+};
+
+__device__ inline int rr_row(int p, int i, int e) { return 4 * (p + kTPC * i) + e; }
+__device__ inline float f4get(const float4 &v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; }
+__device__ inline void f4set(float4 &v, int e, float a) {
+  if (e == 0) v.x = a; else if (e == 1) v.y = a; else if (e == 2) v.z = a; else v.w = a;
+}
+
+// Step j of the factorization, run by every lane of the warp that holds column
+// j (owner: the kTPC lanes of column j).  vj: V[j] (rows floats); on exit it holds
+// v_j, *tau = tau_j, and the owners' registers hold beta (row j) and v_j below.
+__device__ inline void rr_reflector_warp(RRCol &c, bool owner, int p, int j, int rows, float *vj,
+                                         float *tau, float *beta_out) {
+  const int lane = threadIdx.x & 31;
+  if (owner) {
+#pragma unroll
+    for (int i = 0; i < kRRChunks; ++i) {
+      if (i >= c.nch) break;
+      reinterpret_cast<float4 *>(vj)[p + kTPC * i] = c.x[i];
+    }
+  }
+  __syncwarp();
+  // lane k holds rows [k * rpl, (k + 1) * rpl), rpl = rows / 32 (4 or 2)
+  const int rpl = rows >> 5;
+  float a[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) a[e] = e < rpl ? vj[lane * rpl + e] : 0.f;
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (e < rpl && lane * rpl + e >= j) amax = fmaxf(amax, fabsf(a[e]));
+  amax = warp_max(amax);
+  const float alpha = vj[j];
+  float tj = 0.f, beta = alpha, sc = 0.f;
+  if (amax >= FLT_MIN) {
+    const float inv = 1.f / amax;
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float xs = (e < rpl && lane * rpl + e > j) ? a[e] * inv : 0.f;
+      ss = fmaf(xs, xs, ss);
+    }
+    ss = warp_sum(ss);
+    if (ss > 0.f) {
+      const float as = alpha * inv;
+      const float nrm = sqrtf(fmaf(as, as, ss));
+      const float bs = as >= 0.f ? -nrm : nrm;
+      tj = (bs - as) / bs;
+      sc = 1.f / ((as - bs) * amax);  // v_i = x_i / (alpha - beta), |v_i| <= 1
+      beta = bs * amax;
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int row = lane * rpl + e;
+    if (e < rpl) vj[row] = row < j ? 0.f : row == j ? 1.f : a[e] * sc;
+  }
+  if (lane == 0) {
+    *tau = tj;
+    *beta_out = beta;
+  }
+  __syncwarp();
+  if (owner) {
+    // my row 4p + 4 TPC i + e is compared with j as 4 TPC i + e against jj
+    const int jj = j - 4 * p;
+#pragma unroll
+    for (int i = 0; i < kRRChunks; ++i) {
+      if (i >= c.nch) break;
+      const float4 v = reinterpret_cast<const float4 *>(vj)[p + kTPC * i];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = 4 * kTPC * i + e;
+        if (d == jj) f4set(c.x[i], e, beta);
+        else if (d > jj) f4set(c.x[i], e, f4get(v, e));
+      }
+    }
+  }
+}
+
+// a_l -= tau (v . a_l) v over my rows.  All kTPC lanes of the column call it
+// (pmask: those lanes).
+__device__ inline void rr_apply(RRCol &c, int p, const float *v, float tau, unsigned pmask) {
+  const float4 *v4 = reinterpret_cast<const float4 *>(v);
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRRChunks; ++i) {
+    if (i >= c.nch) break;
+    const float4 w = v4[p + kTPC * i];
+    s0 = fmaf(w.x, c.x[i].x, s0); s1 = fmaf(w.y, c.x[i].y, s1);
+    s2 = fmaf(w.z, c.x[i].z, s2); s3 = fmaf(w.w, c.x[i].w, s3);
+  }
+  float dot = (s0 + s1) + (s2 + s3);
+#pragma unroll
+  for (int o = 1; o < kTPC; o <<= 1) dot += __shfl_xor_sync(pmask, dot, o);
+  const float sv = tau * dot;
+  // read v again rather than keeping a second copy of the chunk in registers
+  asm volatile("" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < kRRChunks; ++i) {
+    if (i >= c.nch) break;
+    const float4 w = v4[p + kTPC * i];
+    c.x[i].x = fmaf(-sv, w.x, c.x[i].x); c.x[i].y = fmaf(-sv, w.y, c.x[i].y);
+    c.x[i].z = fmaf(-sv, w.z, c.x[i].z); c.x[i].w = fmaf(-sv, w.w, c.x[i].w);
+  }
+}
+
+// My part of e_l.
+__device__ inline void rr_unit(RRCol &c, int p, int l) {
+  const int ll = l - 4 * p;
+#pragma unroll
+  for (int i = 0; i < kRRChunks; ++i) {
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (4 * kTPC * i + e == ll) f4set(u, e, 1.f);
+    c.x[i] = u;
+  }
+}
+
+}  // namespace seedk

@@ -259,8 +259,10 @@ __global__ void __launch_bounds__(128) recompress_kernel(const CompressArgs p) {
   for (int idx = tid; idx < m * m4; idx += NT) {
     const int j = idx / m4, i = idx % m4;  // K[j][i]: column j, row i
     float acc = 0.f;
+    // l from j for every lane of column j (B element a broadcast), l < i skipped
     if (i < m)
-      for (int l = max(i, j); l < m; ++l) acc = fmaf(A[l * lda + i], B[l * ldb + j], acc);
+      for (int l = j; l < m; ++l)
+        if (l >= i) acc = fmaf(A[l * lda + i], B[l * ldb + j], acc);
     Kb[j * cs + i] = acc;
     K0[j * cs + i] = acc;
   }

@@ -21,6 +21,7 @@
 // up to 256 bytes, with m the largest column count of any head at this call and
 // r the largest rank.
 #include "recompress_core.cuh"
+#include "qr_registers.cuh"
 
 namespace seedk {
 
@@ -58,8 +59,13 @@ __device__ inline bool split_head_ok(const StateView &sv, int h, int m_max, int 
 }
 
 // ---- phase 1: QR of both factors, core, explicit Q --------------------------------------
+// Two teams of kTPC x m_max threads (the second starts on a warp boundary),
+// kTPC threads per column, the panels in registers (qr_registers.cuh).
+__host__ __device__ inline int qr_team_stride(int m_max) { return (kTPC * m_max + 31) / 32 * 32; }
+
+// 80 registers: two CTAs of 384 threads (m_max = 48) per SM, a few bytes of spill
 template <int VAR, typename TF, int DV>
-__global__ void __launch_bounds__(kSplitThreads) qr_phase(const SplitArgs p) {
+__global__ void __maxnreg__(80) qr_phase(const SplitArgs p) {
   constexpr int DK = kDK;
   extern __shared__ __align__(16) float smem[];
   const int h = p.head0 + blockIdx.x;
@@ -67,46 +73,97 @@ __global__ void __launch_bounds__(kSplitThreads) qr_phase(const SplitArgs p) {
   const StateView &sv = p.sv;
   int r, m;
   if (!split_head_ok(sv, h, p.m_max, r, m)) return;  // reported by the SVD phase
-  constexpr int lda = DK + 4, ldb = DV + 4;
-  float *A = smem;
-  float *B = A + ((p.m_max * lda + 3) & ~3);
-  float *tauA = B + ((p.m_max * ldb + 3) & ~3);
-  float *tauB = tauA + ((p.m_max + 3) & ~3);
+  const int mm = p.m_max;
+  const int up = (mm + 3) & ~3;
+  const int wbase = qr_team_stride(mm);
+  const bool teamU = tid < wbase;   // warps of the U_eff panel, then those of W
+  const int t = teamU ? tid : tid - wbase;
+  const int l = t / kTPC, part = t % kTPC;
+  const int rows = teamU ? DK : DV;
+  const bool mine = l < m;
+  const unsigned pmask = ((1u << kTPC) - 1) << ((tid & 31) & ~(kTPC - 1));
+  // shared: V of each panel [m_max][rows], tau and beta of each panel, R of each panel
+  float *V = smem + (teamU ? 0 : mm * DK);
+  float *tau = smem + mm * (DK + DV) + (teamU ? 0 : up);
+  float *betas = smem + mm * (DK + DV) + 2 * up + (teamU ? 0 : up);
+  float *RsU = smem + mm * (DK + DV) + 4 * up;  // [m_max][m_max]: column l, row i
+  float *RsW = RsU + mm * mm;
   const int64_t c0 = sv.col0(h);
-  const TF *Uh = reinterpret_cast<const TF *>(sv.U) + c0 * DK;
-  const TF *Wh = reinterpret_cast<const TF *>(sv.W) + c0 * DV;
-  for (int idx = tid; idx < m * DK; idx += kSplitThreads) {
-    const int j = idx / DK, i = idx % DK;
-    const float u = Elem<TF>::load(Uh + idx);
-    const float f = VAR == SEED_KDA ? sv.scale[(int64_t)h * DK + i] : sv.scale[c0 + j];
-    A[j * lda + i] = u * f;
-  }
-  for (int idx = tid; idx < m * DV; idx += kSplitThreads) {
-    const int j = idx / DV, i = idx % DV;
-    B[j * ldb + i] = Elem<TF>::load(Wh + idx);
-  }
-  __syncthreads();
-  const int team = tid / 64, ttid = tid % 64;
-  if (team == 0) householder_qr(A, lda, DK, m, tauA, ttid, 64, 1);
-  else householder_qr(B, ldb, DV, m, tauB, ttid, 64, 2);
-  __syncthreads();
 
+  // ---- my half of column l: U_eff (scaled) or W -----------------------------------------
+  RRCol c;
+  c.nch = rows / (4 * kTPC);
+#pragma unroll
+  for (int i = 0; i < kRRChunks; ++i) c.x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (mine) {
+    const TF *col = reinterpret_cast<const TF *>(teamU ? sv.U : sv.W) + (c0 + l) * rows;
+    const float cscale = (teamU && VAR != SEED_KDA) ? sv.scale[c0 + l] : 1.f;
+#pragma unroll
+    for (int i = 0; i < kRRChunks; ++i) {
+      if (i >= c.nch) break;
+      const int row = rr_row(part, i, 0);
+      float4 a;
+      if (sizeof(TF) == 2) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(col + row);
+        a = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+      } else {
+        a = *reinterpret_cast<const float4 *>(col + row);
+      }
+      if (teamU && VAR == SEED_KDA) {
+        const float4 d = *reinterpret_cast<const float4 *>(sv.scale + (int64_t)h * DK + row);
+        a = make_float4(a.x * d.x, a.y * d.y, a.z * d.z, a.w * d.w);
+      } else if (teamU) {
+        a = make_float4(a.x * cscale, a.y * cscale, a.z * cscale, a.w * cscale);
+      }
+      c.x[i] = a;
+    }
+  }
+
+  // ---- Householder QR of both panels ------------------------------------------------------
+  for (int j = 0; j < m; ++j) {
+    if ((t >> 5) == ((kTPC * j) >> 5))  // the warp that holds column j of my panel
+      rr_reflector_warp(c, l == j, part, j, rows, V + j * rows, tau + j, betas + j);
+    __syncthreads();
+    if (mine && l > j) rr_apply(c, part, V + j * rows, tau[j], pmask);
+  }
+  // ---- R factors to shared memory ------------------------------------------------------------
+  if (mine) {
+    float *Rs = teamU ? RsU : RsW;
+#pragma unroll
+    for (int i = 0; i < kRRChunks; ++i) {
+      if (i >= c.nch) break;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = rr_row(part, i, e);
+        if (row < m) Rs[l * mm + row] = row <= l ? f4get(c.x[i], e) : 0.f;
+      }
+    }
+  }
+  __syncthreads();
   const SplitLayout L(p.m_max, p.r_max, DK, DV);
   float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
+  // ---- explicit thin Q: column l = H_0 ... H_l e_l, each column on its own ------------------
+  if (mine) {
+    rr_unit(c, part, l);
+    for (int j = l; j >= 0; --j) rr_apply(c, part, V + j * rows, tau[j], pmask);
+    float *Q = ws + (teamU ? L.qa : L.qb) + (int64_t)l * rows;
+#pragma unroll
+    for (int i = 0; i < kRRChunks; ++i) {
+      if (i >= c.nch) break;
+      *reinterpret_cast<float4 *>(Q + rr_row(part, i, 0)) = c.x[i];
+    }
+  }
+  // ---- core K = R_a R_b^T to the workspace ----------------------------------------------------
+  // R is zero below the diagonal, so every lane of a column j of K runs k = j..m-1:
+  // the R_b element is a broadcast, the R_a elements are consecutive
   float *Kw = ws + L.k;
-  for (int idx = tid; idx < m * m; idx += kSplitThreads) {
+  for (int idx = tid; idx < m * m; idx += blockDim.x) {
     const int j = idx / m, i = idx % m;  // K[j][i]: column j, row i
     float acc = 0.f;
-    for (int l = max(i, j); l < m; ++l) acc = fmaf(A[l * lda + i], B[l * ldb + j], acc);
+    for (int k = j; k < m; ++k) acc = fmaf(RsU[k * mm + i], RsW[k * mm + j], acc);
     Kw[idx] = acc;
   }
-  __syncthreads();
-  if (team == 0) form_q(A, lda, DK, m, tauA, ttid, 64, 1);
-  else form_q(B, ldb, DV, m, tauB, ttid, 64, 2);
-  __syncthreads();
-  float *Qa = ws + L.qa, *Qb = ws + L.qb;
-  for (int idx = tid; idx < m * DK; idx += kSplitThreads) Qa[idx] = A[(idx / DK) * lda + idx % DK];
-  for (int idx = tid; idx < m * DV; idx += kSplitThreads) Qb[idx] = B[(idx / DV) * ldb + idx % DV];
 }
 
 // ---- phase 2: SVD of the core ------------------------------------------------------------
@@ -268,7 +325,8 @@ int64_t split_floats_per_head(int m_max, int r_max, int d_v) {
 template <int VAR, typename TF, int DV>
 static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaStream_t s) {
   const int up = (a.m_max + 3) & ~3;
-  const int qr_bytes = (((a.m_max * (kDK + 4) + 3) & ~3) + ((a.m_max * (DV + 4) + 3) & ~3) + 2 * up) * 4;
+  const int qr_bytes = (a.m_max * (kDK + DV) + 4 * up + 2 * a.m_max * a.m_max) * 4;
+  const int qr_threads = a.m_max > 0 ? qr_team_stride(a.m_max) * 2 : 32;
   a.cs_alloc = seat_cs_alloc(a.m_max, kSplitThreads);
   const int svd_bytes = (2 * (a.m_max + 1) * a.cs_alloc + 5 * up + 8) * 4;
   const int rb_bytes = (a.r_max * up > 0 ? a.r_max * up : 4) * 4;
@@ -282,7 +340,7 @@ static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaS
   for (int64_t h0 = 0; h0 < n_heads; h0 += chunk) {
     const int n = (int)(n_heads - h0 < chunk ? n_heads - h0 : chunk);
     a.head0 = (int)h0;
-    k1<<<n, kSplitThreads, qr_bytes, s>>>(a);
+    k1<<<n, qr_threads, qr_bytes, s>>>(a);
     k2<<<n, kSplitThreads, svd_bytes, s>>>(a);
     k3<<<dim3(n, 2), kSplitThreads, rb_bytes, s>>>(a);
     e = cudaGetLastError();
