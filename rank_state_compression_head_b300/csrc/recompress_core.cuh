@@ -375,14 +375,18 @@ __host__ inline int seat_cs_alloc(int m_max, int nthreads) {
 // read from one buffer and written, rotated, to their next seats in the other,
 // so the 16-byte chunks that the threads of two adjacent pairs touch always
 // fall in distinct bank groups (chunk c of a pair's column goes to thread
-// c mod tpp).  Rotation rule and tolerance as jacobi_svd.  buf0 holds column j
+// c mod tpp).  Rotation rule and tolerance as jacobi_svd.  The sweeps stop
+// after the first one in which no pair was further from orthogonal than
+// tol_stop (|cos| of the pair's angle): rotations converge quadratically, so
+// what is left after such a sweep is of order tol_stop^2 (tol_stop = sqrt(tol)
+// leaves about tol), and the sweep that would only confirm it is saved.  buf0 holds column j
 // at seat j (seat stride g.cs, rows padded with zeros to g.ld; an odd n gets a
 // zero column at seat n).  After whole sweeps every column is back at its
 // seat; *out points to the buffer that holds them.  Whole block of NT threads.
 // Returns the number of sweeps, or -1 if the sweep limit was reached.
 template <int NT, int RMAX>
 __device__ static int jacobi_seats(float *buf0, float *buf1, int n, const JacobiGeom &g, float tol,
-                                   float **out) {
+                                   float tol_stop, float **out) {
   *out = buf0;
   if (n < 2) return 0;
   const int tid = threadIdx.x;
@@ -392,14 +396,14 @@ __device__ static int jacobi_seats(float *buf0, float *buf1, int n, const Jacobi
   const int R4 = g.ld / tpp / 4;
   const int pair = tid / tpp, sub = tid % tpp;
   const bool active = pair < P;
-  const float tol2 = tol * tol;
+  const float tol2 = tol * tol, stop2 = tol_stop * tol_stop;
   const int st = active ? pair : 0, sb = active ? nn - 1 - pair : 1;
   const int nt = st == 0 ? 0 : (st == nn - 1 ? 1 : st + 1);
   const int nb = sb == nn - 1 ? 1 : sb + 1;
   int p = st, q = sb;  // columns at my seats; column at seat s >= 1 steps down by one per round
   float *cur = buf0, *nxt = buf1;
   for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
-    int rotated = 0;
+    int far = 0;  // a pair in this sweep was further from orthogonal than tol_stop
     for (int round = 0; round < nn - 1; ++round) {
       float4 xp[RMAX / 4], xq[RMAX / 4];
       float al = 0.f, be = 0.f, ga = 0.f;
@@ -446,7 +450,7 @@ __device__ static int jacobi_seats(float *buf0, float *buf1, int n, const Jacobi
                                         fmaf(s, a.w, c * b.w));
             }
           }
-          rotated = 1;
+          far |= ga * ga > stop2 * al * be;
         } else {
 #pragma unroll
           for (int v = 0; v < RMAX / 4; ++v) {
@@ -464,7 +468,7 @@ __device__ static int jacobi_seats(float *buf0, float *buf1, int n, const Jacobi
       nxt = t;
       if (round < nn - 2) __syncthreads();
     }
-    if (!__syncthreads_or(rotated)) {
+    if (!__syncthreads_or(far)) {
       *out = cur;
       return sweep + 1;
     }
@@ -493,7 +497,7 @@ __device__ static int core_factor(float *Kb, float *Tb, int m, const JacobiGeom 
     Tb[j * cs + i] = (j < m && i < m && i >= j) ? Kb[i * cs + j] : 0.f;
   }
   __syncthreads();
-  const int sweeps = jacobi_seats<NT, 16>(Tb, Kb, m, g, tol, fin);
+  const int sweeps = jacobi_seats<NT, 16>(Tb, Kb, m, g, tol, sqrtf(tol), fin);
   const float *F = *fin;
   for (int j = tid; j < m; j += NT) {
     float acc = 0.f;
