@@ -203,6 +203,27 @@ int seed_recompress_ws(seed_state *st, float *trunc_err, int32_t *sweeps, void *
                        int64_t workspace_bytes, seed_stream_t stream);
 
 /*
+ * seed_recompress_noalloc — seed_recompress_ws on a scratch array that the
+ * library holds in device memory, for callers that cannot provide a
+ * workspace.  The pages have no counterpart of this call: it is plumbing of
+ * this library.
+ *   The scratch is a fixed 64 MiB per device, reserved when the library's
+ *   kernels are loaded on that device; all heads are recompressed in one group,
+ *   so a state whose heads need more than that (n_heads x the per-head size
+ *   that seed_recompress_workspace_bytes reports for one head, at the current
+ *   column count) is rejected with SEED_ERR_UNSUPPORTED_SHAPE before any CUDA
+ *   call; use seed_recompress_ws for such states.
+ *   All calls on a device share the one scratch: two calls that may overlap
+ *   (on different streams or host threads) race on it and must be ordered by
+ *   the caller.
+ *   The first call on a device looks the scratch up and sets kernel attributes
+ *   on the host; make it before any stream capture.
+ * Results are bit-identical to seed_recompress_ws.  SEED_ERR_CUDA if the
+ * scratch cannot be found.  Sets st->steps_since_compress = 0.
+ */
+int seed_recompress_noalloc(seed_state *st, float *trunc_err, int32_t *sweeps, seed_stream_t stream);
+
+/*
  * seed_materialize — S = a vbar^T + U_eff W^T for every head (tests, export).
  *   S_out  [n_heads][d_k][d_v] fp32, row-major per head.
  */

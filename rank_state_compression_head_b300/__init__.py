@@ -83,6 +83,7 @@ _PROTOS = {
     'seed_recompress_ex': (ctypes.c_int, [_sp, _vp, _vp, _vp]),
     'seed_recompress_workspace_bytes': (ctypes.c_int, [_sp, _i32, _vp]),
     'seed_recompress_ws': (ctypes.c_int, [_sp, _vp, _vp, _vp, _i64, _vp]),
+    'seed_recompress_noalloc': (ctypes.c_int, [_sp, _vp, _vp, _vp]),
     'seed_materialize': (ctypes.c_int, [_sp, _vp, _vp]),
     'seed_dense_decode_step': (ctypes.c_int, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                               _vp, _vp, _vp, _vp, _vp]),
@@ -174,6 +175,11 @@ def seed_recompress_ws(st: seed_state, trunc_err=None, sweeps=None, workspace=No
     _check('seed_recompress_ws',
            _lib.seed_recompress_ws(ctypes.byref(st), _ptr(trunc_err), _ptr(sweeps), _ptr(workspace),
                                    int(workspace_bytes), _stream(stream)))
+
+
+def seed_recompress_noalloc(st: seed_state, trunc_err=None, sweeps=None, stream=None) -> None:
+    _check('seed_recompress_noalloc',
+           _lib.seed_recompress_noalloc(ctypes.byref(st), _ptr(trunc_err), _ptr(sweeps), _stream(stream)))
 
 
 def seed_materialize(st: seed_state, S_out, stream=None) -> None:

@@ -159,6 +159,24 @@ extern "C" int seed_recompress_ws(seed_state *st, float *trunc_err, int32_t *swe
   return c;
 }
 
+extern "C" int seed_recompress_noalloc(seed_state *st, float *trunc_err, int32_t *sweeps,
+                                       seed_stream_t stream) {
+  int c = check_state(st);
+  if (c) return c;
+  if (st->steps_since_compress > st->T) return SEED_ERR_CAPACITY;
+  if (st->n_heads == 0) { st->steps_since_compress = 0; return SEED_OK; }
+  const int rmax = rmax_of(st);
+  const int m_max = rmax + growth_of(st->variant) * st->steps_since_compress;
+  const int64_t need = (int64_t)st->n_heads * split_floats_per_head(m_max, rmax, st->d_v);
+  if (need > kNoAllocScratchFloats) return SEED_ERR_UNSUPPORTED_SHAPE;  // checked before any CUDA call
+  float *scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return SEED_ERR_CUDA;
+  c = cuda_status(launch_recompress_split(view_of(st), st->factor_dtype, trunc_err, sweeps, m_max, rmax,
+                                          scratch, st->n_heads, (cudaStream_t)stream));
+  if (c == SEED_OK) st->steps_since_compress = 0;
+  return c;
+}
+
 extern "C" int seed_recompress(seed_state *st, float *trunc_err, seed_stream_t stream) {
   return seed_recompress_ex(st, trunc_err, nullptr, stream);
 }

@@ -207,6 +207,9 @@ cudaError_t launch_recompress_split(const StateView &sv, int factor_dtype, float
                                     int32_t *sweeps, int m_max, int r_max, float *ws,
                                     int64_t chunk, cudaStream_t s);
 int64_t split_floats_per_head(int m_max, int r_max, int d_v);
+// Fixed device scratch of seed_recompress_noalloc: 64 MiB.
+constexpr int64_t kNoAllocScratchFloats = (int64_t)16 << 20;
+cudaError_t noalloc_scratch(float **ptr);
 cudaError_t launch_compress_dense(const StateView &sv, int factor_dtype, const float *S,
                                   float *trunc_err, cudaStream_t s);
 cudaError_t launch_materialize(const StateView &sv, int factor_dtype, float *S_out, int m_max,

@@ -23,6 +23,8 @@
 #include "recompress_core.cuh"
 #include "qr_registers.cuh"
 
+#include <mutex>
+
 namespace seedk {
 
 struct SplitLayout {
@@ -366,6 +368,31 @@ cudaError_t launch_recompress_split(const StateView &sv, int factor_dtype, float
     return sv.d_v == 64 ? launch_split_v<__nv_bfloat16, 64>(a, n, chunk, s)
                         : launch_split_v<__nv_bfloat16, 128>(a, n, chunk, s);
   return sv.d_v == 64 ? launch_split_v<float, 64>(a, n, chunk, s) : launch_split_v<float, 128>(a, n, chunk, s);
+}
+
+// ---- fixed scratch for seed_recompress_noalloc ---------------------------------------------
+// One array per device that loads the library; its address is looked up once
+// per device and cached.
+static __device__ __align__(256) float g_recompress_scratch[kNoAllocScratchFloats];
+
+cudaError_t noalloc_scratch(float **ptr) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static float *cache[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < kMaxDevices && cache[dev]) {
+    *ptr = cache[dev];
+    return cudaSuccess;
+  }
+  void *p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_recompress_scratch);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev] = static_cast<float *>(p);
+  *ptr = static_cast<float *>(p);
+  return cudaSuccess;
 }
 
 }  // namespace seedk

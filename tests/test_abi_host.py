@@ -175,3 +175,18 @@ def test_recompress_ws_rejects_on_host():
     empty = make_state(n_heads=0, a=None, U=None, W=None, scale=None, vbar=None, steps_since_compress=5)
     assert f(ctypes.byref(empty), None, None, None, 0, None) == R.SEED_OK
     assert empty.steps_since_compress == 0
+
+
+def test_recompress_noalloc_rejects_oversize_before_cuda():
+    f = R._lib.seed_recompress_noalloc
+    per_head = _ws_floats(48, 32, 128, 128)
+    limit = 16 << 20                                    # 64 MiB of fp32 scratch
+    n_over = limit // per_head + 1
+    st = make_state(n_heads=n_over, steps_since_compress=16)
+    assert f(ctypes.byref(st), None, None, None) == R.SEED_ERR_UNSUPPORTED_SHAPE
+    assert st.steps_since_compress == 16
+    st.steps_since_compress = 17
+    assert f(ctypes.byref(st), None, None, None) == R.SEED_ERR_CAPACITY
+    empty = make_state(n_heads=0, a=None, U=None, W=None, scale=None, vbar=None, steps_since_compress=3)
+    assert f(ctypes.byref(empty), None, None, None) == R.SEED_OK
+    assert empty.steps_since_compress == 0
