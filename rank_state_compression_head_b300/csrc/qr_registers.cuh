@@ -16,9 +16,11 @@
 // (H_j e_l = e_l for j > l), so every column starts from e_l and applies its
 // reflectors from H_l down to H_0 on its own, with no barrier.
 //
-// The reflector is the one of householder_qr (formed from the column scaled by
-// its largest magnitude; zero below the smallest normal float), so the result
-// differs from householder_qr / form_q only in summation order.
+// The reflector is the one of householder_qr (zero below the smallest normal
+// float); its norm is taken unscaled unless the sum of squares nears the ends
+// of the fp32 range, where it is scaled by the column's largest magnitude as in
+// householder_qr.  The result differs from householder_qr / form_q only in
+// rounding.
 #pragma once
 
 #include "common.cuh"
@@ -61,30 +63,43 @@ __device__ inline void rr_reflector_warp(RRCol &c, bool owner, int p, int j, int
   float a[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) a[e] = e < rpl ? vj[lane * rpl + e] : 0.f;
-  float amax = 0.f;
-#pragma unroll
-  for (int e = 0; e < 4; ++e)
-    if (e < rpl && lane * rpl + e >= j) amax = fmaxf(amax, fabsf(a[e]));
-  amax = warp_max(amax);
   const float alpha = vj[j];
   float tj = 0.f, beta = alpha, sc = 0.f;
-  if (amax >= FLT_MIN) {
-    const float inv = 1.f / amax;
-    float ss = 0.f;
+  // The sum of squares below row j in one reduction; only where it leaves
+  // [1e-30, 1e30] (entries near the ends of the fp32 range) is it formed again
+  // from the column scaled by its largest magnitude.
+  float ss = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float xs = (e < rpl && lane * rpl + e > j) ? a[e] * inv : 0.f;
-      ss = fmaf(xs, xs, ss);
+  for (int e = 0; e < 4; ++e) {
+    const float x = (e < rpl && lane * rpl + e > j) ? a[e] : 0.f;
+    ss = fmaf(x, x, ss);
+  }
+  ss = warp_sum(ss);
+  float amax = 1.f;
+  if (!(ss >= 1e-30f && ss <= 1e30f)) {
+    amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < rpl && lane * rpl + e >= j) amax = fmaxf(amax, fabsf(a[e]));
+    amax = warp_max(amax);
+    ss = 0.f;
+    if (amax >= FLT_MIN) {
+      const float inv = 1.f / amax;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float xs = (e < rpl && lane * rpl + e > j) ? a[e] * inv : 0.f;
+        ss = fmaf(xs, xs, ss);
+      }
+      ss = warp_sum(ss);
     }
-    ss = warp_sum(ss);
-    if (ss > 0.f) {
-      const float as = alpha * inv;
-      const float nrm = sqrtf(fmaf(as, as, ss));
-      const float bs = as >= 0.f ? -nrm : nrm;
-      tj = (bs - as) / bs;
-      sc = 1.f / ((as - bs) * amax);  // v_i = x_i / (alpha - beta), |v_i| <= 1
-      beta = bs * amax;
-    }
+  }
+  if (ss > 0.f && amax >= FLT_MIN) {
+    const float as = alpha / amax;
+    const float nrm = sqrtf(fmaf(as, as, ss));
+    const float bs = as >= 0.f ? -nrm : nrm;
+    tj = (bs - as) / bs;
+    sc = 1.f / ((as - bs) * amax);  // v_i = x_i / (alpha - beta), |v_i| <= 1
+    beta = bs * amax;
   }
   __syncwarp();
 #pragma unroll

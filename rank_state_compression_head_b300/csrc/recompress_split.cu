@@ -22,6 +22,7 @@
 // r the largest rank.
 #include "recompress_core.cuh"
 #include "qr_registers.cuh"
+#include "svd_warp.cuh"
 
 #include <mutex>
 
@@ -46,6 +47,7 @@ struct SplitArgs {
   StateView sv;
   float *ws;
   int head0;     // first head of this chunk; workspace slot b serves head head0 + b
+  int n_group;   // heads in this chunk
   int m_max, r_max;
   float *trunc_err;
   int32_t *sweeps;
@@ -168,84 +170,79 @@ __global__ void __maxnreg__(80) qr_phase(const SplitArgs p) {
   }
 }
 
-// ---- phase 2: SVD of the core ------------------------------------------------------------
-template <typename TF, int DV>
-__global__ void __launch_bounds__(kSplitThreads, 8) svd_phase(const SplitArgs p) {
+// ---- phase 2: SVD of the core, one warp per head (svd_warp.cuh) ---------------------------
+// MR: rows and columns of the core held per lane (m_max rounded up to 16).
+template <typename TF, int DV, int MR>
+__global__ void __launch_bounds__(32 * kSvdWarps) svd_phase(const SplitArgs p) {
   constexpr int DK = kDK;
-  constexpr int NT = kSplitThreads;
+  using SW = SvdWarpSmem<MR>;
   extern __shared__ __align__(16) float smem[];
-  const int h = p.head0 + blockIdx.x;
-  const int tid = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kSvdWarps + warp;
+  if (b >= p.n_group) return;
+  const int h = p.head0 + b;
   const StateView &sv = p.sv;
   int r, m;
   if (!split_head_ok(sv, h, p.m_max, r, m)) {  // rank table disagrees with r_max: touch nothing
-    if (tid == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
+    if (lane == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
     return;
   }
+  float *sw = smem + warp * SW::FLOATS;
+  float *T = sw + SW::T_OFF;
   const SplitLayout L(p.m_max, p.r_max, DK, DV);
-  float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
-  const JacobiGeom g = seat_geom(m, NT);
-  const int cs = g.cs;
-  const int m4 = (m + 3) & ~3;
-  const int up = (p.m_max + 3) & ~3;
-  const int buf = (p.m_max + 1) * p.cs_alloc;
-  float *Kb = smem, *Tb = smem + buf;
-  float *sig2 = Tb + buf, *inv = sig2 + up, *vn = inv + up;
-  int *order = reinterpret_cast<int *>(vn + up);
-  int *piv = order + up;
-  float *red = reinterpret_cast<float *>(piv + up);
-
-  // core, rows m..m4-1 zero, scaled by a power of two to a largest entry in [1/2, 1)
+  float *ws = p.ws + (int64_t)b * L.per_head;
   const float *Kw = ws + L.k;
-  for (int idx = tid; idx < m * m4; idx += NT) {
-    const int j = idx / m4, i = idx % m4;
-    Kb[j * cs + i] = i < m ? Kw[j * m + i] : 0.f;
-  }
-  __syncthreads();
+
+  // core through the square (coalesced reads), scaled by a power of two to a
+  // largest entry in [1/2, 1); lane l takes columns l and l + 32
   float kmax = 0.f;
-  for (int idx = tid; idx < m * m4; idx += NT) kmax = fmaxf(kmax, fabsf(Kb[(idx / m4) * cs + idx % m4]));
+  for (int idx = lane; idx < m * m; idx += 32) {
+    const float x = Kw[idx];  // column idx / m, row idx % m
+    T[(idx / m) * SW::TP + idx % m] = x;
+    kmax = fmaxf(kmax, fabsf(x));
+  }
   kmax = warp_max(kmax);
-  if ((tid & 31) == 0) red[tid >> 5] = kmax;
-  __syncthreads();
-  kmax = 0.f;
-  for (int w = 0; w < NT / 32; ++w) kmax = fmaxf(kmax, red[w]);
   int kexp = 0;
   if (kmax > 0.f) frexpf(kmax, &kexp);
   const float kscale = ldexpf(1.f, -kexp), kunscale = ldexpf(1.f, kexp);
-  for (int idx = tid; idx < m * m4; idx += NT) Kb[(idx / m4) * cs + idx % m4] *= kscale;
-  __syncthreads();
+  __syncwarp();
+  float c0[MR], c1[MR];
+#pragma unroll
+  for (int rr = 0; rr < MR; ++rr) {
+    c0[rr] = (lane < m && rr < m) ? T[lane * SW::TP + rr] * kscale : 0.f;
+    c1[rr] = (MR > 32 && lane + 32 < m && rr < m) ? T[(lane + 32) * SW::TP + rr] * kscale : 0.f;
+  }
+  __syncwarp();
   // bf16 factors: 1e-4 (their own rounding is 2^-9); fp32: a few units of rounding
   const float tol = sizeof(TF) == 2 ? 1e-4f : (float)(m > 16 ? m : 16) * FLT_EPSILON;
-  float *F;
-  const int sweeps = core_factor<NT>(Kb, Tb, m, g, tol, piv, vn, sig2, inv, order, red, &F);
-  if (tid == 0) {
+  const int sweeps = svd_warp_core<MR>(c0, c1, m, tol, sw);
+  const float *sig2 = sw + SW::S_OFF, *inv = sw + SW::I_OFF;
+  const int *order = reinterpret_cast<const int *>(sw + SW::O_OFF);
+  const int *piv = reinterpret_cast<const int *>(sw + SW::P_OFF);
+  if (lane == 0) {
     float e = 0.f;
     for (int k = r; k < m; ++k) e += sig2[order[k]];
     if (p.trunc_err) p.trunc_err[h] = sqrtf(e) * kunscale;
     if (p.sweeps) p.sweeps[h] = sweeps;
     if (sv.status) sv.status[h] = sweeps < 0 ? SEED_ERR_NOT_CONVERGED : SEED_OK;
   }
-  // the unscaled core into the free buffer; y_k[piv[i]] = (R^T J)_{i,order[k]} / sigma_k
-  // and z_k = K y_k, rows m..m4-1 zero
-  float *K0 = F == Kb ? Tb : Kb;
-  for (int idx = tid; idx < m * m; idx += NT) K0[(idx / m) * cs + idx % m] = Kw[idx];
-  __syncthreads();
+  // kept right singular vectors y_k[piv[s]] = (R^T J)_{s, order[k]} / sigma_k and
+  // z_k = K y_k (unscaled K, column piv[s] contiguous in the workspace); rows
+  // m..m4-1 zero
   const int rk = r < m ? r : m;
+  const int m4 = (m + 3) & ~3;
   float *Z = ws + L.z, *Y = ws + L.y;
-  for (int idx = tid; idx < rk * m4; idx += NT) {
-    const int k = idx / m4, l = idx % m4;
+  for (int k = 0; k < rk; ++k) {
     const int col = order[k];
-    const float *f = F + col * cs;
-    float z = 0.f;
-    if (l < m) {
+    const float ik = inv[col];
+    const float *f = T + col * SW::TP;
+    for (int s = lane; s < m4; s += 32) Y[k * L.m4 + (s < m ? piv[s] : s)] = s < m ? f[s] * ik : 0.f;
+    for (int l = lane; l < m4; l += 32) {
       float acc = 0.f;
-      for (int i = 0; i < m; ++i) acc = fmaf(K0[piv[i] * cs + l], f[i], acc);
-      z = acc * inv[col];
-      Y[k * L.m4 + piv[l]] = f[l] * inv[col];
-    } else {
-      Y[k * L.m4 + l] = 0.f;
+      if (l < m)
+        for (int s = 0; s < m; ++s) acc = fmaf(Kw[piv[s] * m + l], f[s], acc);
+      Z[k * L.m4 + l] = l < m ? acc * ik : 0.f;
     }
-    Z[k * L.m4 + l] = z;
   }
 }
 
@@ -325,16 +322,15 @@ int64_t split_floats_per_head(int m_max, int r_max, int d_v) {
   return SplitLayout(m_max, r_max, kDK, d_v).per_head;
 }
 
-template <int VAR, typename TF, int DV>
+template <int VAR, typename TF, int DV, int MR>
 static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaStream_t s) {
   const int up = (a.m_max + 3) & ~3;
   const int qr_bytes = (a.m_max * (kDK + DV) + 4 * up + 2 * a.m_max * a.m_max) * 4;
   const int qr_threads = a.m_max > 0 ? qr_team_stride(a.m_max) * 2 : 32;
-  a.cs_alloc = seat_cs_alloc(a.m_max, kSplitThreads);
-  const int svd_bytes = (2 * (a.m_max + 1) * a.cs_alloc + 5 * up + 8) * 4;
+  const int svd_bytes = kSvdWarps * SvdWarpSmem<MR>::FLOATS * 4;
   const int rb_bytes = (a.r_max * up > 0 ? a.r_max * up : 4) * 4;
   auto k1 = qr_phase<VAR, TF, DV>;
-  auto k2 = svd_phase<TF, DV>;
+  auto k2 = svd_phase<TF, DV, MR>;
   auto k3 = rebuild_phase<VAR, TF, DV>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, qr_bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, svd_bytes);
@@ -343,8 +339,9 @@ static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaS
   for (int64_t h0 = 0; h0 < n_heads; h0 += chunk) {
     const int n = (int)(n_heads - h0 < chunk ? n_heads - h0 : chunk);
     a.head0 = (int)h0;
+    a.n_group = n;
     k1<<<n, qr_threads, qr_bytes, s>>>(a);
-    k2<<<n, kSplitThreads, svd_bytes, s>>>(a);
+    k2<<<(n + kSvdWarps - 1) / kSvdWarps, 32 * kSvdWarps, svd_bytes, s>>>(a);
     k3<<<dim3(n, 2), kSplitThreads, rb_bytes, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -352,17 +349,25 @@ static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaS
   return cudaSuccess;
 }
 
+template <int VAR, typename TF, int DV>
+static cudaError_t launch_split_m(const SplitArgs &a, int n, int64_t chunk, cudaStream_t s) {
+  if (a.m_max <= 16) return launch_split_t<VAR, TF, DV, 16>(a, n, chunk, s);
+  if (a.m_max <= 32) return launch_split_t<VAR, TF, DV, 32>(a, n, chunk, s);
+  if (a.m_max <= 48) return launch_split_t<VAR, TF, DV, 48>(a, n, chunk, s);
+  return launch_split_t<VAR, TF, DV, 64>(a, n, chunk, s);
+}
+
 template <typename TF, int DV>
 static cudaError_t launch_split_v(const SplitArgs &a, int n, int64_t chunk, cudaStream_t s) {
   // Only the scale layout differs between variants here.
-  if (a.sv.variant == SEED_KDA) return launch_split_t<SEED_KDA, TF, DV>(a, n, chunk, s);
-  return launch_split_t<SEED_GDN, TF, DV>(a, n, chunk, s);
+  if (a.sv.variant == SEED_KDA) return launch_split_m<SEED_KDA, TF, DV>(a, n, chunk, s);
+  return launch_split_m<SEED_GDN, TF, DV>(a, n, chunk, s);
 }
 
 cudaError_t launch_recompress_split(const StateView &sv, int factor_dtype, float *trunc_err,
                                     int32_t *sweeps, int m_max, int r_max, float *ws,
                                     int64_t chunk, cudaStream_t s) {
-  SplitArgs a{sv, ws, 0, m_max, r_max, trunc_err, sweeps, 0};
+  SplitArgs a{sv, ws, 0, 0, m_max, r_max, trunc_err, sweeps, 0};
   const int n = sv.n_heads;
   if (factor_dtype == SEED_BF16)
     return sv.d_v == 64 ? launch_split_v<__nv_bfloat16, 64>(a, n, chunk, s)
