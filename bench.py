@@ -210,26 +210,37 @@ def measured_peaks():
     return dict(hbm_gbs=6400.0, src='fallback')
 
 
-def profiled_traffic(kernel_tag: str):
-    """Per-launch DRAM bytes from the committed ncu summary of this kernel, if its source is unchanged."""
-    path = os.path.join(ROOT, 'profiles', f'ncu_{kernel_tag}.md')
-    src = os.path.join(ROOT, 'rank_state_compression_head_b300', 'csrc', 'decode.cu')
+# Sources whose compiled kernels a committed ncu summary describes; a summary
+# counts only while the hash of these files is the one it records.
+PROFILE_SOURCES = {
+    'decode': ['decode_mma.cu', 'common.cuh'],
+    'recompress': ['recompress_split.cu', 'qr_registers.cuh', 'svd_warp.cuh', 'recompress_core.cuh',
+                   'common.cuh'],
+}
+
+
+def source_hash(kind: str) -> str:
+    h = hashlib.sha256()
+    for f in PROFILE_SOURCES[kind]:
+        with open(os.path.join(ROOT, 'rank_state_compression_head_b300', 'csrc', f), 'rb') as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_record(kind: str, workload: str):
+    """Key/value lines of profiles/ncu_<kind>_<workload>.md if its sources are unchanged, else None."""
+    path = os.path.join(ROOT, 'profiles', f'ncu_{kind}_{workload}.md')
     if not os.path.exists(path):
         return None
-    with open(src, 'rb') as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
     rec = {}
     with open(path) as f:
         for line in f:
             if ':' in line and line.startswith('- '):
                 k, v = line[2:].split(':', 1)
                 rec[k.strip()] = v.strip()
-    if rec.get('source_sha256_16') != sha:
+    if rec.get('source_sha256_16') != source_hash(kind):
         return None
-    try:
-        return float(rec['traffic_bytes_per_launch'])
-    except (KeyError, ValueError):
-        return None
+    return rec
 
 
 def run_gpu(args, w):
@@ -367,16 +378,33 @@ def run_gpu(args, w):
     fp32_peak = 148 * 128 * 2 * (clocks['sm_max_mhz'] or 2032) * 1e6 / 1e12  # TFLOP/s, FFMA issue rate
     rec_tflops = rec_flops / (rec_avg_ms / 1e3) / 1e12 if rec_ms else None
     dec_total, rec_total = sum(dec_ms), sum(rec_ms)
-    traffic = profiled_traffic(f'decode_{w.variant}_{w.name}')
-    roof_dec = dict(kernel='decode_kernel', bound='hbm', achieved=round(dec_gbs, 1),
+    # DRAM bytes per launch from the committed ncu captures: the decode capture is
+    # one launch at a known column count, scaled to this run's mean algorithmic
+    # bytes; the recompression capture covers its three kernels at m = r + growth*T.
+    traffic, rec_traffic = None, None
+    prof = profiled_record('decode', w.name)
+    if prof is not None:
+        try:
+            traffic = round(float(prof['traffic_bytes_per_launch']) * (bytes_decode / K)
+                            / float(prof['algorithmic_bytes_per_launch']))
+        except (KeyError, ValueError, ZeroDivisionError):
+            traffic = None
+    prof = profiled_record('recompress', w.name)
+    if prof is not None and run.ws is not None:
+        try:
+            rec_traffic = round(float(prof['traffic_bytes_per_launch']))
+        except (KeyError, ValueError):
+            rec_traffic = None
+    roof_dec = dict(kernel='decode_mma_kernel' if w.factor_dtype == 'bf16' else 'decode_kernel', bound='hbm',
+                    achieved=round(dec_gbs, 1),
                     peak=peaks['hbm_gbs'], unit='GB/s', frac=round(dec_gbs / peaks['hbm_gbs'], 4),
                     traffic=traffic, peak_src=peaks['src'],
                     algorithmic_bytes_per_launch=round(bytes_decode / K),
                     avg_launch_us=round(dec_avg_ms * 1e3, 3))
-    rec_kernels = 'qr_phase + svd_phase + rebuild_phase' if run.ws is not None else 'compress_kernel'
+    rec_kernels = 'qr_phase + svd_phase + rebuild_phase' if run.ws is not None else 'recompress_kernel'
     roof_rec = dict(kernel=f'{rec_kernels} (recompress)', bound='alu', achieved=rec_tflops and round(rec_tflops, 3),
                     peak=round(fp32_peak, 1), unit='TFLOP/s',
-                    frac=rec_tflops and round(rec_tflops / fp32_peak, 4), traffic=None,
+                    frac=rec_tflops and round(rec_tflops / fp32_peak, 4), traffic=rec_traffic,
                     peak_src='148 SMs x 128 FP32 lanes x 2 FLOP x max SM clock',
                     algorithmic_flops_per_launch=round(rec_flops), avg_launch_us=round(rec_avg_ms * 1e3, 1),
                     jacobi_sweeps_mean=float(np.mean(sw)), jacobi_sweeps_max=int(np.max(sw)))
