@@ -60,13 +60,17 @@ def recompress_flops(d_k: int, d_v: int, m: int, r: int, sweeps: float) -> float
 
     Householder QR of a p x m panel: 2 p m^2 - 2 m^3 / 3 (both factors);
     forming Q explicitly: the same again; core K = R_a R_b^T: 2 m^3 / 3;
-    one Jacobi sweep: m (m - 1) / 2 pairs, each 3 dot products and two
-    rotated column pairs of length m (6 m + 6 m + 6 m); rebuild of the r kept
+    pivoted QR of the m x m core: 4 m^3 / 3; one Jacobi sweep: m (m - 1) / 2
+    pairs, each three dot products of length m (6 m) and one rotation of a
+    column pair (6 m), counted for every pair of every sweep; the kept
+    directions through the core, K y_k: 2 m^2 r; rebuild of the r kept
     columns: 2 (d_k + d_v) m r.
     """
     qr = sum(2 * p * m * m - 2 * m ** 3 / 3 for p in (d_k, d_v))
     formq = qr
     core = 2 * m ** 3 / 3
-    jac = sweeps * (m * (m - 1) / 2) * 18 * m
+    qrcp = 4 * m ** 3 / 3
+    jac = sweeps * (m * (m - 1) / 2) * 12 * m
+    kept = 2 * m * m * r
     rebuild = 2 * (d_k + d_v) * m * r
-    return qr + formq + core + jac + rebuild
+    return qr + formq + core + qrcp + jac + kept + rebuild

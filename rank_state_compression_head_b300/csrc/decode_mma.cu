@@ -102,7 +102,7 @@ __device__ static inline uint32_t split_bf16x2(float2 v, int part) {
 }
 
 template <int VAR, int DV, int MAXC, int NS>
-__global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArgs p) {
+__global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const DecodeArgs p) {
   using TF = __nv_bfloat16;
   constexpr int DK = kDK;
   constexpr int NT = kMmaThreads;
@@ -423,24 +423,23 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeArg
 }
 
 // One stage and one head per CTA (grid = heads): several CTAs per SM keep
-// several heads' loads in flight.  With NS > 1 the same kernel runs
-// persistently over a ring of NS stages.
+// several heads' loads in flight.  (The same kernel can run persistently over a
+// ring of NS > 1 stages; with two 64-column stages only two CTAs fit per SM and
+// the serving-scale decode ran at 0.32 of the copy bandwidth against 0.55 here.)
 template <int VAR, int DV, int MAXC>
 static cudaError_t launch_mma_t(const DecodeArgs &a, cudaStream_t s) {
   constexpr int NS = 1;
   using L = MmaSmem<VAR, DV, MAXC, NS>;
   auto kern = decode_mma_kernel<VAR, DV, MAXC, NS>;
-  static int per_sm = 0;
-  if (per_sm == 0) {
+  static bool ready = false;
+  if (!ready) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+    if (e == cudaSuccess)  // all of the unified L1/shared capacity as shared memory: more heads per SM
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMmaThreads, L::BYTES);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
+    ready = true;
   }
-  int grid = NS == 1 ? a.sv.n_heads : sm_count() * per_sm;
-  if (grid > a.sv.n_heads) grid = a.sv.n_heads;
-  kern<<<grid, kMmaThreads, L::BYTES, s>>>(a);
+  kern<<<a.sv.n_heads, kMmaThreads, L::BYTES, s>>>(a);
   return cudaGetLastError();
 }
 
