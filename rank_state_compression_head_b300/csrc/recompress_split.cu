@@ -193,12 +193,13 @@ __global__ void __launch_bounds__(32 * kSvdWarps) svd_phase(const SplitArgs p) {
   float *ws = p.ws + (int64_t)b * L.per_head;
   const float *Kw = ws + L.k;
 
-  // core through the square (coalesced reads), scaled by a power of two to a
-  // largest entry in [1/2, 1); lane l takes columns l and l + 32
+  // core into the square (coalesced reads; rows m..MR-1 zero), scaled by a power
+  // of two to a largest entry in [1/2, 1)
   float kmax = 0.f;
-  for (int idx = lane; idx < m * m; idx += 32) {
-    const float x = Kw[idx];  // column idx / m, row idx % m
-    T[(idx / m) * SW::TP + idx % m] = x;
+  for (int idx = lane; idx < m * MR; idx += 32) {
+    const int c = idx / MR, rr = idx % MR;
+    const float x = rr < m ? Kw[c * m + rr] : 0.f;  // column c, row rr
+    T[c * SW::TP + rr] = x;
     kmax = fmaxf(kmax, fabsf(x));
   }
   kmax = warp_max(kmax);
@@ -206,16 +207,11 @@ __global__ void __launch_bounds__(32 * kSvdWarps) svd_phase(const SplitArgs p) {
   if (kmax > 0.f) frexpf(kmax, &kexp);
   const float kscale = ldexpf(1.f, -kexp), kunscale = ldexpf(1.f, kexp);
   __syncwarp();
-  float c0[MR], c1[MR];
-#pragma unroll
-  for (int rr = 0; rr < MR; ++rr) {
-    c0[rr] = (lane < m && rr < m) ? T[lane * SW::TP + rr] * kscale : 0.f;
-    c1[rr] = (MR > 32 && lane + 32 < m && rr < m) ? T[(lane + 32) * SW::TP + rr] * kscale : 0.f;
-  }
+  for (int idx = lane; idx < m * MR; idx += 32) T[(idx / MR) * SW::TP + idx % MR] *= kscale;
   __syncwarp();
   // bf16 factors: 1e-4 (their own rounding is 2^-9); fp32: a few units of rounding
   const float tol = sizeof(TF) == 2 ? 1e-4f : (float)(m > 16 ? m : 16) * FLT_EPSILON;
-  const int sweeps = svd_warp_core<MR>(c0, c1, m, tol, sw);
+  const int sweeps = svd_warp_core<MR>(m, tol, sw);
   const float *sig2 = sw + SW::S_OFF, *inv = sw + SW::I_OFF;
   const int *order = reinterpret_cast<const int *>(sw + SW::O_OFF);
   const int *piv = reinterpret_cast<const int *>(sw + SW::P_OFF);

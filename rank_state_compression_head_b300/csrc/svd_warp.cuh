@@ -3,13 +3,14 @@
 // columns of R^T (the algorithm of core_factor in recompress_core.cuh, laid
 // out for a warp instead of a CTA, so that no block barrier is needed).
 //
-// Pivoted QR: lane l holds columns l and l + 32 of K (all rows, in
-// registers).  Each step the warp picks the remaining column of largest
-// trailing norm (shuffle argmax, ties to the lower index), its owner lays it
-// out in a shared row, the 32 lanes form the reflector there (scaled by the
-// column's largest magnitude, as householder_qr), and every lane applies it to
-// its remaining columns, refreshing their trailing norms.  Columns keep their
-// lanes; only the pivot order is recorded.
+// Pivoted QR: the core sits in the warp's shared square, column c at
+// c * TP (TP = MR + 4: the 16-byte chunks of eight consecutive columns fall in
+// distinct bank groups); lane l looks after columns l and l + 32.  Each step
+// the warp picks the remaining column of largest trailing norm (shuffle argmax,
+// ties to the lower index), the 32 lanes form the reflector from it (norm in one
+// reduction, max-scaled near the fp32 range ends, as householder_qr), and every
+// lane applies it to its remaining columns with 16-byte loads, refreshing their
+// trailing norms.  Columns stay in place; only the pivot order is recorded.
 //
 // Jacobi: lane i (i < P = n'/2) holds two seats in registers, A and B:
 // lane 0 has seat n'-1 in A and the fixed seat 0 in B, lane i >= 1 has seat i
@@ -25,11 +26,12 @@ namespace seedk {
 
 constexpr int kSvdWarps = 2;  // heads (warps) per CTA
 
-// Per-warp shared layout (floats): a row-pitch-(MR+1) square for transposes,
-// the reflector row, sigma^2, 1/sigma, the column order and the pivots.
+// Per-warp shared layout (floats): the square (pitch MR + 4) that holds the
+// core, then R^T's seats' results, the reflector row, sigma^2, 1/sigma, the
+// column order and the pivots.
 template <int MR>
 struct SvdWarpSmem {
-  static constexpr int TP = MR + 1;
+  static constexpr int TP = MR + 4;
   static constexpr int T_OFF = 0;
   static constexpr int V_OFF = (MR * TP + 3) & ~3;
   static constexpr int S_OFF = V_OFF + MR;
@@ -39,30 +41,41 @@ struct SvdWarpSmem {
   static constexpr int FLOATS = P_OFF + MR;
 };
 
-// One warp: pivoted QR of the scaled core (columns c0 = K[:, lane], c1 =
-// K[:, lane + 32]), then Jacobi on R^T.  Leaves in the warp's shared square F
-// (row pitch TP) the columns of R^T J by seat (F[seat * TP + s]), sig2/inv by
-// seat, order, piv.  Returns the sweeps (or -1).
+// One warp: pivoted QR of the scaled core held in the square T (column c at
+// T[c * TP], rows m..MR-1 zero), then Jacobi on R^T.  Leaves in T the columns
+// of R^T J by seat (T[seat * TP + s]), sig2/inv by seat, order, piv.  Returns
+// the sweeps (or -1).
 template <int MR>
-__device__ int svd_warp_core(float (&c0)[MR], float (&c1)[MR], int m, float tol, float *sw) {
+__device__ int svd_warp_core(int m, float tol, float *sw) {
   using L = SvdWarpSmem<MR>;
   constexpr bool TWO = MR > 32;
   constexpr int RPL = (MR + 31) / 32;  // rows per lane in the reflector
+  constexpr int TP = L::TP;
   const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
   float *T = sw + L::T_OFF, *vrow = sw + L::V_OFF, *sig2 = sw + L::S_OFF, *inv = sw + L::I_OFF;
   int *order = reinterpret_cast<int *>(sw + L::O_OFF);
   int *piv = reinterpret_cast<int *>(sw + L::P_OFF);
+  const float4 *v4 = reinterpret_cast<const float4 *>(vrow);
 
   // ---- pivoted QR ------------------------------------------------------------------------
-  float vn0 = 0.f, vn1 = 0.f;
+  auto colnorm = [&](int c, int from) {  // sum of squares of rows >= from of column c
+    const float4 *x4 = reinterpret_cast<const float4 *>(T + c * TP);
+    float a = 0.f;
 #pragma unroll
-  for (int r = 0; r < MR; ++r) {
-    vn0 = fmaf(c0[r], c0[r], vn0);
-    if (TWO) vn1 = fmaf(c1[r], c1[r], vn1);
-  }
+    for (int q = 0; q < MR / 4; ++q) {
+      const float4 x = x4[q];
+      const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float y = 4 * q + e >= from ? xs[e] : 0.f;
+        a = fmaf(y, y, a);
+      }
+    }
+    return a;
+  };
   bool done0 = lane >= m, done1 = !TWO || lane + 32 >= m;
-  int s0 = 0, s1 = 0;  // step at which my column was chosen (its column index in R)
+  float vn0 = done0 ? 0.f : colnorm(lane, 0), vn1 = done1 ? 0.f : colnorm(lane + 32, 0);
   for (int j = 0; j < m; ++j) {
     float best = -1.f;
     int bi = 1 << 20;
@@ -74,17 +87,12 @@ __device__ int svd_warp_core(float (&c0)[MR], float (&c1)[MR], int m, float tol,
       const int oi = __shfl_xor_sync(full, bi, o);
       if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
     }
-    const int pc = bi, owner = pc & 31;
-    const bool hi = pc >= 32;
-    if (lane == owner) {
-#pragma unroll
-      for (int r = 0; r < MR; ++r) vrow[r] = hi ? c1[r] : c0[r];
-    }
-    __syncwarp();
+    const int pc = bi;
+    float *cp = T + pc * TP;
     float a[RPL];
 #pragma unroll
-    for (int e = 0; e < RPL; ++e) a[e] = lane + 32 * e < MR ? vrow[lane + 32 * e] : 0.f;
-    const float alpha = vrow[j];
+    for (int e = 0; e < RPL; ++e) a[e] = lane + 32 * e < MR ? cp[lane + 32 * e] : 0.f;
+    const float alpha = cp[j];
     float tj = 0.f, beta = alpha, sc = 0.f;
     // one reduction for the norm unless it nears the ends of the fp32 range
     // (then scaled by the largest magnitude, as householder_qr)
@@ -122,76 +130,65 @@ __device__ int svd_warp_core(float (&c0)[MR], float (&c1)[MR], int m, float tol,
       beta = bs * amax;
     }
     __syncwarp();
+    // v_j into the reflector row; the chosen column becomes column j of R (rows
+    // above j were finished by the earlier steps, row j is beta, rows below zero)
 #pragma unroll
     for (int e = 0; e < RPL; ++e) {
       const int r = lane + 32 * e;
-      if (r < MR) vrow[r] = r < j ? 0.f : r == j ? 1.f : a[e] * sc;
+      if (r < MR) {
+        vrow[r] = r < j ? 0.f : r == j ? 1.f : a[e] * sc;
+        if (r >= j) cp[r] = r == j ? beta : 0.f;
+      }
     }
     if (lane == 0) piv[j] = pc;
-    __syncwarp();
-    // the chosen column becomes column j of R (rows above j were finished by
-    // the earlier steps, row j is beta, rows below are zero)
-    if (lane == owner) {
-#pragma unroll
-      for (int r = 0; r < MR; ++r) {
-        if (hi) { if (r == j) c1[r] = beta; else if (r > j) c1[r] = 0.f; }
-        else { if (r == j) c0[r] = beta; else if (r > j) c0[r] = 0.f; }
-      }
-      if (hi) { done1 = true; s1 = j; } else { done0 = true; s0 = j; }
+    if (lane == (pc & 31)) {
+      if (pc >= 32) done1 = true;
+      else done0 = true;
     }
+    __syncwarp();
     // the remaining columns: a -= tau (v . a) v, then their norms below row j
-    const float4 *v4 = reinterpret_cast<const float4 *>(vrow);
-    if (!done0 || !done1) {
-      float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+    for (int h = 0; h < (TWO ? 2 : 1); ++h) {
+      if (h == 0 ? done0 : done1) continue;
+      float4 *x4 = reinterpret_cast<float4 *>(T + (lane + 32 * h) * TP);
+      float d = 0.f;
 #pragma unroll
       for (int q = 0; q < MR / 4; ++q) {
-        const float4 v = v4[q];
-        d0 = fmaf(v.x, c0[4 * q], fmaf(v.y, c0[4 * q + 1], fmaf(v.z, c0[4 * q + 2], fmaf(v.w, c0[4 * q + 3], d0))));
-        if (TWO) d1 = fmaf(v.x, c1[4 * q], fmaf(v.y, c1[4 * q + 1], fmaf(v.z, c1[4 * q + 2], fmaf(v.w, c1[4 * q + 3], d1))));
+        const float4 v = v4[q], x = x4[q];
+        d = fmaf(v.x, x.x, fmaf(v.y, x.y, fmaf(v.z, x.z, fmaf(v.w, x.w, d))));
       }
-      const float t0 = done0 ? 0.f : tj * d0, t1 = done1 ? 0.f : tj * d1;
-      float n0 = 0.f, n1 = 0.f;
+      const float t = tj * d;
+      float nrm = 0.f;
 #pragma unroll
       for (int q = 0; q < MR / 4; ++q) {
         const float4 v = v4[q];
-        const float vv[4] = {v.x, v.y, v.z, v.w};
+        float4 x = x4[q];
+        x.x = fmaf(-t, v.x, x.x); x.y = fmaf(-t, v.y, x.y); x.z = fmaf(-t, v.z, x.z); x.w = fmaf(-t, v.w, x.w);
+        x4[q] = x;
+        const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int r = 4 * q + e;
-          c0[r] = fmaf(-t0, vv[e], c0[r]);
-          const float y0 = r > j ? c0[r] : 0.f;
-          n0 = fmaf(y0, y0, n0);
-          if (TWO) {
-            c1[r] = fmaf(-t1, vv[e], c1[r]);
-            const float y1 = r > j ? c1[r] : 0.f;
-            n1 = fmaf(y1, y1, n1);
-          }
+          const float y = 4 * q + e > j ? xs[e] : 0.f;
+          nrm = fmaf(y, y, nrm);
         }
       }
-      if (!done0) vn0 = n0;
-      if (!done1) vn1 = n1;
+      if (h == 0) vn0 = nrm;
+      else vn1 = nrm;
     }
     __syncwarp();
   }
 
-  // ---- R^T to the seats of the Jacobi: seat i = row i of R --------------------------------
-  if (lane < m) {
-#pragma unroll
-    for (int r = 0; r < MR; ++r) T[s0 * L::TP + r] = c0[r];
-  }
-  if (TWO && lane + 32 < m) {
-#pragma unroll
-    for (int r = 0; r < MR; ++r) T[s1 * L::TP + r] = c1[r];
-  }
-  __syncwarp();
+  // ---- R^T to the seats of the Jacobi: seat i = row i of R = T[s * TP + i] over s ----------
+  // (R column s is the column chosen at step s: T[piv[s] * TP + i])
   const int nn = m + (m & 1), P = nn / 2;
   const bool active = lane < P;
   const int seatA = lane == 0 ? nn - 1 : lane, seatB = lane == 0 ? 0 : nn - 1 - lane;
   float A[MR], B[MR];
 #pragma unroll
   for (int s = 0; s < MR; ++s) {
-    A[s] = (active && s < m && seatA < m) ? T[s * L::TP + seatA] : 0.f;
-    B[s] = (active && s < m && seatB < m) ? T[s * L::TP + seatB] : 0.f;
+    const int c = s < m ? piv[s] : 0;
+    A[s] = (active && s < m && seatA < m) ? T[c * TP + seatA] : 0.f;
+    B[s] = (active && s < m && seatB < m) ? T[c * TP + seatB] : 0.f;
   }
   __syncwarp();
 
@@ -263,13 +260,13 @@ __device__ int svd_warp_core(float (&c0)[MR], float (&c1)[MR], int m, float tol,
   if (active) {
     if (seatA < m) {
 #pragma unroll
-      for (int s = 0; s < MR; ++s) T[seatA * L::TP + s] = A[s];
+      for (int s = 0; s < MR; ++s) T[seatA * TP + s] = A[s];
       sig2[seatA] = sa;
       inv[seatA] = sa > kNegligible ? rsqrtf(sa) : 0.f;
     }
     if (seatB < m) {
 #pragma unroll
-      for (int s = 0; s < MR; ++s) T[seatB * L::TP + s] = B[s];
+      for (int s = 0; s < MR; ++s) T[seatB * TP + s] = B[s];
       sig2[seatB] = sb;
       inv[seatB] = sb > kNegligible ? rsqrtf(sb) : 0.f;
     }
