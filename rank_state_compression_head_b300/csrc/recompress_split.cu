@@ -243,11 +243,13 @@ __global__ void __launch_bounds__(32 * kSvdWarps) svd_phase(const SplitArgs p) {
 }
 
 // ---- phase 3: rebuild the factors ---------------------------------------------------------
-// One row of the factor per thread: Q row in registers, the kept coefficient
-// vectors from shared memory as broadcast 16-byte loads, two outputs at a time.
-template <int VAR, typename TF, int DV>
+// One row of the factor per thread: Q row in registers (MR = m_max rounded up
+// to 16 entries), the kept coefficient vectors from shared memory as broadcast
+// 16-byte loads, four outputs at a time.
+template <int VAR, typename TF, int DV, int MR>
 __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p) {
   constexpr int DK = kDK;
+  constexpr int NO = 4;  // outputs per pass
   extern __shared__ __align__(16) float smem[];
   const int h = p.head0 + blockIdx.x;
   const int panel = blockIdx.y;  // 0: U from Q_a and Z, 1: W from Q_b and Y
@@ -259,50 +261,36 @@ __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p
   const float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
   const int rows = panel == 0 ? DK : DV;
   const int rk = r < m ? r : m;
-  const int m4 = (m + 3) & ~3;
-  float *zs = smem;  // [rk][m4]
+  float *zs = smem;  // [rk rounded up to NO][MR], zero beyond m and rk
   const float *src = ws + (panel == 0 ? L.z : L.y);
-  for (int idx = tid; idx < rk * m4; idx += kSplitThreads) zs[idx] = src[(idx / m4) * L.m4 + idx % m4];
+  const int rk4 = (rk + NO - 1) / NO * NO;
+  for (int idx = tid; idx < rk4 * MR; idx += kSplitThreads) {
+    const int k = idx / MR, l = idx % MR;
+    zs[idx] = (k < rk && l < m) ? src[k * L.m4 + l] : 0.f;
+  }
   __syncthreads();
   const int64_t c0 = sv.col0(h);
   if (tid < rows) {
     const float *Q = ws + (panel == 0 ? L.qa : L.qb);
-    float q[kMaxCols];
+    float q[MR];
 #pragma unroll
-    for (int l = 0; l < kMaxCols; ++l) q[l] = l < m ? Q[l * rows + tid] : 0.f;
+    for (int l = 0; l < MR; ++l) q[l] = l < m ? Q[l * rows + tid] : 0.f;
     TF *out = reinterpret_cast<TF *>(panel == 0 ? sv.U : sv.W) + c0 * rows;
-    int k = 0;
-    for (; k + 1 < rk; k += 2) {
-      const float4 *z0 = reinterpret_cast<const float4 *>(zs + k * m4);
-      const float4 *z1 = reinterpret_cast<const float4 *>(zs + (k + 1) * m4);
-      float a0 = 0.f, a1 = 0.f;
+    for (int k = 0; k < rk; k += NO) {
+      float acc[NO];
 #pragma unroll
-      for (int l4 = 0; l4 < kMaxCols / 4; ++l4) {
-        if (4 * l4 < m) {
-          const float4 u = z0[l4], w = z1[l4];
-          a0 = fmaf(q[4 * l4], u.x, a0); a1 = fmaf(q[4 * l4], w.x, a1);
-          if (4 * l4 + 1 < m) { a0 = fmaf(q[4 * l4 + 1], u.y, a0); a1 = fmaf(q[4 * l4 + 1], w.y, a1); }
-          if (4 * l4 + 2 < m) { a0 = fmaf(q[4 * l4 + 2], u.z, a0); a1 = fmaf(q[4 * l4 + 2], w.z, a1); }
-          if (4 * l4 + 3 < m) { a0 = fmaf(q[4 * l4 + 3], u.w, a0); a1 = fmaf(q[4 * l4 + 3], w.w, a1); }
+      for (int o = 0; o < NO; ++o) acc[o] = 0.f;
+#pragma unroll
+      for (int l4 = 0; l4 < MR / 4; ++l4) {
+#pragma unroll
+        for (int o = 0; o < NO; ++o) {
+          const float4 z = reinterpret_cast<const float4 *>(zs + (k + o) * MR)[l4];
+          acc[o] = fmaf(q[4 * l4], z.x, fmaf(q[4 * l4 + 1], z.y, fmaf(q[4 * l4 + 2], z.z, fmaf(q[4 * l4 + 3], z.w, acc[o]))));
         }
       }
-      Elem<TF>::store(out + (int64_t)k * rows + tid, a0);
-      Elem<TF>::store(out + (int64_t)(k + 1) * rows + tid, a1);
-    }
-    if (k < rk) {
-      const float4 *z0 = reinterpret_cast<const float4 *>(zs + k * m4);
-      float a0 = 0.f;
 #pragma unroll
-      for (int l4 = 0; l4 < kMaxCols / 4; ++l4) {
-        if (4 * l4 < m) {
-          const float4 u = z0[l4];
-          a0 = fmaf(q[4 * l4], u.x, a0);
-          if (4 * l4 + 1 < m) a0 = fmaf(q[4 * l4 + 1], u.y, a0);
-          if (4 * l4 + 2 < m) a0 = fmaf(q[4 * l4 + 2], u.z, a0);
-          if (4 * l4 + 3 < m) a0 = fmaf(q[4 * l4 + 3], u.w, a0);
-        }
-      }
-      Elem<TF>::store(out + (int64_t)k * rows + tid, a0);
+      for (int o = 0; o < NO; ++o)
+        if (k + o < rk) Elem<TF>::store(out + (int64_t)(k + o) * rows + tid, acc[o]);
     }
   }
   if (panel == 0) {
@@ -324,10 +312,10 @@ static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaS
   const int qr_bytes = (a.m_max * (kDK + DV) + 4 * up + 2 * a.m_max * a.m_max) * 4;
   const int qr_threads = a.m_max > 0 ? qr_team_stride(a.m_max) * 2 : 32;
   const int svd_bytes = kSvdWarps * SvdWarpSmem<MR>::FLOATS * 4;
-  const int rb_bytes = (a.r_max * up > 0 ? a.r_max * up : 4) * 4;
+  const int rb_bytes = ((a.r_max + 3) / 4 * 4 * MR > 0 ? (a.r_max + 3) / 4 * 4 * MR : 4) * 4;
   auto k1 = qr_phase<VAR, TF, DV>;
   auto k2 = svd_phase<TF, DV, MR>;
-  auto k3 = rebuild_phase<VAR, TF, DV>;
+  auto k3 = rebuild_phase<VAR, TF, DV, MR>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, qr_bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, svd_bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, rb_bytes);
