@@ -12,12 +12,13 @@
 // lane applies it to its remaining columns with 16-byte loads, refreshing their
 // trailing norms.  Columns stay in place; only the pivot order is recorded.
 //
-// Jacobi: lane i (i < P = n'/2) holds two seats in registers, A and B:
-// lane 0 has seat n'-1 in A and the fixed seat 0 in B, lane i >= 1 has seat i
-// in A and seat n'-1-i in B.  After each round the column at seat s >= 1 moves
-// to seat s + 1 (n'-1 to 1); with this assignment that is one shuffle up of A
-// and one shuffle down of B per element, plus the ends of the chain.  Rotation
-// rule, tolerance and stopping rule as jacobi_seats.
+// Jacobi: lane i (i < P = n'/2) looks after two seats, A and B: lane 0 has
+// seat n'-1 in A and the fixed seat 0 in B, lane i >= 1 has seat i in A and
+// seat n'-1-i in B.  The seats live in the square (seat s at s * TP, rows of
+// R^T); each round a lane reads its two seats into registers, rotates them and
+// writes them to their next seats (the column at seat s >= 1 moves to s + 1,
+// n'-1 to 1), one warp barrier between the reads and the writes and one at the
+// end of the round.  Rotation rule, tolerance and stopping rule as jacobi_seats.
 #pragma once
 
 #include "recompress_core.cuh"
@@ -178,70 +179,93 @@ __device__ int svd_warp_core(int m, float tol, float *sw) {
     __syncwarp();
   }
 
-  // ---- R^T to the seats of the Jacobi: seat i = row i of R = T[s * TP + i] over s ----------
-  // (R column s is the column chosen at step s: T[piv[s] * TP + i])
+  // ---- R^T to the seats of the Jacobi: seat i = row i of R, R column s = T[piv[s] * TP] -------
   const int nn = m + (m & 1), P = nn / 2;
   const bool active = lane < P;
   const int seatA = lane == 0 ? nn - 1 : lane, seatB = lane == 0 ? 0 : nn - 1 - lane;
-  float A[MR], B[MR];
+  {
+    float A[MR], B[MR];
 #pragma unroll
-  for (int s = 0; s < MR; ++s) {
-    const int c = s < m ? piv[s] : 0;
-    A[s] = (active && s < m && seatA < m) ? T[c * TP + seatA] : 0.f;
-    B[s] = (active && s < m && seatB < m) ? T[c * TP + seatB] : 0.f;
+    for (int s = 0; s < MR; ++s) {
+      const int c = s < m ? piv[s] : 0;
+      A[s] = (active && s < m && seatA < m) ? T[c * TP + seatA] : 0.f;
+      B[s] = (active && s < m && seatB < m) ? T[c * TP + seatB] : 0.f;
+    }
+    __syncwarp();
+    if (active) {  // seat s at T[s * TP] from here on (the core is no longer needed)
+#pragma unroll
+      for (int q = 0; q < MR / 4; ++q) {
+        reinterpret_cast<float4 *>(T + seatA * TP)[q] = make_float4(A[4 * q], A[4 * q + 1], A[4 * q + 2], A[4 * q + 3]);
+        reinterpret_cast<float4 *>(T + seatB * TP)[q] = make_float4(B[4 * q], B[4 * q + 1], B[4 * q + 2], B[4 * q + 3]);
+      }
+    }
+    __syncwarp();
   }
-  __syncwarp();
 
-  // ---- Jacobi -------------------------------------------------------------------------------
+  // ---- Jacobi: each round every lane reads its two seats, rotates them in
+  // registers and writes them to their next seats (seat s >= 1 to s + 1, n'-1 to
+  // 1; seat 0 stays); the square holds every seat between rounds ------------------------------
   int sweeps = 0;
   if (m >= 2) {
     const float tol2 = tol * tol, stop2 = tol;  // tol_stop = sqrt(tol)
-    int colA = seatA, colB = seatB;            // column indices at my seats (>= m: the zero seat)
+    const int nextA = seatA == nn - 1 ? 1 : seatA + 1;
+    const int nextB = seatB == 0 ? 0 : (seatB == nn - 1 ? 1 : seatB + 1);
+    int colA = seatA, colB = seatB;  // columns at my seats (>= m: the zero seat)
+    const unsigned amask = P >= 32 ? full : (1u << P) - 1;  // the active lanes
     sweeps = -1;
     for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
       int far = 0;
       for (int round = 0; round < nn - 1; ++round) {
-        float al0 = 0.f, al1 = 0.f, be0 = 0.f, be1 = 0.f, ga0 = 0.f, ga1 = 0.f;
+        if (active) {
+          float4 a4[MR / 4], b4[MR / 4];
+          const float4 *pa = reinterpret_cast<const float4 *>(T + seatA * TP);
+          const float4 *pb = reinterpret_cast<const float4 *>(T + seatB * TP);
+          float al0 = 0.f, al1 = 0.f, be0 = 0.f, be1 = 0.f, ga0 = 0.f, ga1 = 0.f;
 #pragma unroll
-        for (int s = 0; s < MR; s += 2) {
-          al0 = fmaf(A[s], A[s], al0); be0 = fmaf(B[s], B[s], be0); ga0 = fmaf(A[s], B[s], ga0);
-          al1 = fmaf(A[s + 1], A[s + 1], al1); be1 = fmaf(B[s + 1], B[s + 1], be1);
-          ga1 = fmaf(A[s + 1], B[s + 1], ga1);
-        }
-        const float al = al0 + al1, be = be0 + be1, ga = ga0 + ga1;
-        if (active && colA < m && colB < m && al > kNegligible && be > kNegligible && ga * ga > tol2 * al * be) {
-          const float zeta = (be - al) * __frcp_rn(2.f * ga);
-          const float az = fabsf(zeta);
-          const float root = az < 1e18f ? az + fmaf(az, az, 1.f) * rsqrtf(fmaf(az, az, 1.f)) : 2.f * az;
-          const float t = copysignf(__frcp_rn(root), zeta);
-          const float c = rsqrtf(fmaf(t, t, 1.f));
-          const float sn = c * t;
-#pragma unroll
-          for (int s = 0; s < MR; ++s) {
-            const float a = A[s], b = B[s];
-            A[s] = fmaf(c, a, -sn * b);
-            B[s] = fmaf(sn, a, c * b);
+          for (int q = 0; q < MR / 4; ++q) {
+            a4[q] = pa[q];
+            b4[q] = pb[q];
+            al0 = fmaf(a4[q].x, a4[q].x, fmaf(a4[q].y, a4[q].y, al0));
+            al1 = fmaf(a4[q].z, a4[q].z, fmaf(a4[q].w, a4[q].w, al1));
+            be0 = fmaf(b4[q].x, b4[q].x, fmaf(b4[q].y, b4[q].y, be0));
+            be1 = fmaf(b4[q].z, b4[q].z, fmaf(b4[q].w, b4[q].w, be1));
+            ga0 = fmaf(a4[q].x, b4[q].x, fmaf(a4[q].y, b4[q].y, ga0));
+            ga1 = fmaf(a4[q].z, b4[q].z, fmaf(a4[q].w, b4[q].w, ga1));
           }
-          far |= ga * ga > stop2 * al * be;
-        }
-        if (P > 1) {
-          // seat s >= 1 moves to s + 1 (n'-1 to 1): A up one lane, B down one lane;
-          // lane 0 takes lane 1's B into A, lane P-1 keeps its A as B
-#pragma unroll
-          for (int s = 0; s < MR; ++s) {
-            const float up = __shfl_up_sync(full, A[s], 1);
-            const float dn = __shfl_down_sync(full, B[s], 1);
-            const float a = A[s];
-            A[s] = lane == 0 ? dn : up;
-            if (lane == P - 1) B[s] = a;
-            else if (lane != 0) B[s] = dn;
+          const float al = al0 + al1, be = be0 + be1, ga = ga0 + ga1;
+          float c = 1.f, sn = 0.f;
+          if (colA < m && colB < m && al > kNegligible && be > kNegligible && ga * ga > tol2 * al * be) {
+            const float zeta = (be - al) * __frcp_rn(2.f * ga);
+            const float az = fabsf(zeta);
+            const float root = az < 1e18f ? az + fmaf(az, az, 1.f) * rsqrtf(fmaf(az, az, 1.f)) : 2.f * az;
+            const float t = copysignf(__frcp_rn(root), zeta);
+            c = rsqrtf(fmaf(t, t, 1.f));
+            sn = c * t;
+            far |= ga * ga > stop2 * al * be;
           }
-          const int cu = __shfl_up_sync(full, colA, 1), cd = __shfl_down_sync(full, colB, 1);
-          const int ca = colA;
-          colA = lane == 0 ? cd : cu;
-          if (lane == P - 1) colB = ca;
-          else if (lane != 0) colB = cd;
+          __syncwarp(amask);  // every active lane has read its seats
+          float4 *wa = reinterpret_cast<float4 *>(T + nextA * TP);
+          float4 *wb = reinterpret_cast<float4 *>(T + nextB * TP);
+          if (sn != 0.f) {
+#pragma unroll
+            for (int q = 0; q < MR / 4; ++q) {
+              const float4 a = a4[q], b = b4[q];
+              wa[q] = make_float4(fmaf(c, a.x, -sn * b.x), fmaf(c, a.y, -sn * b.y), fmaf(c, a.z, -sn * b.z),
+                                  fmaf(c, a.w, -sn * b.w));
+              wb[q] = make_float4(fmaf(sn, a.x, c * b.x), fmaf(sn, a.y, c * b.y), fmaf(sn, a.z, c * b.z),
+                                  fmaf(sn, a.w, c * b.w));
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < MR / 4; ++q) {
+              wa[q] = a4[q];
+              wb[q] = b4[q];
+            }
+          }
+          if (seatA != 0) colA = colA == 1 ? nn - 1 : colA - 1;
+          if (seatB != 0) colB = colB == 1 ? nn - 1 : colB - 1;
         }
+        __syncwarp();
       }
       if (!__any_sync(full, far)) {
         sweeps = sweep + 1;
@@ -250,25 +274,20 @@ __device__ int svd_warp_core(int m, float tol, float *sw) {
     }
   }
 
-  // ---- columns of R^T J by seat, sigma^2, order -----------------------------------------------
-  float sa = 0.f, sb = 0.f;
+  // ---- columns of R^T J by seat (already in place after whole sweeps), sigma^2 -------------
 #pragma unroll
-  for (int s = 0; s < MR; ++s) {
-    sa = fmaf(A[s], A[s], sa);
-    sb = fmaf(B[s], B[s], sb);
-  }
-  if (active) {
-    if (seatA < m) {
+  for (int e = 0; e < 2; ++e) {
+    const int j = lane + 32 * e;
+    if (j < m) {
+      const float4 *f4 = reinterpret_cast<const float4 *>(T + j * TP);
+      float acc = 0.f;
 #pragma unroll
-      for (int s = 0; s < MR; ++s) T[seatA * TP + s] = A[s];
-      sig2[seatA] = sa;
-      inv[seatA] = sa > kNegligible ? rsqrtf(sa) : 0.f;
-    }
-    if (seatB < m) {
-#pragma unroll
-      for (int s = 0; s < MR; ++s) T[seatB * TP + s] = B[s];
-      sig2[seatB] = sb;
-      inv[seatB] = sb > kNegligible ? rsqrtf(sb) : 0.f;
+      for (int q = 0; q < MR / 4; ++q) {
+        const float4 f = f4[q];
+        acc = fmaf(f.x, f.x, fmaf(f.y, f.y, fmaf(f.z, f.z, fmaf(f.w, f.w, acc))));
+      }
+      sig2[j] = acc;
+      inv[j] = acc > kNegligible ? rsqrtf(acc) : 0.f;
     }
   }
   __syncwarp();
