@@ -60,9 +60,14 @@ __device__ inline void rr_reflector_warp(RRCol &c, bool owner, int p, int j, int
   __syncwarp();
   // lane k holds rows [k * rpl, (k + 1) * rpl), rpl = rows / 32 (4 or 2)
   const int rpl = rows >> 5;
-  float a[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) a[e] = e < rpl ? vj[lane * rpl + e] : 0.f;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+  if (rpl == 4) {  // one 16-byte (or 8-byte) access per lane: no bank conflicts
+    const float4 t = reinterpret_cast<const float4 *>(vj)[lane];
+    a[0] = t.x; a[1] = t.y; a[2] = t.z; a[3] = t.w;
+  } else {
+    const float2 t = reinterpret_cast<const float2 *>(vj)[lane];
+    a[0] = t.x; a[1] = t.y;
+  }
   const float alpha = vj[j];
   float tj = 0.f, beta = alpha, sc = 0.f;
   // The sum of squares below row j in one reduction; only where it leaves
@@ -102,11 +107,14 @@ __device__ inline void rr_reflector_warp(RRCol &c, bool owner, int p, int j, int
     beta = bs * amax;
   }
   __syncwarp();
+  float w[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int row = lane * rpl + e;
-    if (e < rpl) vj[row] = row < j ? 0.f : row == j ? 1.f : a[e] * sc;
+    w[e] = row < j ? 0.f : row == j ? 1.f : a[e] * sc;
   }
+  if (rpl == 4) reinterpret_cast<float4 *>(vj)[lane] = make_float4(w[0], w[1], w[2], w[3]);
+  else reinterpret_cast<float2 *>(vj)[lane] = make_float2(w[0], w[1]);
   if (lane == 0) {
     *tau = tj;
     *beta_out = beta;
