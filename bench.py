@@ -265,8 +265,13 @@ def run_gpu(args, w):
     run = DeviceRun(w, device=dev, steps_buffered=total_steps, ws_heads=ws_heads)
     rec_groups = -(-run.H // min(run.H, ws_heads)) if ws_heads else 1
     rec_launches = 3 * rec_groups if ws_heads else 1
+    # setup, timed once (not part of the decode metric): dense prefill and compression
+    ev_setup = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ev_setup[0].record(stream)
     S_dense = run.prefill()
+    ev_setup[1].record(stream)
     run.compress(S_dense)
+    ev_setup[2].record(stream)
     for t in range(total_steps):
         run.gen_inputs(t % w.steps, slot=t)
     torch.cuda.synchronize()
@@ -425,6 +430,9 @@ def run_gpu(args, w):
                          bytes_per_head_step=round(bytes_decode / K / run.H, 1),
                          mean_columns=round(m_sum / K / run.H, 2))
     out['recompress'] = roof_rec
+    out['setup'] = dict(dense_prefill_ms=round(ev_setup[0].elapsed_time(ev_setup[1]), 3),
+                        compress_dense_ms=round(ev_setup[1].elapsed_time(ev_setup[2]), 3),
+                        compress_dense_us_per_head=round(ev_setup[1].elapsed_time(ev_setup[2]) * 1e3 / run.H, 3))
     out['time_share'] = dict(decode=round(dec_total / total_ms, 4), recompress=round(rec_total / total_ms, 4))
 
     # ---- dense-state comparator ----------------------------------------------------------

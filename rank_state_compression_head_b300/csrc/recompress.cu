@@ -34,105 +34,117 @@ struct CompressArgs {
   int cs_alloc;     // column stride of the core buffers in the allocation
 };
 
-// Dynamic shared-memory layout of compress_dense (offsets in floats, multiples of 4).
+// Dynamic shared-memory layout of compress_dense (offsets in floats, multiples
+// of 4): two buffers that hold in turn C (column pitch d_k + 4), the seats of the
+// Jacobi (pitch cs) and C again; then a, vbar and the vectors of the core stage.
 struct DenseSmem {
-  int lda;
-  int offA, offK, offK0, offTa, offS, offI, offO, offR;
+  int pc, buf;
+  int offB0, offB1, offA, offVb, offVn, offP, offS, offI, offO, offR;
   int total_floats;
-  __host__ __device__ DenseSmem(int m, int dk, int cs) {
-    lda = dk + 4;  // 16-byte aligned columns, 4 banks apart
+  __host__ __device__ DenseSmem(int dk, int dv, int cs) {
     auto up4 = [](int x) { return (x + 3) & ~3; };
-    offA = 0;
-    offK = up4(offA + m * lda);
-    offK0 = up4(offK + m * cs);
-    offTa = up4(offK0 + m * cs);
-    offS = offTa + up4(m);
-    offI = offS + up4(m);
-    offO = offI + up4(m);
-    offR = offO + up4(m);     // 8 floats of reduction scratch
+    pc = dk + 4;
+    const int c_sz = dv * pc, seat_sz = (dv + 1) * cs;
+    buf = up4(c_sz > seat_sz ? c_sz : seat_sz);
+    offB0 = 0;
+    offB1 = offB0 + buf;
+    offA = offB1 + buf;
+    offVb = offA + up4(dk);
+    offVn = offVb + up4(dv);
+    offP = offVn + up4(dv);
+    offS = offP + up4(dv);
+    offI = offS + up4(dv);
+    offO = offI + up4(dv);
+    offR = offO + up4(dv);
     total_floats = offR + 8;
   }
 };
 
+// compress_dense, one CTA of 256 threads per head:
+//   a = S vbar / |vbar|^2, C = S - a vbar^T (C in shared memory as columns)
+//   C P = Q R (pivoted Householder QR, qrcp_rect), R^T to the seats, scaled by a
+//   power of two; one-sided Jacobi on R^T (jacobi_seats): R^T J = V Sigma
+//   keep the rank(h) largest sigma: y_k = P v_k, U = C y_k (= sigma_k x_k), W = y_k
+// the same numerics as the recompression's core stage, with the 128 x d_v state
+// in place of the core.
 template <int VAR, typename TF, int DV>
 __global__ void __launch_bounds__(256) compress_dense_kernel(const CompressArgs p) {
   constexpr int DK = kDK;
   constexpr int NT = 256;
+  constexpr int m = DV;
   extern __shared__ __align__(16) float smem[];
   const int h = blockIdx.x;
   const int tid = threadIdx.x;
   const StateView &sv = p.sv;
   const int r = sv.rank_of(h);
-  const int m = DV;
   if (r < 0) {  // rank table disagrees with r_max: touch nothing
     if (tid == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
     return;
   }
   const int64_t c0 = sv.col0(h);
-  const DenseSmem L(DV, DK, p.cs_alloc);
-  const JacobiGeom jg = jacobi_geom(m, NT);
-  const int cs = jg.cs, ldr = jg.ld;
-  float *A = smem + L.offA, *K = smem + L.offK, *K0 = smem + L.offK0;
-  float *tauA = smem + L.offTa, *sig2 = smem + L.offS, *inv = smem + L.offI;
+  const JacobiGeom g = seat_geom(m, NT);
+  const DenseSmem L(DK, DV, p.cs_alloc);
+  const int pc = L.pc, cs = g.cs;
+  float *B0 = smem + L.offB0, *B1 = smem + L.offB1, *as = smem + L.offA, *vb = smem + L.offVb;
+  float *vn = smem + L.offVn, *sig2 = smem + L.offS, *inv = smem + L.offI, *red = smem + L.offR;
+  int *piv = reinterpret_cast<int *>(smem + L.offP);
   int *order = reinterpret_cast<int *>(smem + L.offO);
-  float *red = smem + L.offR;
-  const int lda = L.lda;
   TF *Uh = reinterpret_cast<TF *>(sv.U) + c0 * DK;
   TF *Wh = reinterpret_cast<TF *>(sv.W) + c0 * DV;
-
-  // ---- A[j][i] = S[i][j]; then a = S vbar / |vbar|^2 and C = S - a vbar^T in place -------
   const float *Sh = p.S + (int64_t)h * DK * DV;
+
+  // ---- C = S - a vbar^T as columns of B0 --------------------------------------------------
   for (int idx = tid; idx < DK * DV; idx += NT) {
     const int i = idx / DV, j = idx % DV;
-    A[j * lda + i] = Sh[idx];
+    B0[j * pc + i] = Sh[idx];
   }
+  for (int j = tid; j < DV; j += NT) vb[j] = sv.vbar[(int64_t)sv.dir_of(h) * DV + j];
   __syncthreads();
-  const float *vb = sv.vbar + (int64_t)sv.dir_of(h) * DV;
   float vv = 0.f;
   for (int j = 0; j < DV; ++j) vv = fmaf(vb[j], vb[j], vv);
   if (tid < DK) {
     float acc = 0.f;
-    for (int j = 0; j < DV; ++j) acc = fmaf(A[j * lda + tid], vb[j], acc);
+    for (int j = 0; j < DV; ++j) acc = fmaf(B0[j * pc + tid], vb[j], acc);
     const float ai = acc / vv;
     sv.a[(int64_t)h * DK + tid] = ai;
-    for (int j = 0; j < DV; ++j) A[j * lda + tid] = fmaf(-ai, vb[j], A[j * lda + tid]);
+    as[tid] = ai;
+    for (int j = 0; j < DV; ++j) B0[j * pc + tid] = fmaf(-ai, vb[j], B0[j * pc + tid]);
   }
   __syncthreads();
 
-  // ---- QR of C; K = R_a (rows padded with zeros to ld), K0 keeps a copy -------------------
-  householder_qr(A, lda, DK, m, tauA, tid, NT, 1);
-  __syncthreads();
-  for (int idx = tid; idx < m * ldr; idx += NT) {
-    const int j = idx / ldr, i = idx % ldr;  // K[j][i]: column j, row i
-    const float x = (i < m && i <= j) ? A[j * lda + i] : 0.f;
-    K[j * cs + i] = x;
-    K0[j * cs + i] = x;
-  }
-  __syncthreads();
-  form_q(A, lda, DK, m, tauA, tid, NT, 1);
-
-  // ---- SVD of the core, scaled by a power of two to a largest entry in [1/2, 1) ----------
+  // ---- pivoted QR of C; R^T to the seats of B1, scaled to a largest entry in [1/2, 1) ------
+  qrcp_rect<NT>(B0, DK, DV, pc, piv, vn, red);
   float kmax = 0.f;
-  for (int idx = tid; idx < m * ldr; idx += NT) kmax = fmaxf(kmax, fabsf(K[(idx / ldr) * cs + idx % ldr]));
+  for (int idx = tid; idx < m * m; idx += NT) {
+    const int i = idx / m, s = idx % m;  // seat i = row i of R, entry s
+    const float x = s >= i ? B0[s * pc + i] : 0.f;
+    B1[i * cs + s] = x;
+    kmax = fmaxf(kmax, fabsf(x));
+  }
   kmax = warp_max(kmax);
-  if ((tid & 31) == 0) red[tid >> 5] = kmax;
+  static_assert(NT / 32 <= 8, "one reduction slot per warp");
+  if ((tid & 31) == 0) red[tid >> 5] = kmax;  // qrcp_rect is done with red (it ends with a barrier)
   __syncthreads();
   kmax = 0.f;
   for (int w = 0; w < NT / 32; ++w) kmax = fmaxf(kmax, red[w]);
   int kexp = 0;
   if (kmax > 0.f) frexpf(kmax, &kexp);
   const float kscale = ldexpf(1.f, -kexp), kunscale = ldexpf(1.f, kexp);
-  for (int idx = tid; idx < m * ldr; idx += NT) K[(idx / ldr) * cs + idx % ldr] *= kscale;
+  for (int idx = tid; idx < m * m; idx += NT) B1[(idx / m) * cs + idx % m] *= kscale;
   __syncthreads();
-  const float tol = sizeof(TF) == 2 ? 1e-5f : (float)m * FLT_EPSILON;
-  const int sweeps = jacobi_svd<NT, 32>(K, m, jg, tol);
+  // bf16 factors: 1e-4 (their own rounding is 2^-9), stop once no pair is beyond
+  // sqrt(tol); fp32: four times the rounding noise of a length-m dot product
+  // (sqrt(m) eps), run until no pair is beyond tol
+  const float tol = sizeof(TF) == 2 ? 1e-4f : 4.f * sqrtf((float)m) * FLT_EPSILON;
+  float *F;
+  const int sweeps = jacobi_seats<NT, 32>(B1, B0, m, g, tol, sizeof(TF) == 2 ? sqrtf(tol) : tol, &F);
 
-  // ---- order by sigma, truncation error -----------------------------------------------
+  // ---- sigma^2, order, truncation error ---------------------------------------------------
   for (int j = tid; j < m; j += NT) {
     float acc = 0.f;
-    for (int i = 0; i < m; ++i) acc = fmaf(K[j * cs + i], K[j * cs + i], acc);
+    for (int i = 0; i < m; ++i) acc = fmaf(F[j * cs + i], F[j * cs + i], acc);
     sig2[j] = acc;
-    inv[j] = acc > kNegligible ? rsqrtf(acc) : 0.f;  // x_j = (K J)_j / sigma_j
+    inv[j] = acc > kNegligible ? rsqrtf(acc) : 0.f;
   }
   __syncthreads();
   for (int j = tid; j < m; j += NT) {
@@ -152,25 +164,26 @@ __global__ void __launch_bounds__(256) compress_dense_kernel(const CompressArgs 
     if (sv.status) sv.status[h] = sweeps < 0 ? SEED_ERR_NOT_CONVERGED : SEED_OK;
   }
 
-  // ---- U = Q_a X_r,  W = R_a^T X_r ------------------------------------------------------------
-  const int rk = r < m ? r : m;
-  if (tid < DK) {
-    for (int k = 0; k < rk; ++k) {
-      const int col = order[k];
-      const float *z = K + col * cs;
-      float acc = 0.f;
-      for (int l = 0; l < m; ++l) acc = fmaf(A[l * lda + tid], z[l], acc);
-      Elem<TF>::store(Uh + (int64_t)k * DK + tid, acc * inv[col]);
-    }
+  // ---- C again into the free buffer; U = C y_k, W = y_k, y_k[piv[s]] = (R^T J)_{s,k} / sigma --
+  float *Cs = F == B0 ? B1 : B0;
+  for (int idx = tid; idx < DK * DV; idx += NT) {
+    const int i = idx / DV, j = idx % DV;
+    Cs[j * pc + i] = fmaf(-as[i], vb[j], Sh[idx]);
   }
-  for (int i = tid; i < DV; i += NT) {
-    for (int k = 0; k < rk; ++k) {
-      const int col = order[k];
-      const float *z = K + col * cs;
-      float acc = 0.f;
-      for (int l = 0; l < m; ++l) acc = fmaf(K0[i * cs + l], z[l], acc);
-      Elem<TF>::store(Wh + (int64_t)k * DV + i, acc * inv[col]);
-    }
+  __syncthreads();
+  const int rk = r < m ? r : m;
+  for (int idx = tid; idx < rk * DK; idx += NT) {
+    const int k = idx / DK, i = idx % DK;
+    const int col = order[k];
+    const float *f = F + col * cs;
+    float acc = 0.f;
+    for (int s2 = 0; s2 < m; ++s2) acc = fmaf(Cs[piv[s2] * pc + i], f[s2], acc);
+    Elem<TF>::store(Uh + (int64_t)k * DK + i, acc * inv[col]);
+  }
+  for (int idx = tid; idx < rk * DV; idx += NT) {
+    const int k = idx / DV, s2 = idx % DV;
+    const int col = order[k];
+    Elem<TF>::store(Wh + (int64_t)k * DV + piv[s2], F[col * cs + s2] * inv[col]);
   }
   if (VAR == SEED_KDA) {
     for (int i = tid; i < DK; i += NT) sv.scale[(int64_t)h * DK + i] = 1.f;
@@ -283,10 +296,13 @@ __global__ void __launch_bounds__(128) recompress_kernel(const CompressArgs p) {
   const float kscale = ldexpf(1.f, -kexp), kunscale = ldexpf(1.f, kexp);
   for (int idx = tid; idx < m * m4; idx += NT) Kb[(idx / m4) * cs + idx % m4] *= kscale;
   __syncthreads();
-  // bf16 factors: 1e-4 (their own rounding is 2^-9); fp32: a few units of rounding
-  const float tol = sizeof(TF) == 2 ? 1e-4f : (float)(m > 16 ? m : 16) * FLT_EPSILON;
+  // bf16 factors: 1e-4 (their own rounding is 2^-9), stop once no pair is beyond
+  // sqrt(tol); fp32: four times the rounding noise of a length-m dot product
+  // (sqrt(m) eps), run until no pair is beyond tol
+  const float tol = sizeof(TF) == 2 ? 1e-4f : 4.f * sqrtf((float)(m > 16 ? m : 16)) * FLT_EPSILON;
   float *F;
-  const int sweeps = core_factor<NT>(Kb, Tb, m, g, tol, piv, vn, sig2, inv, order, red, &F);
+  const int sweeps = core_factor<NT>(Kb, Tb, m, g, tol, sizeof(TF) == 2 ? sqrtf(tol) : tol, piv, vn, sig2, inv,
+                                     order, red, &F);
   if (tid == 0) {
     float e = 0.f;
     for (int k = r; k < m; ++k) e += sig2[order[k]];
@@ -350,8 +366,8 @@ static cudaError_t launch_recompress_t(const CompressArgs &a, cudaStream_t s) {
 template <int VAR, typename TF, int DV>
 static cudaError_t launch_dense_t(const CompressArgs &a, cudaStream_t s) {
   CompressArgs args = a;
-  args.cs_alloc = jacobi_cs_alloc(DV, 256);
-  const DenseSmem L(DV, kDK, args.cs_alloc);
+  args.cs_alloc = seat_geom(DV, 256).cs;
+  const DenseSmem L(kDK, DV, args.cs_alloc);
   const size_t bytes = (size_t)L.total_floats * sizeof(float);
   auto kern = compress_dense_kernel<VAR, TF, DV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);

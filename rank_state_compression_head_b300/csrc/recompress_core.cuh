@@ -263,29 +263,30 @@ __device__ static inline float col_axpy_ss(float a, const float *__restrict__ x,
   return ss;
 }
 
-// Householder QR with column pivoting of the m x m matrix A (column-major,
-// column stride cs a multiple of 4, rows m..m4-1 zero with m4 = m rounded up to
-// 4).  Each step moves the remaining column of largest trailing norm to the
-// front (ties: the lower index); the trailing norms are recomputed from the
-// updated columns rather than downdated.  On exit the upper triangle holds R
-// and piv[j] is the original index of column j: A[:, piv] = Q R.  Warp 0 forms
-// the pivot and the reflector, all NT threads update the trailing columns.
-// vn (m floats) and red (2 floats) are shared scratch.
+// Householder QR with column pivoting of the nrows x ncols matrix A (nrows >=
+// ncols; column-major, column stride cs a multiple of 4, rows nrows..n4-1 zero
+// with n4 = nrows rounded up to 4).  Each step moves the remaining column of
+// largest trailing norm to the front (ties: the lower index); the trailing norms
+// are recomputed from the updated columns rather than downdated.  On exit the
+// upper triangle holds R and piv[j] is the original index of column j:
+// A[:, piv] = Q R.  Warp 0 forms the pivot and the reflector, all NT threads
+// update the trailing columns.  vn (ncols floats) and red (2 floats) are
+// shared scratch.
 template <int NT>
-__device__ static void qrcp(float *A, int m, int cs, int *piv, float *vn, float *red) {
+__device__ static void qrcp_rect(float *A, int nrows, int ncols, int cs, int *piv, float *vn, float *red) {
   const int tid = threadIdx.x, lane = tid & 31;
-  const int m4 = (m + 3) & ~3;
-  for (int l = tid; l < m; l += NT) {
-    vn[l] = col_dot(A + l * cs, A + l * cs, 0, m4);
+  const int n4 = (nrows + 3) & ~3;
+  for (int l = tid; l < ncols; l += NT) {
+    vn[l] = col_dot(A + l * cs, A + l * cs, 0, n4);
     piv[l] = l;
   }
   __syncthreads();
-  for (int j = 0; j < m; ++j) {
+  for (int j = 0; j < ncols; ++j) {
     float *cj = A + j * cs;
     if (tid < 32) {
       float best = -1.f;
-      int bi = m;
-      for (int l = j + lane; l < m; l += 32)
+      int bi = ncols;
+      for (int l = j + lane; l < ncols; l += 32)
         if (vn[l] > best) { best = vn[l]; bi = l; }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -293,9 +294,9 @@ __device__ static void qrcp(float *A, int m, int cs, int *piv, float *vn, float 
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
       }
-      if (bi != j && bi < m) {
+      if (bi != j && bi < ncols) {
         float *cb = A + bi * cs;
-        for (int i = lane; i < m; i += 32) {
+        for (int i = lane; i < nrows; i += 32) {
           const float t = cj[i];
           cj[i] = cb[i];
           cb[i] = t;
@@ -309,14 +310,14 @@ __device__ static void qrcp(float *A, int m, int cs, int *piv, float *vn, float 
       }
       __syncwarp();
       float amax = 0.f;
-      for (int i = j + lane; i < m4; i += 32) amax = fmaxf(amax, fabsf(cj[i]));
+      for (int i = j + lane; i < n4; i += 32) amax = fmaxf(amax, fabsf(cj[i]));
       amax = warp_max(amax);
       const float alpha = cj[j];
       float tj = 0.f, beta = alpha;
       if (amax >= FLT_MIN) {
         const float inv = 1.f / amax;
         float ss = 0.f;
-        for (int i = j + 1 + lane; i < m4; i += 32) {
+        for (int i = j + 1 + lane; i < n4; i += 32) {
           const float x = cj[i] * inv;
           ss = fmaf(x, x, ss);
         }
@@ -327,29 +328,34 @@ __device__ static void qrcp(float *A, int m, int cs, int *piv, float *vn, float 
           const float bs = as >= 0.f ? -nrm : nrm;
           tj = (bs - as) / bs;
           const float sc = 1.f / ((as - bs) * amax);
-          for (int i = j + 1 + lane; i < m4; i += 32) cj[i] *= sc;
+          for (int i = j + 1 + lane; i < n4; i += 32) cj[i] *= sc;
           beta = bs * amax;
         }
       } else {
-        for (int i = j + 1 + lane; i < m4; i += 32) cj[i] = 0.f;
+        for (int i = j + 1 + lane; i < n4; i += 32) cj[i] = 0.f;
       }
       __syncwarp();
       if (lane == 0) { cj[j] = beta; red[0] = tj; }
     }
     __syncthreads();
     const float tj = red[0];
-    for (int l = j + 1 + tid; l < m; l += NT) {
+    for (int l = j + 1 + tid; l < ncols; l += NT) {
       float *cl = A + l * cs;
       if (tj != 0.f) {
-        const float sv = tj * (cl[j] + col_dot(cj, cl, j + 1, m4));
+        const float sv = tj * (cl[j] + col_dot(cj, cl, j + 1, n4));
         cl[j] -= sv;
-        vn[l] = col_axpy_ss(sv, cj, cl, j + 1, m4);
+        vn[l] = col_axpy_ss(sv, cj, cl, j + 1, n4);
       } else {
-        vn[l] = col_dot(cl, cl, j + 1, m4);
+        vn[l] = col_dot(cl, cl, j + 1, n4);
       }
     }
     __syncthreads();
   }
+}
+
+template <int NT>
+__device__ static void qrcp(float *A, int m, int cs, int *piv, float *vn, float *red) {
+  qrcp_rect<NT>(A, m, m, cs, piv, vn, red);
 }
 
 // Geometry of the seat-indexed Jacobi: as jacobi_geom, with the seat stride cs
@@ -482,12 +488,14 @@ __device__ static int jacobi_seats(float *buf0, float *buf1, int n, const Jacobi
 // the same size (n' seats).  Pivoted QR of K in Kb, R^T into Tb, Jacobi between
 // the two; then the squared column norms sig2 (= sigma^2 of the core), their
 // inverse square roots inv (0 below fp32 resolution), and order (column
-// indices by decreasing sigma, ties by index).  *fin is the buffer that holds
+// indices by decreasing sigma, ties by index); the Jacobi stops after a sweep
+// with no pair beyond tol_stop from orthogonal.  *fin is the buffer that holds
 // the columns V Sigma of R^T J; piv the column pivots of the QR.  Returns the
 // Jacobi sweeps (or -1).  Whole block of NT threads; ends with a barrier.
 template <int NT>
-__device__ static int core_factor(float *Kb, float *Tb, int m, const JacobiGeom &g, float tol, int *piv,
-                                  float *vn, float *sig2, float *inv, int *order, float *red, float **fin) {
+__device__ static int core_factor(float *Kb, float *Tb, int m, const JacobiGeom &g, float tol, float tol_stop,
+                                  int *piv, float *vn, float *sig2, float *inv, int *order, float *red,
+                                  float **fin) {
   const int tid = threadIdx.x;
   const int cs = g.cs, ld = g.ld;
   qrcp<NT>(Kb, m, cs, piv, vn, red);
@@ -497,7 +505,7 @@ __device__ static int core_factor(float *Kb, float *Tb, int m, const JacobiGeom 
     Tb[j * cs + i] = (j < m && i < m && i >= j) ? Kb[i * cs + j] : 0.f;
   }
   __syncthreads();
-  const int sweeps = jacobi_seats<NT, 16>(Tb, Kb, m, g, tol, sqrtf(tol), fin);
+  const int sweeps = jacobi_seats<NT, 16>(Tb, Kb, m, g, tol, tol_stop, fin);
   const float *F = *fin;
   for (int j = tid; j < m; j += NT) {
     float acc = 0.f;

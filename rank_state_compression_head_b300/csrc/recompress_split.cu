@@ -209,9 +209,11 @@ __global__ void __launch_bounds__(32 * kSvdWarps) svd_phase(const SplitArgs p) {
   __syncwarp();
   for (int idx = lane; idx < m * MR; idx += 32) T[(idx / MR) * SW::TP + idx % MR] *= kscale;
   __syncwarp();
-  // bf16 factors: 1e-4 (their own rounding is 2^-9); fp32: a few units of rounding
-  const float tol = sizeof(TF) == 2 ? 1e-4f : (float)(m > 16 ? m : 16) * FLT_EPSILON;
-  const int sweeps = svd_warp_core<MR>(m, tol, sw);
+  // bf16 factors: 1e-4 (their own rounding is 2^-9), stop once no pair is beyond
+  // sqrt(tol); fp32: four times the rounding noise of a length-m dot product
+  // (sqrt(m) eps), run until no pair is beyond tol
+  const float tol = sizeof(TF) == 2 ? 1e-4f : 4.f * sqrtf((float)(m > 16 ? m : 16)) * FLT_EPSILON;
+  const int sweeps = svd_warp_core<MR>(m, tol, sizeof(TF) == 2 ? sqrtf(tol) : tol, sw);
   const float *sig2 = sw + SW::S_OFF, *inv = sw + SW::I_OFF;
   const int *order = reinterpret_cast<const int *>(sw + SW::O_OFF);
   const int *piv = reinterpret_cast<const int *>(sw + SW::P_OFF);

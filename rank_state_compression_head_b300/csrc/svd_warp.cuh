@@ -47,7 +47,7 @@ struct SvdWarpSmem {
 // of R^T J by seat (T[seat * TP + s]), sig2/inv by seat, order, piv.  Returns
 // the sweeps (or -1).
 template <int MR>
-__device__ int svd_warp_core(int m, float tol, float *sw) {
+__device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
   using L = SvdWarpSmem<MR>;
   constexpr bool TWO = MR > 32;
   constexpr int RPL = (MR + 31) / 32;  // rows per lane in the reflector
@@ -207,7 +207,7 @@ __device__ int svd_warp_core(int m, float tol, float *sw) {
   // 1; seat 0 stays); the square holds every seat between rounds ------------------------------
   int sweeps = 0;
   if (m >= 2) {
-    const float tol2 = tol * tol, stop2 = tol;  // tol_stop = sqrt(tol)
+    const float tol2 = tol * tol, stop2 = tol_stop * tol_stop;
     const int nextA = seatA == nn - 1 ? 1 : seatA + 1;
     const int nextB = seatB == 0 ? 0 : (seatB == nn - 1 ? 1 : seatB + 1);
     int colA = seatA, colB = seatB;  // columns at my seats (>= m: the zero seat)
