@@ -248,11 +248,13 @@ def run_gpu(args, w):
     import torch
     import torch.distributed as dist
     from rank_state_compression_head_b300 import accounting as acc
+    from rank_state_compression_head_b300 import sharding
     from rank_state_compression_head_b300.workload import DEFAULT_WS_HEADS, DeviceRun
 
     ws, rank, local = dist_env()
     if ws > 1:
         dist.init_process_group('nccl')
+    w = sharding.shard(w, rank, ws)  # each rank: its own batch of requests of the workload's shapes
     torch.cuda.set_device(local)
     dev = torch.device('cuda', local)
     stream = torch.cuda.current_stream()
@@ -363,11 +365,8 @@ def run_gpu(args, w):
     rec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in rec_steps]
     step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
     total_ms = sum(step_ms)
-    if ws > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    heads_all = run.H * ws
+    total_ms = sharding.max_over_ranks(total_ms, device=dev)
+    heads_all = sharding.job_heads(run.H, ws)
     value = heads_all * K / (total_ms / 1e3)
     clocks = clk.summary(c0, c1)
     sw = sweeps.cpu().numpy()
@@ -421,7 +420,7 @@ def run_gpu(args, w):
                config=dict(workload=w.name, heads_per_gpu=run.H, d_k=w.d_k, d_v=w.d_v, r=w.r_max,
                            T=w.T, factor_dtype=w.factor_dtype, variant=w.variant,
                            l2='flushed before every timed step (256 MiB write then 256 MiB read, untimed)',
-                           parallelism=f'heads sharded, {ws} replica(s)'),
+                           parallelism=f'heads sharded over {ws} rank(s), one batch of requests each'),
                roofline=dominant, gpu_launches=K + rec_launches * len(rec_ms), clocks=clocks)
     out['decode'] = dict(head_steps_per_s=round(heads_all * K / (dec_total / 1e3)),
                          us_per_step=round(dec_avg_ms * 1e3, 3), gbs=round(dec_gbs, 1),
@@ -550,10 +549,7 @@ def run_gpu(args, w):
         for e in h2d_done + comp_done + d2h_done:
             rt.cudaEventDestroy(e)
         e2e_ms = e0.elapsed_time(e1)
-        if ws > 1:
-            tt = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = sharding.max_over_ranks(e2e_ms, device=dev)
         out['e2e'] = dict(value=round(heads_all * K / (e2e_ms / 1e3)), unit=UNIT,
                           h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
                           ms_per_step=round(e2e_ms / K, 5))
@@ -561,7 +557,7 @@ def run_gpu(args, w):
     # ---- CPU oracle baseline (rank 0, N = 1) --------------------------------------------
     if rank == 0 and ws == 1 and not args.no_cpu:
         out['cpu_baseline'] = oracle_sample(w, args.cpu_seconds)
-    if rank == 0:
+    if sharding.reports(rank):
         print(json.dumps(out), flush=True)
     if ws > 1:
         dist.destroy_process_group()
