@@ -1,8 +1,10 @@
 // Device building blocks of the compression kernels: Householder QR of a
-// factor panel, the explicit Q, and the one-sided Jacobi SVD of the core.
-// Used by the single-kernel compression (recompress.cu) and by the
-// three-phase recompression over a workspace (recompress_split.cu), which
-// therefore perform the same arithmetic.
+// factor panel in shared memory, the explicit Q, pivoted QR and the
+// seat-indexed one-sided Jacobi SVD of the core.  Used whole by the single-kernel
+// recompression and the dense compression (recompress.cu); the three-phase
+// recompression (recompress_split.cu) takes the constants, the seat geometry
+// and the column helpers from here and lays the same steps out in registers
+// (qr_registers.cuh) and per warp (svd_warp.cuh).
 #pragma once
 
 #include "common.cuh"
@@ -128,10 +130,10 @@ __device__ static void form_q(float *A, int ld, int nrows, int ncols, const floa
   }
 }
 
-// Geometry of the core K (n x n) in shared memory for the Jacobi rounds: the
-// threads of a column pair own contiguous chunks of R = ld / tpp rows (R a
-// multiple of 4, rows n..ld-1 are zero), columns are cs = ld + 4 floats apart
-// so that 16-byte accesses of different columns spread over the banks.
+// Thread geometry of the Jacobi rounds on an n x n core: tpp threads per column
+// pair (as many as fit in nthreads, at most 32, at least 8 rows each), each
+// owning R = ld / tpp rows (R a multiple of 4, rows n..ld-1 zero); cs is the
+// column stride (refined by seat_geom).
 struct JacobiGeom {
   int tpp, ld, cs;
 };
@@ -143,95 +145,7 @@ __host__ __device__ inline JacobiGeom jacobi_geom(int n, int nthreads) {
   const int ld = (n + 4 * tpp - 1) / (4 * tpp) * (4 * tpp);
   return JacobiGeom{tpp, ld, ld + 4};
 }
-__host__ inline int jacobi_cs_alloc(int m_max, int nthreads) {
-  int cs = 4;
-  for (int n = 0; n <= m_max; ++n) {
-    const int c = jacobi_geom(n, nthreads).cs;
-    cs = c > cs ? c : cs;
-  }
-  return cs;
-}
 
-// One-sided (Hestenes) Jacobi on the n columns of K: rotate pairs of columns
-// until every pair is orthogonal, K <- K J, so that the columns of K J are
-// X Sigma.  The rotations J are not kept: the rebuild uses the original core.
-// Round-robin pair order: n' = n rounded up to even seats, seat 0 fixed, the
-// others move one seat each round; pair i joins seats i and n'-1-i.  A pair is
-// rotated when (k_p . k_q)^2 > tol^2 |k_p|^2 |k_q|^2 and both columns are above
-// fp32 resolution of the core (scaled to a largest entry in [1/2, 1)).  Each
-// thread keeps its chunk of both columns in registers through a round.  Whole
-// block of NT threads.  Returns the number of sweeps, or -1 if the sweep limit
-// was reached.
-template <int NT, int RMAX>
-__device__ static int jacobi_svd(float *K, int n, const JacobiGeom &g, float tol) {
-  if (n < 2) return 0;
-  const int tid = threadIdx.x;
-  const int nn = n + (n & 1);
-  const int P = nn / 2;
-  const int tpp = g.tpp, cs = g.cs;
-  const int R = g.ld / tpp, R4 = R / 4;
-  const int pair = tid / tpp, sub = tid % tpp;
-  const bool active = pair < P;
-  const float tol2 = tol * tol;
-  // seat s >= 1 holds column 1 + (s - 1 + round) mod (n' - 1): advance by one per round
-  int p = active ? pair : 0, q = active ? nn - 1 - pair : 0;
-  for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
-    int rotated = 0;
-    for (int round = 0; round < nn - 1; ++round) {
-      const bool real = active && p < n && q < n;
-      float4 xp[RMAX / 4], xq[RMAX / 4];
-      float al = 0.f, be = 0.f, ga = 0.f;
-      float4 *kp = reinterpret_cast<float4 *>(K + p * cs + sub * R);
-      float4 *kq = reinterpret_cast<float4 *>(K + q * cs + sub * R);
-      if (real) {
-#pragma unroll
-        for (int v = 0; v < RMAX / 4; ++v) {
-          if (v < R4) {
-            xp[v] = kp[v];
-            xq[v] = kq[v];
-            al = fmaf(xp[v].x, xp[v].x, fmaf(xp[v].y, xp[v].y, fmaf(xp[v].z, xp[v].z, fmaf(xp[v].w, xp[v].w, al))));
-            be = fmaf(xq[v].x, xq[v].x, fmaf(xq[v].y, xq[v].y, fmaf(xq[v].z, xq[v].z, fmaf(xq[v].w, xq[v].w, be))));
-            ga = fmaf(xp[v].x, xq[v].x, fmaf(xp[v].y, xq[v].y, fmaf(xp[v].z, xq[v].z, fmaf(xp[v].w, xq[v].w, ga))));
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        if (o < tpp) {
-          al += __shfl_xor_sync(0xffffffffu, al, o);
-          be += __shfl_xor_sync(0xffffffffu, be, o);
-          ga += __shfl_xor_sync(0xffffffffu, ga, o);
-        }
-      }
-      if (real && al > kNegligible && be > kNegligible && ga * ga > tol2 * al * be) {
-        // Any t gives an exact rotation (c^2 + s^2 = 1 to rounding), so the angle
-        // may use fast reciprocals; |zeta| large (tiny ga) gives t ~ 1/(2 zeta).
-        const float zeta = (be - al) * __frcp_rn(2.f * ga);
-        const float az = fabsf(zeta);
-        const float root = az < 1e18f ? az + fmaf(az, az, 1.f) * rsqrtf(fmaf(az, az, 1.f)) : 2.f * az;
-        const float t = copysignf(__frcp_rn(root), zeta);
-        const float c = rsqrtf(fmaf(t, t, 1.f));
-        const float s = c * t;
-#pragma unroll
-        for (int v = 0; v < RMAX / 4; ++v) {
-          if (v < R4) {
-            const float4 a = xp[v], b = xq[v];
-            kp[v] = make_float4(fmaf(c, a.x, -s * b.x), fmaf(c, a.y, -s * b.y), fmaf(c, a.z, -s * b.z),
-                                fmaf(c, a.w, -s * b.w));
-            kq[v] = make_float4(fmaf(s, a.x, c * b.x), fmaf(s, a.y, c * b.y), fmaf(s, a.z, c * b.z),
-                                fmaf(s, a.w, c * b.w));
-          }
-        }
-        rotated = 1;
-      }
-      if (p != 0) p = p == nn - 1 ? 1 : p + 1;
-      q = q == nn - 1 ? 1 : q + 1;
-      __syncthreads();
-    }
-    if (!__syncthreads_or(rotated)) return sweep + 1;
-  }
-  return -1;
-}
 
 
 // ---------------------------------------------------------------------------
@@ -381,7 +295,11 @@ __host__ inline int seat_cs_alloc(int m_max, int nthreads) {
 // read from one buffer and written, rotated, to their next seats in the other,
 // so the 16-byte chunks that the threads of two adjacent pairs touch always
 // fall in distinct bank groups (chunk c of a pair's column goes to thread
-// c mod tpp).  Rotation rule and tolerance as jacobi_svd.  The sweeps stop
+// c mod tpp).  A pair is rotated when (k_p . k_q)^2 > tol^2 |k_p|^2 |k_q|^2 and
+// both columns are above fp32 resolution of the core (scaled to a largest entry
+// in [1/2, 1)); the angle comes from fast reciprocals, which is exact enough
+// because any t gives an orthogonal rotation (c^2 + s^2 = 1 to rounding), and
+// |zeta| large (tiny k_p . k_q) gives t ~ 1/(2 zeta).  The sweeps stop
 // after the first one in which no pair was further from orthogonal than
 // tol_stop (|cos| of the pair's angle): rotations converge quadratically, so
 // what is left after such a sweep is of order tol_stop^2 (tol_stop = sqrt(tol)

@@ -1,16 +1,16 @@
 // Recompression in three phases over a caller-provided device workspace.
 //
-// Same arithmetic, in the same order, as the single-kernel recompression in
-// recompress.cu ("Shallow Encoding Emits Deep Memories", thelatestinai.com list
-// view, Table 1: the decode compresses back to rank R every W steps), so both
-// give bit-identical factors.  Splitting it lets each phase hold only what it
-// needs in shared memory: the Jacobi rounds (the longest, latency-bound phase)
-// then run with about three times as many heads resident per SM.
+// The algorithm of the single-kernel recompression in recompress.cu ("Shallow
+// Encoding Emits Deep Memories", thelatestinai.com list view, Table 1: the
+// decode compresses back to rank R every W steps), laid out so that each phase
+// holds only what it needs: the factor panels in registers for the QR, one warp
+// per head for the core SVD, a GEMM-like rebuild.  The two paths agree to
+// rounding (the summation orders differ), not bit for bit.
 //
-//   qr_phase      one CTA of 128 threads per head: Householder QR of U_eff and
-//                 of W in two 64-thread teams, core K = R_a R_b^T, explicit Q_a
-//                 and Q_b; writes K, Q_a, Q_b to the workspace
-//   svd_phase     one CTA of 128 threads per head: pivoted QR of the core and
+//   qr_phase      one CTA per head, two teams (U_eff, W) of four threads per
+//                 column (qr_registers.cuh): Householder QR, explicit thin Q,
+//                 core K = R_a R_b^T; writes K, Q_a, Q_b to the workspace
+//   svd_phase     one warp per head (svd_warp.cuh): pivoted QR of the core and
 //                 one-sided Jacobi on R^T, ordering, truncation error; writes
 //                 the kept right singular vectors Y (y_k) and Z (z_k = K y_k)
 //   rebuild_phase one CTA per (head, factor): U = Q_a Z, W = Q_b Y; resets the
