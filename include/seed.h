@@ -188,10 +188,11 @@ int seed_recompress_workspace_bytes(const seed_state *st, int32_t heads, int64_t
  * intermediates through a caller-provided workspace: (1) per head, Householder
  * QR of U_eff and of W, the core K, the explicit Q_a and Q_b; (2) per head, the
  * Jacobi SVD of K, ordering and truncation error; (3) per head and factor, the
- * rebuild.  Each phase holds only its own operands in shared memory, so more
- * heads are resident per SM than in the single kernel of seed_recompress.
- * Results (factors, trunc_err, sweeps, status) are bit-identical to
- * seed_recompress_ex.
+ * rebuild.  Each phase has its own layout (the factor panels in registers, one
+ * warp per head for the core SVD), so more heads are resident per SM than in
+ * the single kernel of seed_recompress.  Same algorithm as seed_recompress_ex;
+ * the results agree with it to rounding (summation orders differ), not bit for
+ * bit.
  *   workspace        DEVICE memory owned by the caller, 16-byte aligned
  *   workspace_bytes  its size; heads are processed in groups of as many as it
  *                    holds (SEED_ERR_INVALID_ARG if not even one); groups of at
