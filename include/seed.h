@@ -122,10 +122,12 @@ int32_t seed_columns_per_head(int32_t variant, int32_t r, int32_t T);
  *   S          [n_heads][d_k][d_v] fp32, row-major per head (read only).
  *   st         writes a, the first rank(h) columns of U and W (U = X_r Sigma_r,
  *              W = Y_r from the SVD C = X Sigma Y^T, largest singular values
- *              first), scales (or D) = 1; sets st->steps_since_compress = 0.
+ *              first; computed as U = C y_k, W = y_k), scales (or D) = 1; sets
+ *              st->steps_since_compress = 0.
  *   trunc_err  [n_heads] |C - U W^T|_F, or NULL.
- * One-sided Jacobi SVD after a Householder QR, fp32; per-head status 6 if the
- * sweep limit is reached (the factors are still written).
+ * Householder QR with column pivoting C P = Q R, then one-sided Jacobi on R^T
+ * (R^T J = V Sigma, y = P v), fp32; per-head status 6 if the sweep limit is
+ * reached (the factors are still written).
  */
 int seed_compress_dense(const float *S, seed_state *st, float *trunc_err, seed_stream_t stream);
 
@@ -159,9 +161,9 @@ int seed_decode_step(seed_state *st, const float *q, const float *k, const float
  * seed_recompress — factors back to rank r (list view, Table 1, every T steps;
  * error bound: summary, Open-Loop Error Bound (Corollary 4)).
  * A = U_eff, B = W (m columns each); Householder QR A = Q_a R_a, B = Q_b R_b;
- * core K = R_a R_b^T; one-sided Jacobi SVD K = X Sigma Y^T; keep the rank(h)
- * largest: U = Q_a X_r, W = Q_b K^T X_r (= Q_b Y_r Sigma_r); scales (or D) = 1;
- * a unchanged.
+ * core K = R_a R_b^T = X Sigma Y^T, found as K P = Q R (column pivoting) and a
+ * one-sided Jacobi on R^T (R^T J = V Sigma, Y = P V); keep the rank(h) largest:
+ * U = Q_a K Y_r (= Q_a X_r Sigma_r), W = Q_b Y_r; scales (or D) = 1; a unchanged.
  *   trunc_err  [n_heads] sqrt(sum of the discarded sigma^2), or NULL.
  * Sets st->steps_since_compress = 0.  Per-head status 6 if the sweep limit is hit.
  */
