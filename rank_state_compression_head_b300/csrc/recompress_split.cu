@@ -48,7 +48,10 @@ struct SplitArgs {
   float *ws;
   int head0;     // first head of this chunk; workspace slot b serves head head0 + b
   int n_group;   // heads in this chunk
-  int m_max, r_max;
+  int m_max;     // this launch serves heads with m_lo < m <= m_max (its thread and
+  int m_lo;      //   shared-memory sizes follow m_max); m_lo = -1: every head
+  int layout_m;  // column count the workspace layout is sized for (the call's m_max)
+  int r_max;
   float *trunc_err;
   int32_t *sweeps;
   int cs_alloc;
@@ -61,6 +64,7 @@ __device__ inline bool split_head_ok(const StateView &sv, int h, int m_max, int 
   m = r + sv.growth * sv.steps;
   return r >= 0 && m <= m_max;
 }
+__device__ inline bool in_class(const SplitArgs &p, int m) { return m > p.m_lo && m <= p.m_max; }
 
 // ---- phase 1: QR of both factors, core, explicit Q --------------------------------------
 // Two teams of kTPC x m_max threads (the second starts on a warp boundary),
@@ -76,7 +80,7 @@ __global__ void __maxnreg__(80) qr_phase(const SplitArgs p) {
   const int tid = threadIdx.x;
   const StateView &sv = p.sv;
   int r, m;
-  if (!split_head_ok(sv, h, p.m_max, r, m)) return;  // reported by the SVD phase
+  if (!split_head_ok(sv, h, p.layout_m, r, m) || !in_class(p, m)) return;  // bad ranks: reported by the SVD phase
   const int mm = p.m_max;
   const int up = (mm + 3) & ~3;
   const int wbase = qr_team_stride(mm);
@@ -145,7 +149,7 @@ __global__ void __maxnreg__(80) qr_phase(const SplitArgs p) {
     }
   }
   __syncthreads();
-  const SplitLayout L(p.m_max, p.r_max, DK, DV);
+  const SplitLayout L(p.layout_m, p.r_max, DK, DV);
   float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
   // ---- explicit thin Q: column l = H_0 ... H_l e_l, each column on its own ------------------
   if (mine) {
@@ -183,13 +187,14 @@ __global__ void __launch_bounds__(32 * kSvdWarps) svd_phase(const SplitArgs p) {
   const int h = p.head0 + b;
   const StateView &sv = p.sv;
   int r, m;
-  if (!split_head_ok(sv, h, p.m_max, r, m)) {  // rank table disagrees with r_max: touch nothing
+  if (!split_head_ok(sv, h, p.layout_m, r, m)) {  // rank table disagrees with r_max: touch nothing
     if (lane == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
     return;
   }
+  if (!in_class(p, m)) return;  // served by the launch of its column class
   float *sw = smem + warp * SW::FLOATS;
   float *T = sw + SW::T_OFF;
-  const SplitLayout L(p.m_max, p.r_max, DK, DV);
+  const SplitLayout L(p.layout_m, p.r_max, DK, DV);
   float *ws = p.ws + (int64_t)b * L.per_head;
   const float *Kw = ws + L.k;
 
@@ -258,8 +263,8 @@ __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p
   const int tid = threadIdx.x;
   const StateView &sv = p.sv;
   int r, m;
-  if (!split_head_ok(sv, h, p.m_max, r, m)) return;
-  const SplitLayout L(p.m_max, p.r_max, DK, DV);
+  if (!split_head_ok(sv, h, p.layout_m, r, m) || !in_class(p, m)) return;
+  const SplitLayout L(p.layout_m, p.r_max, DK, DV);
   const float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
   const int rows = panel == 0 ? DK : DV;
   const int rk = r < m ? r : m;
@@ -353,12 +358,26 @@ static cudaError_t launch_split_v(const SplitArgs &a, int n, int64_t chunk, cuda
 cudaError_t launch_recompress_split(const StateView &sv, int factor_dtype, float *trunc_err,
                                     int32_t *sweeps, int m_max, int r_max, float *ws,
                                     int64_t chunk, cudaStream_t s) {
-  SplitArgs a{sv, ws, 0, 0, m_max, r_max, trunc_err, sweeps, 0};
+  SplitArgs a{sv, ws, 0, 0, m_max, -1, m_max, r_max, trunc_err, sweeps, 0};
   const int n = sv.n_heads;
-  if (factor_dtype == SEED_BF16)
-    return sv.d_v == 64 ? launch_split_v<__nv_bfloat16, 64>(a, n, chunk, s)
-                        : launch_split_v<__nv_bfloat16, 128>(a, n, chunk, s);
-  return sv.d_v == 64 ? launch_split_v<float, 64>(a, n, chunk, s) : launch_split_v<float, 128>(a, n, chunk, s);
+  auto one = [&](const SplitArgs &x) {
+    if (factor_dtype == SEED_BF16)
+      return sv.d_v == 64 ? launch_split_v<__nv_bfloat16, 64>(x, n, chunk, s)
+                          : launch_split_v<__nv_bfloat16, 128>(x, n, chunk, s);
+    return sv.d_v == 64 ? launch_split_v<float, 64>(x, n, chunk, s) : launch_split_v<float, 128>(x, n, chunk, s);
+  };
+  if (!sv.rank || m_max <= 16) return one(a);
+  // Ragged ranks: one launch per column class (m in (16c - 16, 16c]), each sized
+  // for its class, so that small heads do not run in the threads, registers and
+  // loop lengths of the largest; heads of other classes leave at once.
+  for (int hi = 16; hi - 16 < m_max; hi += 16) {
+    SplitArgs c = a;
+    c.m_max = hi < m_max ? hi : m_max;
+    c.m_lo = hi - 16;
+    const cudaError_t e = one(c);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // ---- fixed scratch for seed_recompress_noalloc ---------------------------------------------
