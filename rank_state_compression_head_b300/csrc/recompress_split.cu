@@ -174,15 +174,23 @@ __global__ void __maxnreg__(80) qr_phase(const SplitArgs p) {
   }
 }
 
-// ---- phase 2: SVD of the core, one warp per head (svd_warp.cuh) ---------------------------
-// MR: rows and columns of the core held per lane (m_max rounded up to 16).
+// ---- phase 2: SVD of the core, one lane group per head (svd_warp.cuh) ---------------------
+// MR: rows and columns of the core held per lane (m_max rounded up to 16); a
+// group is a warp, or a half warp when MR <= 32 (two heads per warp).
+template <int MR>
+constexpr int svd_group() { return MR <= 32 ? 16 : 32; }
+template <int MR>
+constexpr int svd_heads_per_cta() { return kSvdWarps * (32 / svd_group<MR>()); }
+
 template <typename TF, int DV, int MR>
 __global__ void __launch_bounds__(32 * kSvdWarps) svd_phase(const SplitArgs p) {
   constexpr int DK = kDK;
+  constexpr int HW = svd_group<MR>();
   using SW = SvdWarpSmem<MR>;
   extern __shared__ __align__(16) float smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kSvdWarps + warp;
+  const int grp = threadIdx.x / HW, lane = threadIdx.x & (HW - 1);
+  const unsigned gmask = HW == 32 ? 0xffffffffu : 0xffffu << (threadIdx.x & 16);
+  const int b = blockIdx.x * svd_heads_per_cta<MR>() + grp;
   if (b >= p.n_group) return;
   const int h = p.head0 + b;
   const StateView &sv = p.sv;
@@ -192,7 +200,7 @@ __global__ void __launch_bounds__(32 * kSvdWarps) svd_phase(const SplitArgs p) {
     return;
   }
   if (!in_class(p, m)) return;  // served by the launch of its column class
-  float *sw = smem + warp * SW::FLOATS;
+  float *sw = smem + grp * SW::FLOATS;
   float *T = sw + SW::T_OFF;
   const SplitLayout L(p.layout_m, p.r_max, DK, DV);
   float *ws = p.ws + (int64_t)b * L.per_head;
@@ -201,24 +209,25 @@ __global__ void __launch_bounds__(32 * kSvdWarps) svd_phase(const SplitArgs p) {
   // core into the square (coalesced reads; rows m..MR-1 zero), scaled by a power
   // of two to a largest entry in [1/2, 1)
   float kmax = 0.f;
-  for (int idx = lane; idx < m * MR; idx += 32) {
+  for (int idx = lane; idx < m * MR; idx += HW) {
     const int c = idx / MR, rr = idx % MR;
     const float x = rr < m ? Kw[c * m + rr] : 0.f;  // column c, row rr
     T[c * SW::TP + rr] = x;
     kmax = fmaxf(kmax, fabsf(x));
   }
-  kmax = warp_max(kmax);
+#pragma unroll
+  for (int o = HW / 2; o > 0; o >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(gmask, kmax, o));
   int kexp = 0;
   if (kmax > 0.f) frexpf(kmax, &kexp);
   const float kscale = ldexpf(1.f, -kexp), kunscale = ldexpf(1.f, kexp);
-  __syncwarp();
-  for (int idx = lane; idx < m * MR; idx += 32) T[(idx / MR) * SW::TP + idx % MR] *= kscale;
-  __syncwarp();
+  __syncwarp(gmask);
+  for (int idx = lane; idx < m * MR; idx += HW) T[(idx / MR) * SW::TP + idx % MR] *= kscale;
+  __syncwarp(gmask);
   // bf16 factors: 1e-4 (their own rounding is 2^-9), stop once no pair is beyond
   // sqrt(tol); fp32: four times the rounding noise of a length-m dot product
   // (sqrt(m) eps), run until no pair is beyond tol
   const float tol = sizeof(TF) == 2 ? 1e-4f : 4.f * sqrtf((float)(m > 16 ? m : 16)) * FLT_EPSILON;
-  const int sweeps = svd_warp_core<MR>(m, tol, sizeof(TF) == 2 ? sqrtf(tol) : tol, sw);
+  const int sweeps = svd_warp_core<MR, HW>(m, tol, sizeof(TF) == 2 ? sqrtf(tol) : tol, sw);
   const float *sig2 = sw + SW::S_OFF, *inv = sw + SW::I_OFF;
   const int *order = reinterpret_cast<const int *>(sw + SW::O_OFF);
   const int *piv = reinterpret_cast<const int *>(sw + SW::P_OFF);
@@ -239,8 +248,8 @@ __global__ void __launch_bounds__(32 * kSvdWarps) svd_phase(const SplitArgs p) {
     const int col = order[k];
     const float ik = inv[col];
     const float *f = T + col * SW::TP;
-    for (int s = lane; s < m4; s += 32) Y[k * L.m4 + (s < m ? piv[s] : s)] = s < m ? f[s] * ik : 0.f;
-    for (int l = lane; l < m4; l += 32) {
+    for (int s = lane; s < m4; s += HW) Y[k * L.m4 + (s < m ? piv[s] : s)] = s < m ? f[s] * ik : 0.f;
+    for (int l = lane; l < m4; l += HW) {
       float acc = 0.f;
       if (l < m)
         for (int s = 0; s < m; ++s) acc = fmaf(Kw[piv[s] * m + l], f[s], acc);
@@ -318,7 +327,7 @@ static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaS
   const int up = (a.m_max + 3) & ~3;
   const int qr_bytes = (a.m_max * (kDK + DV) + 4 * up + 2 * a.m_max * a.m_max) * 4;
   const int qr_threads = a.m_max > 0 ? qr_team_stride(a.m_max) * 2 : 32;
-  const int svd_bytes = kSvdWarps * SvdWarpSmem<MR>::FLOATS * 4;
+  const int svd_bytes = svd_heads_per_cta<MR>() * SvdWarpSmem<MR>::FLOATS * 4;
   const int rb_bytes = ((a.r_max + 3) / 4 * 4 * MR > 0 ? (a.r_max + 3) / 4 * 4 * MR : 4) * 4;
   auto k1 = qr_phase<VAR, TF, DV>;
   auto k2 = svd_phase<TF, DV, MR>;
@@ -332,7 +341,7 @@ static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaS
     a.head0 = (int)h0;
     a.n_group = n;
     k1<<<n, qr_threads, qr_bytes, s>>>(a);
-    k2<<<(n + kSvdWarps - 1) / kSvdWarps, 32 * kSvdWarps, svd_bytes, s>>>(a);
+    k2<<<(n + svd_heads_per_cta<MR>() - 1) / svd_heads_per_cta<MR>(), 32 * kSvdWarps, svd_bytes, s>>>(a);
     k3<<<dim3(n, 2), kSplitThreads, rb_bytes, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -1,13 +1,16 @@
-// SVD of the recompression core with one warp per head and the core in
-// registers: pivoted Householder QR K P = Q R, then one-sided Jacobi on the
-// columns of R^T (the algorithm of core_factor in recompress_core.cuh, laid
-// out for a warp instead of a CTA, so that no block barrier is needed).
+// SVD of the recompression core with one lane group per head: pivoted
+// Householder QR K P = Q R, then one-sided Jacobi on the columns of R^T (the
+// algorithm of core_factor in recompress_core.cuh, laid out for a group of HW
+// lanes instead of a CTA, so that no block barrier is needed).  A group is a
+// warp, or a half warp for cores of at most 32 columns (two heads per warp:
+// such a core has at most 16 column pairs); every shuffle, vote and warp
+// barrier names only the group's lanes.
 //
 // Pivoted QR: the core sits in the warp's shared square, column c at
 // c * TP (TP = MR + 4: the 16-byte chunks of eight consecutive columns fall in
-// distinct bank groups); lane l looks after columns l and l + 32.  Each step
-// the warp picks the remaining column of largest trailing norm (shuffle argmax,
-// ties to the lower index), the 32 lanes form the reflector from it (norm in one
+// distinct bank groups); lane l looks after columns l and l + HW.  Each step
+// the group picks the remaining column of largest trailing norm (shuffle argmax,
+// ties to the lower index), its lanes form the reflector from it (norm in one
 // reduction, max-scaled near the fp32 range ends, as householder_qr), and every
 // lane applies it to its remaining columns with 16-byte loads, refreshing their
 // trailing norms.  Columns stay in place; only the pivot order is recorded.
@@ -42,18 +45,30 @@ struct SvdWarpSmem {
   static constexpr int FLOATS = P_OFF + MR;
 };
 
-// One warp: pivoted QR of the scaled core held in the square T (column c at
+// One lane group: pivoted QR of the scaled core held in the square T (column c at
 // T[c * TP], rows m..MR-1 zero), then Jacobi on R^T.  Leaves in T the columns
 // of R^T J by seat (T[seat * TP + s]), sig2/inv by seat, order, piv.  Returns
 // the sweeps (or -1).
-template <int MR>
+template <int MR, int HW>
 __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
   using L = SvdWarpSmem<MR>;
-  constexpr bool TWO = MR > 32;
-  constexpr int RPL = (MR + 31) / 32;  // rows per lane in the reflector
+  static_assert(HW == 16 || HW == 32, "a lane group is a half warp or a warp");
+  static_assert(MR <= 2 * HW, "two columns per lane at most");
+  constexpr bool TWO = MR > HW;
+  constexpr int RPL = (MR + HW - 1) / HW;  // rows per lane in the reflector
   constexpr int TP = L::TP;
-  const int lane = threadIdx.x & 31;
-  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & (HW - 1);
+  const unsigned full = HW == 32 ? 0xffffffffu : 0xffffu << (threadIdx.x & 16);  // my group
+  auto gsum = [&](float x) {
+#pragma unroll
+    for (int o = HW / 2; o > 0; o >>= 1) x += __shfl_xor_sync(full, x, o);
+    return x;
+  };
+  auto gmax = [&](float x) {
+#pragma unroll
+    for (int o = HW / 2; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(full, x, o));
+    return x;
+  };
   float *T = sw + L::T_OFF, *vrow = sw + L::V_OFF, *sig2 = sw + L::S_OFF, *inv = sw + L::I_OFF;
   int *order = reinterpret_cast<int *>(sw + L::O_OFF);
   int *piv = reinterpret_cast<int *>(sw + L::P_OFF);
@@ -75,15 +90,15 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
     }
     return a;
   };
-  bool done0 = lane >= m, done1 = !TWO || lane + 32 >= m;
-  float vn0 = done0 ? 0.f : colnorm(lane, 0), vn1 = done1 ? 0.f : colnorm(lane + 32, 0);
+  bool done0 = lane >= m, done1 = !TWO || lane + HW >= m;
+  float vn0 = done0 ? 0.f : colnorm(lane, 0), vn1 = done1 ? 0.f : colnorm(lane + HW, 0);
   for (int j = 0; j < m; ++j) {
     float best = -1.f;
     int bi = 1 << 20;
     if (!done0) { best = vn0; bi = lane; }
-    if (!done1 && vn1 > best) { best = vn1; bi = lane + 32; }
+    if (!done1 && vn1 > best) { best = vn1; bi = lane + HW; }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int o = HW / 2; o > 0; o >>= 1) {
       const float ob = __shfl_xor_sync(full, best, o);
       const int oi = __shfl_xor_sync(full, bi, o);
       if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
@@ -92,7 +107,7 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
     float *cp = T + pc * TP;
     float a[RPL];
 #pragma unroll
-    for (int e = 0; e < RPL; ++e) a[e] = lane + 32 * e < MR ? cp[lane + 32 * e] : 0.f;
+    for (int e = 0; e < RPL; ++e) a[e] = lane + HW * e < MR ? cp[lane + HW * e] : 0.f;
     const float alpha = cp[j];
     float tj = 0.f, beta = alpha, sc = 0.f;
     // one reduction for the norm unless it nears the ends of the fp32 range
@@ -100,26 +115,26 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
     float ss = 0.f;
 #pragma unroll
     for (int e = 0; e < RPL; ++e) {
-      const float x = lane + 32 * e > j ? a[e] : 0.f;
+      const float x = lane + HW * e > j ? a[e] : 0.f;
       ss = fmaf(x, x, ss);
     }
-    ss = warp_sum(ss);
+    ss = gsum(ss);
     float amax = 1.f;
     if (!(ss >= 1e-30f && ss <= 1e30f)) {
       amax = 0.f;
 #pragma unroll
       for (int e = 0; e < RPL; ++e)
-        if (lane + 32 * e >= j) amax = fmaxf(amax, fabsf(a[e]));
-      amax = warp_max(amax);
+        if (lane + HW * e >= j) amax = fmaxf(amax, fabsf(a[e]));
+      amax = gmax(amax);
       ss = 0.f;
       if (amax >= FLT_MIN) {
         const float rinv = 1.f / amax;
 #pragma unroll
         for (int e = 0; e < RPL; ++e) {
-          const float xs = lane + 32 * e > j ? a[e] * rinv : 0.f;
+          const float xs = lane + HW * e > j ? a[e] * rinv : 0.f;
           ss = fmaf(xs, xs, ss);
         }
-        ss = warp_sum(ss);
+        ss = gsum(ss);
       }
     }
     if (ss > 0.f && amax >= FLT_MIN) {
@@ -130,28 +145,28 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
       sc = 1.f / ((as - bs) * amax);
       beta = bs * amax;
     }
-    __syncwarp();
+    __syncwarp(full);
     // v_j into the reflector row; the chosen column becomes column j of R (rows
     // above j were finished by the earlier steps, row j is beta, rows below zero)
 #pragma unroll
     for (int e = 0; e < RPL; ++e) {
-      const int r = lane + 32 * e;
+      const int r = lane + HW * e;
       if (r < MR) {
         vrow[r] = r < j ? 0.f : r == j ? 1.f : a[e] * sc;
         if (r >= j) cp[r] = r == j ? beta : 0.f;
       }
     }
     if (lane == 0) piv[j] = pc;
-    if (lane == (pc & 31)) {
-      if (pc >= 32) done1 = true;
+    if (lane == (pc & (HW - 1))) {
+      if (pc >= HW) done1 = true;
       else done0 = true;
     }
-    __syncwarp();
+    __syncwarp(full);
     // the remaining columns: a -= tau (v . a) v, then their norms below row j
 #pragma unroll
     for (int h = 0; h < (TWO ? 2 : 1); ++h) {
       if (h == 0 ? done0 : done1) continue;
-      float4 *x4 = reinterpret_cast<float4 *>(T + (lane + 32 * h) * TP);
+      float4 *x4 = reinterpret_cast<float4 *>(T + (lane + HW * h) * TP);
       float d = 0.f;
 #pragma unroll
       for (int q = 0; q < MR / 4; ++q) {
@@ -176,7 +191,7 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
       if (h == 0) vn0 = nrm;
       else vn1 = nrm;
     }
-    __syncwarp();
+    __syncwarp(full);
   }
 
   // ---- R^T to the seats of the Jacobi: seat i = row i of R, R column s = T[piv[s] * TP] -------
@@ -191,7 +206,7 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
       A[s] = (active && s < m && seatA < m) ? T[c * TP + seatA] : 0.f;
       B[s] = (active && s < m && seatB < m) ? T[c * TP + seatB] : 0.f;
     }
-    __syncwarp();
+    __syncwarp(full);
     if (active) {  // seat s at T[s * TP] from here on (the core is no longer needed)
 #pragma unroll
       for (int q = 0; q < MR / 4; ++q) {
@@ -199,7 +214,7 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
         reinterpret_cast<float4 *>(T + seatB * TP)[q] = make_float4(B[4 * q], B[4 * q + 1], B[4 * q + 2], B[4 * q + 3]);
       }
     }
-    __syncwarp();
+    __syncwarp(full);
   }
 
   // ---- Jacobi: each round every lane reads its two seats, rotates them in
@@ -211,7 +226,7 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
     const int nextA = seatA == nn - 1 ? 1 : seatA + 1;
     const int nextB = seatB == 0 ? 0 : (seatB == nn - 1 ? 1 : seatB + 1);
     int colA = seatA, colB = seatB;  // columns at my seats (>= m: the zero seat)
-    const unsigned amask = P >= 32 ? full : (1u << P) - 1;  // the active lanes
+    const unsigned amask = P >= HW ? full : ((1u << P) - 1) << (HW == 32 ? 0 : (threadIdx.x & 16));  // active lanes
     sweeps = -1;
     for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
       int far = 0;
@@ -265,7 +280,7 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
           if (seatA != 0) colA = colA == 1 ? nn - 1 : colA - 1;
           if (seatB != 0) colB = colB == 1 ? nn - 1 : colB - 1;
         }
-        __syncwarp();
+        __syncwarp(full);
       }
       if (!__any_sync(full, far)) {
         sweeps = sweep + 1;
@@ -277,7 +292,7 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
   // ---- columns of R^T J by seat (already in place after whole sweeps), sigma^2 -------------
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    const int j = lane + 32 * e;
+    const int j = lane + HW * e;
     if (j < m) {
       const float4 *f4 = reinterpret_cast<const float4 *>(T + j * TP);
       float acc = 0.f;
@@ -290,10 +305,10 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
       inv[j] = acc > kNegligible ? rsqrtf(acc) : 0.f;
     }
   }
-  __syncwarp();
+  __syncwarp(full);
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    const int j = lane + 32 * e;
+    const int j = lane + HW * e;
     if (j < m) {
       int rank = 0;
       const float sj = sig2[j];
@@ -304,7 +319,7 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
       order[rank] = j;
     }
   }
-  __syncwarp();
+  __syncwarp(full);
   return sweeps;
 }
 
