@@ -382,7 +382,7 @@ cudaError_t launch_recompress_split(const StateView &sv, int factor_dtype, float
   for (int hi = 16; hi - 16 < m_max; hi += 16) {
     SplitArgs c = a;
     c.m_max = hi < m_max ? hi : m_max;
-    c.m_lo = hi - 16;
+    c.m_lo = hi == 16 ? -1 : hi - 16;  // the first class also takes heads with no columns
     const cudaError_t e = one(c);
     if (e != cudaSuccess) return e;
   }

@@ -118,3 +118,29 @@ def test_ws_rank_zero_and_no_columns():
     for h in range(H):
         assert rel_err(S[h], oracle.materialize(states[h])) < 1e-6
     assert int(buf.status.abs().sum()) == 0
+
+
+@pytest.mark.parametrize('s', [0, 3])
+def test_ws_ragged_with_empty_heads(s):
+    # a rank table with rank-0 heads: with s = 0 they hold no column at all and
+    # still get status OK, zero truncation error and zero sweeps
+    H, T = 8, 8
+    ranks = np.array([0, 5, 0, 20, 0, 33, 12, 0], dtype=np.int32)
+    states, vbar = random_states(47 + s, H, 128, 128, ranks, s, T, 'gdn', 'bf16')
+    buf = make_buffers('gdn', 'bf16', H, 128, 128, T, vbar, ranks)
+    upload(buf, states, s)
+    buf.status.fill_(-1)
+    ws, nbytes = workspace(buf, H)
+    err = torch.full((H,), -1.0, device='cuda')
+    sw = torch.full((H,), -7, device='cuda', dtype=torch.int32)
+    R.seed_recompress_ws(buf.st, err, sw, ws, nbytes)
+    S = gpu_dense(buf)
+    assert int(buf.status.abs().sum()) == 0
+    err = err.double().cpu().numpy()
+    sw = sw.cpu().numpy()
+    for h in range(H):
+        ref, e_ref = oracle.recompress(states[h], int(ranks[h]))
+        assert rel_err(S[h], oracle.materialize(ref)) < TOL['bf16'], h
+        assert abs(err[h] - e_ref) <= TOL['bf16'] * max(e_ref, 1e-3 * np.linalg.norm(S[h])), h
+        if ranks[h] + s == 0:
+            assert err[h] == 0.0 and sw[h] == 0, h
