@@ -183,7 +183,7 @@ template <int MR>
 constexpr int svd_heads_per_cta() { return kSvdWarps * (32 / svd_group<MR>()); }
 
 template <typename TF, int DV, int MR>
-__global__ void __launch_bounds__(32 * kSvdWarps) svd_phase(const SplitArgs p) {
+__global__ void __launch_bounds__(32 * kSvdWarps, MR <= 48 ? 8 : 6) svd_phase(const SplitArgs p) {
   constexpr int DK = kDK;
   constexpr int HW = svd_group<MR>();
   using SW = SvdWarpSmem<MR>;

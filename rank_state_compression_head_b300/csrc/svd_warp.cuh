@@ -12,16 +12,18 @@
 // the group picks the remaining column of largest trailing norm (shuffle argmax,
 // ties to the lower index), its lanes form the reflector from it (norm in one
 // reduction, max-scaled near the fp32 range ends, as householder_qr), and every
-// lane applies it to its remaining columns with 16-byte loads, refreshing their
-// trailing norms.  Columns stay in place; only the pivot order is recorded.
+// lane applies it to its remaining columns with 16-byte loads and downdates
+// their trailing norms (summed in full again once cancellation has eaten most
+// of them).  Columns stay in place; only the pivot order is recorded.
 //
 // Jacobi: lane i (i < P = n'/2) looks after two seats, A and B: lane 0 has
 // seat n'-1 in A and the fixed seat 0 in B, lane i >= 1 has seat i in A and
-// seat n'-1-i in B.  The seats live in the square (seat s at s * TP, rows of
-// R^T); each round a lane reads its two seats into registers, rotates them and
-// writes them to their next seats (the column at seat s >= 1 moves to s + 1,
-// n'-1 to 1), one warp barrier between the reads and the writes and one at the
-// end of the round.  Rotation rule, tolerance and stopping rule as jacobi_seats.
+// seat n'-1-i in B.  The columns of R^T stay in the square (column i at
+// i * TP); a lane reads the two columns on its seats this round, rotates them in
+// registers and writes them back in place (only if it rotated them), one warp
+// barrier a round.  Rotation rule, tolerance and stopping rule as jacobi_seats;
+// the rotation is applied to scaled columns and the norms are carried from
+// round to round (see the loop).
 #pragma once
 
 #include "recompress_core.cuh"
@@ -92,6 +94,7 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
   };
   bool done0 = lane >= m, done1 = !TWO || lane + HW >= m;
   float vn0 = done0 ? 0.f : colnorm(lane, 0), vn1 = done1 ? 0.f : colnorm(lane + HW, 0);
+  float vr0 = vn0, vr1 = vn1;  // each column's trailing norm when last summed in full
   for (int j = 0; j < m; ++j) {
     float best = -1.f;
     int bi = 1 << 20;
@@ -174,19 +177,23 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
         d = fmaf(v.x, x.x, fmaf(v.y, x.y, fmaf(v.z, x.z, fmaf(v.w, x.w, d))));
       }
       const float t = tj * d;
-      float nrm = 0.f;
 #pragma unroll
       for (int q = 0; q < MR / 4; ++q) {
         const float4 v = v4[q];
         float4 x = x4[q];
         x.x = fmaf(-t, v.x, x.x); x.y = fmaf(-t, v.y, x.y); x.z = fmaf(-t, v.z, x.z); x.w = fmaf(-t, v.w, x.w);
         x4[q] = x;
-        const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float y = 4 * q + e > j ? xs[e] : 0.f;
-          nrm = fmaf(y, y, nrm);
-        }
+      }
+      // trailing norm below row j: take row j's square off the old one, and sum
+      // it in full again once that has cancelled to below sqrt(eps) of the last
+      // full sum (the column downdate of Businger and Golub's pivoted QR)
+      const int c = lane + HW * h;
+      const float xj = T[c * TP + j];
+      float nrm = (h == 0 ? vn0 : vn1) - xj * xj;
+      if (nrm <= 3.5e-4f * (h == 0 ? vr0 : vr1)) {
+        nrm = colnorm(c, j + 1);
+        if (h == 0) vr0 = nrm;
+        else vr1 = nrm;
       }
       if (h == 0) vn0 = nrm;
       else vn1 = nrm;
@@ -217,79 +224,131 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
     __syncwarp(full);
   }
 
-  // ---- Jacobi: each round every lane reads its two seats, rotates them in
-  // registers and writes them to their next seats (seat s >= 1 to s + 1, n'-1 to
-  // 1; seat 0 stays); the square holds every seat between rounds ------------------------------
+  // ---- Jacobi: the columns of R^T stay where they are (column i at T[i * TP]);
+  // each round lane i takes the pair that the round-robin puts on its two seats
+  // (the column at seat s >= 1 moves on to s + 1, n'-1 to 1, seat 0 stays) and
+  // writes the pair back only if it rotated it.  A column is kept scaled, true
+  // column = d * stored, with d and its squared norm in the row's pad
+  // (T[i * TP + MR], MR + 1): a rotation [c -s; s c] becomes
+  // a' = a - t (d_b / d_a) b, b' = b + t (d_a / d_b) a with both scales times c
+  // (one FMA an element instead of two), and the norms move as alpha - t gamma,
+  // beta + t gamma (Rutishauser's update).  Norms are summed in full on a
+  // sweep's first round and for a norm marked stale (negative) because its
+  // update lost more than two bits to cancellation; a pair with a column whose
+  // norm is known to be negligible is not read at all.
   int sweeps = 0;
   if (m >= 2) {
     const float tol2 = tol * tol, stop2 = tol_stop * tol_stop;
-    const int nextA = seatA == nn - 1 ? 1 : seatA + 1;
-    const int nextB = seatB == 0 ? 0 : (seatB == nn - 1 ? 1 : seatB + 1);
-    int colA = seatA, colB = seatB;  // columns at my seats (>= m: the zero seat)
-    const unsigned amask = P >= HW ? full : ((1u << P) - 1) << (HW == 32 ? 0 : (threadIdx.x & 16));  // active lanes
+    int colA = seatA, colB = seatB;  // the pair on my seats this round (>= m: the zero column)
+    if (active) {
+      *reinterpret_cast<float2 *>(T + seatA * TP + MR) = make_float2(1.f, -1.f);
+      *reinterpret_cast<float2 *>(T + seatB * TP + MR) = make_float2(1.f, -1.f);
+    }
+    __syncwarp(full);
     sweeps = -1;
     for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
       int far = 0;
       for (int round = 0; round < nn - 1; ++round) {
         if (active) {
-          float4 a4[MR / 4], b4[MR / 4];
-          const float4 *pa = reinterpret_cast<const float4 *>(T + seatA * TP);
-          const float4 *pb = reinterpret_cast<const float4 *>(T + seatB * TP);
-          float al0 = 0.f, al1 = 0.f, be0 = 0.f, be1 = 0.f, ga0 = 0.f, ga1 = 0.f;
-#pragma unroll
-          for (int q = 0; q < MR / 4; ++q) {
-            a4[q] = pa[q];
-            b4[q] = pb[q];
-            al0 = fmaf(a4[q].x, a4[q].x, fmaf(a4[q].y, a4[q].y, al0));
-            al1 = fmaf(a4[q].z, a4[q].z, fmaf(a4[q].w, a4[q].w, al1));
-            be0 = fmaf(b4[q].x, b4[q].x, fmaf(b4[q].y, b4[q].y, be0));
-            be1 = fmaf(b4[q].z, b4[q].z, fmaf(b4[q].w, b4[q].w, be1));
-            ga0 = fmaf(a4[q].x, b4[q].x, fmaf(a4[q].y, b4[q].y, ga0));
-            ga1 = fmaf(a4[q].z, b4[q].z, fmaf(a4[q].w, b4[q].w, ga1));
-          }
-          const float al = al0 + al1, be = be0 + be1, ga = ga0 + ga1;
-          float c = 1.f, sn = 0.f;
-          if (colA < m && colB < m && al > kNegligible && be > kNegligible && ga * ga > tol2 * al * be) {
-            const float zeta = (be - al) * __frcp_rn(2.f * ga);
-            const float az = fabsf(zeta);
-            const float root = az < 1e18f ? az + fmaf(az, az, 1.f) * rsqrtf(fmaf(az, az, 1.f)) : 2.f * az;
-            const float t = copysignf(__frcp_rn(root), zeta);
-            c = rsqrtf(fmaf(t, t, 1.f));
-            sn = c * t;
-            far |= ga * ga > stop2 * al * be;
-          }
-          __syncwarp(amask);  // every active lane has read its seats
-          float4 *wa = reinterpret_cast<float4 *>(T + nextA * TP);
-          float4 *wb = reinterpret_cast<float4 *>(T + nextB * TP);
-          if (sn != 0.f) {
+          float *ca = T + colA * TP, *cb = T + colB * TP;
+          const float2 sa = *reinterpret_cast<const float2 *>(ca + MR);
+          const float2 sb = *reinterpret_cast<const float2 *>(cb + MR);
+          const bool nega = sa.y >= 0.f && sa.y <= kNegligible, negb = sb.y >= 0.f && sb.y <= kNegligible;
+          if (colA < m && colB < m && !nega && !negb) {
+            float4 a4[MR / 4], b4[MR / 4];
+            const float4 *pa = reinterpret_cast<const float4 *>(ca);
+            const float4 *pb = reinterpret_cast<const float4 *>(cb);
+            float ga0 = 0.f, ga1 = 0.f;
 #pragma unroll
             for (int q = 0; q < MR / 4; ++q) {
-              const float4 a = a4[q], b = b4[q];
-              wa[q] = make_float4(fmaf(c, a.x, -sn * b.x), fmaf(c, a.y, -sn * b.y), fmaf(c, a.z, -sn * b.z),
-                                  fmaf(c, a.w, -sn * b.w));
-              wb[q] = make_float4(fmaf(sn, a.x, c * b.x), fmaf(sn, a.y, c * b.y), fmaf(sn, a.z, c * b.z),
-                                  fmaf(sn, a.w, c * b.w));
+              a4[q] = pa[q];
+              b4[q] = pb[q];
+              ga0 = fmaf(a4[q].x, b4[q].x, fmaf(a4[q].y, b4[q].y, ga0));
+              ga1 = fmaf(a4[q].z, b4[q].z, fmaf(a4[q].w, b4[q].w, ga1));
             }
-          } else {
+            const float da = sa.x, db = sb.x;
+            float al = sa.y, be = sb.y;
+            const bool fresh_a = round == 0 || al < 0.f, fresh_b = round == 0 || be < 0.f;
+            if (fresh_a) {
+              float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int q = 0; q < MR / 4; ++q) {
-              wa[q] = a4[q];
-              wb[q] = b4[q];
+              for (int q = 0; q < MR / 4; ++q) {
+                s0 = fmaf(a4[q].x, a4[q].x, fmaf(a4[q].y, a4[q].y, s0));
+                s1 = fmaf(a4[q].z, a4[q].z, fmaf(a4[q].w, a4[q].w, s1));
+              }
+              al = (s0 + s1) * (da * da);
+            }
+            if (fresh_b) {
+              float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+              for (int q = 0; q < MR / 4; ++q) {
+                s0 = fmaf(b4[q].x, b4[q].x, fmaf(b4[q].y, b4[q].y, s0));
+                s1 = fmaf(b4[q].z, b4[q].z, fmaf(b4[q].w, b4[q].w, s1));
+              }
+              be = (s0 + s1) * (db * db);
+            }
+            const float ga = (ga0 + ga1) * (da * db);
+            if (al > kNegligible && be > kNegligible && ga * ga > tol2 * al * be) {
+              const float zeta = (be - al) * __frcp_rn(2.f * ga);
+              const float az = fabsf(zeta);
+              const float root = az < 1e18f ? az + fmaf(az, az, 1.f) * rsqrtf(fmaf(az, az, 1.f)) : 2.f * az;
+              const float t = copysignf(__frcp_rn(root), zeta);
+              const float c = rsqrtf(fmaf(t, t, 1.f));
+              const float ta = t * db * __frcp_rn(da), tb = t * da * __frcp_rn(db);
+              const float tg = t * ga;  // > 0: alpha shrinks, < 0: beta shrinks
+              float nal = al - tg, nbe = be + tg;
+              if (tg > 0.f && nal < 0.25f * al) nal = -1.f;
+              if (tg < 0.f && nbe < 0.25f * be) nbe = -1.f;
+              far |= ga * ga > stop2 * al * be;
+              float4 *wa = reinterpret_cast<float4 *>(ca);
+              float4 *wb = reinterpret_cast<float4 *>(cb);
+#pragma unroll
+              for (int q = 0; q < MR / 4; ++q) {
+                const float4 a = a4[q], b = b4[q];
+                wa[q] = make_float4(fmaf(-ta, b.x, a.x), fmaf(-ta, b.y, a.y), fmaf(-ta, b.z, a.z), fmaf(-ta, b.w, a.w));
+                wb[q] = make_float4(fmaf(tb, a.x, b.x), fmaf(tb, a.y, b.y), fmaf(tb, a.z, b.z), fmaf(tb, a.w, b.w));
+              }
+              *reinterpret_cast<float2 *>(ca + MR) = make_float2(c * da, nal);
+              *reinterpret_cast<float2 *>(cb + MR) = make_float2(c * db, nbe);
+            } else {
+              if (fresh_a) ca[MR + 1] = al;
+              if (fresh_b) cb[MR + 1] = be;
             }
           }
           if (seatA != 0) colA = colA == 1 ? nn - 1 : colA - 1;
           if (seatB != 0) colB = colB == 1 ? nn - 1 : colB - 1;
         }
-        __syncwarp(full);
+        __syncwarp(full);  // the next round's pairs were written by other lanes
       }
-      if (!__any_sync(full, far)) {
+      const bool conv = !__any_sync(full, far);
+      // fold the scales into the columns: at the end, or once one has shrunk
+      // below 2^-20 (each rotation takes at most a factor 1/sqrt(2) off it);
+      // after a whole sweep my pair is (seatA, seatB) again
+      if (active) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float *col = T + (e == 0 ? seatA : seatB) * TP;
+          const float d = col[MR];
+          if (conv || sweep + 1 == kMaxSweeps || d < 9.5367e-7f) {
+            float4 *c4 = reinterpret_cast<float4 *>(col);
+#pragma unroll
+            for (int q = 0; q < MR / 4; ++q) {
+              const float4 x = c4[q];
+              c4[q] = make_float4(x.x * d, x.y * d, x.z * d, x.w * d);
+            }
+            col[MR] = 1.f;
+          }
+        }
+      }
+      __syncwarp(full);
+      if (conv) {
         sweeps = sweep + 1;
         break;
       }
     }
   }
 
-  // ---- columns of R^T J by seat (already in place after whole sweeps), sigma^2 -------------
+  // ---- columns of R^T J (in place: column i at T[i * TP]), sigma^2 ---------------------------
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     const int j = lane + HW * e;
