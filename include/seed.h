@@ -188,13 +188,15 @@ int seed_recompress_workspace_bytes(const seed_state *st, int32_t heads, int64_t
 /*
  * seed_recompress_ws — seed_recompress_ex in three phases that pass their
  * intermediates through a caller-provided workspace: (1) per head, Householder
- * QR of U_eff and of W, the core K, the explicit Q_a and Q_b; (2) per head, the
- * Jacobi SVD of K, ordering and truncation error; (3) per head and factor, the
- * rebuild.  Each phase has its own layout (the factor panels in registers, one
- * warp per head for the core SVD), so more heads are resident per SM than in
- * the single kernel of seed_recompress.  Same algorithm as seed_recompress_ex;
- * the results agree with it to rounding (summation orders differ), not bit for
- * bit.
+ * QR of U_eff and of W (W's reflectors kept) and the core K = R_a R_b^T;
+ * (2) per head, the Jacobi SVD of K, ordering and truncation error; (3) per head
+ * and factor, the rebuild: U = U_eff (R_b^T Y_r), which equals Q_a K Y_r since
+ * U_eff = Q_a R_a, and W = Q_b Y_r by W's reflectors applied to [Y_r; 0], so
+ * that no Q is formed.  Each phase has its own layout (the factor panels in
+ * registers, one warp per head for the core SVD), so more heads are resident per
+ * SM than in the single kernel of seed_recompress.  Same factorization and
+ * truncation as seed_recompress_ex; the results agree with it to rounding
+ * (summation orders differ), not bit for bit.
  *   workspace        DEVICE memory owned by the caller, 16-byte aligned
  *   workspace_bytes  its size; heads are processed in groups of as many as it
  *                    holds (SEED_ERR_INVALID_ARG if not even one); groups of at

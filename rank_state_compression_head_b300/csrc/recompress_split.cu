@@ -8,18 +8,21 @@
 // rounding (the summation orders differ), not bit for bit.
 //
 //   qr_phase      one CTA per head, two teams (U_eff, W) of four threads per
-//                 column (qr_registers.cuh): Householder QR, explicit thin Q,
-//                 core K = R_a R_b^T; writes K, Q_a, Q_b to the workspace
+//                 column (qr_registers.cuh): Householder QR of both panels; the
+//                 U_eff team forms the core K = R_a R_b^T while the W team
+//                 writes out W's reflectors (V_b, tau_b) and R_b; no Q is formed
 //   svd_phase     one warp per head (svd_warp.cuh): pivoted QR of the core and
 //                 one-sided Jacobi on R^T, ordering, truncation error; writes
-//                 the kept right singular vectors Y (y_k) and Z (z_k = K y_k)
-//   rebuild_phase one CTA per (head, factor): U = Q_a Z, W = Q_b Y; resets the
-//                 lazy scales
+//                 the kept right singular vectors Y (y_k)
+//   rebuild_phase one CTA per (head, factor): U = U_eff (R_b^T Y), which is
+//                 Q_a K Y because U_eff = Q_a R_a; W = Q_b Y by W's reflectors
+//                 applied to [Y; 0]; resets the lazy scales
 //
-// Workspace per head (fp32, column-major panels): Q_a [m][d_k], Q_b [m][d_v],
-// K [m][m], Z [r][m4], Y [r][m4] (m4 = m rounded up to 4, zero padded), rounded
-// up to 256 bytes, with m the largest column count of any head at this call and
-// r the largest rank.
+// Workspace per head (fp32): V_b [m][d_v] (reflector j in row j), tau_b [m4],
+// R_b^T [m][m] (row i = row i of R_b), K [m][m] (column-major), Y [r][m4]
+// (m4 = m rounded up to 4, zero padded), each region starting on 16 bytes, the
+// whole rounded up to 256 bytes, with m the largest column count of any head at
+// this call and r the largest rank.
 #include "recompress_core.cuh"
 #include "qr_registers.cuh"
 #include "svd_warp.cuh"
@@ -29,15 +32,17 @@
 namespace seedk {
 
 struct SplitLayout {
-  int64_t qa, qb, k, z, y, per_head;  // offsets and stride in floats
-  int m4;                             // row stride of Z and Y
+  int64_t vb, tau, rb, k, y, per_head;  // offsets and stride in floats
+  int m4;                               // row stride of Y
   __host__ __device__ SplitLayout(int m, int r, int dk, int dv) {
+    (void)dk;
     m4 = (m + 3) & ~3;
-    qa = 0;
-    qb = qa + (int64_t)m * dk;
-    k = qb + (int64_t)m * dv;
-    z = k + (int64_t)m * m;
-    y = z + (int64_t)r * m4;
+    const int64_t mm4 = ((int64_t)m * m + 3) & ~(int64_t)3;
+    vb = 0;
+    tau = vb + (int64_t)m * dv;
+    rb = tau + m4;
+    k = rb + mm4;
+    y = k + mm4;
     per_head = (y + (int64_t)r * m4 + 63) & ~(int64_t)63;
     if (per_head == 0) per_head = 64;  // no columns: keep a nonzero stride
   }
@@ -151,26 +156,29 @@ __global__ void __maxnreg__(80) qr_phase(const SplitArgs p) {
   __syncthreads();
   const SplitLayout L(p.layout_m, p.r_max, DK, DV);
   float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
-  // ---- explicit thin Q: column l = H_0 ... H_l e_l, each column on its own ------------------
-  if (mine) {
-    rr_unit(c, part, l);
-    for (int j = l; j >= 0; --j) rr_apply(c, part, V + j * rows, tau[j], pmask);
-    float *Q = ws + (teamU ? L.qa : L.qb) + (int64_t)l * rows;
-#pragma unroll
-    for (int i = 0; i < kRRChunks; ++i) {
-      if (i >= c.nch) break;
-      *reinterpret_cast<float4 *>(Q + rr_row(part, i, 0)) = c.x[i];
+  const int team = wbase;  // threads per team
+  if (teamU) {
+    // ---- core K = R_a R_b^T to the workspace ----------------------------------------------
+    // R is zero below the diagonal, so every lane of a column j of K runs k = j..m-1:
+    // the R_b element is a broadcast, the R_a elements are consecutive
+    float *Kw = ws + L.k;
+    for (int idx = t; idx < m * m; idx += team) {
+      const int j = idx / m, i = idx % m;  // K[j][i]: column j, row i
+      float acc = 0.f;
+      for (int k = j; k < m; ++k) acc = fmaf(RsU[k * mm + i], RsW[k * mm + j], acc);
+      Kw[idx] = acc;
     }
-  }
-  // ---- core K = R_a R_b^T to the workspace ----------------------------------------------------
-  // R is zero below the diagonal, so every lane of a column j of K runs k = j..m-1:
-  // the R_b element is a broadcast, the R_a elements are consecutive
-  float *Kw = ws + L.k;
-  for (int idx = tid; idx < m * m; idx += blockDim.x) {
-    const int j = idx / m, i = idx % m;  // K[j][i]: column j, row i
-    float acc = 0.f;
-    for (int k = j; k < m; ++k) acc = fmaf(RsU[k * mm + i], RsW[k * mm + j], acc);
-    Kw[idx] = acc;
+  } else {
+    // ---- W's reflectors and R_b to the workspace ------------------------------------------------
+    const float4 *v4 = reinterpret_cast<const float4 *>(V);
+    float4 *vb4 = reinterpret_cast<float4 *>(ws + L.vb);
+    for (int idx = t; idx < m * (DV / 4); idx += team) vb4[idx] = v4[idx];
+    for (int j = t; j < m; j += team) ws[L.tau + j] = tau[j];
+    float *rbt = ws + L.rb;
+    for (int idx = t; idx < m * m; idx += team) {
+      const int i = idx / m, l = idx % m;  // R_b^T row i = row i of R_b
+      rbt[idx] = RsW[l * mm + i];
+    }
   }
 }
 
@@ -238,82 +246,126 @@ __global__ void __launch_bounds__(32 * kSvdWarps, MR <= 48 ? 8 : 6) svd_phase(co
     if (p.sweeps) p.sweeps[h] = sweeps;
     if (sv.status) sv.status[h] = sweeps < 0 ? SEED_ERR_NOT_CONVERGED : SEED_OK;
   }
-  // kept right singular vectors y_k[piv[s]] = (R^T J)_{s, order[k]} / sigma_k and
-  // z_k = K y_k (unscaled K, column piv[s] contiguous in the workspace); rows
+  // kept right singular vectors y_k[piv[s]] = (R^T J)_{s, order[k]} / sigma_k; rows
   // m..m4-1 zero
   const int rk = r < m ? r : m;
   const int m4 = (m + 3) & ~3;
-  float *Z = ws + L.z, *Y = ws + L.y;
+  float *Y = ws + L.y;
   for (int k = 0; k < rk; ++k) {
     const int col = order[k];
     const float ik = inv[col];
     const float *f = T + col * SW::TP;
     for (int s = lane; s < m4; s += HW) Y[k * L.m4 + (s < m ? piv[s] : s)] = s < m ? f[s] * ik : 0.f;
-    for (int l = lane; l < m4; l += HW) {
-      float acc = 0.f;
-      if (l < m)
-        for (int s = 0; s < m; ++s) acc = fmaf(Kw[piv[s] * m + l], f[s], acc);
-      Z[k * L.m4 + l] = l < m ? acc * ik : 0.f;
-    }
   }
 }
 
 // ---- phase 3: rebuild the factors ---------------------------------------------------------
-// One row of the factor per thread: Q row in registers (MR = m_max rounded up
-// to 16 entries), the kept coefficient vectors from shared memory as broadcast
-// 16-byte loads, four outputs at a time.
+// U (blockIdx.y = 0): one row of U_eff per thread in registers (MR = m_max
+// rounded up to 16 entries), M = R_b^T Y formed in shared memory first and read
+// as broadcast 16-byte loads, four outputs at a time; the row is read in full
+// before it is overwritten, and every thread has read the scales before they
+// are reset.  W (blockIdx.y = 1): kTPC threads per kept column k hold
+// [y_k; 0] in registers (qr_registers.cuh) and apply H_{m-1}, ..., H_0.
 template <int VAR, typename TF, int DV, int MR>
 __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p) {
   constexpr int DK = kDK;
   constexpr int NO = 4;  // outputs per pass
   extern __shared__ __align__(16) float smem[];
   const int h = p.head0 + blockIdx.x;
-  const int panel = blockIdx.y;  // 0: U from Q_a and Z, 1: W from Q_b and Y
   const int tid = threadIdx.x;
   const StateView &sv = p.sv;
   int r, m;
   if (!split_head_ok(sv, h, p.layout_m, r, m) || !in_class(p, m)) return;
   const SplitLayout L(p.layout_m, p.r_max, DK, DV);
   const float *ws = p.ws + (int64_t)blockIdx.x * L.per_head;
-  const int rows = panel == 0 ? DK : DV;
   const int rk = r < m ? r : m;
-  float *zs = smem;  // [rk rounded up to NO][MR], zero beyond m and rk
-  const float *src = ws + (panel == 0 ? L.z : L.y);
   const int rk4 = (rk + NO - 1) / NO * NO;
-  for (int idx = tid; idx < rk4 * MR; idx += kSplitThreads) {
-    const int k = idx / MR, l = idx % MR;
-    zs[idx] = (k < rk && l < m) ? src[k * L.m4 + l] : 0.f;
-  }
-  __syncthreads();
   const int64_t c0 = sv.col0(h);
-  if (tid < rows) {
-    const float *Q = ws + (panel == 0 ? L.qa : L.qb);
-    float q[MR];
-#pragma unroll
-    for (int l = 0; l < MR; ++l) q[l] = l < m ? Q[l * rows + tid] : 0.f;
-    TF *out = reinterpret_cast<TF *>(panel == 0 ? sv.U : sv.W) + c0 * rows;
-    for (int k = 0; k < rk; k += NO) {
-      float acc[NO];
-#pragma unroll
-      for (int o = 0; o < NO; ++o) acc[o] = 0.f;
-#pragma unroll
-      for (int l4 = 0; l4 < MR / 4; ++l4) {
-#pragma unroll
-        for (int o = 0; o < NO; ++o) {
-          const float4 z = reinterpret_cast<const float4 *>(zs + (k + o) * MR)[l4];
-          acc[o] = fmaf(q[4 * l4], z.x, fmaf(q[4 * l4 + 1], z.y, fmaf(q[4 * l4 + 2], z.z, fmaf(q[4 * l4 + 3], z.w, acc[o]))));
-        }
-      }
-#pragma unroll
-      for (int o = 0; o < NO; ++o)
-        if (k + o < rk) Elem<TF>::store(out + (int64_t)(k + o) * rows + tid, acc[o]);
+  if (blockIdx.y == 0) {
+    // ---- U = U_eff M, M = R_b^T Y ---------------------------------------------------------
+    float *rbt = smem;            // [MR][MR]: row i of R_b
+    float *ys = rbt + MR * MR;    // [rk4][MR]: y_k
+    float *zs = ys + rk4 * MR;    // [rk4][MR]: column k of M, zero beyond m and rk
+    for (int idx = tid; idx < m * m; idx += kSplitThreads) rbt[(idx / m) * MR + idx % m] = ws[L.rb + idx];
+    for (int idx = tid; idx < rk4 * MR; idx += kSplitThreads) {
+      const int k = idx / MR, l = idx % MR;
+      ys[idx] = (k < rk && l < m) ? ws[L.y + k * L.m4 + l] : 0.f;
     }
-  }
-  if (panel == 0) {
+    __syncthreads();
+    for (int idx = tid; idx < rk4 * MR; idx += kSplitThreads) {
+      const int k = idx / MR, l = idx % MR;  // M[l][k] = sum_{i <= l} R_b[i][l] y_k[i]
+      float acc = 0.f;
+      if (k < rk && l < m)
+        for (int i = 0; i <= l; ++i) acc = fmaf(rbt[i * MR + l], ys[k * MR + i], acc);
+      zs[idx] = acc;
+    }
+    __syncthreads();
+    if (tid < DK) {
+      TF *pool = reinterpret_cast<TF *>(sv.U) + c0 * DK;
+      const float rs = VAR == SEED_KDA ? sv.scale[(int64_t)h * DK + tid] : 1.f;
+      float q[MR];
+#pragma unroll
+      for (int l = 0; l < MR; ++l) {
+        q[l] = 0.f;
+        if (l < m) q[l] = Elem<TF>::load(pool + (int64_t)l * DK + tid) * (VAR == SEED_KDA ? rs : sv.scale[c0 + l]);
+      }
+      for (int k = 0; k < rk; k += NO) {
+        float acc[NO];
+#pragma unroll
+        for (int o = 0; o < NO; ++o) acc[o] = 0.f;
+#pragma unroll
+        for (int l4 = 0; l4 < MR / 4; ++l4) {
+#pragma unroll
+          for (int o = 0; o < NO; ++o) {
+            const float4 z = reinterpret_cast<const float4 *>(zs + (k + o) * MR)[l4];
+            acc[o] = fmaf(q[4 * l4], z.x, fmaf(q[4 * l4 + 1], z.y, fmaf(q[4 * l4 + 2], z.z, fmaf(q[4 * l4 + 3], z.w, acc[o]))));
+          }
+        }
+#pragma unroll
+        for (int o = 0; o < NO; ++o)
+          if (k + o < rk) Elem<TF>::store(pool + (int64_t)(k + o) * DK + tid, acc[o]);
+      }
+    }
+    __syncthreads();  // every thread has read the scales
     if (VAR == SEED_KDA) {
       for (int i = tid; i < DK; i += kSplitThreads) sv.scale[(int64_t)h * DK + i] = 1.f;
     } else {
       for (int k = tid; k < rk; k += kSplitThreads) sv.scale[c0 + k] = 1.f;
+    }
+  } else {
+    // ---- W = Q_b [Y; 0] = H_0 ... H_{m-1} [Y; 0] --------------------------------------------
+    float *vs = smem;          // [m][DV]: v_j, zero above row j
+    float *ts = vs + m * DV;   // [m]: tau_j
+    const float4 *src = reinterpret_cast<const float4 *>(ws + L.vb);
+    for (int idx = tid; idx < m * (DV / 4); idx += kSplitThreads) reinterpret_cast<float4 *>(vs)[idx] = src[idx];
+    for (int j = tid; j < m; j += kSplitThreads) ts[j] = ws[L.tau + j];
+    __syncthreads();
+    constexpr int kCols = kSplitThreads / kTPC;  // columns per pass
+    const int part = tid % kTPC;
+    const unsigned pmask = ((1u << kTPC) - 1) << ((tid & 31) & ~(kTPC - 1));
+    TF *pool = reinterpret_cast<TF *>(sv.W) + c0 * DV;
+    const int m4 = (m + 3) & ~3;  // rows of y_k written by the SVD phase (zero beyond m)
+    for (int k0 = 0; k0 < rk; k0 += kCols) {
+      const int k = k0 + tid / kTPC;
+      if (k >= rk) break;  // whole groups of kTPC lanes leave together
+      RRCol c;
+      c.nch = DV / (4 * kTPC);
+      const float *y = ws + L.y + (int64_t)k * L.m4;
+#pragma unroll
+      for (int i = 0; i < kRRChunks; ++i) {
+        c.x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i >= c.nch) continue;
+        const int row = rr_row(part, i, 0);
+        if (row < m4) c.x[i] = *reinterpret_cast<const float4 *>(y + row);
+      }
+      for (int j = m - 1; j >= 0; --j) rr_apply(c, part, vs + j * DV, ts[j], pmask);
+#pragma unroll
+      for (int i = 0; i < kRRChunks; ++i) {
+        if (i >= c.nch) break;
+        const int row = rr_row(part, i, 0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) Elem<TF>::store(pool + (int64_t)k * DV + row + e, f4get(c.x[i], e));
+      }
     }
   }
 }
@@ -328,7 +380,9 @@ static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaS
   const int qr_bytes = (a.m_max * (kDK + DV) + 4 * up + 2 * a.m_max * a.m_max) * 4;
   const int qr_threads = a.m_max > 0 ? qr_team_stride(a.m_max) * 2 : 32;
   const int svd_bytes = svd_heads_per_cta<MR>() * SvdWarpSmem<MR>::FLOATS * 4;
-  const int rb_bytes = ((a.r_max + 3) / 4 * 4 * MR > 0 ? (a.r_max + 3) / 4 * 4 * MR : 4) * 4;
+  const int rk4 = (a.r_max + 3) / 4 * 4;
+  const int rb_u = MR * MR + 2 * rk4 * MR, rb_w = a.m_max * DV + a.m_max;
+  const int rb_bytes = ((rb_u > rb_w ? rb_u : rb_w) + 4) * 4;
   auto k1 = qr_phase<VAR, TF, DV>;
   auto k2 = svd_phase<TF, DV, MR>;
   auto k3 = rebuild_phase<VAR, TF, DV, MR>;

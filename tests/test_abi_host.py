@@ -140,8 +140,10 @@ def test_synth_calls_reject_on_host():
 
 
 def _ws_floats(m, r, dk, dv):
+    # W's reflectors, their tau, R_b^T, K, Y; each region on 16 bytes
     m4 = (m + 3) // 4 * 4
-    n = m * dk + m * dv + m * m + 2 * r * m4
+    mm4 = (m * m + 3) // 4 * 4
+    n = m * dv + m4 + 2 * mm4 + r * m4
     n = (n + 63) // 64 * 64
     return max(n, 64)
 

@@ -54,7 +54,8 @@ def test_noalloc_matches_workspace_call_twice(variant, dtype):
 
 
 def test_noalloc_rejects_oversize_without_launch():
-    H, T = 1000, 16
+    # 2000 heads at m = 48, r = 32 need 2000 x 12352 floats, more than the 16 Mi of the scratch
+    H, T = 2000, 16
     ranks = np.full(H, 32, dtype=np.int32)
     vbar = np.ones((H, 128)) / np.sqrt(128)
     buf = make_buffers('gdn', 'bf16', H, 128, 128, T, vbar, ranks, ragged=False)
