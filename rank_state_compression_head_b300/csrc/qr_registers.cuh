@@ -164,6 +164,40 @@ __device__ inline void rr_apply(RRCol &c, int p, const float *v, float tau, unsi
   }
 }
 
+// a_l <- H_a H_b a_l for two reflectors at once (H = I - tau v v^T, g = v_a . v_b):
+// with d_b = v_b . a_l and d_a = v_a . a_l, H_b first takes x_b = tau_b d_b of
+// v_b off, which leaves v_a . a_l = d_a - x_b g, so H_a takes x_a = tau_a (d_a -
+// x_b g) of v_a.  The two dot products and their reductions run side by side.
+__device__ inline void rr_apply2(RRCol &c, int p, const float *va, const float *vb, float tau_a, float tau_b,
+                                 float g, unsigned pmask) {
+  const float4 *a4 = reinterpret_cast<const float4 *>(va);
+  const float4 *b4 = reinterpret_cast<const float4 *>(vb);
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRRChunks; ++i) {
+    if (i >= c.nch) break;
+    const float4 wa = a4[p + kTPC * i], wb = b4[p + kTPC * i];
+    a0 = fmaf(wa.x, c.x[i].x, fmaf(wa.y, c.x[i].y, a0)); a1 = fmaf(wa.z, c.x[i].z, fmaf(wa.w, c.x[i].w, a1));
+    b0 = fmaf(wb.x, c.x[i].x, fmaf(wb.y, c.x[i].y, b0)); b1 = fmaf(wb.z, c.x[i].z, fmaf(wb.w, c.x[i].w, b1));
+  }
+  float da = a0 + a1, db = b0 + b1;
+#pragma unroll
+  for (int o = 1; o < kTPC; o <<= 1) {
+    da += __shfl_xor_sync(pmask, da, o);
+    db += __shfl_xor_sync(pmask, db, o);
+  }
+  const float xb = tau_b * db;
+  const float xa = tau_a * fmaf(-xb, g, da);
+  asm volatile("" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < kRRChunks; ++i) {
+    if (i >= c.nch) break;
+    const float4 wa = a4[p + kTPC * i], wb = b4[p + kTPC * i];
+    c.x[i].x = fmaf(-xa, wa.x, fmaf(-xb, wb.x, c.x[i].x)); c.x[i].y = fmaf(-xa, wa.y, fmaf(-xb, wb.y, c.x[i].y));
+    c.x[i].z = fmaf(-xa, wa.z, fmaf(-xb, wb.z, c.x[i].z)); c.x[i].w = fmaf(-xa, wa.w, fmaf(-xb, wb.w, c.x[i].w));
+  }
+}
+
 // My part of e_l.
 __device__ inline void rr_unit(RRCol &c, int p, int l) {
   const int ll = l - 4 * p;

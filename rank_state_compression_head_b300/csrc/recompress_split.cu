@@ -134,10 +134,13 @@ __global__ void __maxnreg__(80) qr_phase(const SplitArgs p) {
   }
 
   // ---- Householder QR of both panels ------------------------------------------------------
+  // The teams share nothing until R is in shared memory: each waits only for its
+  // own reflector (named barrier 1 or 2 over its wbase threads)
   for (int j = 0; j < m; ++j) {
     if ((t >> 5) == ((kTPC * j) >> 5))  // the warp that holds column j of my panel
       rr_reflector_warp(c, l == j, part, j, rows, V + j * rows, tau + j, betas + j);
-    __syncthreads();
+    if (teamU) asm volatile("bar.sync 1, %0;" ::"r"(wbase) : "memory");
+    else asm volatile("bar.sync 2, %0;" ::"r"(wbase) : "memory");
     if (mine && l > j) rr_apply(c, part, V + j * rows, tau[j], pmask);
   }
   // ---- R factors to shared memory ------------------------------------------------------------
@@ -265,7 +268,8 @@ __global__ void __launch_bounds__(32 * kSvdWarps, MR <= 48 ? 8 : 6) svd_phase(co
 // as broadcast 16-byte loads, four outputs at a time; the row is read in full
 // before it is overwritten, and every thread has read the scales before they
 // are reset.  W (blockIdx.y = 1): kTPC threads per kept column k hold
-// [y_k; 0] in registers (qr_registers.cuh) and apply H_{m-1}, ..., H_0.
+// [y_k; 0] in registers (qr_registers.cuh) and apply H_{m-1}, ..., H_0, two
+// reflectors a pass.
 template <int VAR, typename TF, int DV, int MR>
 __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p) {
   constexpr int DK = kDK;
@@ -334,11 +338,23 @@ __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p
     }
   } else {
     // ---- W = Q_b [Y; 0] = H_0 ... H_{m-1} [Y; 0] --------------------------------------------
-    float *vs = smem;          // [m][DV]: v_j, zero above row j
-    float *ts = vs + m * DV;   // [m]: tau_j
+    float *vs = smem;                    // [m][DV]: v_j, zero above row j
+    float *ts = vs + m * DV;             // [m]: tau_j
+    float *gs = ts + ((m + 3) & ~3);     // [m]: g_j = v_j . v_{j+1} for j = m-2, m-4, ...
     const float4 *src = reinterpret_cast<const float4 *>(ws + L.vb);
     for (int idx = tid; idx < m * (DV / 4); idx += kSplitThreads) reinterpret_cast<float4 *>(vs)[idx] = src[idx];
     for (int j = tid; j < m; j += kSplitThreads) ts[j] = ws[L.tau + j];
+    __syncthreads();
+    {
+      constexpr int kWarps = kSplitThreads / 32;
+      const int warp = tid >> 5, ln = tid & 31;
+      for (int j = m - 2 - 2 * warp; j >= 0; j -= 2 * kWarps) {
+        float acc = 0.f;
+        for (int i = ln; i < DV; i += 32) acc = fmaf(vs[j * DV + i], vs[(j + 1) * DV + i], acc);
+        acc = warp_sum(acc);
+        if (ln == 0) gs[j] = acc;
+      }
+    }
     __syncthreads();
     constexpr int kCols = kSplitThreads / kTPC;  // columns per pass
     const int part = tid % kTPC;
@@ -358,7 +374,10 @@ __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p
         const int row = rr_row(part, i, 0);
         if (row < m4) c.x[i] = *reinterpret_cast<const float4 *>(y + row);
       }
-      for (int j = m - 1; j >= 0; --j) rr_apply(c, part, vs + j * DV, ts[j], pmask);
+      // H_{m-1} first: pairs (j - 1, j) for j = m-1, m-3, ..., then H_0 alone if m is odd
+      int j = m - 1;
+      for (; j >= 1; j -= 2) rr_apply2(c, part, vs + (j - 1) * DV, vs + j * DV, ts[j - 1], ts[j], gs[j - 1], pmask);
+      if (j == 0) rr_apply(c, part, vs, ts[0], pmask);
 #pragma unroll
       for (int i = 0; i < kRRChunks; ++i) {
         if (i >= c.nch) break;
@@ -381,7 +400,7 @@ static cudaError_t launch_split_t(SplitArgs a, int n_heads, int64_t chunk, cudaS
   const int qr_threads = a.m_max > 0 ? qr_team_stride(a.m_max) * 2 : 32;
   const int svd_bytes = svd_heads_per_cta<MR>() * SvdWarpSmem<MR>::FLOATS * 4;
   const int rk4 = (a.r_max + 3) / 4 * 4;
-  const int rb_u = MR * MR + 2 * rk4 * MR, rb_w = a.m_max * DV + a.m_max;
+  const int rb_u = MR * MR + 2 * rk4 * MR, rb_w = a.m_max * DV + 2 * ((a.m_max + 3) & ~3);
   const int rb_bytes = ((rb_u > rb_w ? rb_u : rb_w) + 4) * 4;
   auto k1 = qr_phase<VAR, TF, DV>;
   auto k2 = svd_phase<TF, DV, MR>;
