@@ -288,20 +288,30 @@ __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p
   if (blockIdx.y == 0) {
     // ---- U = U_eff M, M = R_b^T Y ---------------------------------------------------------
     float *rbt = smem;            // [MR][MR]: row i of R_b
-    float *ys = rbt + MR * MR;    // [rk4][MR]: y_k
-    float *zs = ys + rk4 * MR;    // [rk4][MR]: column k of M, zero beyond m and rk
+    float *yt = rbt + MR * MR;    // [MR][rk4]: y_k[i] at i * rk4 + k
+    float *zs = yt + rk4 * MR;    // [rk4][MR]: column k of M, zero beyond m and rk
     for (int idx = tid; idx < m * m; idx += kSplitThreads) rbt[(idx / m) * MR + idx % m] = ws[L.rb + idx];
-    for (int idx = tid; idx < rk4 * MR; idx += kSplitThreads) {
-      const int k = idx / MR, l = idx % MR;
-      ys[idx] = (k < rk && l < m) ? ws[L.y + k * L.m4 + l] : 0.f;
+    for (int idx = tid; idx < MR * rk4; idx += kSplitThreads) {
+      const int i = idx / rk4, k = idx % rk4;
+      yt[idx] = (k < rk && i < m) ? ws[L.y + k * L.m4 + i] : 0.f;
     }
     __syncthreads();
-    for (int idx = tid; idx < rk4 * MR; idx += kSplitThreads) {
-      const int k = idx / MR, l = idx % MR;  // M[l][k] = sum_{i <= l} R_b[i][l] y_k[i]
-      float acc = 0.f;
-      if (k < rk && l < m)
-        for (int i = 0; i <= l; ++i) acc = fmaf(rbt[i * MR + l], ys[k * MR + i], acc);
-      zs[idx] = acc;
+    // M[l][k] = sum_{i <= l} R_b[i][l] y_k[i], four k a task: one R_b element and
+    // one 16-byte broadcast of y an i
+    for (int task = tid; task < (rk4 / 4) * MR; task += kSplitThreads) {
+      const int l = task % MR, k = 4 * (task / MR);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (l < m)
+        for (int i = 0; i <= l; ++i) {
+          const float rv = rbt[i * MR + l];
+          const float4 y = *reinterpret_cast<const float4 *>(yt + i * rk4 + k);
+          acc.x = fmaf(rv, y.x, acc.x); acc.y = fmaf(rv, y.y, acc.y);
+          acc.z = fmaf(rv, y.z, acc.z); acc.w = fmaf(rv, y.w, acc.w);
+        }
+      zs[k * MR + l] = acc.x;
+      zs[(k + 1) * MR + l] = acc.y;
+      zs[(k + 2) * MR + l] = acc.z;
+      zs[(k + 3) * MR + l] = acc.w;
     }
     __syncthreads();
     if (tid < DK) {
