@@ -64,7 +64,9 @@ def recompress_flops(d_k: int, d_v: int, m: int, r: int, sweeps: float) -> float
     pairs, each three dot products of length m (6 m) and one rotation of a
     column pair (6 m), counted for every pair of every sweep; the kept
     directions through the core, K y_k: 2 m^2 r; rebuild of the r kept
-    columns: 2 (d_k + d_v) m r.
+    columns: 2 (d_k + d_v) m r.  This is the method's count; the three-phase
+    kernels reach the same factors without forming Q and with scaled Jacobi
+    rotations, so they execute fewer FLOPs than it.
     """
     qr = sum(2 * p * m * m - 2 * m ** 3 / 3 for p in (d_k, d_v))
     formq = qr
