@@ -4,23 +4,19 @@
 // rows 4c..4c+3 of the column for the chunks c = p + TPC i, i < rows / (4 TPC).
 //
 // Factorization (one barrier per step j): the warp that holds column j turns
-// it into the reflector together - the two owners lay the column out in V[j]
+// it into the reflector together - the owners lay the column out in V[j]
 // (shared), the 32 lanes form amax, the scaled norm and v_j (v_j[j] = 1, zeros
 // above) in place, the owners read back beta (row j) and v_j (rows below).
 // After the barrier every later column takes v_j . a_l over its rows (two
 // shuffles join the parts) and subtracts tau_j (v_j . a_l) v_j in its
 // registers.  The panel itself never goes through shared memory; V keeps all
-// reflectors for the explicit Q.
-//
-// Explicit Q: column l of Q = H_0 H_1 ... H_{m-1} [I; 0] is H_0 ... H_l e_l
-// (H_j e_l = e_l for j > l), so every column starts from e_l and applies its
-// reflectors from H_l down to H_0 on its own, with no barrier.
+// reflectors, so that they can be applied to other vectors afterwards
+// (rr_apply, rr_apply2).
 //
 // The reflector is the one of householder_qr (zero below the smallest normal
 // float); its norm is taken unscaled unless the sum of squares nears the ends
 // of the fp32 range, where it is scaled by the column's largest magnitude as in
-// householder_qr.  The result differs from householder_qr / form_q only in
-// rounding.
+// householder_qr.  The result differs from householder_qr only in rounding.
 #pragma once
 
 #include "common.cuh"
@@ -195,19 +191,6 @@ __device__ inline void rr_apply2(RRCol &c, int p, const float *va, const float *
     const float4 wa = a4[p + kTPC * i], wb = b4[p + kTPC * i];
     c.x[i].x = fmaf(-xa, wa.x, fmaf(-xb, wb.x, c.x[i].x)); c.x[i].y = fmaf(-xa, wa.y, fmaf(-xb, wb.y, c.x[i].y));
     c.x[i].z = fmaf(-xa, wa.z, fmaf(-xb, wb.z, c.x[i].z)); c.x[i].w = fmaf(-xa, wa.w, fmaf(-xb, wb.w, c.x[i].w));
-  }
-}
-
-// My part of e_l.
-__device__ inline void rr_unit(RRCol &c, int p, int l) {
-  const int ll = l - 4 * p;
-#pragma unroll
-  for (int i = 0; i < kRRChunks; ++i) {
-    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (4 * kTPC * i + e == ll) f4set(u, e, 1.f);
-    c.x[i] = u;
   }
 }
 
