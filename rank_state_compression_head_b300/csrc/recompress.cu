@@ -15,9 +15,10 @@
 //   U_new = Q_a K y_k (= sigma_k Q_a x_k),  W_new = Q_b y_k
 //   (no rotation is kept: the kept directions are read off R^T J and applied
 //   to the original core)
-// compress_dense (one CTA of 256 threads per head): A = C and B = I, so
-// K = R_a; plain one-sided Jacobi on K: K J = X Sigma, U_new = Q_a X_r,
-// W_new = R_a^T X_r.
+// compress_dense (one CTA of 256 threads per head): sink split, then the
+// d_k x d_v matrix C itself takes the place of the core: C P = Q R (pivoted
+// QR), one-sided Jacobi on R^T, y_k = P v_k, U_new = C y_k (= sigma_k x_k, C
+// read again from S and a), W_new = y_k.
 //
 // The arithmetic is fp32 FMA: the QR and Jacobi steps are sequences of small
 // dependent reductions that do not map onto tensor-core tiles.

@@ -71,7 +71,7 @@ __device__ inline bool split_head_ok(const StateView &sv, int h, int m_max, int 
 }
 __device__ inline bool in_class(const SplitArgs &p, int m) { return m > p.m_lo && m <= p.m_max; }
 
-// ---- phase 1: QR of both factors, core, explicit Q --------------------------------------
+// ---- phase 1: QR of both factors, core, W's reflectors -------------------------------
 // Two teams of kTPC x m_max threads (the second starts on a warp boundary),
 // kTPC threads per column, the panels in registers (qr_registers.cuh).
 __host__ __device__ inline int qr_team_stride(int m_max) { return (kTPC * m_max + 31) / 32 * 32; }
