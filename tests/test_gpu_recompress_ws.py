@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import rank_state_compression_head_b300 as R
-from _gpu import TOL, gpu_dense, make_buffers, random_states, rel_err, upload
+from _gpu import TOL, gpu_dense, make_buffers, random_states, rel_err, stored, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -144,3 +144,44 @@ def test_ws_ragged_with_empty_heads(s):
         assert abs(err[h] - e_ref) <= TOL['bf16'] * max(e_ref, 1e-3 * np.linalg.norm(S[h])), h
         if ranks[h] + s == 0:
             assert err[h] == 0.0 and sw[h] == 0, h
+
+
+def test_ws_cancelling_factors_stay_within_stability_bound():
+    # A delta-rule erasure leaves column pairs whose products cancel, so that
+    # U_eff W^T is far smaller than |U_eff| |W|.  Forming the core K = R_a R_b^T
+    # already costs an error of order eps |U_eff| |W|; the three-phase path's
+    # U = U_eff (R_b^T Y) (no Q_a) and the single kernel's U = Q_a K Y must both
+    # stay within eps |U_eff|_F |W|_F / |S|_F of the oracle (relative to |S|_F,
+    # and never below the fp32 parity tolerance).  A CPU fp32 model of both forms
+    # on these states lands near 1e-4, about 1/30 of that bound.
+    H, T, r, s = 6, 8, 32, 8
+    ranks = np.full(H, r, dtype=np.int32)
+    states, vbar = random_states(53, H, 128, 128, ranks, s, T, 'gdn', 'f32')
+    rng = np.random.default_rng(53)
+    bounds = []
+    for st in states:
+        k = rng.standard_normal((128, s // 2))
+        k /= np.linalg.norm(k, axis=0)
+        big = 1e4 * rng.standard_normal((128, s // 2))
+        # both copies of each key are k in U_eff, whatever their lazy column scales
+        sc = st.scale[r:]
+        st.U = stored(np.hstack([st.U[:, :r], k / sc[:s // 2], k / sc[s // 2:]]), 'f32')
+        st.W = stored(np.hstack([st.W[:, :r], big, -big + 1e-2 * rng.standard_normal((128, s // 2))]), 'f32')
+        S = oracle.materialize(st)
+        ratio = np.linalg.norm(st.U * st.scale) * np.linalg.norm(st.W) / np.linalg.norm(S)
+        assert ratio > 1e4  # the case is a cancelling one
+        bounds.append(max(TOL['f32'], 2.0 ** -24 * ratio))
+    one = make_buffers('gdn', 'f32', H, 128, 128, T, vbar, ranks, ragged=False)
+    two = make_buffers('gdn', 'f32', H, 128, 128, T, vbar, ranks, ragged=False)
+    upload(one, states, s)
+    upload(two, states, s)
+    R.seed_recompress_ex(one.st, None, None)
+    ws, nbytes = workspace(two, H)
+    R.seed_recompress_ws(two.st, None, None, ws, nbytes)
+    S1, S2 = gpu_dense(one), gpu_dense(two)
+    for h in range(H):
+        ref, _ = oracle.recompress(states[h], r)
+        S_ref = oracle.materialize(ref)
+        assert rel_err(S1[h], S_ref) < bounds[h], (h, 'single kernel')
+        assert rel_err(S2[h], S_ref) < bounds[h], (h, 'three phases')
+    assert int(one.status.abs().sum()) == 0 and int(two.status.abs().sum()) == 0
