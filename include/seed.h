@@ -209,9 +209,11 @@ int seed_recompress_ws(seed_state *st, float *trunc_err, int32_t *sweeps, void *
 
 /*
  * seed_recompress_noalloc — seed_recompress_ws on a scratch array that the
- * library holds in device memory, for callers that cannot provide a
- * workspace.  The pages have no counterpart of this call: it is plumbing of
- * this library.
+ * library holds in device memory, for callers that cannot call cudaMalloc to
+ * provide a workspace: a host runtime that owns no CUDA allocator of its own,
+ * or a serving loop that must not allocate (allocation can synchronise the
+ * device and fragment a pool sized in advance) on the decode path.  The pages
+ * have no counterpart of this call: it is plumbing of this library.
  *   The scratch is a fixed 64 MiB per device, reserved when the library's
  *   kernels are loaded on that device; all heads are recompressed in one group,
  *   so a state whose heads need more than that (n_heads x the per-head size
