@@ -6,7 +6,7 @@
 // Factorization (one barrier per step j): the warp that holds column j turns
 // it into the reflector together - the owners lay the column out in V[j]
 // (shared), the 32 lanes form amax, the scaled norm and v_j (v_j[j] = 1, zeros
-// above) in place, the owners read back beta (row j) and v_j (rows below).
+// above) in place and keep beta = R[j][j] beside it.
 // After the barrier every later column takes v_j . a_l over its rows (two
 // shuffles join the parts) and subtracts tau_j (v_j . a_l) v_j in its
 // registers.  The panel itself never goes through shared memory; V keeps all
@@ -42,8 +42,9 @@ __device__ inline void f4set(float4 &v, int e, float a) {
 
 // Step j of the factorization, run by every lane of the warp that holds column
 // j (owner: the kTPC lanes of column j).  vj: V[j] (rows floats); on exit it holds
-// v_j, *tau = tau_j, and the owners' registers hold beta (row j) and v_j below.
-__device__ inline void rr_reflector_warp(RRCol &c, bool owner, int p, int j, int rows, float *vj,
+// v_j, *tau = tau_j and *beta_out = beta (R[j][j]).  The owners' registers are
+// left as they were: rows above j already hold R, and nothing reads the rest.
+__device__ inline void rr_reflector_warp(const RRCol &c, bool owner, int p, int j, int rows, float *vj,
                                          float *tau, float *beta_out) {
   const int lane = threadIdx.x & 31;
   if (owner) {
@@ -114,22 +115,6 @@ __device__ inline void rr_reflector_warp(RRCol &c, bool owner, int p, int j, int
   if (lane == 0) {
     *tau = tj;
     *beta_out = beta;
-  }
-  __syncwarp();
-  if (owner) {
-    // my row 4p + 4 TPC i + e is compared with j as 4 TPC i + e against jj
-    const int jj = j - 4 * p;
-#pragma unroll
-    for (int i = 0; i < kRRChunks; ++i) {
-      if (i >= c.nch) break;
-      const float4 v = reinterpret_cast<const float4 *>(vj)[p + kTPC * i];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d = 4 * kTPC * i + e;
-        if (d == jj) f4set(c.x[i], e, beta);
-        else if (d > jj) f4set(c.x[i], e, f4get(v, e));
-      }
-    }
   }
 }
 

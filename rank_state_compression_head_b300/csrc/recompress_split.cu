@@ -152,7 +152,7 @@ __global__ void __maxnreg__(80) qr_phase(const SplitArgs p) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int row = rr_row(part, i, e);
-        if (row < m) Rs[l * mm + row] = row <= l ? f4get(c.x[i], e) : 0.f;
+        if (row < m) Rs[l * mm + row] = row < l ? f4get(c.x[i], e) : row == l ? betas[l] : 0.f;
       }
     }
   }
