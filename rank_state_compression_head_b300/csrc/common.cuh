@@ -45,14 +45,6 @@ template <> struct Elem<__nv_bfloat16> {
   __device__ static inline float load(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 };
 
-// 16-byte global load that bypasses L1 allocation (streamed factor data)
-__device__ static inline uint4 ld_stream16(const void *p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-  return r;
-}
-
 __device__ static inline float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -84,9 +76,6 @@ __device__ static inline void mbar_init(uint64_t *bar, uint32_t count) {
 }
 __device__ static inline void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ static inline void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ static inline void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)

@@ -36,9 +36,6 @@ struct RRCol {
 
 __device__ inline int rr_row(int p, int i, int e) { return 4 * (p + kTPC * i) + e; }
 __device__ inline float f4get(const float4 &v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; }
-__device__ inline void f4set(float4 &v, int e, float a) {
-  if (e == 0) v.x = a; else if (e == 1) v.y = a; else if (e == 2) v.z = a; else v.w = a;
-}
 
 // Step j of the factorization, run by every lane of the warp that holds column
 // j (owner: the kTPC lanes of column j).  vj: V[j] (rows floats); on exit it holds
