@@ -2,7 +2,10 @@
 
 One "step" = one decode step of every head of the workload (fused read-out +
 factored update), with the recompression back to rank r that runs after
-every T-th step included, so the figure is whole-job head-steps/s.
+every T-th step amortised over its T steps, so the figure is whole-job
+head-steps/s: value = heads / (mean decode time + mean recompression time / T).
+The default workload is the largest one that fits one GPU, the serving-scale
+Gated DeltaNet batch (589,824 heads of 128 x 128, ragged ranks 16/32/48).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -28,15 +31,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = 'factored-state decode head-steps/s and HBM GB/s vs 8 TB/s; dense-state ratio'
 UNIT = 'head-steps/s'
-DEFAULT_WORKLOAD = 'gdn_batched_b64_h32_r32'
+DEFAULT_WORKLOAD = 'gdn_serving_b512_l36_h32_ragged'
 FLUSH_BYTES = 256 << 20
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument('--gpus', type=int, default=1)
-    ap.add_argument('--steps', type=int, default=256)
-    ap.add_argument('--warmup', type=int, default=16)
+    ap.add_argument('--steps', type=int, default=32)
+    ap.add_argument('--warmup', type=int, default=4)
     ap.add_argument('--workload', default=DEFAULT_WORKLOAD)
     ap.add_argument('--impl', default='seed', choices=['seed', 'reference'])
     ap.add_argument('--cpu-seconds', type=float, default=12.0, help='budget of the CPU-oracle sample')
@@ -265,8 +268,7 @@ def run_gpu(args, w):
     # ---- setup: constants, prefill, compression, inputs of every step -----------------
     ws_heads = DEFAULT_WS_HEADS if args.recompress == 'phases' else 0
     run = DeviceRun(w, device=dev, steps_buffered=total_steps, ws_heads=ws_heads)
-    rec_groups = -(-run.H // min(run.H, ws_heads)) if ws_heads else 1
-    rec_launches = 3 * rec_groups if ws_heads else 1
+    rec_launches = run.recompress_launches()
     # setup, timed once (not part of the decode metric): dense prefill and compression
     ev_setup = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     ev_setup[0].record(stream)
@@ -359,13 +361,27 @@ def run_gpu(args, w):
                 raise RuntimeError(f'library call failed with status {rc}')
         torch.cuda.synchronize()
         c1 = time.perf_counter()
+        # Fewer than T timed steps hold no recompression: run the schedule on (untimed)
+        # to the next boundary and time that recompression alone, the same way.
+        if not rec_steps:
+            while run.state.steps_since_compress < T:
+                run.decode(slot=(W_ + K) % total_steps)
+            l2_flush()
+            ev_extra = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev_extra[0].record(stream)
+            rc = rec_fn(*rec_args)
+            ev_extra[1].record(stream)
+            if rc:
+                raise RuntimeError(f'library call failed with status {rc}')
+            torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     dec_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    rec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in rec_steps]
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
-    total_ms = sum(step_ms)
-    total_ms = sharding.max_over_ranks(total_ms, device=dev)
+    rec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in rec_steps] or [ev_extra[0].elapsed_time(ev_extra[1])]
+    # Whole-job time of one step: its decode plus 1/T of a recompression (one runs
+    # after every T-th step), so any K gives the long-run rate.
+    step_ms_amortised = statistics.mean(dec_ms) + statistics.mean(rec_ms) / T
+    total_ms = sharding.max_over_ranks(step_ms_amortised * K, device=dev)
     heads_all = sharding.job_heads(run.H, ws)
     value = heads_all * K / (total_ms / 1e3)
     clocks = clk.summary(c0, c1)
@@ -381,7 +397,7 @@ def run_gpu(args, w):
     rec_avg_ms = statistics.mean(rec_ms) if rec_ms else float('nan')
     fp32_peak = 148 * 128 * 2 * (clocks['sm_max_mhz'] or 2032) * 1e6 / 1e12  # TFLOP/s, FFMA issue rate
     rec_tflops = rec_flops / (rec_avg_ms / 1e3) / 1e12 if rec_ms else None
-    dec_total, rec_total = sum(dec_ms), sum(rec_ms)
+    dec_total, rec_total = statistics.mean(dec_ms) * K, statistics.mean(rec_ms) * K / T  # amortised
     # DRAM bytes per launch from the committed ncu captures: the decode capture is
     # one launch at a known column count, scaled to this run's mean algorithmic
     # bytes; the recompression capture covers its three kernels at m = r + growth*T.
@@ -422,6 +438,8 @@ def run_gpu(args, w):
                            l2='flushed before every timed step (256 MiB write then 256 MiB read, untimed)',
                            parallelism=f'heads sharded over {ws} rank(s), one batch of requests each'),
                roofline=dominant, gpu_launches=K + rec_launches * len(rec_ms), clocks=clocks)
+    out['config']['recompression'] = (f'after every {T}th step, amortised: ms_per_step = mean decode + '
+                                      f'mean recompression / {T} ({len(rec_ms)} recompression(s) timed)')
     out['decode'] = dict(head_steps_per_s=round(heads_all * K / (dec_total / 1e3)),
                          us_per_step=round(dec_avg_ms * 1e3, 3), gbs=round(dec_gbs, 1),
                          frac_of_measured_hbm=round(dec_gbs / peaks['hbm_gbs'], 4),
@@ -467,17 +485,24 @@ def run_gpu(args, w):
     # device and its output device -> host inside the timed region.  Copies run on
     # their own streams into two device slots, so that the upload of step t+1 and
     # the download of step t-1 overlap the kernels of step t; events keep each slot
-    # from being overwritten before it has been consumed.
+    # from being overwritten before it has been consumed.  The pinned host side is a
+    # ring of a few step-sized slots (the serving workload moves ~0.9 GB in per step).
+    # One untimed interval of T steps warms the copy engines and the recompression up;
+    # the timed run covers whole intervals (K rounded up to a multiple of T), so each
+    # recompression is counted once per T steps.
     if not args.no_e2e:
         H = run.H
         segs = [run.q[0].numel(), run.k[0].numel(), run.v[0].numel(), run.gate[0].numel(), run.beta[0].numel()]
         offs = np.concatenate([[0], np.cumsum(segs)]).astype(np.int64)
         n_in = int(offs[-1])
         assert all(int(o) % 4 == 0 for o in offs)          # 16-byte aligned segments
-        hin = torch.empty(K, n_in, pin_memory=True)
+        K_e2e = -(-K // T) * T
+        W_e2e = max(T, W_)
+        n_host = min(4, total_steps)
+        hin = torch.empty(n_host, n_in, pin_memory=True)
         for j, src in enumerate((run.q, run.k, run.v, run.gate, run.beta)):
-            hin[:, offs[j]:offs[j + 1]].copy_(src[W_:W_ + K].reshape(K, -1))
-        hout = torch.empty(K, *run.o.shape, pin_memory=True)
+            hin[:, offs[j]:offs[j + 1]].copy_(src[:n_host].reshape(n_host, -1))
+        hout = torch.empty(n_host, *run.o.shape, pin_memory=True)
         din = [torch.empty(n_in, device=dev) for _ in range(2)]
         dout = [torch.empty_like(run.o) for _ in range(2)]
         up, down = torch.cuda.Stream(), torch.cuda.Stream()
@@ -499,60 +524,70 @@ def run_gpu(args, w):
                     raise RuntimeError('cudaEventCreateWithFlags failed')
                 out_.append(e)
             return out_
-        h2d_done, comp_done, d2h_done = new_events(K), new_events(K), new_events(K)
-        torch.cuda.synchronize()
-        if run.state.steps_since_compress:
-            run.recompress()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_ev = max(K_e2e, W_e2e)
+        h2d_done, comp_done, d2h_done = new_events(n_ev), new_events(n_ev), new_events(n_ev)
         h2d = n_in * 4
         d2h = run.o.numel() * 4
         s_up, s_down = vp(up.cuda_stream), vp(down.cuda_stream)
         s_comp = vp(sptr)
-        hin_p = [hin[i].data_ptr() for i in range(K)]
-        hout_p = [hout[i].data_ptr() for i in range(K)]
+        hin_p = [hin[i].data_ptr() for i in range(n_host)]
+        hout_p = [hout[i].data_ptr() for i in range(n_host)]
         din_p = [t.data_ptr() for t in din]
         dout_p = [t.data_ptr() for t in dout]
         in_args = [[dp + int(o) * 4 for o in offs[:5]] for dp in din_p]
+
+        def e2e_loop(n):
+            """n steps from a compression boundary; the last ends on one when T | n."""
+            def upload(i):
+                if i >= 2:
+                    rt.cudaStreamWaitEvent(s_up, comp_done[i - 2], 0)  # slot i % 2 consumed by step i-2
+                rc_ = rt.cudaMemcpyAsync(din_p[i % 2], hin_p[i % n_host], h2d, 1, s_up)
+                rt.cudaEventRecord(h2d_done[i], s_up)
+                return rc_
+
+            up.wait_stream(stream)
+            down.wait_stream(stream)
+            rc = upload(0)
+            for i in range(n):
+                slot = i % 2
+                if i + 1 < n:
+                    rc |= upload(i + 1)
+                rt.cudaStreamWaitEvent(s_comp, h2d_done[i], 0)
+                if i >= 2:
+                    rt.cudaStreamWaitEvent(s_comp, d2h_done[i - 2], 0)  # output slot read back
+                a_ = in_args[slot]
+                rc |= dec_fn(st_ref, a_[0], a_[1], a_[2], a_[3], a_[4], A_ptr, dout_p[slot], sptr)
+                if run.state.steps_since_compress == T:
+                    rc |= rec_fn(*rec_args)
+                rt.cudaEventRecord(comp_done[i], s_comp)
+                rt.cudaStreamWaitEvent(s_down, comp_done[i], 0)
+                rc |= rt.cudaMemcpyAsync(hout_p[i % n_host], dout_p[slot], d2h, 2, s_down)
+                rt.cudaEventRecord(d2h_done[i], s_down)
+            if rc:
+                raise RuntimeError(f'end-to-end loop: a call failed (status {rc})')
+            rt.cudaStreamWaitEvent(s_comp, d2h_done[n - 1], 0)
+
         torch.cuda.synchronize()
-
-        def upload(i):
-            if i >= 2:
-                rt.cudaStreamWaitEvent(s_up, comp_done[i - 2], 0)  # slot i % 2 consumed by step i-2
-            rc_ = rt.cudaMemcpyAsync(din_p[i % 2], hin_p[i], h2d, 1, s_up)
-            rt.cudaEventRecord(h2d_done[i], s_up)
-            return rc_
-
+        if run.state.steps_since_compress:
+            run.recompress()
+        e2e_loop(W_e2e)                                   # untimed warm-up interval
+        torch.cuda.synchronize()
+        if run.state.steps_since_compress:
+            run.recompress()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        up.wait_stream(stream)
-        down.wait_stream(stream)
-        rc = upload(0)
-        for i in range(K):
-            slot = i % 2
-            if i + 1 < K:
-                rc |= upload(i + 1)
-            rt.cudaStreamWaitEvent(s_comp, h2d_done[i], 0)
-            if i >= 2:
-                rt.cudaStreamWaitEvent(s_comp, d2h_done[i - 2], 0)  # output slot read back
-            a_ = in_args[slot]
-            rc |= dec_fn(st_ref, a_[0], a_[1], a_[2], a_[3], a_[4], A_ptr, dout_p[slot], sptr)
-            if run.state.steps_since_compress == T:
-                rc |= rec_fn(*rec_args)
-            rt.cudaEventRecord(comp_done[i], s_comp)
-            rt.cudaStreamWaitEvent(s_down, comp_done[i], 0)
-            rc |= rt.cudaMemcpyAsync(hout_p[i], dout_p[slot], d2h, 2, s_down)
-            rt.cudaEventRecord(d2h_done[i], s_down)
-        if rc:
-            raise RuntimeError(f'end-to-end loop: a call failed (status {rc})')
-        rt.cudaStreamWaitEvent(s_comp, d2h_done[K - 1], 0)
+        e2e_loop(K_e2e)
         e1.record(stream)
         torch.cuda.synchronize()
         for e in h2d_done + comp_done + d2h_done:
             rt.cudaEventDestroy(e)
         e2e_ms = e0.elapsed_time(e1)
         e2e_ms = sharding.max_over_ranks(e2e_ms, device=dev)
-        out['e2e'] = dict(value=round(heads_all * K / (e2e_ms / 1e3)), unit=UNIT,
+        out['e2e'] = dict(value=round(heads_all * K_e2e / (e2e_ms / 1e3)), unit=UNIT,
                           h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-                          ms_per_step=round(e2e_ms / K, 5))
+                          ms_per_step=round(e2e_ms / K_e2e, 5), steps=K_e2e, warmup_steps=W_e2e,
+                          host_slots=n_host)
 
     # ---- CPU oracle baseline (rank 0, N = 1) --------------------------------------------
     if rank == 0 and ws == 1 and not args.no_cpu:

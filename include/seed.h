@@ -21,7 +21,9 @@
  *
  * Conventions for every call:
  *  - All array pointers are DEVICE pointers owned by the caller; the library
- *    allocates nothing and keeps no global state.
+ *    allocates nothing and keeps no state between calls, with one exception:
+ *    the fixed 64 MiB device scratch of seed_recompress_noalloc (one array per
+ *    device that loads the library, held until the process exits).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *    stream).  Arguments are validated on the host before any launch; on a
  *    validation error nothing is launched and a seed_status code is returned.
@@ -216,15 +218,19 @@ int seed_recompress_ws(seed_state *st, float *trunc_err, int32_t *sweeps, void *
  * have no counterpart of this call: it is plumbing of this library.
  *   The scratch is a fixed 64 MiB per device, reserved when the library's
  *   kernels are loaded on that device; all heads are recompressed in one group,
- *   so a state whose heads need more than that (n_heads x the per-head size
- *   that seed_recompress_workspace_bytes reports for one head, at the current
- *   column count) is rejected with SEED_ERR_UNSUPPORTED_SHAPE before any CUDA
- *   call; use seed_recompress_ws for such states.
+ *   so a state whose heads need more than that is rejected with
+ *   SEED_ERR_UNSUPPORTED_SHAPE before any CUDA call; use seed_recompress_ws for
+ *   such states.  The need is n_heads x the per-head workspace at the current
+ *   column count m = r_max + growth * steps_since_compress;
+ *   seed_recompress_workspace_bytes(st, 1) reports the per-head size at full
+ *   capacity (steps_since_compress = T), an upper bound of it.
  *   All calls on a device share the one scratch: two calls that may overlap
  *   (on different streams or host threads) race on it and must be ordered by
  *   the caller.
- *   The first call on a device looks the scratch up and sets kernel attributes
- *   on the host; make it before any stream capture.
+ *   Every call looks the scratch's device address up on the host
+ *   (cudaGetSymbolAddress, no allocation) and sets kernel attributes; the first
+ *   call on a device also loads the library's kernels there, so make it before
+ *   any stream capture.
  * Results are bit-identical to seed_recompress_ws.  SEED_ERR_CUDA if the
  * scratch cannot be found.  Sets st->steps_since_compress = 0.
  */

@@ -3,7 +3,9 @@
 // Every call validates its arguments on the host and launches nothing when
 // they are wrong; kernels run asynchronously on the caller's stream.  The
 // library allocates no memory and keeps no state between calls: the state
-// lives in the caller's seed_state and device buffers.
+// lives in the caller's seed_state and device buffers.  The one exception is
+// the fixed device scratch of seed_recompress_noalloc (recompress_split.cu),
+// a file-scope __device__ array that every device loading the library holds.
 #include "common.cuh"
 
 #include <stdint.h>

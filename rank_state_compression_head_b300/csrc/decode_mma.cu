@@ -24,6 +24,8 @@
 // columns then follow Lemma 2 exactly as in the CUDA-core kernel (decode.cu).
 #include "common.cuh"
 
+#include <atomic>
+
 namespace seedk {
 
 constexpr int kMmaThreads = 128;
@@ -431,13 +433,19 @@ static cudaError_t launch_mma_t(const DecodeArgs &a, cudaStream_t s) {
   constexpr int NS = 1;
   using L = MmaSmem<VAR, DV, MAXC, NS>;
   auto kern = decode_mma_kernel<VAR, DV, MAXC, NS>;
-  static bool ready = false;
-  if (!ready) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+  // attributes belong to (kernel, device): set them the first time this kernel
+  // runs on each device of the process
+  static std::atomic<uint64_t> ready{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+  if (!bit || !(ready.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
     if (e == cudaSuccess)  // all of the unified L1/shared capacity as shared memory: more heads per SM
       e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    ready = true;
+    ready.fetch_or(bit, std::memory_order_acq_rel);
   }
   kern<<<a.sv.n_heads, kMmaThreads, L::BYTES, s>>>(a);
   return cudaGetLastError();

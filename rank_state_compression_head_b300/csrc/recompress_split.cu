@@ -27,8 +27,6 @@
 #include "qr_registers.cuh"
 #include "svd_warp.cuh"
 
-#include <mutex>
-
 namespace seedk {
 
 struct SplitLayout {
@@ -473,26 +471,16 @@ cudaError_t launch_recompress_split(const StateView &sv, int factor_dtype, float
 }
 
 // ---- fixed scratch for seed_recompress_noalloc ---------------------------------------------
-// One array per device that loads the library; its address is looked up once
-// per device and cached.
+// One array per device that loads the library.  Host code sees only a stand-in
+// for it, so its device address is asked for on every call (a host-side lookup
+// that allocates nothing): an address kept from an earlier call would go stale
+// if the caller reset the device in between.
 static __device__ __align__(256) float g_recompress_scratch[kNoAllocScratchFloats];
 
 cudaError_t noalloc_scratch(float **ptr) {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static float *cache[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lock(mu);
-  if (dev >= 0 && dev < kMaxDevices && cache[dev]) {
-    *ptr = cache[dev];
-    return cudaSuccess;
-  }
   void *p = nullptr;
-  e = cudaGetSymbolAddress(&p, g_recompress_scratch);
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_recompress_scratch);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < kMaxDevices) cache[dev] = static_cast<float *>(p);
   *ptr = static_cast<float *>(p);
   return cudaSuccess;
 }

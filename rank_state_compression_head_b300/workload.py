@@ -59,6 +59,7 @@ class DeviceRun:
         self.trunc = torch.zeros(max(H, 1), **f32)
         self.nb = nb
         self.ws, self.ws_bytes = None, 0
+        self.ws_heads = ws_heads
         if ws_heads > 0 and H > 0:
             self.ws_bytes = seed_recompress_workspace_bytes(self.state.st, min(H, ws_heads))
             self.ws = torch.empty(self.ws_bytes, device=self.dev, dtype=torch.uint8)
@@ -90,6 +91,17 @@ class DeviceRun:
             seed_recompress_ws(self.state.st, trunc_err, sweeps, self.ws, self.ws_bytes, stream)
         else:
             seed_recompress_ex(self.state.st, trunc_err, sweeps, stream)
+
+    def recompress_launches(self) -> int:
+        """Kernels one recompression after T steps launches (bookkeeping of the count
+        a benchmark reports; mirrors the launcher in recompress_split.cu)."""
+        if self.ws is None:
+            return 1
+        st = self.state
+        m_max = st.r_max + st.growth * self.w.T
+        groups = -(-self.H // min(self.H, self.ws_heads))
+        classes = 1 if st.ranks is None or m_max <= 16 else -(-m_max // 16)
+        return 3 * groups * classes
 
     def step(self, t: int, slot: int = 0, stream=None) -> bool:
         """Decode step t (1-based) with inputs already in ``slot``; recompress when T divides t."""

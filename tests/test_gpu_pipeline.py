@@ -109,7 +109,7 @@ CASES = {
 
 
 @pytest.mark.parametrize('name', list(CASES))
-def test_workload_matches_oracle(name):
+def test_workload_matches_oracle(name, record_property):
     w = synth.WORKLOADS[name]
     steps = CASES[name]['steps'] or w.steps
     sample = sample_heads(w, CASES[name]['n']) if w.n_heads > 4 else list(range(w.n_heads))
@@ -118,21 +118,24 @@ def test_workload_matches_oracle(name):
     run, S_gpu, outs, states, final, err0 = run_pipeline(w, sample, steps, record)
     tol = TOL[w.factor_dtype]
     worst = dict(state=0.0, out=0.0, pooled=0.0, final=0.0)
+    every = list(range(1, steps + 1))
     for i, h in enumerate(sample):
-        traj, tok, A = oracle_head(w, h, steps, record)
+        # the oracle's state at every step: the normwise read-out error is checked at each one
+        traj, tok, A = oracle_head(w, h, steps, every)
         for t in record:
             worst['state'] = max(worst['state'], rel_err(states[t][i], traj.states[t]))
         ref_final = oracle.materialize(traj.final)
         worst['final'] = max(worst['final'], rel_err(final[i], ref_final))
         o_ref = np.array(traj.outputs)
         worst['pooled'] = max(worst['pooled'], rel_err(outs[:, i], o_ref))
-        # normwise read-out error at the recorded steps (state norm of the oracle there)
-        for t in record:
+        # normwise read-out error at every step (state norm of the oracle there)
+        for t in every:
             q = tok(t - 1)['C' if w.variant == 'mamba2' else 'q']
             worst['out'] = max(worst['out'], normwise_out_err(outs[t - 1, i], o_ref[t - 1], traj.states[t], q))
         # truncation error of the end-of-prefill compression, up to fp32 rounding of the state
         e_ref = traj.compress_errors[0]
         assert abs(err0[i] - e_ref) <= tol * e_ref + 1e-5 * np.linalg.norm(traj.prefill_state), h
+    record_property('parity', dict(case=name, tol=tol, heads=len(sample), steps=steps, **worst))
     print(name, {k: f'{v:.2e}' for k, v in worst.items()})
     assert max(worst.values()) < tol, worst
 

@@ -64,3 +64,24 @@ def test_noalloc_rejects_oversize_without_launch():
         R.seed_recompress_noalloc(buf.st)
     assert e.value.status == R.SEED_ERR_UNSUPPORTED_SHAPE
     assert buf.st.steps_since_compress == T
+
+
+def test_noalloc_leaves_device_memory_unchanged():
+    # The point of the call: nothing is allocated.  After one call (which loads the
+    # kernels it launches), a second call changes neither the free device memory the
+    # driver reports nor what the caching allocator holds.
+    H, T = 40, 16
+    ranks = _ranks(H, T)
+    states, vbar = random_states(91, H, 128, 128, ranks, T, T, 'gdn', 'bf16')
+    buf = make_buffers('gdn', 'bf16', H, 128, 128, T, vbar, ranks)
+    err = torch.zeros(H, device='cuda')
+    upload(buf, states, T)
+    R.seed_recompress_noalloc(buf.st, err)
+    upload(buf, states, T)
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    R.seed_recompress_noalloc(buf.st, err)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == alloc0
+    assert int(buf.status.abs().sum()) == 0
