@@ -415,7 +415,7 @@ def run_gpu(args, w):
             rec_traffic = round(float(prof['traffic_bytes_per_launch']))
         except (KeyError, ValueError):
             rec_traffic = None
-    roof_dec = dict(kernel='decode_mma_kernel' if w.factor_dtype == 'bf16' else 'decode_kernel', bound='hbm',
+    roof_dec = dict(kernel='decode_mma_kernel' if w.factor_dtype != 'f32' else 'decode_kernel', bound='hbm',
                     achieved=round(dec_gbs, 1),
                     peak=peaks['hbm_gbs'], unit='GB/s', frac=round(dec_gbs / peaks['hbm_gbs'], 4),
                     traffic=traffic, peak_src=peaks['src'],

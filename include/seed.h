@@ -31,8 +31,10 @@
  *    not converge) are written per head to `status[h]` when `status` is not
  *    NULL; read it after synchronising.  0 = OK, otherwise a seed_status code.
  *  - Floating-point vectors (q, k, v, o, a, S, scales, the per-channel gate)
- *    are fp32, contiguous per head, with 16-byte aligned base pointers.  Factors U and W are fp32 or bf16 (round to nearest
- *    even on store), arithmetic is fp32.
+ *    are fp32, contiguous per head, with 16-byte aligned base pointers.
+ *    Factors U and W are fp32, bf16 or fp16, rounded on store as
+ *    seed_state.rounding says; arithmetic is fp32.  fp16 factors must stay
+ *    within its range (|x| < 65504): the library does not rescale them.
  *  - d_k must be 128; d_v must be 128 or 64.  The largest number of factor
  *    columns a head may hold is SEED_MAX_COLUMNS.
  */
@@ -67,7 +69,18 @@ typedef enum {
   SEED_MAMBA2 = 2  /* Mamba-2:              S' = exp(dt A) S + dt B x^T  (N = d_k, P = d_v)      */
 } seed_variant;
 
-typedef enum { SEED_F32 = 0, SEED_BF16 = 1 } seed_dtype;
+typedef enum { SEED_F32 = 0, SEED_BF16 = 1, SEED_F16 = 2 } seed_dtype;
+
+/* How a factor element is rounded when it is stored in a 16-bit factor dtype
+ * (picx.dev summary, Practical implications: 16-bit factors; list view, the
+ * drift table by storage format and rounding).  32-bit factors ignore it. */
+typedef enum {
+  SEED_ROUND_NEAREST = 0,    /* round to nearest even                                 */
+  SEED_ROUND_STOCHASTIC = 1  /* up with probability (x - lo) / (hi - lo), so that the
+                                stored value is x on average; the random bits come
+                                from Philox4x32-10 keyed by seed_state.sr_seed, with
+                                the pool column and element as counter               */
+} seed_rounding;
 
 #define SEED_MAX_COLUMNS 64
 
@@ -100,7 +113,7 @@ typedef struct {
   int32_t r_max;                 /* an upper bound of rank[] (== r when rank == NULL)     */
   int32_t steps_since_compress;  /* s: advanced by seed_decode_step on success, reset to 0
                                     by seed_compress_dense and seed_recompress            */
-  int32_t reserved_;             /* set to 0                                               */
+  int32_t rounding;              /* seed_rounding of stored 16-bit factor elements         */
   const int32_t *rank;           /* [n_heads] per-head rank, or NULL                       */
   const int64_t *col_offset;     /* [n_heads] first column of each head, or NULL           */
   float *a;                      /* [n_heads][d_k] sink coefficients                       */
@@ -111,6 +124,9 @@ typedef struct {
   const float *vbar;             /* [n_dir][d_v] unit sink directions                      */
   const int32_t *vbar_index;     /* [n_heads] direction of each head, or NULL (= h)        */
   int32_t *status;               /* [n_heads] per-head device status, or NULL              */
+  uint64_t sr_seed;              /* key of the stochastic-rounding bits: change it from call
+                                    to call (e.g. the global step number) for fresh bits; the
+                                    same seed and inputs give the same bits                */
 } seed_state;
 
 /* Columns one head needs: r + growth * T. */
@@ -182,23 +198,31 @@ int seed_recompress_ex(seed_state *st, float *trunc_err, int32_t *sweeps, seed_s
  * seed_recompress_workspace_bytes — size of the device workspace that
  * seed_recompress_ws needs to recompress `heads` heads per group, at the
  * state's full capacity (r_max + growth*T columns per head), so that one
- * allocation serves every call on this state.  Written to *bytes.
+ * allocation serves every call on this state (it depends on the factor dtype:
+ * about 24 KB a head at 48 columns for 16-bit factors, 49 KB for 32-bit).
+ * Written to *bytes.
  * Returns a seed_status code (SEED_ERR_INVALID_ARG for heads < 1 or bytes NULL).
  */
 int seed_recompress_workspace_bytes(const seed_state *st, int32_t heads, int64_t *bytes);
 
 /*
- * seed_recompress_ws — seed_recompress_ex in three phases that pass their
- * intermediates through a caller-provided workspace: (1) per head, Householder
- * QR of U_eff and of W (W's reflectors kept) and the core K = R_a R_b^T;
- * (2) per head, the Jacobi SVD of K, ordering and truncation error; (3) per head
- * and factor, the rebuild: U = U_eff (R_b^T Y_r), which equals Q_a K Y_r since
- * U_eff = Q_a R_a, and W = Q_b Y_r by W's reflectors applied to [Y_r; 0], so
- * that no Q is formed.  Each phase has its own layout (the factor panels in
- * registers, one warp per head for the core SVD), so more heads are resident per
- * SM than in the single kernel of seed_recompress.  Same factorization and
- * truncation as seed_recompress_ex; the results agree with it to rounding
- * (summation orders differ), not bit for bit.
+ * seed_recompress_ws — the recompression of seed_recompress_ex in three phases
+ * that pass their intermediates through a caller-provided workspace; the same
+ * truncation (the rank(h) largest singular values of U_eff W^T kept, U = X_r
+ * Sigma_r, W orthonormal, scales reset), agreeing with seed_recompress_ex to
+ * rounding, not bit for bit.  The route depends on the factor dtype:
+ *   32-bit factors: (1) per head, Householder QR of U_eff and of W (W's
+ *     reflectors kept) and the core K = R_a R_b^T; (2) per head, the Jacobi
+ *     SVD of K; (3) per head and factor, U = U_eff (R_b^T Y_r) (= Q_a K Y_r) and
+ *     W = Q_b Y_r by W's reflectors applied to [Y_r; 0]; no Q is formed.
+ *   16-bit factors: (1) per head, the Gram matrix W^T W on the tensor cores, its
+ *     Cholesky R_b^T R_b, B = U_eff R_b^T (tensor cores) and M = B^T B; (2) per
+ *     head, the eigenvectors Y of M (pivoted Cholesky, then one-sided Jacobi);
+ *     (3) per head and factor, U = U_eff R_b^T Y_r and W = W R_b^{-1} Y_r on the
+ *     tensor cores.  Its resolution of nearly dependent columns of W, about
+ *     1e-3 of their norm, is finer than the rounding of a stored 16-bit column.
+ * Each phase has its own layout, so more heads are resident per SM than in the
+ * single kernel of seed_recompress.
  *   workspace        DEVICE memory owned by the caller, 16-byte aligned
  *   workspace_bytes  its size; heads are processed in groups of as many as it
  *                    holds (SEED_ERR_INVALID_ARG if not even one); groups of at

@@ -38,10 +38,12 @@ SEED_ERR_NOT_CONVERGED = 6
 SEED_ERR_NONFINITE = 7
 SEED_ERR_TIMEOUT = 8
 SEED_GDN, SEED_KDA, SEED_MAMBA2 = 0, 1, 2
-SEED_F32, SEED_BF16 = 0, 1
+SEED_F32, SEED_BF16, SEED_F16 = 0, 1, 2
+SEED_ROUND_NEAREST, SEED_ROUND_STOCHASTIC = 0, 1
 SEED_MAX_COLUMNS = 64
 VARIANTS = {'gdn': SEED_GDN, 'kda': SEED_KDA, 'mamba2': SEED_MAMBA2}
-DTYPES = {'f32': SEED_F32, 'bf16': SEED_BF16}
+DTYPES = {'f32': SEED_F32, 'bf16': SEED_BF16, 'f16': SEED_F16}
+ROUNDINGS = {'nearest': SEED_ROUND_NEAREST, 'stochastic': SEED_ROUND_STOCHASTIC}
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -54,9 +56,9 @@ class seed_state(ctypes.Structure):
     """Mirror of ``seed_state`` in seed.h (same field order and types)."""
     _fields_ = [
         ('variant', _i32), ('factor_dtype', _i32), ('n_heads', _i32), ('d_k', _i32), ('d_v', _i32),
-        ('T', _i32), ('r', _i32), ('r_max', _i32), ('steps_since_compress', _i32), ('reserved_', _i32),
+        ('T', _i32), ('r', _i32), ('r_max', _i32), ('steps_since_compress', _i32), ('rounding', _i32),
         ('rank', _vp), ('col_offset', _vp), ('a', _vp), ('U', _vp), ('W', _vp), ('scale', _vp),
-        ('vbar', _vp), ('vbar_index', _vp), ('status', _vp),
+        ('vbar', _vp), ('vbar_index', _vp), ('status', _vp), ('sr_seed', ctypes.c_uint64),
     ]
 
 

@@ -13,7 +13,7 @@ F32 = 4
 
 
 def factor_bytes(factor_dtype: str) -> int:
-    return 2 if factor_dtype == 'bf16' else 4
+    return 2 if factor_dtype in ('bf16', 'f16') else 4
 
 
 def decode_bytes(variant: str, d_k: int, d_v: int, m: int, factor_dtype: str) -> int:

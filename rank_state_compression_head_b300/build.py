@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, 'csrc')
 INCLUDE = os.path.join(ROOT, 'include')
 BUILD = os.path.join(ROOT, '_build')
 LIB = os.path.join(PKG, 'libseed.so')
-SOURCES = ['api.cu', 'decode.cu', 'decode_mma.cu', 'recompress.cu', 'recompress_split.cu', 'dense.cu', 'synth.cu']
+SOURCES = ['api.cu', 'decode.cu', 'decode_mma.cu', 'recompress.cu', 'recompress_split.cu', 'recompress_gram.cu', 'dense.cu', 'synth.cu']
 ARCH = ['-gencode', 'arch=compute_103a,code=sm_103a']
 FLAGS = ['-O3', '-lineinfo', '-std=c++17', '-Xcompiler', '-fPIC', '--expt-relaxed-constexpr',
          '-I', INCLUDE, '-I', CSRC]

@@ -22,7 +22,9 @@ inline int growth_of(int variant) { return variant == SEED_KDA ? 2 : 1; }
 int check_state(const seed_state *st) {
   if (!st) return SEED_ERR_INVALID_ARG;
   if (st->variant < SEED_GDN || st->variant > SEED_MAMBA2) return SEED_ERR_INVALID_ARG;
-  if (st->factor_dtype != SEED_F32 && st->factor_dtype != SEED_BF16) return SEED_ERR_INVALID_ARG;
+  if (st->factor_dtype != SEED_F32 && st->factor_dtype != SEED_BF16 && st->factor_dtype != SEED_F16)
+    return SEED_ERR_INVALID_ARG;
+  if (st->rounding != SEED_ROUND_NEAREST && st->rounding != SEED_ROUND_STOCHASTIC) return SEED_ERR_INVALID_ARG;
   if (st->n_heads < 0 || st->T < 1 || st->steps_since_compress < 0) return SEED_ERR_INVALID_ARG;
   if (st->d_k != kDK || (st->d_v != 64 && st->d_v != 128)) return SEED_ERR_UNSUPPORTED_SHAPE;
   const int rmax = st->rank ? st->r_max : st->r;
@@ -48,6 +50,8 @@ StateView view_of(const seed_state *st) {
   v.T = st->T;
   v.r = st->r;
   v.steps = st->steps_since_compress;
+  v.rounding = st->factor_dtype == SEED_F32 ? SEED_ROUND_NEAREST : st->rounding;
+  v.sr_seed = st->sr_seed;
   v.growth = growth_of(st->variant);
   v.cap_uniform = (st->rank ? st->r_max : st->r) + v.growth * st->T;
   v.rank = st->rank;
@@ -138,7 +142,7 @@ extern "C" int seed_recompress_workspace_bytes(const seed_state *st, int32_t hea
   if (heads < 1 || !bytes) return SEED_ERR_INVALID_ARG;
   const int rmax = rmax_of(st);
   const int m_cap = rmax + growth_of(st->variant) * st->T;
-  *bytes = (int64_t)heads * split_floats_per_head(m_cap, rmax, st->d_v) * (int64_t)sizeof(float);
+  *bytes = (int64_t)heads * split_floats_per_head(st->factor_dtype, m_cap, rmax, st->d_v) * (int64_t)sizeof(float);
   return SEED_OK;
 }
 
@@ -152,7 +156,7 @@ extern "C" int seed_recompress_ws(seed_state *st, float *trunc_err, int32_t *swe
   if (misaligned(workspace)) return SEED_ERR_ALIGNMENT;
   const int rmax = rmax_of(st);
   const int m_max = rmax + growth_of(st->variant) * st->steps_since_compress;
-  const int64_t per_head = split_floats_per_head(m_max, rmax, st->d_v) * (int64_t)sizeof(float);
+  const int64_t per_head = split_floats_per_head(st->factor_dtype, m_max, rmax, st->d_v) * (int64_t)sizeof(float);
   const int64_t chunk = workspace_bytes / per_head;
   if (chunk < 1) return SEED_ERR_INVALID_ARG;
   c = cuda_status(launch_recompress_split(view_of(st), st->factor_dtype, trunc_err, sweeps, m_max, rmax,
@@ -169,7 +173,7 @@ extern "C" int seed_recompress_noalloc(seed_state *st, float *trunc_err, int32_t
   if (st->n_heads == 0) { st->steps_since_compress = 0; return SEED_OK; }
   const int rmax = rmax_of(st);
   const int m_max = rmax + growth_of(st->variant) * st->steps_since_compress;
-  const int64_t need = (int64_t)st->n_heads * split_floats_per_head(m_max, rmax, st->d_v);
+  const int64_t need = (int64_t)st->n_heads * split_floats_per_head(st->factor_dtype, m_max, rmax, st->d_v);
   if (need > kNoAllocScratchFloats) return SEED_ERR_UNSUPPORTED_SHAPE;  // checked before any CUDA call
   float *scratch = nullptr;
   if (noalloc_scratch(&scratch) != cudaSuccess) return SEED_ERR_CUDA;

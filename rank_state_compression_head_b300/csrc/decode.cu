@@ -467,8 +467,8 @@ cudaError_t launch_decode(const StateView &sv, int factor_dtype, const float *q,
                           const float *v, const float *gate, const float *beta, const float *A,
                           float *o, int cols_max, cudaStream_t s) {
   DecodeArgs a{sv, q, k, v, gate, beta, A, o};
-  // bf16 factors: the two contractions run on the tensor cores (decode_mma.cu)
-  if (factor_dtype == SEED_BF16) return launch_decode_mma(a, cols_max, s);
+  // 16-bit factors: the two contractions run on the tensor cores (decode_mma.cu)
+  if (factor_dtype != SEED_F32) return launch_decode_mma(a, factor_dtype, cols_max, s);
   return launch_decode_v<float>(a, cols_max, s);
 }
 

@@ -1,27 +1,31 @@
-// Fused read-out + exact factored update for bf16 factors, with the two
-// contractions of a step on the tensor cores.
+// Fused read-out + exact factored update for 16-bit factors (bf16 or fp16), with
+// the two contractions of a step on the tensor cores.
 //
 // "Shallow Encoding Emits Deep Memories", picx.dev summary, Methodology >
 // Exact Update (Lemma 2); thelatestinai.com list view, Table 1 (decode
 // column: read-out and update of each recurrent state).
 //
-// CTAs of 256 threads walk the heads blockIdx.x, blockIdx.x + gridDim.x, ...
+// CTAs of 128 threads walk the heads blockIdx.x, blockIdx.x + gridDim.x, ...
 // through a ring of NS shared-memory stages (NS - 1 heads in flight while one
 // is computed); launched with one stage and one head per CTA, as many CTAs per
-// SM as fit keep several heads' loads in flight.  The threads copy the factor columns
-// (contiguous in HBM) with asynchronous 16-byte copies into rows padded to
-// 272 bytes, so that the ldmatrix reads below hit 32 distinct banks.  Per
+// SM as fit keep several heads' loads in flight.  The threads copy the factor
+// columns (contiguous in HBM) with asynchronous 16-byte copies into rows padded
+// to 272 bytes, so that the ldmatrix reads below hit 32 distinct banks.  Per
 // head the CTA does
 //
+//   split    rows [k_hi; k_lo; q_hi; q_lo] of the U-pass operand, once (smem)
 //   U pass   X[4][m] = [k_hi; k_lo; q_hi; q_lo] U_stored          (mma m16n8k16)
 //   scale    x_k = c * (X0 + X1),  x_q = c * (X2 + X3)              (column scales)
 //   W pass   [Wx_k Wx_q] = W [x_k_hi x_k_lo x_q_hi x_q_lo]           (mma m16n8k16)
 //
-// Products of bf16 values are exact in fp32 and the accumulation is fp32.  The
-// fp32 operands (k, q, x) enter as a bf16 pair hi + lo, so they carry 16
-// significant bits; the result differs from fp32 dot products by less than
-// fp32 summation-order noise times ~2^-8.  The read-out and the appended
-// columns then follow Lemma 2 exactly as in the CUDA-core kernel (decode.cu).
+// Products of 16-bit values are exact in fp32 and the accumulation is fp32.
+// The fp32 operands (k, q, x) enter as a 16-bit pair hi + lo, so they carry 16
+// (bf16) or 22 (fp16) significant bits; the result differs from fp32 dot
+// products by less than fp32 summation-order noise times ~2^-8.  The read-out
+// and the appended columns then follow Lemma 2 exactly as in the CUDA-core
+// kernel (decode.cu); an appended element is rounded to the factor type once,
+// to nearest or stochastically (seed.h, seed_rounding), and the read-out uses
+// the rounded value.
 #include "common.cuh"
 
 #include <atomic>
@@ -59,7 +63,9 @@ struct MmaSmem {
   static constexpr int XS_OFF = NS * S::BYTES;                             // bf16 [2 NX][XLD]
   static constexpr int WX_OFF = XS_OFF + ((2 * NX * XLD * 2 + 15) & ~15);  // f32 [NX][DV]
   static constexpr int SCAL_OFF = WX_OFF + NX * DV * 4;                    // f32 [NW][8]
-  static constexpr int BYTES = SCAL_OFF + (kMmaThreads / 32) * 8 * 4;
+  static constexpr int ALD = kDK + 8;                                      // 16-bit per operand row
+  static constexpr int AS_OFF = SCAL_OFF + (kMmaThreads / 32) * 8 * 4;     // [2 NX][ALD]: U-pass rows
+  static constexpr int BYTES = AS_OFF + 2 * NX * ALD * 2;
 };
 
 __device__ static inline void cp_async16(void *dst, const void *src) {
@@ -83,29 +89,8 @@ __device__ static inline void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
-// D += A B, m16n8k16, bf16 inputs, fp32 accumulate
-__device__ static inline void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                       uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// Two fp32 values as packed bf16: their high parts (part = 0) or the
-// remainders x - hi (part = 1); element .x goes to the low half.
-__device__ static inline uint32_t split_bf16x2(float2 v, int part) {
-  __nv_bfloat162 hi = __float22bfloat162_rn(v);
-  if (part) {
-    const float2 h = __bfloat1622float2(hi);
-    hi = __float22bfloat162_rn(make_float2(v.x - h.x, v.y - h.y));
-  }
-  return *reinterpret_cast<uint32_t *>(&hi);
-}
-
-template <int VAR, int DV, int MAXC, int NS>
+template <typename TF, int VAR, int DV, int MAXC, int NS>
 __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const DecodeArgs p) {
-  using TF = __nv_bfloat16;
   constexpr int DK = kDK;
   constexpr int NT = kMmaThreads;
   using S = MmaStage<VAR, DV, MAXC>;
@@ -118,7 +103,7 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
   static_assert(MAXC % 16 == 0 && MAXC <= 64, "column tiles");
 
   extern __shared__ __align__(128) unsigned char smem[];
-  __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem + L::XS_OFF);
+  TF *xs = reinterpret_cast<TF *>(smem + L::XS_OFF);
   float *wxs = reinterpret_cast<float *>(smem + L::WX_OFF);
   float *scal = reinterpret_cast<float *>(smem + L::SCAL_OFF);
 
@@ -143,14 +128,21 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
         const int dir = sv.dir_of(h);
         const TF *Ug = reinterpret_cast<const TF *>(sv.U) + c0 * DK;
         const TF *Wg = reinterpret_cast<const TF *>(sv.W) + c0 * DV;
+        // 16-byte chunk c of column j: a thread keeps its chunk and walks the
+        // columns NT / chunks-per-column apart (pointer increments only)
         constexpr int UCH = DK * 2 / 16, WCH = DV * 2 / 16;  // 16-byte chunks per column
-        for (int idx = tid; idx < m * UCH; idx += NT) {
-          const int j = idx / UCH, c = idx % UCH;
-          cp_async16(st + S::U_OFF + j * S::USTR + c * 16, Ug + (int64_t)j * DK + c * 8);
+        constexpr int UJS = NT / UCH, WJS = NT / WCH;         // column step of a thread
+        {
+          const int c = tid % UCH;
+          unsigned char *d = st + S::U_OFF + (tid / UCH) * S::USTR + c * 16;
+          const TF *src = Ug + (int64_t)(tid / UCH) * DK + c * 8;
+          for (int j = tid / UCH; j < m; j += UJS, d += UJS * S::USTR, src += UJS * DK) cp_async16(d, src);
         }
-        for (int idx = tid; idx < m * WCH; idx += NT) {
-          const int j = idx / WCH, c = idx % WCH;
-          cp_async16(st + S::W_OFF + j * S::WSTR + c * 16, Wg + (int64_t)j * DV + c * 8);
+        {
+          const int c = tid % WCH;
+          unsigned char *d = st + S::W_OFF + (tid / WCH) * S::WSTR + c * 16;
+          const TF *src = Wg + (int64_t)(tid / WCH) * DV + c * 8;
+          for (int j = tid / WCH; j < m; j += WJS, d += WJS * S::WSTR, src += WJS * DV) cp_async16(d, src);
         }
         if (tid < DK / 4) {
           cp_async16(st + S::Q_OFF + tid * 16, p.q + (int64_t)h * DK + tid * 4);
@@ -220,7 +212,7 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
     // padding: x rows and W columns [m, m16) must be zero for the W pass
     for (int idx = tid; idx < NA * (L::XLD - m); idx += NT) {
       const int row = idx / (L::XLD - m), j = m + idx % (L::XLD - m);
-      xs[row * L::XLD + j] = __float2bfloat16_rn(0.f);
+      xs[row * L::XLD + j] = Mma16<TF>::cvt(0.f);
     }
     {
       constexpr int CH = S::WSTR / 16;
@@ -230,30 +222,38 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
       }
     }
 
+    // ---- U-pass operand rows, split once: [k_hi; k_lo; q_hi; q_lo] (KDA: D k and
+    // alpha D q; Mamba-2: C alone), thread t splits element t of each vector ---------------
+    {
+      TF *as_ = reinterpret_cast<TF *>(smem + L::AS_OFF);
+      if (tid < DK) {
+        float vk = M2 ? qs[tid] : ks[tid], vq = qs[tid];
+        if (KDA) {
+          vk *= scs[tid];
+          vq *= als[tid] * scs[tid];
+        }
+        const TF kh = Mma16<TF>::cvt(vk);
+        as_[tid] = kh;
+        as_[L::ALD + tid] = Mma16<TF>::cvt(vk - Mma16<TF>::back(kh));
+        if (NX == 2) {
+          const TF qh = Mma16<TF>::cvt(vq);
+          as_[2 * L::ALD + tid] = qh;
+          as_[3 * L::ALD + tid] = Mma16<TF>::cvt(vq - Mma16<TF>::back(qh));
+        }
+      }
+    }
+    __syncthreads();  // barrier A2: the split operand rows are visible
+
     // ---- U pass: column tiles of 8, round robin over the warps -----------------------
     if (warp * 8 < m) {
       uint32_t a0[8], a2[8];
+      {
+        const TF *row = reinterpret_cast<const TF *>(smem + L::AS_OFF) + (gq < NA ? gq : 0) * L::ALD;
 #pragma unroll
-      for (int ks_ = 0; ks_ < 8; ++ks_) {
-        a0[ks_] = 0u;
-        a2[ks_] = 0u;
-        if (gq < NA) {
+        for (int ks_ = 0; ks_ < 8; ++ks_) {
           const int k0 = ks_ * 16 + 2 * tq;
-          const float *vec = (gq < 2) ? (M2 ? qs : ks) : qs;
-          float2 lo2 = *reinterpret_cast<const float2 *>(vec + k0);
-          float2 hi2 = *reinterpret_cast<const float2 *>(vec + k0 + 8);
-          if (KDA) {  // D k for the k rows, alpha D q for the q rows
-            const float2 d_lo = *reinterpret_cast<const float2 *>(scs + k0);
-            const float2 d_hi = *reinterpret_cast<const float2 *>(scs + k0 + 8);
-            lo2.x *= d_lo.x; lo2.y *= d_lo.y; hi2.x *= d_hi.x; hi2.y *= d_hi.y;
-            if (gq >= 2) {
-              const float2 l_lo = *reinterpret_cast<const float2 *>(als + k0);
-              const float2 l_hi = *reinterpret_cast<const float2 *>(als + k0 + 8);
-              lo2.x *= l_lo.x; lo2.y *= l_lo.y; hi2.x *= l_hi.x; hi2.y *= l_hi.y;
-            }
-          }
-          a0[ks_] = split_bf16x2(lo2, gq & 1);
-          a2[ks_] = split_bf16x2(hi2, gq & 1);
+          a0[ks_] = gq < NA ? *reinterpret_cast<const uint32_t *>(row + k0) : 0u;
+          a2[ks_] = gq < NA ? *reinterpret_cast<const uint32_t *>(row + k0 + 8) : 0u;
         }
       }
       for (int n0 = warp * 8; n0 < m; n0 += NT / 4) {
@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
       for (int kk = 0; kk < 4; ++kk) {
         uint32_t b[4];
         ldsm_x4(row_addr + kk * 64, b);
-        mma_bf16(d, a0[2 * kk], 0u, a2[2 * kk], 0u, b[0], b[1]);
-        mma_bf16(e, a0[2 * kk + 1], 0u, a2[2 * kk + 1], 0u, b[2], b[3]);
+        Mma16<TF>::mma(d, a0[2 * kk], 0u, a2[2 * kk], 0u, b[0], b[1]);
+        Mma16<TF>::mma(e, a0[2 * kk + 1], 0u, a2[2 * kk + 1], 0u, b[2], b[3]);
       }
       d[0] += e[0];
       d[1] += e[1];
@@ -278,9 +278,9 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
           if (j < m) {
             const float c = KDA ? 1.f : scs[j];
             const float x = c * (e ? d[1] + o1 : d[0] + o0);
-            const __nv_bfloat16 xh = __float2bfloat16_rn(x);
+            const TF xh = Mma16<TF>::cvt(x);
             xs[gq * L::XLD + j] = xh;
-            xs[(gq + 1) * L::XLD + j] = __float2bfloat16_rn(x - __bfloat162float(xh));
+            xs[(gq + 1) * L::XLD + j] = Mma16<TF>::cvt(x - Mma16<TF>::back(xh));
           }
         }
       }
@@ -288,6 +288,10 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
     }
 
     // ---- block scalars: thread t owns row t (< DK) and value column t (< DV) ----------
+    // stochastic rounding of the appended elements: one Philox block a thread, words
+    // x, y for U and W of column m, z, w for column m + 1 (KDA)
+    uint4 rb = make_uint4(0u, 0u, 0u, 0u);
+    if (sv.rounding == kRoundStochastic) rb = sr_bits(sv.sr_seed, c0 + m, (uint32_t)tid, kSrAppend);
     float S_loc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) S_loc[j] = 0.f;
@@ -296,18 +300,18 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
     if (tid < DK) {
       kt = ks[tid]; qt = qs[tid]; at = as[tid];
       if (VAR == SEED_GDN) {
-        unew0 = Elem<TF>::round(kt);
+        unew0 = store_value<TF>(kt, sv.rounding, rb.x);
         S_loc[0] = kt * at; S_loc[1] = qt * at; S_loc[2] = kt * qt; S_loc[3] = unew0 * qt;
       } else if (KDA) {
         alt = als[tid];
         Dt = scs[tid];
         const float Dn = alt * Dt;
-        unew0 = Elem<TF>::round(kt / Dt);
-        unew1 = Elem<TF>::round(kt / Dn);
+        unew0 = store_value<TF>(kt / Dt, sv.rounding, rb.x);
+        unew1 = store_value<TF>(kt / Dn, sv.rounding, rb.z);
         S_loc[0] = kt * at; S_loc[1] = alt * at * qt; S_loc[2] = alt * kt * qt; S_loc[3] = kt * qt;
         S_loc[6] = unew0 * Dn * qt; S_loc[7] = unew1 * Dn * qt;
       } else {
-        unew0 = Elem<TF>::round(dt * kt);
+        unew0 = store_value<TF>(dt * kt, sv.rounding, rb.x);
         S_loc[0] = at * qt; S_loc[1] = kt * qt; S_loc[2] = unew0 * qt;
       }
     }
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
           b0 = *reinterpret_cast<const uint32_t *>(xs + gq * L::XLD + j0 + 2 * tq);
           b1 = *reinterpret_cast<const uint32_t *>(xs + gq * L::XLD + j0 + 2 * tq + 8);
         }
-        mma_bf16(d, a[0], a[1], a[2], a[3], b0, b1);
+        Mma16<TF>::mma(d, a[0], a[1], a[2], a[3], b0, b1);
       }
       if (tq < NX) {
         wxs[tq * DV + i0 + gq] = d[0] + d[1];
@@ -366,12 +370,12 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
       if (tid < DK) {
         const float an = fmaf(g, at, coef * kt);
         sv.a[(int64_t)h * DK + tid] = an;
-        Elem<TF>::store(Uo + tid, kt);
+        Elem<TF>::store(Uo + tid, unew0);
         bad |= !finite(an);
       }
       if (tid < DV) {
         const float eps = fmaf(-omega, vbt, vt);
-        const float wn = Elem<TF>::round(beta * fmaf(-g, wx[0], eps));
+        const float wn = store_value<TF>(beta * fmaf(-g, wx[0], eps), sv.rounding, rb.y);
         Elem<TF>::store(Wo + tid, wn);
         const float o = fmaf(vbt, aq, fmaf(g, wx[NX - 1], Sg[3] * wn));
         p.o[(int64_t)h * DV + tid] = o;
@@ -391,8 +395,8 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
       }
       if (tid < DV) {
         const float eps = fmaf(-omega, vbt, vt);
-        const float w1 = Elem<TF>::round(-beta * wx[0]);
-        const float w2 = Elem<TF>::round(beta * eps);
+        const float w1 = store_value<TF>(-beta * wx[0], sv.rounding, rb.y);
+        const float w2 = store_value<TF>(beta * eps, sv.rounding, rb.w);
         Elem<TF>::store(Wo + tid, w1);
         Elem<TF>::store(Wo + DV + tid, w2);
         const float o = fmaf(vbt, aq, wx[NX - 1] + w1 * Sg[6] + w2 * Sg[7]);
@@ -409,7 +413,7 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
         bad |= !finite(an);
       }
       if (tid < DV) {
-        const float wn = Elem<TF>::round(fmaf(-omega, vbt, vt));
+        const float wn = store_value<TF>(fmaf(-omega, vbt, vt), sv.rounding, rb.y);
         Elem<TF>::store(Wo + tid, wn);
         const float o = fmaf(vbt, aC, fmaf(g, wx[0], Sg[2] * wn));
         p.o[(int64_t)h * DV + tid] = o;
@@ -428,11 +432,11 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
 // several heads' loads in flight.  (The same kernel can run persistently over a
 // ring of NS > 1 stages; with two 64-column stages only two CTAs fit per SM and
 // the serving-scale decode ran at 0.32 of the copy bandwidth against 0.55 here.)
-template <int VAR, int DV, int MAXC>
+template <typename TF, int VAR, int DV, int MAXC>
 static cudaError_t launch_mma_t(const DecodeArgs &a, cudaStream_t s) {
   constexpr int NS = 1;
   using L = MmaSmem<VAR, DV, MAXC, NS>;
-  auto kern = decode_mma_kernel<VAR, DV, MAXC, NS>;
+  auto kern = decode_mma_kernel<TF, VAR, DV, MAXC, NS>;
   // attributes belong to (kernel, device): set them the first time this kernel
   // runs on each device of the process
   static std::atomic<uint64_t> ready{0};
@@ -451,26 +455,32 @@ static cudaError_t launch_mma_t(const DecodeArgs &a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int VAR, int DV>
+template <typename TF, int VAR, int DV>
 static cudaError_t launch_mma_c(const DecodeArgs &a, int cols_max, cudaStream_t s) {
-  if (cols_max <= 16) return launch_mma_t<VAR, DV, 16>(a, s);
-  if (cols_max <= 32) return launch_mma_t<VAR, DV, 32>(a, s);
-  if (cols_max <= 48) return launch_mma_t<VAR, DV, 48>(a, s);
-  return launch_mma_t<VAR, DV, 64>(a, s);
+  if (cols_max <= 16) return launch_mma_t<TF, VAR, DV, 16>(a, s);
+  if (cols_max <= 32) return launch_mma_t<TF, VAR, DV, 32>(a, s);
+  if (cols_max <= 48) return launch_mma_t<TF, VAR, DV, 48>(a, s);
+  return launch_mma_t<TF, VAR, DV, 64>(a, s);
 }
 
-template <int VAR>
+template <typename TF, int VAR>
 static cudaError_t launch_mma_d(const DecodeArgs &a, int cols_max, cudaStream_t s) {
-  if (a.sv.d_v == 64) return launch_mma_c<VAR, 64>(a, cols_max, s);
-  return launch_mma_c<VAR, 128>(a, cols_max, s);
+  if (a.sv.d_v == 64) return launch_mma_c<TF, VAR, 64>(a, cols_max, s);
+  return launch_mma_c<TF, VAR, 128>(a, cols_max, s);
 }
 
-cudaError_t launch_decode_mma(const DecodeArgs &a, int cols_max, cudaStream_t s) {
+template <typename TF>
+static cudaError_t launch_mma_v(const DecodeArgs &a, int cols_max, cudaStream_t s) {
   switch (a.sv.variant) {
-    case SEED_GDN: return launch_mma_d<SEED_GDN>(a, cols_max, s);
-    case SEED_KDA: return launch_mma_d<SEED_KDA>(a, cols_max, s);
-    default: return launch_mma_d<SEED_MAMBA2>(a, cols_max, s);
+    case SEED_GDN: return launch_mma_d<TF, SEED_GDN>(a, cols_max, s);
+    case SEED_KDA: return launch_mma_d<TF, SEED_KDA>(a, cols_max, s);
+    default: return launch_mma_d<TF, SEED_MAMBA2>(a, cols_max, s);
   }
+}
+
+cudaError_t launch_decode_mma(const DecodeArgs &a, int factor_dtype, int cols_max, cudaStream_t s) {
+  if (factor_dtype == SEED_F16) return launch_mma_v<__half>(a, cols_max, s);
+  return launch_mma_v<__nv_bfloat16>(a, cols_max, s);
 }
 
 }  // namespace seedk

@@ -200,6 +200,8 @@ cudaError_t launch_materialize(const StateView &sv, int factor_dtype, float *S_o
   if (factor_dtype == SEED_BF16)
     return kda ? launch_mat_t<__nv_bfloat16, true>(sv, S_out, m_max, s)
                : launch_mat_t<__nv_bfloat16, false>(sv, S_out, m_max, s);
+  if (factor_dtype == SEED_F16)
+    return kda ? launch_mat_t<__half, true>(sv, S_out, m_max, s) : launch_mat_t<__half, false>(sv, S_out, m_max, s);
   return kda ? launch_mat_t<float, true>(sv, S_out, m_max, s)
              : launch_mat_t<float, false>(sv, S_out, m_max, s);
 }

@@ -179,12 +179,13 @@ __global__ void __launch_bounds__(256) compress_dense_kernel(const CompressArgs 
     const float *f = F + col * cs;
     float acc = 0.f;
     for (int s2 = 0; s2 < m; ++s2) acc = fmaf(Cs[piv[s2] * pc + i], f[s2], acc);
-    Elem<TF>::store(Uh + (int64_t)k * DK + i, acc * inv[col]);
+    Elem<TF>::store(Uh + (int64_t)k * DK + i, stored_elem<TF>(sv, acc * inv[col], c0 + k, i, kSrRebuildU));
   }
   for (int idx = tid; idx < rk * DV; idx += NT) {
     const int k = idx / DV, s2 = idx % DV;
     const int col = order[k];
-    Elem<TF>::store(Wh + (int64_t)k * DV + piv[s2], F[col * cs + s2] * inv[col]);
+    Elem<TF>::store(Wh + (int64_t)k * DV + piv[s2],
+                    stored_elem<TF>(sv, F[col * cs + s2] * inv[col], c0 + k, piv[s2], kSrRebuildW));
   }
   if (VAR == SEED_KDA) {
     for (int i = tid; i < DK; i += NT) sv.scale[(int64_t)h * DK + i] = 1.f;
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(128) recompress_kernel(const CompressArgs p) {
     for (int k = 0; k < rk; ++k) {
       float acc = 0.f;
       for (int l = 0; l < m; ++l) acc = fmaf(A[l * lda + tid], Z[k * m + l], acc);
-      Elem<TF>::store(Uh + (int64_t)k * DK + tid, acc);
+      Elem<TF>::store(Uh + (int64_t)k * DK + tid, stored_elem<TF>(sv, acc, c0 + k, tid, kSrRebuildU));
     }
   }
   if (tid < DV) {
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(128) recompress_kernel(const CompressArgs p) {
       const float ik = inv[col];
       float acc = 0.f;
       for (int l = 0; l < m; ++l) acc = fmaf(B[l * ldb + tid], f[pinv[l]] * ik, acc);
-      Elem<TF>::store(Wh + (int64_t)k * DV + tid, acc);
+      Elem<TF>::store(Wh + (int64_t)k * DV + tid, stored_elem<TF>(sv, acc, c0 + k, tid, kSrRebuildW));
     }
   }
   if (VAR == SEED_KDA) {
@@ -393,6 +394,7 @@ cudaError_t launch_recompress(const StateView &sv, int factor_dtype, float *trun
                               int32_t *sweeps, int m_max, cudaStream_t s) {
   CompressArgs a{sv, trunc_err, sweeps, nullptr, m_max, 0};
   if (factor_dtype == SEED_BF16) return launch_compress_v<__nv_bfloat16, false>(a, s);
+  if (factor_dtype == SEED_F16) return launch_compress_v<__half, false>(a, s);
   return launch_compress_v<float, false>(a, s);
 }
 
@@ -400,6 +402,7 @@ cudaError_t launch_compress_dense(const StateView &sv, int factor_dtype, const f
                                   float *trunc_err, cudaStream_t s) {
   CompressArgs a{sv, trunc_err, nullptr, S, sv.d_v, 0};
   if (factor_dtype == SEED_BF16) return launch_compress_v<__nv_bfloat16, true>(a, s);
+  if (factor_dtype == SEED_F16) return launch_compress_v<__half, true>(a, s);
   return launch_compress_v<float, true>(a, s);
 }
 

@@ -1,0 +1,694 @@
+// Recompression of 16-bit factors through a Cholesky of the value-side Gram
+// matrix, in three phases over a caller-provided device workspace.
+//
+// What is computed is the recompression of "Shallow Encoding Emits Deep
+// Memories" (thelatestinai.com list view, Table 1: the decode compresses back to
+// rank R every W steps): the best rank-r approximation of U_eff W^T.  The route
+// differs from the QR-of-both-factors route of recompress_split.cu:
+//
+//   G_w = W^T W = R_b^T R_b    (tensor cores; Cholesky, so Q_b = W R_b^{-1} has
+//                               orthonormal columns and U_eff W^T = B Q_b^T)
+//   B   = U_eff R_b^T          (tensor cores, R_b in three bf16 terms)
+//   M   = B^T B = Y Sigma^2 Y^T (fp32; pivoted Cholesky + one-sided Jacobi, evd_warp.cuh)
+//   U'  = U_eff R_b^T Y_r = B Y_r,   W' = W R_b^{-1} Y_r = Q_b Y_r  (tensor cores)
+//
+// With Q_b orthonormal the singular values of U_eff W^T are those of B, Y holds
+// B's right singular vectors, and B Y_r Y_r^T Q_b^T is the best rank-r
+// approximation, written U' W'^T with W' orthonormal and U' = X_r Sigma_r, the
+// same layout as the QR route.  Neither factor is QR-factorized.
+//
+// Accuracy.  G_w is formed from exact products of the stored 16-bit values with
+// fp32 accumulation; B carries an error of order eps |U_eff| |W| (as the QR
+// route's core does), M = B^T B one of order eps sigma_1 (sigma_1 + |U_eff| |W|),
+// so the kept directions (the r largest) are resolved to about that over
+// sigma_r^2 - sigma_{r+1}^2.  Through G_w, a column of W is resolved down to its
+// part outside the span of the earlier columns at about sqrt(kCholFloor) = 1e-3
+// of its norm: finer than the 2^-9 rounding that a stored 16-bit column already
+// carries, so nothing the storage keeps is lost.  Below that, the pivot's row of
+// R_b is dropped and the column is carried by its projections.  32-bit factors
+// keep the QR route.
+//
+//   gram_phase     one CTA per head: both factors into shared memory (cp.async),
+//                  G_w on mma.sync, Cholesky by one warp, B = U diag(c) R_b^T on
+//                  mma.sync (KDA: rows times D), M = B^T B in fp32 4 x 4 blocks;
+//                  M and R_b to the workspace
+//   evd_phase      one lane group per head: eigenvectors of M (evd_warp.cuh),
+//                  truncation error, the kept Y to the workspace
+//   gram_rebuild   one CTA per (head, factor): Z = diag(c) R_b^T Y_r (U) or
+//                  R_b^{-1} Y_r (W, back substitution), F' = F Z on mma.sync
+//                  with Z split into three bf16 terms (24 significant bits),
+//                  KDA's row scale applied to U', lazy scales reset
+//
+// Workspace per head (fp32): M [m][m], R_b [m][m] (upper, row-major), Y [r][m4]
+// (m4 = m rounded up to 4), each region on 16 bytes, the whole on 256 bytes.
+#include "evd_warp.cuh"
+
+#include <type_traits>
+
+namespace seedk {
+
+// Cholesky pivot floor, relative to the column's squared norm (1e-3 in norm, finer
+// than the 2^-9 rounding of a stored 16-bit column).
+constexpr float kCholFloor = 1e-6f;
+constexpr int kGramThreads = 128;
+
+struct GramLayout {
+  int64_t mq, rb, y, per_head;  // offsets and stride in floats
+  int m4;
+  __host__ __device__ GramLayout(int m, int r) {
+    m4 = (m + 3) & ~3;
+    const int64_t mm4 = ((int64_t)m * m + 3) & ~(int64_t)3;
+    mq = 0;
+    rb = mq + mm4;
+    y = rb + mm4;
+    per_head = (y + (int64_t)r * m4 + 63) & ~(int64_t)63;
+    if (per_head == 0) per_head = 64;
+  }
+};
+
+int64_t gram_floats_per_head(int m_max, int r_max) { return GramLayout(m_max, r_max).per_head; }
+
+struct GramArgs {
+  StateView sv;
+  float *ws;
+  int head0, n_group;
+  int m_max, m_lo;  // this launch serves heads with m_lo < m <= m_max
+  int layout_m, r_max;
+  float *trunc_err;
+  int32_t *sweeps;
+};
+
+__device__ inline bool gram_head(const GramArgs &p, int h, int &r, int &m) {
+  r = p.sv.rank_of(h);
+  m = r + p.sv.growth * p.sv.steps;
+  return r >= 0 && r <= p.r_max && m <= p.layout_m;
+}
+__device__ inline bool gram_in_class(const GramArgs &p, int m) { return m > p.m_lo && m <= p.m_max; }
+
+// ---- tensor-core helpers (mma.sync m16n8k16, bf16/fp16 in, fp32 accumulate) --------------
+__device__ static inline void g_cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ static inline void g_cp_commit_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+__device__ static inline void g_ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ static inline void g_ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+template <typename TF>
+__device__ static inline void g_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  Mma16<TF>::mma(d, a[0], a[1], a[2], a[3], b0, b1);
+}
+// (x, y) as three packed 16-bit terms t0 + t1 + t2 (24 significant bits while the
+// terms stay in the type's normal range: fp16 callers scale Z by a power of two)
+template <typename TF>
+__device__ static inline void g_split3(float x, float y, uint32_t (&t)[3]) {
+  t[0] = Mma16<TF>::pack(x, y);
+  float2 h = Mma16<TF>::unpack(t[0]);
+  x -= h.x; y -= h.y;
+  t[1] = Mma16<TF>::pack(x, y);
+  h = Mma16<TF>::unpack(t[1]);
+  t[2] = Mma16<TF>::pack(x - h.x, y - h.y);
+}
+
+// fp16 operands of F Z: each row n of Z^T (a column of Z) scaled by a power of two so
+// that its largest magnitude lies in [2^10, 2^11), which keeps the three terms of the
+// split inside fp16's normal range; the output column is scaled back exactly.  bf16
+// shares fp32's exponent range and needs no scaling (factor 1).
+template <typename TF>
+__device__ inline void scale_z_rows(float *Zt, int zp, int rows, int cols, float *unscale) {
+  for (int n = threadIdx.x; n < rows; n += blockDim.x) {
+    float mx = 0.f;
+    for (int j = 0; j < cols; ++j) mx = fmaxf(mx, fabsf(Zt[n * zp + j]));
+    int e = 0;
+    if (std::is_same<TF, __half>::value && mx > 0.f) frexpf(mx, &e);  // mx in [2^(e-1), 2^e)
+    const int sh = std::is_same<TF, __half>::value && mx > 0.f ? 11 - e : 0;
+    const float f = ldexpf(1.f, sh);
+    if (sh)
+      for (int j = 0; j < cols; ++j) Zt[n * zp + j] *= f;
+    unscale[n] = ldexpf(1.f, -sh);
+  }
+}
+
+// Shared layout of gram_phase (bytes): both factor tiles (column j of the factor
+// in row j, rows padded by 16 bytes so that ldmatrix hits distinct banks; the W
+// tile's space is reused for Z once G_w is formed), G_w / R_b (row i at i * GP
+// floats; GP odd: row-per-thread access is conflict-free), B = U_eff R_b^T
+// (row i at i * BP floats), the scales, the original diagonal of G_w.
+template <int DV, int MR>
+struct GramSmem {
+  static constexpr int USTR = kDK * 2 + 16, WSTR = DV * 2 + 16;
+  static constexpr int GP = MR + 1;
+  static constexpr int ZP = MR + 8;  // Z row pitch (floats): row n = column n of Z
+  static constexpr int BP = MR + 4;
+  static constexpr int WZ_BYTES = MR * WSTR > MR * ZP * 4 ? MR * WSTR : MR * ZP * 4;
+  static constexpr int U_OFF = 0;
+  static constexpr int W_OFF = U_OFF + MR * USTR;  // W tile, then Z
+  static constexpr int G_OFF = W_OFF + WZ_BYTES;
+  static constexpr int B_OFF = G_OFF + ((MR * GP * 4 + 15) & ~15);
+  static constexpr int SC_OFF = B_OFF + kDK * BP * 4;
+  static constexpr int DG_OFF = SC_OFF + (MR > kDK ? MR : kDK) * 4;
+  static constexpr int RR_OFF = DG_OFF + MR * 4;  // row j of R_b, two buffers
+  static constexpr int ZS_OFF = RR_OFF + 2 * MR * 4;  // per-column unscale of Z (fp16)
+  static constexpr int BYTES = ZS_OFF + MR * 4;
+};
+
+// G[i0..i0+15][j0..j0+7] += F^T F over `depth` rows of the tiles, F column j in
+// smem row j (stride STR bytes): exact products of the stored 16-bit values,
+// fp32 accumulation.
+template <typename TF, int STR>
+__device__ inline void gram_tile(uint32_t base, int i0, int j0, int depth, float (&d)[4]) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t a_row = base + (uint32_t)((i0 + (lane & 7) + ((lane >> 3) & 1) * 8) * STR + (lane >> 4) * 16);
+  const uint32_t b_row = base + (uint32_t)((j0 + (lane & 7)) * STR + (lane >> 3) * 16);
+  for (int k0 = 0; k0 < depth; k0 += 32) {
+    uint32_t b[4], a0[4], a1[4];
+    g_ldsm_x4(b_row + k0 * 2, b);
+    g_ldsm_x4(a_row + k0 * 2, a0);
+    g_ldsm_x4(a_row + (k0 + 16) * 2, a1);
+    g_mma<TF>(d, a0, b[0], b[1]);
+    g_mma<TF>(d, a1, b[2], b[3]);
+  }
+}
+
+// D[i0..i0+15][n0..n0+7] = sum_j F[i][j] Z[j][n] for j < depth16, F column j in smem
+// row j of the tile at `tile` (stride STR bytes), Z row n at Zt + n * ZP (fp32, split
+// into three bf16 terms: 24 significant bits, products exact, fp32 accumulation).
+template <typename TF, int STR, int ZP>
+__device__ inline void tile_times_z(uint32_t tile, const float *Zt, int i0, int n0, int depth16,
+                                    float (&d)[4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int rsel = (lane & 7) + ((lane >> 4) << 3);
+  const int csel = i0 + ((lane >> 3) & 1) * 8;
+  for (int j0 = 0; j0 < depth16; j0 += 16) {
+    uint32_t a[4];
+    g_ldsm_x4_t(tile + (uint32_t)((j0 + rsel) * STR + csel * 2), a);
+    const float2 z0 = *reinterpret_cast<const float2 *>(Zt + (n0 + g) * ZP + j0 + 2 * t);
+    const float2 z1 = *reinterpret_cast<const float2 *>(Zt + (n0 + g) * ZP + j0 + 8 + 2 * t);
+    uint32_t b0[3], b1[3];
+    g_split3<TF>(z0.x, z0.y, b0);
+    g_split3<TF>(z1.x, z1.y, b1);
+#pragma unroll
+    for (int q = 0; q < 3; ++q) g_mma<TF>(d, a, b0[q], b1[q]);
+  }
+}
+
+// ---- phase 1: G_w, its Cholesky, B = U_eff R_b^T, M = B^T B ---------------------------------
+template <typename TF, int VAR, int DV, int MR>
+__global__ void __launch_bounds__(kGramThreads) gram_phase(const GramArgs p) {
+  constexpr int DK = kDK;
+  using L = GramSmem<DV, MR>;
+  constexpr int GP = L::GP, ZP = L::ZP, BP = L::BP;
+  constexpr bool KDA = VAR == SEED_KDA;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int h = p.head0 + blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const StateView &sv = p.sv;
+  int r, m;
+  if (!gram_head(p, h, r, m) || !gram_in_class(p, m)) return;  // bad ranks: reported by evd_phase
+  const int m16 = (m + 15) & ~15;
+  const int64_t c0 = sv.col0(h);
+  float *Gw = reinterpret_cast<float *>(smem + L::G_OFF);
+  float *Zt = reinterpret_cast<float *>(smem + L::W_OFF);
+  float *B = reinterpret_cast<float *>(smem + L::B_OFF);
+  float *sc = reinterpret_cast<float *>(smem + L::SC_OFF);
+  float *dg = reinterpret_cast<float *>(smem + L::DG_OFF);
+  float *rrow = reinterpret_cast<float *>(smem + L::RR_OFF);
+  float *zsc = reinterpret_cast<float *>(smem + L::ZS_OFF);
+
+  // ---- factors into shared memory, padding columns zero ---------------------------------
+  {
+    const TF *Ug = reinterpret_cast<const TF *>(sv.U) + c0 * DK;
+    const TF *Wg = reinterpret_cast<const TF *>(sv.W) + c0 * DV;
+    constexpr int UCH = DK / 8, WCH = DV / 8;  // 16-byte chunks per column
+    for (int idx = tid; idx < m16 * UCH; idx += kGramThreads) {
+      const int j = idx / UCH, c = idx % UCH;
+      unsigned char *dst = smem + L::U_OFF + j * L::USTR + c * 16;
+      if (j < m) g_cp_async16(dst, Ug + (int64_t)j * DK + c * 8);
+      else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    for (int idx = tid; idx < m16 * WCH; idx += kGramThreads) {
+      const int j = idx / WCH, c = idx % WCH;
+      unsigned char *dst = smem + L::W_OFF + j * L::WSTR + c * 16;
+      if (j < m) g_cp_async16(dst, Wg + (int64_t)j * DV + c * 8);
+      else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    if (KDA) {
+      for (int i = tid; i < DK; i += kGramThreads) sc[i] = sv.scale[(int64_t)h * DK + i];
+    } else {
+      for (int j = tid; j < m16; j += kGramThreads) sc[j] = j < m ? sv.scale[c0 + j] : 0.f;
+    }
+    g_cp_commit_wait_all();
+  }
+  __syncthreads();
+
+  // ---- G_w = W^T W on the tensor cores ----------------------------------------------------------
+  {
+    const int ncol = m16 / 8, per = (m16 / 16) * ncol;
+    const uint32_t wb = smem_u32(smem + L::W_OFF);
+    for (int task = warp; task < per; task += kGramThreads / 32) {
+      const int i0 = (task / ncol) * 16, j0 = (task % ncol) * 8;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      gram_tile<TF, L::WSTR>(wb, i0, j0, DV, d);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) Gw[(i0 + g + (e >> 1) * 8) * GP + j0 + 2 * t + (e & 1)] = d[e];
+    }
+  }
+  __syncthreads();
+
+  // ---- Cholesky G_w = R_b^T R_b (upper, in place) by warps 0-1 (warp 0 up to 32 columns) -----------
+  // Thread l owns column l of the upper triangle (entries at i * GP + l: threads of
+  // one row touch consecutive words).  Step j: every owner of a column l >= j reads
+  // the pivot, forms R_b[j][l] and publishes it in rrow (double-buffered by step
+  // parity); after the barrier each owner of l > j updates its entries i in (j, l].
+  // A pivot below kCholFloor of its column's squared norm means the column lies in
+  // the span of the earlier ones to within the resolution of the Gram matrix: its
+  // row of R_b is dropped (zero), the column is represented by its projections.
+  constexpr int NCH = MR <= 32 ? 32 : 64;  // column owners: one warp or two
+  if (tid < NCH) {
+    const int l = tid;
+    const bool own = l < m;
+    if (own) dg[l] = Gw[l * GP + l];
+    for (int j = 0; j < m; ++j) {
+      team_sync(2, NCH);  // step j-1's updates (and the diagonal) are visible
+      float rl = 0.f;
+      if (own && l >= j) {
+        const float d = Gw[j * GP + j], g0 = dg[j];
+        const float rjj = d > kCholFloor * g0 ? sqrtf(d) : 0.f;
+        const float inv = rjj > 0.f ? 1.f / rjj : 0.f;
+        rl = l == j ? rjj : Gw[j * GP + l] * inv;
+        rrow[(j & 1) * MR + l] = rl;
+      }
+      team_sync(2, NCH);  // row j of R_b is published
+      if (own && l > j) {
+        Gw[j * GP + l] = rl;
+        const float *rr = rrow + (j & 1) * MR;
+        int i = j + 1;
+        for (; i + 3 <= l; i += 4) {
+          const float r0 = rr[i], r1 = rr[i + 1], r2 = rr[i + 2], r3 = rr[i + 3];
+          const float g0 = Gw[i * GP + l], g1 = Gw[(i + 1) * GP + l], g2 = Gw[(i + 2) * GP + l],
+                      g3 = Gw[(i + 3) * GP + l];
+          Gw[i * GP + l] = fmaf(-r0, rl, g0);
+          Gw[(i + 1) * GP + l] = fmaf(-r1, rl, g1);
+          Gw[(i + 2) * GP + l] = fmaf(-r2, rl, g2);
+          Gw[(i + 3) * GP + l] = fmaf(-r3, rl, g3);
+        }
+        for (; i <= l; ++i) Gw[i * GP + l] = fmaf(-rr[i], rl, Gw[i * GP + l]);
+      } else if (own && l == j) {
+        Gw[j * GP + j] = rl;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- Z = diag(c) R_b^T (Z[l][j] = c_l R_b[j][l]), stored by rows of Z^T --------------------------
+  // (the W tile is no longer needed); KDA's row scale D is applied to B instead
+  for (int idx = tid; idx < m16 * ZP; idx += kGramThreads) {
+    const int j = idx / ZP, l = idx % ZP;
+    float z = 0.f;
+    if (j < m && l < m && l >= j) z = KDA ? Gw[j * GP + l] : Gw[j * GP + l] * sc[l];
+    Zt[idx] = z;
+  }
+  __syncthreads();
+  scale_z_rows<TF>(Zt, ZP, m16, m16, zsc);
+  __syncthreads();
+
+  // ---- B = U Z (U_eff = U diag(c)), or diag(D) (U R_b^T) for KDA, on the tensor cores -----------
+  {
+    const int ntile = m16 / 8, per = (DK / 16) * ntile;
+    const uint32_t ub = smem_u32(smem + L::U_OFF);
+    for (int task = warp; task < per; task += kGramThreads / 32) {
+      const int i0 = (task / ntile) * 16, n0 = (task % ntile) * 8;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      tile_times_z<TF, L::USTR, ZP>(ub, Zt, i0, n0, m16, d);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = i0 + g + (e >> 1) * 8, n = n0 + 2 * t + (e & 1);
+        const float v = d[e] * zsc[n];
+        B[i * BP + n] = KDA ? v * sc[i] : v;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- M = B^T B in fp32 (4 x 4 blocks of the upper triangle), M and R_b to the workspace -----
+  const GramLayout W(p.layout_m, p.r_max);
+  float *ws = p.ws + (int64_t)blockIdx.x * W.per_head;
+  {
+    const int nb = (m + 3) / 4, nblk = nb * (nb + 1) / 2;
+    for (int blk = tid; blk < nblk; blk += kGramThreads) {
+      int jb = 0, rem = blk;  // blk -> (jb <= lb)
+      while (rem >= nb - jb) { rem -= nb - jb; ++jb; }
+      const int lb = jb + rem;
+      float acc[4][4] = {};
+      for (int i = 0; i < DK; ++i) {
+        const float4 x = *reinterpret_cast<const float4 *>(B + i * BP + 4 * jb);
+        const float4 y = *reinterpret_cast<const float4 *>(B + i * BP + 4 * lb);
+        const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(xs[a], ys[c], acc[a][c]);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int j = 4 * jb + a, l = 4 * lb + c;
+          if (j < m && l < m) {
+            ws[W.mq + j * m + l] = acc[a][c];
+            ws[W.mq + l * m + j] = acc[a][c];
+          }
+        }
+    }
+  }
+  for (int idx = tid; idx < m * m; idx += kGramThreads) {
+    const int i = idx / m, l = idx % m;
+    ws[W.rb + idx] = l >= i ? Gw[i * GP + l] : 0.f;
+  }
+}
+
+// ---- phase 2: eigenvectors of M, one lane group per head -------------------------------------
+template <int MR>
+constexpr int evd_group() { return MR <= 32 ? 16 : 32; }
+template <int MR>
+constexpr int evd_heads_per_cta() { return kSvdWarps * (32 / evd_group<MR>()); }
+
+// Resident CTAs to plan registers for: the register Jacobi (MR <= 48) holds four
+// MR-float arrays per lane, so its larger cores get fewer, fatter lanes.
+template <int MR>
+constexpr int evd_min_blocks() { return MR <= 16 ? 8 : MR <= 32 ? 6 : MR <= 48 ? 4 : 6; }
+
+template <int MR>
+__global__ void __launch_bounds__(32 * kSvdWarps, evd_min_blocks<MR>()) evd_phase(const GramArgs p) {
+  constexpr int HW = evd_group<MR>();
+  using SW = SvdWarpSmem<MR>;
+  extern __shared__ __align__(16) float smem_f[];
+  const int grp = threadIdx.x / HW, lane = threadIdx.x & (HW - 1);
+  const unsigned gmask = HW == 32 ? 0xffffffffu : 0xffffu << (threadIdx.x & 16);
+  const int b = blockIdx.x * evd_heads_per_cta<MR>() + grp;
+  if (b >= p.n_group) return;
+  const int h = p.head0 + b;
+  const StateView &sv = p.sv;
+  int r, m;
+  if (!gram_head(p, h, r, m)) {  // rank table disagrees with r_max: touch nothing
+    if (lane == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
+    return;
+  }
+  if (!gram_in_class(p, m)) return;
+  float *sw = smem_f + grp * SW::FLOATS;
+  float *T = sw + SW::T_OFF;
+  const GramLayout W(p.layout_m, p.r_max);
+  float *ws = p.ws + (int64_t)b * W.per_head;
+  const float *Mw = ws + W.mq;
+
+  // M into the square (column c at T[c * TP], zero beyond m), scaled by a power of
+  // four to a largest diagonal below one (its square root, sigma, by a power of two)
+  float dmax = 0.f;
+  for (int idx = lane; idx < MR * MR; idx += HW) {
+    const int c = idx / MR, x = idx % MR;
+    const float v = (c < m && x < m) ? Mw[c * m + x] : 0.f;
+    T[c * SW::TP + x] = v;
+    if (c == x) dmax = fmaxf(dmax, v);
+  }
+#pragma unroll
+  for (int o = HW / 2; o > 0; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(gmask, dmax, o));
+  int e = 0;
+  if (dmax > 0.f) frexpf(dmax, &e);
+  const int e2 = e >= 0 ? (e + 1) / 2 : -((-e) / 2);  // ceil(e / 2)
+  const float mscale = ldexpf(1.f, -2 * e2), sunscale = ldexpf(1.f, e2);
+  __syncwarp(gmask);
+  for (int idx = lane; idx < m * MR; idx += HW) T[(idx / MR) * SW::TP + idx % MR] *= mscale;
+  __syncwarp(gmask);
+  const float tol = 1e-4f;  // 16-bit factors: their own rounding is 2^-9
+  const int sweeps = evd_warp_core<MR, HW>(m, tol, sqrtf(tol), sw);
+  const float *sig2 = sw + SW::S_OFF, *inv = sw + SW::I_OFF;
+  const int *order = reinterpret_cast<const int *>(sw + SW::O_OFF);
+  if (lane == 0) {
+    float err = 0.f;
+    for (int k = r; k < m; ++k) err += sig2[order[k]];
+    if (p.trunc_err) p.trunc_err[h] = sqrtf(err) * sunscale;
+    if (p.sweeps) p.sweeps[h] = sweeps;
+    if (sv.status) sv.status[h] = sweeps < 0 ? SEED_ERR_NOT_CONVERGED : SEED_OK;
+  }
+  // kept eigenvectors y_k[x] = (Rt^T J)[x][order[k]] / sigma_k, rows m..m4-1 zero
+  const int rk = r < m ? r : m;
+  float *Y = ws + W.y;
+  for (int k = 0; k < rk; ++k) {
+    const int col = order[k];
+    const float ik = inv[col];
+    const float *f = T + col * SW::TP;
+    for (int x = lane; x < W.m4; x += HW) Y[k * W.m4 + x] = x < m ? f[x] * ik : 0.f;
+  }
+}
+
+// ---- phase 3: F' = F Z ---------------------------------------------------------------------------
+// blockIdx.y = 0: U' = U_eff R_b^T Y_r (Z = diag(c) R_b^T Y_r on the stored U; KDA: rows
+// of U Z times D); blockIdx.y = 1: W' = W R_b^{-1} Y_r.
+template <int DV, int MR>
+struct RebuildSmem {
+  static constexpr int STR = kDK * 2 + 16;      // tile row stride (bytes), the larger factor
+  static constexpr int RP = MR + 4;             // R_b row pitch (floats; 16-byte rows)
+  static constexpr int YP = MR + 4;             // Y^T row pitch: row j holds y_n[j] for every n
+  static constexpr int ZP = MR + 2;             // Z row pitch (floats): row n = column n of Z;
+                                                // 2 mod 4 keeps both access patterns at 2-way
+  static constexpr int T_OFF = 0;               // factor tile, then the output tile
+  static constexpr int O_OFF = T_OFF + MR * STR;
+  static constexpr int R_OFF = O_OFF + MR * STR;
+  static constexpr int Y_OFF = R_OFF + MR * RP * 4;
+  static constexpr int Z_OFF = Y_OFF + MR * YP * 4;
+  static constexpr int S_OFF = Z_OFF + MR * ZP * 4;  // scales c [MR] or D [DK]
+  static constexpr int ZS_OFF = S_OFF + (MR > kDK ? MR : kDK) * 4;  // per-column unscale of Z
+  static constexpr int BYTES = ZS_OFF + MR * 4;
+};
+
+template <typename TF, int VAR, int DV, int MR>
+__global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
+  constexpr int DK = kDK;
+  using L = RebuildSmem<DV, MR>;
+  constexpr int RP = L::RP, YP = L::YP, ZP = L::ZP;
+  constexpr bool KDA = VAR == SEED_KDA;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int h = p.head0 + blockIdx.x;
+  const bool isU = blockIdx.y == 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const StateView &sv = p.sv;
+  int r, m;
+  if (!gram_head(p, h, r, m) || !gram_in_class(p, m)) return;
+  const int rk = r < m ? r : m;
+  if (rk == 0) {  // nothing kept: only the scales go back to one
+    if (isU) {
+      if (KDA) for (int i = tid; i < DK; i += kGramThreads) sv.scale[(int64_t)h * DK + i] = 1.f;
+    }
+    return;
+  }
+  const int rows = isU ? DK : DV;
+  const int m16 = (m + 15) & ~15, rk8 = (rk + 7) & ~7;
+  const int64_t c0 = sv.col0(h);
+  const GramLayout W(p.layout_m, p.r_max);
+  const float *ws = p.ws + (int64_t)blockIdx.x * W.per_head;
+  float *Rb = reinterpret_cast<float *>(smem + L::R_OFF);
+  float *Yt = reinterpret_cast<float *>(smem + L::Y_OFF);   // y_n[j] at j * YP + n
+  float *Z = reinterpret_cast<float *>(smem + L::Z_OFF);    // [rk8][ZP]: z_n[j] at n * ZP + j
+  float *sc = reinterpret_cast<float *>(smem + L::S_OFF);
+  TF *pool = reinterpret_cast<TF *>(isU ? sv.U : sv.W) + c0 * rows;
+
+  // ---- the factor tile (cp.async), R_b, Y, the scales --------------------------------------
+  {
+    const int CH = rows / 8;
+    for (int idx = tid; idx < m16 * CH; idx += kGramThreads) {
+      const int j = idx / CH, c = idx % CH;
+      unsigned char *dst = smem + L::T_OFF + j * L::STR + c * 16;
+      if (j < m) g_cp_async16(dst, pool + (int64_t)j * rows + c * 8);
+      else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  // R_b (upper, zero below the diagonal and beyond m), Y^T (zero beyond m and rk),
+  // the scales, Z zero
+  for (int idx = tid; idx < m16 * RP; idx += kGramThreads) {
+    const int i = idx / RP, l = idx % RP;
+    Rb[idx] = (i < m && l < m) ? ws[W.rb + i * m + l] : 0.f;
+  }
+  for (int idx = tid; idx < m16 * YP; idx += kGramThreads) {
+    const int j = idx / YP, n = idx % YP;
+    Yt[idx] = (j < m && n < rk) ? ws[W.y + n * W.m4 + j] : 0.f;
+  }
+  if (isU) {
+    if (KDA) for (int i = tid; i < DK; i += kGramThreads) sc[i] = sv.scale[(int64_t)h * DK + i];
+    else for (int j = tid; j < m; j += kGramThreads) sc[j] = sv.scale[c0 + j];
+  }
+  for (int idx = tid; idx < rk8 * ZP; idx += kGramThreads) Z[idx] = 0.f;
+  __syncthreads();
+
+  // ---- Z ------------------------------------------------------------------------------------
+  if (isU) {
+    // z_n[l] = c_l sum_{j <= l} y_n[j] R_b[j][l], 4 x 4 blocks of (n, l) a thread
+    const int nbn = (rk + 3) / 4, nbl = (m + 3) / 4;
+    for (int blk = tid; blk < nbn * nbl; blk += kGramThreads) {
+      const int nb = blk / nbl, lb = blk % nbl;
+      float acc[4][4] = {};
+      for (int j = 0; j < 4 * lb + 4 && j < m; ++j) {
+        const float4 y = *reinterpret_cast<const float4 *>(Yt + j * YP + 4 * nb);
+        const float4 rv = *reinterpret_cast<const float4 *>(Rb + j * RP + 4 * lb);
+        const float ys[4] = {y.x, y.y, y.z, y.w}, rs[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(ys[a], rs[c], acc[a][c]);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int n = 4 * nb + a, l = 4 * lb + c;
+          if (n < rk && l < m) Z[n * ZP + l] = KDA ? acc[a][c] : acc[a][c] * sc[l];
+        }
+    }
+  } else {
+    // R_b Z = Y by back substitution in row panels of 16 from the bottom: a thread per
+    // column n solves the panel's triangle, then all threads take the panel's
+    // contribution off the rows above.  A zero pivot (dropped row) gives a zero entry.
+    for (int idx = tid; idx < rk * m; idx += kGramThreads) {
+      const int n = idx / m, i = idx % m;
+      Z[n * ZP + i] = Yt[i * YP + n];
+    }
+    __syncthreads();
+    for (int b1 = m; b1 > 0; b1 -= 16) {
+      const int b0 = b1 > 16 ? b1 - 16 : 0;
+      for (int n = tid; n < rk; n += kGramThreads) {
+        float *z = Z + n * ZP;
+        for (int i = b1 - 1; i >= b0; --i) {
+          float s = z[i];
+          for (int l = i + 1; l < b1; ++l) s = fmaf(-Rb[i * RP + l], z[l], s);
+          const float piv = Rb[i * RP + i];
+          z[i] = piv != 0.f ? s / piv : 0.f;
+        }
+      }
+      __syncthreads();
+      for (int idx = tid; idx < rk * b0; idx += kGramThreads) {
+        const int n = idx / b0, i = idx % b0;
+        float s = Z[n * ZP + i];
+        for (int l = b0; l < b1; ++l) s = fmaf(-Rb[i * RP + l], Z[n * ZP + l], s);
+        Z[n * ZP + i] = s;
+      }
+      __syncthreads();
+    }
+  }
+  float *zsc = reinterpret_cast<float *>(smem + L::ZS_OFF);
+  __syncthreads();
+  scale_z_rows<TF>(Z, ZP, rk8, m16, zsc);
+  g_cp_commit_wait_all();
+  __syncthreads();
+
+  // ---- F' = F Z on the tensor cores (Z in three 16-bit terms) -----------------------------------
+  {
+    const int g = lane >> 2, t = lane & 3;
+    const int ntile = rk8 / 8, per = (rows / 16) * ntile;
+    const uint32_t tb = smem_u32(smem + L::T_OFF);
+    TF *out = reinterpret_cast<TF *>(smem + L::O_OFF);
+    for (int task = warp; task < per; task += kGramThreads / 32) {
+      const int i0 = (task / ntile) * 16, n0 = (task % ntile) * 8;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      tile_times_z<TF, L::STR, ZP>(tb, Z, i0, n0, m16, d);
+      // d[e]: row i (element of the column), output column n; stochastic rounding:
+      // one Philox block for the lane's four elements (counter: its even column, row)
+      uint4 rb = make_uint4(0u, 0u, 0u, 0u);
+      if (sv.rounding == kRoundStochastic)
+        rb = sr_bits(sv.sr_seed, c0 + n0 + 2 * t, (uint32_t)(i0 + g), isU ? kSrRebuildU : kSrRebuildW);
+      const uint32_t words[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = i0 + g + (e >> 1) * 8, n = n0 + 2 * t + (e & 1);
+        float v = d[e] * zsc[n];
+        if (isU && KDA) v *= sc[i];
+        out[n * (L::STR / 2) + i] = Mma16<TF>::cvt(store_value<TF>(v, sv.rounding, words[e]));
+      }
+    }
+  }
+  __syncthreads();
+  {
+    const int CH = rows / 8;
+    for (int idx = tid; idx < rk * CH; idx += kGramThreads) {
+      const int n = idx / CH, c = idx % CH;
+      *reinterpret_cast<uint4 *>(pool + (int64_t)n * rows + c * 8) =
+          *reinterpret_cast<const uint4 *>(smem + L::O_OFF + n * L::STR + c * 16);
+    }
+  }
+  if (isU) {  // every read of the scales happened before the last barrier
+    if (KDA) for (int i = tid; i < DK; i += kGramThreads) sv.scale[(int64_t)h * DK + i] = 1.f;
+    else for (int k = tid; k < rk; k += kGramThreads) sv.scale[c0 + k] = 1.f;
+  }
+}
+
+template <typename TF, int VAR, int DV, int MR>
+static cudaError_t launch_gram_t(GramArgs a, int n_heads, int64_t chunk, cudaStream_t s) {
+  using L1 = GramSmem<DV, MR>;
+  using L3 = RebuildSmem<DV, MR>;
+  const int evd_bytes = evd_heads_per_cta<MR>() * SvdWarpSmem<MR>::FLOATS * 4;
+  auto k1 = gram_phase<TF, VAR, DV, MR>;
+  auto k2 = evd_phase<MR>;
+  auto k3 = gram_rebuild<TF, VAR, DV, MR>;
+  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, L1::BYTES);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, evd_bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, L3::BYTES);
+  if (e != cudaSuccess) return e;
+  for (int64_t h0 = 0; h0 < n_heads; h0 += chunk) {
+    const int n = (int)(n_heads - h0 < chunk ? n_heads - h0 : chunk);
+    a.head0 = (int)h0;
+    a.n_group = n;
+    k1<<<n, kGramThreads, L1::BYTES, s>>>(a);
+    k2<<<(n + evd_heads_per_cta<MR>() - 1) / evd_heads_per_cta<MR>(), 32 * kSvdWarps, evd_bytes, s>>>(a);
+    k3<<<dim3(n, 2), kGramThreads, L3::BYTES, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <typename TF, int VAR, int DV>
+static cudaError_t launch_gram_m(const GramArgs &a, int n, int64_t chunk, cudaStream_t s) {
+  if (a.m_max <= 16) return launch_gram_t<TF, VAR, DV, 16>(a, n, chunk, s);
+  if (a.m_max <= 32) return launch_gram_t<TF, VAR, DV, 32>(a, n, chunk, s);
+  if (a.m_max <= 48) return launch_gram_t<TF, VAR, DV, 48>(a, n, chunk, s);
+  return launch_gram_t<TF, VAR, DV, 64>(a, n, chunk, s);
+}
+
+template <typename TF, int DV>
+static cudaError_t launch_gram_v(const GramArgs &a, int n, int64_t chunk, cudaStream_t s) {
+  // Only the scale layout differs between variants here.
+  if (a.sv.variant == SEED_KDA) return launch_gram_m<TF, SEED_KDA, DV>(a, n, chunk, s);
+  return launch_gram_m<TF, SEED_GDN, DV>(a, n, chunk, s);
+}
+
+cudaError_t launch_recompress_gram(const StateView &sv, int factor_dtype, float *trunc_err, int32_t *sweeps,
+                                   int m_max, int r_max, float *ws, int64_t chunk, cudaStream_t s) {
+  GramArgs a{sv, ws, 0, 0, m_max, -1, m_max, r_max, trunc_err, sweeps};
+  const int n = sv.n_heads;
+  auto one = [&](const GramArgs &x) {
+    if (factor_dtype == SEED_F16)
+      return sv.d_v == 64 ? launch_gram_v<__half, 64>(x, n, chunk, s) : launch_gram_v<__half, 128>(x, n, chunk, s);
+    return sv.d_v == 64 ? launch_gram_v<__nv_bfloat16, 64>(x, n, chunk, s)
+                        : launch_gram_v<__nv_bfloat16, 128>(x, n, chunk, s);
+  };
+  if (!sv.rank || m_max <= 16) return one(a);
+  // Ragged ranks: one launch per 16-column class, each sized for its class; heads of
+  // other classes leave at once.
+  for (int hi = 16; hi - 16 < m_max; hi += 16) {
+    GramArgs c = a;
+    c.m_max = hi < m_max ? hi : m_max;
+    c.m_lo = hi == 16 ? -1 : hi - 16;  // the first class also takes heads with no columns
+    const cudaError_t e = one(c);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace seedk

@@ -397,7 +397,8 @@ __global__ void __launch_bounds__(kSplitThreads) rebuild_phase(const SplitArgs p
   }
 }
 
-int64_t split_floats_per_head(int m_max, int r_max, int d_v) {
+int64_t split_floats_per_head(int factor_dtype, int m_max, int r_max, int d_v) {
+  if (factor_dtype != SEED_F32) return gram_floats_per_head(m_max, r_max);
   return SplitLayout(m_max, r_max, kDK, d_v).per_head;
 }
 
@@ -448,12 +449,12 @@ static cudaError_t launch_split_v(const SplitArgs &a, int n, int64_t chunk, cuda
 cudaError_t launch_recompress_split(const StateView &sv, int factor_dtype, float *trunc_err,
                                     int32_t *sweeps, int m_max, int r_max, float *ws,
                                     int64_t chunk, cudaStream_t s) {
+  // 16-bit factors take the Gram route (recompress_gram.cu)
+  if (factor_dtype != SEED_F32)
+    return launch_recompress_gram(sv, factor_dtype, trunc_err, sweeps, m_max, r_max, ws, chunk, s);
   SplitArgs a{sv, ws, 0, 0, m_max, -1, m_max, r_max, trunc_err, sweeps, 0};
   const int n = sv.n_heads;
   auto one = [&](const SplitArgs &x) {
-    if (factor_dtype == SEED_BF16)
-      return sv.d_v == 64 ? launch_split_v<__nv_bfloat16, 64>(x, n, chunk, s)
-                          : launch_split_v<__nv_bfloat16, 128>(x, n, chunk, s);
     return sv.d_v == 64 ? launch_split_v<float, 64>(x, n, chunk, s) : launch_split_v<float, 128>(x, n, chunk, s);
   };
   if (!sv.rank || m_max <= 16) return one(a);

@@ -47,6 +47,9 @@ struct SvdWarpSmem {
   static constexpr int FLOATS = P_OFF + MR;
 };
 
+template <int MR, int HW>
+__device__ int jacobi_warp(int m, float tol, float tol_stop, float *sw);
+
 // One lane group: pivoted QR of the scaled core held in the square T (column c at
 // T[c * TP], rows m..MR-1 zero), then Jacobi on R^T.  Leaves in T the columns
 // of R^T J by seat (T[seat * TP + s]), sig2/inv by seat, order, piv.  Returns
@@ -224,6 +227,26 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
     __syncwarp(full);
   }
 
+  return jacobi_warp<MR, HW>(m, tol, tol_stop, sw);
+}
+
+// One-sided Jacobi with one lane group per head on the seats of the warp's
+// square: seat i (i < n', n' = m rounded up to even) holds column i at
+// T[i * TP], zero for i >= m.  Leaves the columns of (seats) J in place, their
+// squared norms sig2 and reciprocal norms inv by seat, and the seats in order of
+// decreasing sigma.  Returns the sweeps run, or -1 at the sweep limit.
+template <int MR, int HW>
+__device__ int jacobi_warp(int m, float tol, float tol_stop, float *sw) {
+  using L = SvdWarpSmem<MR>;
+  constexpr int TP = L::TP;
+  const int lane = threadIdx.x & (HW - 1);
+  const unsigned full = HW == 32 ? 0xffffffffu : 0xffffu << (threadIdx.x & 16);  // my group
+  float *T = sw + L::T_OFF, *sig2 = sw + L::S_OFF, *inv = sw + L::I_OFF;
+  int *order = reinterpret_cast<int *>(sw + L::O_OFF);
+  const int nn = m + (m & 1), P = nn / 2;
+  const bool active = lane < P;
+  const int seatA = lane == 0 ? nn - 1 : lane, seatB = lane == 0 ? 0 : nn - 1 - lane;
+
   // ---- Jacobi: the columns of R^T stay where they are (column i at T[i * TP]);
   // each round lane i takes the pair that the round-robin puts on its two seats
   // (the column at seat s >= 1 moves on to s + 1, n'-1 to 1, seat 0 stays) and
@@ -372,6 +395,221 @@ __device__ int svd_warp_core(int m, float tol, float tol_stop, float *sw) {
       int rank = 0;
       const float sj = sig2[j];
       for (int i = 0; i < m; ++i) {
+        const float si = sig2[i];
+        rank += (si > sj) || (si == sj && i < j);
+      }
+      order[rank] = j;
+    }
+  }
+  __syncwarp(full);
+  return sweeps;
+}
+
+// ---------------------------------------------------------------------------------------
+// One-sided Jacobi with the columns in registers (cores of at most 48 columns).
+//
+// Same rotation rule, tolerance, stopping rule, scaled columns and carried norms as
+// jacobi_warp; only the pair order and where the columns live differ.  Lane i
+// (i < P = n'/2) holds two columns, A and B, in registers.  The order is the
+// odd-even transposition order on the n' positions with an exchange after every
+// pair (each pair of columns meets exactly once in n' rounds): even rounds pair
+// positions (2i, 2i+1), both held by lane i; odd rounds pair (2i+1, 2i+2), one
+// column of lane i with one of lane i+1.  An exchange within a lane is only a
+// relabelling (which register holds the left position flips every even round),
+// so columns move between lanes only in odd rounds: each lane receives its two
+// partners' columns by neighbour shuffles, computes both rotations (both lanes of a
+// pair compute the same one, bit for bit, from the same values) and keeps the
+// rotated partner column that lands on its own position.
+// ---------------------------------------------------------------------------------------
+
+struct JacCol {     // metadata of a column held in registers
+  float d;          // scale: true column = d * stored
+  float n2;         // squared norm of the true column (carried)
+};
+
+// Rotation of the pair (x, y) (true columns dx x, dy y with squared norms al, be),
+// decided as in jacobi_warp, without branches: a pair left as it is gets the
+// coefficients of the identity (ta = tb = tg = 0, c = 1).  Returns whether it rotates.
+__device__ inline bool jac_rotation(float dot_xy, const JacCol &x, const JacCol &y, float tol2,
+                                    float stop2, float &ta, float &tb, float &c, float &tg, int &far) {
+  const float ga = dot_xy * (x.d * y.d);
+  const float al = x.n2, be = y.n2;
+  const bool rot = al > kNegligible && be > kNegligible && ga * ga > tol2 * al * be;
+  const float gs = rot ? ga : 1.f;
+  const float zeta = (be - al) * __frcp_rn(2.f * gs);
+  const float az = fabsf(zeta);
+  const float root = az < 1e18f ? az + fmaf(az, az, 1.f) * rsqrtf(fmaf(az, az, 1.f)) : 2.f * az;
+  const float t = rot ? copysignf(__frcp_rn(root), zeta) : 0.f;
+  c = rsqrtf(fmaf(t, t, 1.f));
+  ta = t * y.d * __frcp_rn(x.d);
+  tb = t * x.d * __frcp_rn(y.d);
+  tg = t * ga;
+  far |= rot && ga * ga > stop2 * al * be;
+  return rot;
+}
+
+template <int MR>
+__device__ inline float jac_norm2(const float (&x)[MR], float d) {
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < MR; ++k) s[k & 3] = fmaf(x[k], x[k], s[k & 3]);
+  return ((s[0] + s[1]) + (s[2] + s[3])) * (d * d);
+}
+
+// dot product with four accumulation chains (a shorter dependent chain)
+template <int MR>
+__device__ inline float jac_dot(const float (&x)[MR], const float (&y)[MR]) {
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < MR; ++k) s[k & 3] = fmaf(x[k], y[k], s[k & 3]);
+  return (s[0] + s[1]) + (s[2] + s[3]);
+}
+
+// One even round (the lane's own pair) and one odd round (pairs with the
+// neighbours).  RIGHT_A: after the even round the right-facing column is A.  Both
+// pairs of the odd round are decided before either is applied, so that their
+// dependent chains overlap; a rotation not taken has identity coefficients.
+template <int MR, int HW, bool RIGHT_A>
+__device__ inline void jac_round_pair(float (&A)[MR], float (&B)[MR], JacCol &ca, JacCol &cb, bool has_left,
+                                      bool has_right, unsigned full, float tol2, float stop2, int &far) {
+  // ---- even round ----
+  {
+    float ta, tb, c, tg;
+    const bool rot = jac_rotation(jac_dot<MR>(A, B), ca, cb, tol2, stop2, ta, tb, c, tg, far);
+#pragma unroll
+    for (int k = 0; k < MR; ++k) {
+      const float a = A[k], b = B[k];
+      A[k] = fmaf(-ta, b, a);
+      B[k] = fmaf(tb, a, b);
+    }
+    const float na = ca.n2 - tg, nb = cb.n2 + tg;
+    ca.d *= c;
+    cb.d *= c;
+    if (rot && na < 0.25f * ca.n2) ca.n2 = jac_norm2<MR>(A, ca.d); else ca.n2 = na;
+    if (rot && nb < 0.25f * cb.n2) cb.n2 = jac_norm2<MR>(B, cb.d); else cb.n2 = nb;
+  }
+  // ---- odd round ----
+  float (&Xr)[MR] = RIGHT_A ? A : B;   // my right-facing column
+  float (&Xl)[MR] = RIGHT_A ? B : A;   // my left-facing column
+  JacCol &cxr = RIGHT_A ? ca : cb;
+  JacCol &cxl = RIGHT_A ? cb : ca;
+  float R[MR], Lf[MR];
+#pragma unroll
+  for (int k = 0; k < MR; ++k) {
+    R[k] = __shfl_down_sync(full, Xl[k], 1, HW);   // right neighbour's left-facing column
+    Lf[k] = __shfl_up_sync(full, Xr[k], 1, HW);    // left neighbour's right-facing column
+  }
+  JacCol cr, cl;
+  cr.d = __shfl_down_sync(full, cxl.d, 1, HW);
+  cr.n2 = __shfl_down_sync(full, cxl.n2, 1, HW);
+  cl.d = __shfl_up_sync(full, cxr.d, 1, HW);
+  cl.n2 = __shfl_up_sync(full, cxr.n2, 1, HW);
+  // pair (my right-facing x, right neighbour's y): I keep y' on my right position;
+  // pair (left neighbour's x, my left-facing y): I keep x' on my left position
+  float ta1, tb1, c1, tg1, ta2, tb2, c2, tg2;
+  int far1 = 0, far2 = 0;
+  const float d1 = jac_dot<MR>(Xr, R), d2 = jac_dot<MR>(Lf, Xl);
+  const bool rot1 = jac_rotation(d1, cxr, cr, tol2, stop2, ta1, tb1, c1, tg1, far1);
+  const bool rot2 = jac_rotation(d2, cl, cxl, tol2, stop2, ta2, tb2, c2, tg2, far2);
+  far |= (has_right && far1) || (has_left && far2);
+  if (has_right) {
+    const float ny = cr.n2 + tg1;
+#pragma unroll
+    for (int k = 0; k < MR; ++k) Xr[k] = fmaf(tb1, Xr[k], R[k]);
+    cxr.d = cr.d * c1;
+    cxr.n2 = (rot1 && ny < 0.25f * cr.n2) ? jac_norm2<MR>(Xr, cxr.d) : ny;
+  }
+  if (has_left) {
+    const float nx = cl.n2 - tg2;
+#pragma unroll
+    for (int k = 0; k < MR; ++k) Xl[k] = fmaf(-ta2, Xl[k], Lf[k]);
+    cxl.d = cl.d * c2;
+    cxl.n2 = (rot2 && nx < 0.25f * cl.n2) ? jac_norm2<MR>(Xl, cxl.d) : nx;
+  }
+}
+
+// Leaves what jacobi_warp leaves, over all n' seats (the zero column of an odd m
+// among them, ranked last): the columns of (seats) J in the square, sig2, inv and
+// the order of decreasing sigma.  Returns the sweeps run, or -1 at the sweep limit.
+template <int MR, int HW>
+__device__ int jacobi_warp_reg(int m, float tol, float tol_stop, float *sw) {
+  using L = SvdWarpSmem<MR>;
+  constexpr int TP = L::TP;
+  static_assert(MR % 4 == 0 && MR <= 48, "columns in registers");
+  const int lane = threadIdx.x & (HW - 1);
+  const unsigned full = HW == 32 ? 0xffffffffu : 0xffffu << (threadIdx.x & 16);
+  float *T = sw + L::T_OFF, *sig2 = sw + L::S_OFF, *inv = sw + L::I_OFF;
+  int *order = reinterpret_cast<int *>(sw + L::O_OFF);
+  const int nn = m + (m & 1), P = nn / 2;
+  const bool active = lane < P;
+  const bool has_right = lane + 1 < P, has_left = lane > 0 && active;
+  const float tol2 = tol * tol, stop2 = tol_stop * tol_stop;
+
+  float A[MR], B[MR];
+  {
+    const float4 *a4 = reinterpret_cast<const float4 *>(T + (2 * lane) * TP);
+    const float4 *b4 = reinterpret_cast<const float4 *>(T + (2 * lane + 1) * TP);
+#pragma unroll
+    for (int q = 0; q < MR / 4; ++q) {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 a = active ? a4[q] : z, b = active ? b4[q] : z;
+      A[4 * q] = a.x; A[4 * q + 1] = a.y; A[4 * q + 2] = a.z; A[4 * q + 3] = a.w;
+      B[4 * q] = b.x; B[4 * q + 1] = b.y; B[4 * q + 2] = b.z; B[4 * q + 3] = b.w;
+    }
+  }
+  JacCol ca{1.f, 0.f}, cb{1.f, 0.f};
+  int sweeps = 0;
+  if (m >= 2) {
+    sweeps = -1;
+    for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
+      ca.n2 = jac_norm2<MR>(A, ca.d);  // norms summed afresh every sweep
+      cb.n2 = jac_norm2<MR>(B, cb.d);
+      int far = 0;
+      // rounds in pairs (even, odd); after an even round at parity 0 the right-facing
+      // register is A, at parity 1 it is B: two copies of the pair, fixed at compile time
+      for (int rr = 0; rr < P; ++rr) {
+        if ((rr & 1) == 0) jac_round_pair<MR, HW, true>(A, B, ca, cb, has_left, has_right, full, tol2, stop2, far);
+        else jac_round_pair<MR, HW, false>(A, B, ca, cb, has_left, has_right, full, tol2, stop2, far);
+      }
+      const bool conv = !__any_sync(full, far);
+      // fold the scales into the columns: at the end, or once one has shrunk below 2^-20
+      if (conv || sweep + 1 == kMaxSweeps || ca.d < 9.5367e-7f) {
+#pragma unroll
+        for (int k = 0; k < MR; ++k) A[k] *= ca.d;
+        ca.d = 1.f;
+      }
+      if (conv || sweep + 1 == kMaxSweeps || cb.d < 9.5367e-7f) {
+#pragma unroll
+        for (int k = 0; k < MR; ++k) B[k] *= cb.d;
+        cb.d = 1.f;
+      }
+      if (conv) {
+        sweeps = sweep + 1;
+        break;
+      }
+    }
+  }
+  // ---- the columns to the seats (lane i: seats 2i, 2i+1), sigma^2, order ---------------------
+  if (active) {
+#pragma unroll
+    for (int q = 0; q < MR / 4; ++q) {
+      reinterpret_cast<float4 *>(T + (2 * lane) * TP)[q] = make_float4(A[4 * q], A[4 * q + 1], A[4 * q + 2], A[4 * q + 3]);
+      reinterpret_cast<float4 *>(T + (2 * lane + 1) * TP)[q] = make_float4(B[4 * q], B[4 * q + 1], B[4 * q + 2], B[4 * q + 3]);
+    }
+    const float a2 = jac_norm2<MR>(A, 1.f), b2 = jac_norm2<MR>(B, 1.f);
+    sig2[2 * lane] = a2;
+    sig2[2 * lane + 1] = b2;
+    inv[2 * lane] = a2 > kNegligible ? rsqrtf(a2) : 0.f;
+    inv[2 * lane + 1] = b2 > kNegligible ? rsqrtf(b2) : 0.f;
+  }
+  __syncwarp(full);
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int j = lane + HW * e;
+    if (j < nn) {
+      int rank = 0;
+      const float sj = sig2[j];
+      for (int i = 0; i < nn; ++i) {
         const float si = sig2[i];
         rank += (si > sj) || (si == sj && i < j);
       }

@@ -15,23 +15,10 @@
 
 namespace seedk {
 
-constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
-constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
 enum { F_Q = 1, F_K = 2, F_V = 3, F_ALPHA = 4, F_BETA = 5, F_DT = 6,
        F_VBAR = 16, F_SINK = 17, F_A = 18, F_RANK = 19, F_CTX = 20 };
 
-__device__ __forceinline__ uint4 philox(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                        uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    if (r) { k0 += kW0; k1 += kW1; }
-    const uint32_t hi0 = __umulhi(kM0, c0), lo0 = kM0 * c0;
-    const uint32_t hi1 = __umulhi(kM1, c2), lo1 = kM1 * c2;
-    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
-  }
-  return make_uint4(c0, c1, c2, c3);
-}
+// philox(): common.cuh
 
 __device__ __forceinline__ uint32_t fkey(int phase, int field) {
   return ((uint32_t)(phase & 0xFFFF) << 16) | (uint32_t)(field & 0xFFFF);

@@ -9,7 +9,7 @@ from typing import Optional
 
 import torch
 
-from . import (SEED_BF16, SEED_F32, SEED_KDA, VARIANTS, DTYPES, seed_state,
+from . import (SEED_BF16, SEED_F32, SEED_KDA, VARIANTS, DTYPES, ROUNDINGS, seed_state,
                seed_synth_workload)
 
 
@@ -29,12 +29,13 @@ class FactoredStateBuffers:
 
     def __init__(self, variant: str, factor_dtype: str, n_heads: int, d_k: int, d_v: int, T: int,
                  vbar: torch.Tensor, r: int = 0, ranks: Optional[torch.Tensor] = None,
-                 vbar_index: Optional[torch.Tensor] = None, device='cuda'):
+                 vbar_index: Optional[torch.Tensor] = None, device='cuda', rounding: str = 'nearest',
+                 sr_seed: int = 0):
         self.variant = variant
         self.factor_dtype = factor_dtype
         self.n_heads, self.d_k, self.d_v, self.T = n_heads, d_k, d_v, T
         self.growth = 2 if variant == 'kda' else 1
-        tdt = torch.bfloat16 if factor_dtype == 'bf16' else torch.float32
+        tdt = {'bf16': torch.bfloat16, 'f16': torch.float16, 'f32': torch.float32}[factor_dtype]
         dev = torch.device(device)
         if ranks is None:
             self.r_max = r
@@ -68,10 +69,10 @@ class FactoredStateBuffers:
         self.vbar_index = None if vbar_index is None else vbar_index.to(device=dev, dtype=torch.int32).contiguous()
         self.st = seed_state(
             variant=VARIANTS[variant], factor_dtype=DTYPES[factor_dtype], n_heads=n_heads, d_k=d_k,
-            d_v=d_v, T=T, r=r, r_max=self.r_max, steps_since_compress=0, reserved_=0,
+            d_v=d_v, T=T, r=r, r_max=self.r_max, steps_since_compress=0, rounding=ROUNDINGS[rounding],
             rank=_p(self.ranks), col_offset=_p(self.col_offset), a=_p(self.a), U=_p(self.U),
             W=_p(self.W), scale=_p(self.scale), vbar=_p(self.vbar), vbar_index=_p(self.vbar_index),
-            status=_p(self.status))
+            status=_p(self.status), sr_seed=sr_seed)
 
     @property
     def steps_since_compress(self) -> int:

@@ -29,7 +29,8 @@ class DeviceRun:
     ``ws_heads`` > 0 recompresses through the three-phase path with a workspace
     for that many heads per group; 0 uses the single-kernel recompression."""
 
-    def __init__(self, w, device='cuda', steps_buffered: int = 1, ws_heads: int = DEFAULT_WS_HEADS):
+    def __init__(self, w, device='cuda', steps_buffered: int = 1, ws_heads: int = DEFAULT_WS_HEADS,
+                 rounding: str = 'nearest', sr_seed: int = 0):
         self.w = w
         self.dev = torch.device(device)
         self.wst = synth_workload_struct(w)
@@ -48,7 +49,12 @@ class DeviceRun:
         ragged = bool(w.rank_choices)
         self.state = FactoredStateBuffers(
             w.variant, w.factor_dtype, H, dk, dv, w.T, self.vbar, r=w.rank if not ragged else 0,
-            ranks=self.ranks if ragged else None, vbar_index=self.vbar_index, device=self.dev)
+            ranks=self.ranks if ragged else None, vbar_index=self.vbar_index, device=self.dev,
+            rounding=rounding, sr_seed=sr_seed)
+        # stochastic rounding: every call that stores factor elements gets the next
+        # seed of a fixed sequence (fresh bits per call, reproducible per run)
+        self.stochastic = rounding == 'stochastic'
+        self._sr_next = sr_seed
         nb = max(1, steps_buffered)
         self.q = torch.empty(nb, H, dk, **f32)
         self.k = torch.empty(nb, H, dk, **f32)
@@ -74,6 +80,7 @@ class DeviceRun:
         return out
 
     def compress(self, S: torch.Tensor, trunc_err: Optional[torch.Tensor] = None):
+        self._sr_advance()
         seed_compress_dense(S, self.state.st, trunc_err)
 
     # -- decode loop --------------------------------------------------------------
@@ -82,11 +89,18 @@ class DeviceRun:
                                self.q[slot], self.k[slot], self.v[slot], self.gate[slot],
                                self.beta[slot])
 
+    def _sr_advance(self):
+        if self.stochastic:
+            self._sr_next += 1
+            self.state.st.sr_seed = self._sr_next
+
     def decode(self, slot: int = 0, stream=None):
+        self._sr_advance()
         seed_decode_step(self.state.st, self.q[slot], self.k[slot], self.v[slot], self.gate[slot],
                          self.beta[slot], self.A, self.o, stream)
 
     def recompress(self, trunc_err: Optional[torch.Tensor] = None, stream=None, sweeps=None):
+        self._sr_advance()
         if self.ws is not None:
             seed_recompress_ws(self.state.st, trunc_err, sweeps, self.ws, self.ws_bytes, stream)
         else:

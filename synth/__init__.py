@@ -170,7 +170,7 @@ class Workload:
     T: int
     steps: int
     seed: int
-    factor_dtype: str            # 'f32' | 'bf16'
+    factor_dtype: str            # 'f32' | 'bf16' | 'f16'
     rank: int = 0                # uniform rank, or 0 when rank_choices is used
     rank_choices: Tuple[int, ...] = ()
     prefill_len: int = 0         # fixed prompt length, or 0 when prefill_range is used

@@ -11,7 +11,7 @@ import rank_state_compression_head_b300 as R
 
 # Tolerances of the parity bar: relative Frobenius / L2 error of reconstructed
 # states and outputs, fp32 factors and bf16 storage with fp32 accumulation.
-TOL = {'f32': 1e-4, 'bf16': 1e-2}
+TOL = {'f32': 1e-4, 'bf16': 1e-2, 'f16': 1e-2}
 
 
 def stored(x, dtype: str) -> np.ndarray:
@@ -19,6 +19,8 @@ def stored(x, dtype: str) -> np.ndarray:
     t = torch.as_tensor(np.asarray(x, np.float64), dtype=torch.float64)
     if dtype == 'bf16':
         return t.to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    if dtype == 'f16':
+        return t.to(torch.float32).to(torch.float16).to(torch.float64).numpy()
     return t.to(torch.float32).to(torch.float64).numpy()
 
 
@@ -41,12 +43,13 @@ def random_states(seed, H, d_k, d_v, ranks, s, T, variant, dtype):
     return states, raw['vbar']
 
 
-def make_buffers(variant, dtype, H, d_k, d_v, T, vbar, ranks, ragged=True):
+def make_buffers(variant, dtype, H, d_k, d_v, T, vbar, ranks, ragged=True, rounding='nearest', sr_seed=0):
     vb = torch.tensor(np.asarray(vbar), dtype=torch.float32)
+    kw = dict(rounding=rounding, sr_seed=sr_seed)
     if ragged:
         return R.FactoredStateBuffers(variant, dtype, H, d_k, d_v, T, vb,
-                                      ranks=torch.tensor(np.asarray(ranks), dtype=torch.int32))
-    return R.FactoredStateBuffers(variant, dtype, H, d_k, d_v, T, vb, r=int(ranks[0]))
+                                      ranks=torch.tensor(np.asarray(ranks), dtype=torch.int32), **kw)
+    return R.FactoredStateBuffers(variant, dtype, H, d_k, d_v, T, vb, r=int(ranks[0]), **kw)
 
 
 def upload(buf, states, s):

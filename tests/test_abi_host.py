@@ -3,6 +3,8 @@ and rejects bad arguments on the host before any launch."""
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -33,10 +35,25 @@ def test_library_exports_every_declared_function():
     assert names == set(R.EXPORTED_SYMBOLS)
 
 
-def test_struct_layout_matches_header():
-    # 10 int32 fields followed by 9 pointers
-    assert ctypes.sizeof(R.seed_state) == 10 * 4 + 9 * 8
+def test_struct_layout_matches_header(tmp_path):
+    # 10 int32 fields, 9 pointers, the 64-bit stochastic-rounding seed
+    assert ctypes.sizeof(R.seed_state) == 10 * 4 + 9 * 8 + 8
     assert R.seed_state.a.offset == 56
+    # the C compiler's view of seed.h agrees field by field with the ctypes mirror
+    gcc = shutil.which('gcc')
+    if gcc is None:
+        pytest.skip('no C compiler')
+    names = [f[0] for f in R.seed_state._fields_]
+    src = tmp_path / 'layout.c'
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "seed.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(seed_state));\n' +
+                   ''.join(f'  printf("%zu\\n", offsetof(seed_state, {n}));\n' for n in names) +
+                   '  return 0;\n}\n')
+    exe = tmp_path / 'layout'
+    subprocess.run([gcc, '-I', os.path.join(ROOT, 'include'), str(src), '-o', str(exe)], check=True)
+    out = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(R.seed_state)
+    assert out[1:] == [getattr(R.seed_state, n).offset for n in names]
 
 
 def test_status_strings():
@@ -54,7 +71,7 @@ def test_columns_per_head():
 
 def make_state(**kw):
     st = R.seed_state(variant=R.SEED_GDN, factor_dtype=R.SEED_BF16, n_heads=4, d_k=128, d_v=128, T=16,
-                      r=32, r_max=32, steps_since_compress=0, reserved_=0, rank=None, col_offset=None,
+                      r=32, r_max=32, steps_since_compress=0, rounding=0, rank=None, col_offset=None,
                       a=FAKE, U=FAKE, W=FAKE, scale=FAKE, vbar=FAKE, vbar_index=None, status=None)
     for k, v in kw.items():
         setattr(st, k, v)
@@ -139,11 +156,16 @@ def test_synth_calls_reject_on_host():
     assert R._lib.seed_synth_raw(0, 0, 0, 0, 0, 4, 4, FAKE + 4, None) == R.SEED_ERR_ALIGNMENT
 
 
-def _ws_floats(m, r, dk, dv):
-    # W's reflectors, their tau, R_b^T, K, Y; each region on 16 bytes
+def _ws_floats(m, r, dk, dv, dtype='bf16'):
+    # 16-bit factors (Cholesky of the value-side Gram matrix): M, R_b, Y; 32-bit
+    # factors (QR of both factors): W's reflectors, their tau, R_b^T, K, Y; each
+    # region on 16 bytes, the whole on 256 bytes
     m4 = (m + 3) // 4 * 4
     mm4 = (m * m + 3) // 4 * 4
-    n = m * dv + m4 + 2 * mm4 + r * m4
+    if dtype == 'f32':
+        n = m * dv + m4 + 2 * mm4 + r * m4
+    else:
+        n = 2 * mm4 + r * m4
     n = (n + 63) // 64 * 64
     return max(n, 64)
 
@@ -156,6 +178,8 @@ def test_recompress_workspace_bytes():
     assert R.seed_recompress_workspace_bytes(kda, 3) == 3 * 4 * _ws_floats(32, 16, 128, 128)
     m2 = make_state(variant=R.SEED_MAMBA2, d_v=64, r=16, r_max=16)
     assert R.seed_recompress_workspace_bytes(m2, 2) == 2 * 4 * _ws_floats(32, 16, 128, 64)
+    f32 = make_state(factor_dtype=R.SEED_F32)
+    assert R.seed_recompress_workspace_bytes(f32, 5) == 5 * 4 * _ws_floats(48, 32, 128, 128, 'f32')
     out = ctypes.c_int64(0)
     f = R._lib.seed_recompress_workspace_bytes
     assert f(ctypes.byref(st), 0, ctypes.addressof(out)) == R.SEED_ERR_INVALID_ARG

@@ -44,7 +44,7 @@ def head_tok(d, h):
 
 
 @pytest.mark.parametrize('variant', ['gdn', 'kda', 'mamba2'])
-@pytest.mark.parametrize('dtype', ['f32', 'bf16'])
+@pytest.mark.parametrize('dtype', ['f32', 'bf16', 'f16'])
 def test_materialize_matches_oracle(variant, dtype):
     H, T, s = 13, 8, 3
     ranks = ranks_for(variant, H, T)
@@ -57,7 +57,7 @@ def test_materialize_matches_oracle(variant, dtype):
 
 
 @pytest.mark.parametrize('variant', ['gdn', 'kda', 'mamba2'])
-@pytest.mark.parametrize('dtype', ['f32', 'bf16'])
+@pytest.mark.parametrize('dtype', ['f32', 'bf16', 'f16'])
 def test_decode_steps_match_oracle(variant, dtype):
     H, T, s0 = 37, 8, 2
     ranks = ranks_for(variant, H, T)
@@ -92,7 +92,7 @@ def test_decode_steps_match_oracle(variant, dtype):
 
 
 @pytest.mark.parametrize('variant', ['gdn', 'kda', 'mamba2'])
-@pytest.mark.parametrize('dtype', ['f32', 'bf16'])
+@pytest.mark.parametrize('dtype', ['f32', 'bf16', 'f16'])
 def test_recompress_matches_oracle(variant, dtype):
     H, T = 21, 8
     growth = 2 if variant == 'kda' else 1
@@ -116,7 +116,7 @@ def test_recompress_matches_oracle(variant, dtype):
 
 
 @pytest.mark.parametrize('variant', ['gdn', 'kda', 'mamba2'])
-@pytest.mark.parametrize('dtype', ['f32', 'bf16'])
+@pytest.mark.parametrize('dtype', ['f32', 'bf16', 'f16'])
 def test_compress_dense_matches_oracle(variant, dtype):
     H, T, d_v = 9, 8, D_V[variant]
     ranks = ranks_for(variant, H, T)

@@ -29,7 +29,7 @@ def workspace(buf, heads):
 
 
 @pytest.mark.parametrize('variant', ['gdn', 'kda', 'mamba2'])
-@pytest.mark.parametrize('dtype', ['f32', 'bf16'])
+@pytest.mark.parametrize('dtype', ['f32', 'bf16', 'f16'])
 def test_ws_recompress_matches_oracle(variant, dtype):
     H, T = 23, 8
     ranks = ranks_for(variant, H, T)
@@ -52,7 +52,7 @@ def test_ws_recompress_matches_oracle(variant, dtype):
 
 
 @pytest.mark.parametrize('variant', ['gdn', 'kda', 'mamba2'])
-@pytest.mark.parametrize('dtype', ['f32', 'bf16'])
+@pytest.mark.parametrize('dtype', ['f32', 'bf16', 'f16'])
 @pytest.mark.parametrize('group', [1, 4, 1000])
 @pytest.mark.parametrize('s', [3, 8])
 def test_ws_agrees_with_single_kernel(variant, dtype, group, s):

@@ -54,8 +54,14 @@ def test_noalloc_matches_workspace_call_twice(variant, dtype):
 
 
 def test_noalloc_rejects_oversize_without_launch():
-    # 2000 heads at m = 48, r = 32 need 2000 x 12352 floats, more than the 16 Mi of the scratch
-    H, T = 2000, 16
+    # enough heads at m = 48, r = 32 that their per-head workspace (the size that
+    # seed_recompress_workspace_bytes reports at full capacity) no longer fits in
+    # the 64 MiB scratch
+    T = 16
+    probe = make_buffers('gdn', 'bf16', 1, 128, 128, T, np.ones((1, 128)) / np.sqrt(128),
+                         np.full(1, 32, dtype=np.int32), ragged=False)
+    per_head = R.seed_recompress_workspace_bytes(probe.st, 1)
+    H = (64 << 20) // per_head + 16
     ranks = np.full(H, 32, dtype=np.int32)
     vbar = np.ones((H, 128)) / np.sqrt(128)
     buf = make_buffers('gdn', 'bf16', H, 128, 128, T, vbar, ranks, ragged=False)
