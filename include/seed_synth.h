@@ -86,6 +86,27 @@ int seed_synth_dense_prefill(const seed_synth_workload *w, int64_t head0, int32_
                              const int32_t *prompt_len, const float *vbar, const float *sink_scale,
                              const float *A, float *S_out, seed_stream_t stream);
 
+/*
+ * The same prefill, advanced a chunk of tokens at a time (32 tokens for the
+ * scalar gates, 16 for the per-channel gate) in the chunkwise form of the
+ * delta rule: within a chunk the corrections u_t solve a unit lower-triangular
+ * system built from the chunk's key inner products and gate ratios, and the
+ * state takes one rank-C update per chunk (the WY / UT form of Yang et al.,
+ * "Parallelizing Linear Transformers with the Delta Rule over Sequence
+ * Length", NeurIPS 2024, with the gates carried exactly; for the per-channel
+ * gate, which acts after the erase, two update terms per token).  The result is
+ * the token-serial recurrence's up to fp32 rounding order.  Arguments, layout,
+ * ownership and errors as seed_synth_dense_prefill.  Where the smallest scalar
+ * or per-channel gate raised to the chunk length falls below 2^-96 (the
+ * cumulative products could leave fp32's normal range), the call runs
+ * seed_synth_dense_prefill instead.  Mamba-2 chunks work with the logarithm of
+ * the cumulative decay and have no such limit.
+ */
+int seed_synth_dense_prefill_chunked(const seed_synth_workload *w, int64_t head0, int32_t n_heads,
+                                     const int32_t *prompt_len, const float *vbar,
+                                     const float *sink_scale, const float *A, float *S_out,
+                                     seed_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -94,6 +94,7 @@ _PROTOS = {
     'seed_synth_step_inputs': (ctypes.c_int, [_wp, _i32, _i32, _i64, _i32, _vp, _vp, _vp, _vp,
                                               _vp, _vp, _vp, _vp]),
     'seed_synth_dense_prefill': (ctypes.c_int, [_wp, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    'seed_synth_dense_prefill_chunked': (ctypes.c_int, [_wp, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _PROTOS.items():
     _fn = getattr(_lib, _name)
@@ -226,6 +227,14 @@ def seed_synth_dense_prefill(w: seed_synth_workload, head0: int, n_heads: int, p
     _check('seed_synth_dense_prefill',
            _lib.seed_synth_dense_prefill(ctypes.byref(w), head0, n_heads, _ptr(prompt_len), _ptr(vbar),
                                          _ptr(sink_scale), _ptr(A), _ptr(S_out), _stream(stream)))
+
+
+def seed_synth_dense_prefill_chunked(w: seed_synth_workload, head0: int, n_heads: int, prompt_len, vbar,
+                                     sink_scale, A, S_out, stream=None) -> None:
+    _check('seed_synth_dense_prefill_chunked',
+           _lib.seed_synth_dense_prefill_chunked(ctypes.byref(w), head0, n_heads, _ptr(prompt_len),
+                                                 _ptr(vbar), _ptr(sink_scale), _ptr(A), _ptr(S_out),
+                                                 _stream(stream)))
 
 
 from .state import FactoredStateBuffers, synth_workload_struct  # noqa: E402,F401

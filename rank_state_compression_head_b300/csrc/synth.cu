@@ -280,6 +280,282 @@ __global__ void __launch_bounds__(256) prefill_kernel(const seed_synth_workload 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Chunked (parallel-in-time) dense prefill.
+//
+// The same recurrence as prefill_kernel, advanced C tokens at a time in the
+// chunkwise form of the delta rule (the WY / UT-transform form of Yang, Wang,
+// Zhang, Shen, Kim, "Parallelizing Linear Transformers with the Delta Rule over
+// Sequence Length", NeurIPS 2024), with the gates carried exactly.  Within a
+// chunk from S_0, gamma_t is the product of the gates up to token t (per channel
+// for the per-channel gate) and gm_t = gamma_{t-1} (gm_0 = 1).
+//
+//   scalar gate:  S_t = alpha_t S_{t-1} + k_t u_t^T,  u_t = beta_t (v_t - alpha_t S_{t-1}^T k_t),
+//     so (I + A) U = diag(beta) (V - P), P_t = gamma_t k_t^T S_0,
+//     A[t][r] = beta_t (gamma_t / gamma_r) k_t . k_r (r < t), forward substitution,
+//     and S_C = gamma_C S_0 + sum_t (gamma_C / gamma_t) k_t u_t^T.
+//   per-channel gate after the erase (diag(alpha)(I - beta k k^T) S + beta k v^T):
+//     S_t = diag(alpha_t) S_{t-1} + (alpha_t * k_t) x_t^T + k_t y_t^T,
+//     y_t = beta_t v_t,  x_t = -beta_t S_{t-1}^T k_t, so with P_t = k_t^T diag(gm_t) S_0,
+//     Cm[t][r] = sum_i k_t[i] k_r[i] gm_t[i] / gm_r[i],  E[t][r] = sum_i k_t[i] k_r[i] gm_t[i] / gamma_r[i]:
+//       x_t = -beta_t (P_t + sum_{r<t} E[t][r] y_r) - beta_t sum_{r<t} Cm[t][r] x_r,
+//     S_C = diag(gamma_C) S_0 + sum_r (gamma_C / gm_r * k_r) x_r^T + (gamma_C / gamma_r * k_r) y_r^T.
+//   Mamba-2 (no erase): S_C = gamma_C S_0 + sum_t (gamma_C / gamma_t) dt_t B_t x_t^T.
+// All arithmetic is fp32 FMA.  One CTA of 256 threads per head; thread
+// (q, j) holds column j of the state for a quarter or half of its rows in
+// registers; the chunk's tokens are generated in parallel (one warp a token).
+// ---------------------------------------------------------------------------
+
+// One warp generates every input of one prefill token (the values of gen_token).
+__device__ __forceinline__ void gen_token_warp(const seed_synth_workload &w, uint32_t time, uint32_t head,
+                                               const float *vbar_d, float sink_d, bool live, float *kout,
+                                               float *vout, float *gout, float *bout) {
+  const int lane = threadIdx.x & 31;
+  const bool m2 = w.variant == SEED_MAMBA2, kda = w.variant == SEED_KDA;
+  const int phase = SEED_SYNTH_PHASE_PREFILL;
+  float4 z = live ? normal4(w.seed, phase, F_K, time, head, lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (m2) {
+    const float sd = 1.f / sqrtf((float)w.d_k);
+    z = make_float4(z.x * sd, z.y * sd, z.z * sd, z.w * sd);
+  } else {
+    const float nrm = sqrtf(warp_sum(z.x * z.x + z.y * z.y + z.z * z.z + z.w * z.w));
+    if (nrm > 0.f) z = make_float4(z.x / nrm, z.y / nrm, z.z / nrm, z.w / nrm);
+  }
+  reinterpret_cast<float4 *>(kout)[lane] = z;
+  if (lane < w.d_v / 4) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) {
+      const float4 n = normal4(w.seed, phase, F_V, time, head, lane);
+      const float4 vb = reinterpret_cast<const float4 *>(vbar_d)[lane];
+      const float sd = w.noise_std;
+      v = make_float4(fmaf(sink_d, vb.x, sd * n.x), fmaf(sink_d, vb.y, sd * n.y), fmaf(sink_d, vb.z, sd * n.z),
+                      fmaf(sink_d, vb.w, sd * n.w));
+    }
+    reinterpret_cast<float4 *>(vout)[lane] = v;
+  }
+  if (kda) {
+    float4 a = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (live) {
+      const uint4 x = philox((uint32_t)lane, time, head, 0u, w.seed, fkey(phase, F_ALPHA));
+      const float sp = w.alpha_hi - w.alpha_lo;
+      a = make_float4(w.alpha_lo + sp * uni(x.x), w.alpha_lo + sp * uni(x.y), w.alpha_lo + sp * uni(x.z),
+                      w.alpha_lo + sp * uni(x.w));
+    }
+    reinterpret_cast<float4 *>(gout)[lane] = a;
+  }
+  if (lane == 0) {
+    if (m2) {
+      gout[0] = live ? softplusf(w.dt_mu + sqrtf(w.dt_var) * normal4(w.seed, phase, F_DT, time, head, 0u).x) : 0.f;
+    } else {
+      if (!kda) gout[0] = live ? w.alpha_lo + (w.alpha_hi - w.alpha_lo) * uniform1(w.seed, phase, F_ALPHA, time, head) : 1.f;
+      bout[0] = live ? w.beta_lo + (w.beta_hi - w.beta_lo) * uniform1(w.seed, phase, F_BETA, time, head) : 0.f;
+    }
+  }
+}
+
+template <int VAR>
+constexpr int chunk_len() { return VAR == SEED_KDA ? 16 : 32; }
+
+template <int VAR, int DV>
+struct ChunkSmem {
+  static constexpr int DK = kDK, C = chunk_len<VAR>();
+  static constexpr int NQ = 256 / DV;                         // row groups of the state
+  static constexpr bool KDA = VAR == SEED_KDA;
+  static constexpr int K_OFF = 0;                             // [C][DK] keys, later update weights
+  static constexpr int V_OFF = K_OFF + C * DK;                // [C][DV] values, later U (or y)
+  static constexpr int G_OFF = V_OFF + C * DV;                // KDA [C][DK] gates -> gamma, later weights; else [C]
+  static constexpr int GI_OFF = G_OFF + (KDA ? C * DK : C);   // KDA [C][DK] 1/gamma; else [C] gamma
+  static constexpr int GC_OFF = GI_OFF + (KDA ? C * DK : C);  // KDA [DK] gamma_C
+  static constexpr int B_OFF = GC_OFF + (KDA ? DK : 4);       // [C] beta
+  static constexpr int A_OFF = B_OFF + C;                     // [C][C + 1] the strictly lower A (or Cm)
+  static constexpr int E_OFF = A_OFF + C * (C + 1);           // KDA [C][C + 1] E
+  static constexpr int P_OFF = E_OFF + (KDA ? C * (C + 1) : 0);  // [NQ][C][DV] partial P, then x in slice 0
+  static constexpr int FLOATS = (P_OFF + NQ * C * DV + 3) & ~3;
+};
+
+template <int VAR, int DV>
+__global__ void __launch_bounds__(256, 2) prefill_chunk_kernel(const seed_synth_workload w, int64_t head0,
+                                                               const int32_t *plen, const float *vbar,
+                                                               const float *sink, const float *A, float *S_out) {
+  constexpr int DK = kDK;
+  using L = ChunkSmem<VAR, DV>;
+  constexpr int C = L::C, NQ = L::NQ, RPT = DK / NQ;
+  constexpr bool M2 = VAR == SEED_MAMBA2, KDA = VAR == SEED_KDA;
+  extern __shared__ __align__(16) float sm[];
+  float *Kc = sm + L::K_OFF, *Vc = sm + L::V_OFF, *Gc = sm + L::G_OFF, *Gi = sm + L::GI_OFF;
+  float *gCr = sm + L::GC_OFF, *Bc = sm + L::B_OFF, *Am = sm + L::A_OFF, *Em = sm + L::E_OFF, *Pp = sm + L::P_OFF;
+
+  const int64_t h = head0 + blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int j = tid % DV, q = tid / DV, i0 = q * RPT;
+  const int n_dir = w.n_layers * w.n_head;
+  const int dir = (int)(h % n_dir);
+  const int L_tok = plen[h / n_dir];
+  const float *vb = vbar + (int64_t)dir * DV;
+  const float sd = sink[dir];
+  const float Ad = M2 ? A[dir] : 0.f;
+
+  float st[RPT];
+#pragma unroll
+  for (int r = 0; r < RPT; ++r) st[r] = 0.f;
+
+  for (int t0 = 0; t0 < L_tok; t0 += C) {
+    // ---- the chunk's tokens (past the prompt: identity steps) ----------------------------------
+    for (int t = warp; t < C; t += 8)
+      gen_token_warp(w, (uint32_t)(t0 + t), (uint32_t)h, vb, sd, t0 + t < L_tok, Kc + t * DK, Vc + t * DV,
+                     KDA ? Gc + t * DK : Gc + t, Bc + t);
+    __syncthreads();
+    // ---- cumulative gates (products of the per-step gates, as the recurrence) ------------------
+    if (KDA) {
+      if (tid < DK) {
+        float g = 1.f;
+        for (int t = 0; t < C; ++t) {
+          g *= Gc[t * DK + tid];
+          Gc[t * DK + tid] = g;
+          Gi[t * DK + tid] = 1.f / g;
+        }
+        gCr[tid] = g;
+      }
+    } else if (tid == 0) {
+      // gamma_t for the scalar gate; for Mamba-2 its logarithm (sum of dt A), so that
+      // no ratio of two underflowing products is ever formed (Gc keeps the step gate or dt)
+      float g = M2 ? 0.f : 1.f;
+      for (int t = 0; t < C; ++t) {
+        if (M2) g = fmaf(Gc[t], Ad, g);
+        else g *= Gc[t];
+        Gi[t] = g;
+      }
+    }
+    __syncthreads();
+    if (!M2) {
+      // ---- the strictly lower chunk matrices ------------------------------------------------------
+      for (int pr = tid; pr < C * (C - 1) / 2; pr += 256) {
+        int t = 1, rem = pr;  // pr -> (t, r), r < t
+        while (rem >= t) { rem -= t; ++t; }
+        const int r = rem;
+        const float4 *kt = reinterpret_cast<const float4 *>(Kc + t * DK);
+        const float4 *kr = reinterpret_cast<const float4 *>(Kc + r * DK);
+        if (KDA) {
+          // gm_t / gm_r and gm_t / gamma_r, with gm_t = gamma_{t-1} and 1/gm_r = 1/gamma_{r-1}
+          const float4 *gmt = reinterpret_cast<const float4 *>(Gc + (t - 1) * DK);
+          const float4 *igr = reinterpret_cast<const float4 *>(Gi + r * DK);
+          const float4 *igmr = reinterpret_cast<const float4 *>(Gi + (r - 1) * DK);
+          float cm = 0.f, e = 0.f;
+#pragma unroll 4
+          for (int i4 = 0; i4 < DK / 4; ++i4) {
+            const float4 a = kt[i4], b = kr[i4], g = gmt[i4], ig = igr[i4];
+            const float4 igm = r > 0 ? igmr[i4] : make_float4(1.f, 1.f, 1.f, 1.f);
+            const float px = a.x * b.x * g.x, py = a.y * b.y * g.y, pz = a.z * b.z * g.z, pw = a.w * b.w * g.w;
+            cm = fmaf(px, igm.x, fmaf(py, igm.y, fmaf(pz, igm.z, fmaf(pw, igm.w, cm))));
+            e = fmaf(px, ig.x, fmaf(py, ig.y, fmaf(pz, ig.z, fmaf(pw, ig.w, e))));
+          }
+          Am[t * (C + 1) + r] = cm;
+          Em[t * (C + 1) + r] = e;
+        } else {
+          float acc = 0.f;
+#pragma unroll 4
+          for (int i4 = 0; i4 < DK / 4; ++i4) {
+            const float4 a = kt[i4], b = kr[i4];
+            acc = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
+          }
+          Am[t * (C + 1) + r] = Bc[t] * (Gi[t] / Gi[r]) * acc;
+        }
+      }
+      // ---- partial P over my rows: P[q][t][j] = sum_i k_t[i] w_t[i] S_0[i][j] ----------------------
+      // (w_t = gamma_t for the scalar gate, applied after; gm_t per channel)
+      float acc[C];
+#pragma unroll
+      for (int t = 0; t < C; ++t) acc[t] = 0.f;
+#pragma unroll
+      for (int r4 = 0; r4 < RPT / 4; ++r4) {
+#pragma unroll
+        for (int t = 0; t < C; ++t) {
+          float4 kk = *reinterpret_cast<const float4 *>(Kc + t * DK + i0 + 4 * r4);
+          if (KDA && t > 0) {
+            const float4 g = *reinterpret_cast<const float4 *>(Gc + (t - 1) * DK + i0 + 4 * r4);
+            kk = make_float4(kk.x * g.x, kk.y * g.y, kk.z * g.z, kk.w * g.w);
+          }
+          acc[t] = fmaf(kk.x, st[4 * r4], fmaf(kk.y, st[4 * r4 + 1], fmaf(kk.z, st[4 * r4 + 2], fmaf(kk.w, st[4 * r4 + 3], acc[t]))));
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < C; ++t) Pp[(q * C + t) * DV + j] = KDA ? acc[t] : acc[t] * Gi[t];
+      __syncthreads();
+      if (q == 0) {
+        if (KDA) {
+          // x_t = -beta_t (P_t + sum_{r<t} E[t][r] y_r + sum_{r<t} Cm[t][r] x_r), y_r = beta_r v_r;
+          // x_t goes into slice 0 of P, y_t into V
+          for (int t = 0; t < C; ++t) {
+            float p = 0.f;
+#pragma unroll
+            for (int qq = 0; qq < NQ; ++qq) p += Pp[(qq * C + t) * DV + j];
+            for (int r = 0; r < t; ++r)
+              p = fmaf(Em[t * (C + 1) + r], Vc[r * DV + j], fmaf(Am[t * (C + 1) + r], Pp[r * DV + j], p));
+            Pp[t * DV + j] = -Bc[t] * p;
+            Vc[t * DV + j] *= Bc[t];
+          }
+        } else {
+          // u_t = beta_t (v_t - P_t) - sum_{r<t} A[t][r] u_r, then the weight gamma_C / gamma_t
+          for (int t = 0; t < C; ++t) {
+            float p = 0.f;
+#pragma unroll
+            for (int qq = 0; qq < NQ; ++qq) p += Pp[(qq * C + t) * DV + j];
+            float u = Bc[t] * (Vc[t * DV + j] - p);
+            for (int r = 0; r < t; ++r) u = fmaf(-Am[t * (C + 1) + r], Vc[r * DV + j], u);
+            Vc[t * DV + j] = u;
+          }
+          const float gC = Gi[C - 1];
+          for (int t = 0; t < C; ++t) Vc[t * DV + j] *= gC / Gi[t];
+        }
+      } else if (KDA) {
+        // meanwhile the update weights: gamma_C / gm_r * k_r (into G) and gamma_C / gamma_r * k_r (into K)
+        for (int idx = tid - DV; idx < C * DK; idx += 256 - DV) {
+          const int r = idx / DK, i = idx % DK;
+          const float k = Kc[idx], g = gCr[i];
+          Gc[idx] = k * g * (r > 0 ? Gi[idx - DK] : 1.f);
+          Kc[idx] = k * g * Gi[idx];
+        }
+      }
+    } else {
+      // Mamba-2: u_t = (gamma_C / gamma_t) dt_t x_t = exp(log gamma_C - log gamma_t) dt_t x_t
+      const float lC = Gi[C - 1];
+      for (int idx = tid; idx < C * DV; idx += 256) {
+        const int t = idx / DV;
+        Vc[idx] *= Gc[t] * expf(lC - Gi[t]);
+      }
+    }
+    __syncthreads();
+    // ---- S_C = Gamma_C S_0 + sum_t (weights_t) (x) (U or x, y)_t over my rows ---------------------
+    {
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) st[r] *= KDA ? gCr[i0 + r] : (M2 ? expf(Gi[C - 1]) : Gi[C - 1]);
+      for (int t = 0; t < C; ++t) {
+        const float u = Vc[t * DV + j];
+        const float x = KDA ? Pp[t * DV + j] : 0.f;
+#pragma unroll
+        for (int r4 = 0; r4 < RPT / 4; ++r4) {
+          const float4 kk = *reinterpret_cast<const float4 *>(Kc + t * DK + i0 + 4 * r4);
+          st[4 * r4] = fmaf(kk.x, u, st[4 * r4]);
+          st[4 * r4 + 1] = fmaf(kk.y, u, st[4 * r4 + 1]);
+          st[4 * r4 + 2] = fmaf(kk.z, u, st[4 * r4 + 2]);
+          st[4 * r4 + 3] = fmaf(kk.w, u, st[4 * r4 + 3]);
+          if (KDA) {
+            const float4 k1 = *reinterpret_cast<const float4 *>(Gc + t * DK + i0 + 4 * r4);
+            st[4 * r4] = fmaf(k1.x, x, st[4 * r4]);
+            st[4 * r4 + 1] = fmaf(k1.y, x, st[4 * r4 + 1]);
+            st[4 * r4 + 2] = fmaf(k1.z, x, st[4 * r4 + 2]);
+            st[4 * r4 + 3] = fmaf(k1.w, x, st[4 * r4 + 3]);
+          }
+        }
+      }
+    }
+    __syncthreads();  // the chunk's buffers are free
+  }
+  float *out = S_out + (int64_t)blockIdx.x * DK * DV;
+#pragma unroll
+  for (int r = 0; r < RPT; ++r) out[(int64_t)(i0 + r) * DV + j] = st[r];
+}
+
 static int check_workload(const seed_synth_workload *w) {
   if (!w) return SEED_ERR_INVALID_ARG;
   if (w->variant < SEED_GDN || w->variant > SEED_MAMBA2) return SEED_ERR_INVALID_ARG;
@@ -337,6 +613,18 @@ extern "C" int seed_synth_step_inputs(const seed_synth_workload *w, int32_t phas
   return cuda_status(cudaGetLastError());
 }
 
+template <int VAR, int DV>
+static cudaError_t launch_chunk_t(const seed_synth_workload &w, int64_t head0, int32_t n_heads, const int32_t *plen,
+                                  const float *vbar, const float *sink, const float *A, float *S_out,
+                                  cudaStream_t s) {
+  const int bytes = ChunkSmem<VAR, DV>::FLOATS * 4;
+  auto kern = prefill_chunk_kernel<VAR, DV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  kern<<<n_heads, 256, bytes, s>>>(w, head0, plen, vbar, sink, A, S_out);
+  return cudaGetLastError();
+}
+
 extern "C" int seed_synth_dense_prefill(const seed_synth_workload *w, int64_t head0, int32_t n_heads,
                                         const int32_t *prompt_len, const float *vbar,
                                         const float *sink_scale, const float *A, float *S_out,
@@ -366,4 +654,44 @@ extern "C" int seed_synth_dense_prefill(const seed_synth_workload *w, int64_t he
       break;
   }
   return cuda_status(cudaGetLastError());
+}
+
+extern "C" int seed_synth_dense_prefill_chunked(const seed_synth_workload *w, int64_t head0, int32_t n_heads,
+                                                const int32_t *prompt_len, const float *vbar,
+                                                const float *sink_scale, const float *A, float *S_out,
+                                                seed_stream_t stream) {
+  // The delta-rule chunks divide by cumulative gate products; where the smallest
+  // gate raised to the chunk length could leave fp32's normal range, the
+  // token-serial kernel (the same result) runs instead.
+  if (w && w->variant != SEED_MAMBA2) {
+    const int clen = w->variant == SEED_KDA ? chunk_len<SEED_KDA>() : chunk_len<SEED_GDN>();
+    if (!(w->alpha_lo > 0.f) || (double)clen * log2((double)w->alpha_lo) < -96.0)
+      return seed_synth_dense_prefill(w, head0, n_heads, prompt_len, vbar, sink_scale, A, S_out, stream);
+  }
+  const int c = check_workload(w);
+  if (c) return c;
+  if (n_heads < 0 || head0 < 0) return SEED_ERR_INVALID_ARG;
+  if (n_heads == 0) return SEED_OK;
+  if (!prompt_len || !vbar || !sink_scale || !S_out) return SEED_ERR_INVALID_ARG;
+  if (w->variant == SEED_MAMBA2 && !A) return SEED_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(S_out) % 16 || reinterpret_cast<uintptr_t>(vbar) % 16)
+    return SEED_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool d64 = w->d_v == 64;
+  cudaError_t e;
+  switch (w->variant) {
+    case SEED_GDN:
+      e = d64 ? launch_chunk_t<SEED_GDN, 64>(*w, head0, n_heads, prompt_len, vbar, sink_scale, A, S_out, s)
+              : launch_chunk_t<SEED_GDN, 128>(*w, head0, n_heads, prompt_len, vbar, sink_scale, A, S_out, s);
+      break;
+    case SEED_KDA:
+      e = d64 ? launch_chunk_t<SEED_KDA, 64>(*w, head0, n_heads, prompt_len, vbar, sink_scale, A, S_out, s)
+              : launch_chunk_t<SEED_KDA, 128>(*w, head0, n_heads, prompt_len, vbar, sink_scale, A, S_out, s);
+      break;
+    default:
+      e = d64 ? launch_chunk_t<SEED_MAMBA2, 64>(*w, head0, n_heads, prompt_len, vbar, sink_scale, A, S_out, s)
+              : launch_chunk_t<SEED_MAMBA2, 128>(*w, head0, n_heads, prompt_len, vbar, sink_scale, A, S_out, s);
+      break;
+  }
+  return cuda_status(e);
 }

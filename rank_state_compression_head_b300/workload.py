@@ -13,7 +13,8 @@ import torch
 
 from . import (SEED_MAMBA2, VARIANTS, seed_compress_dense, seed_decode_step, seed_dense_decode_step,
                seed_recompress_ex, seed_recompress_workspace_bytes, seed_recompress_ws, seed_synth_constants,
-               seed_synth_dense_prefill, seed_synth_step_inputs)
+               seed_synth_dense_prefill, seed_synth_dense_prefill_chunked,
+               seed_synth_step_inputs)
 from .state import FactoredStateBuffers, synth_workload_struct
 
 PHASE_DECODE = 2
@@ -71,12 +72,18 @@ class DeviceRun:
             self.ws = torch.empty(self.ws_bytes, device=self.dev, dtype=torch.uint8)
 
     # -- setup ------------------------------------------------------------------
-    def prefill(self, head0: int = 0, n: Optional[int] = None, out: Optional[torch.Tensor] = None):
-        """Dense fp32 prefill of heads [head0, head0+n) into ``out`` (allocated if None)."""
+    def prefill(self, head0: int = 0, n: Optional[int] = None, out: Optional[torch.Tensor] = None,
+                chunked: bool = True):
+        """Dense fp32 prefill of heads [head0, head0+n) into ``out`` (allocated if None).
+
+        ``chunked`` selects the chunkwise kernel (a chunk of tokens per pass);
+        otherwise the token-serial one.  Both give the recurrence's state.
+        """
         n = self.H - head0 if n is None else n
         if out is None:
             out = torch.empty(n, self.w.d_k, self.w.d_v, device=self.dev, dtype=torch.float32)
-        seed_synth_dense_prefill(self.wst, head0, n, self.plen, self.vbar, self.sink, self.A, out)
+        fn = seed_synth_dense_prefill_chunked if chunked else seed_synth_dense_prefill
+        fn(self.wst, head0, n, self.plen, self.vbar, self.sink, self.A, out)
         return out
 
     def compress(self, S: torch.Tensor, trunc_err: Optional[torch.Tensor] = None):
