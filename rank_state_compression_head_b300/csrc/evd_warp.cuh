@@ -121,10 +121,8 @@ __device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw) {
     }
     __syncwarp(full);
   }
-  // columns in registers up to 48 (four 48-float arrays per lane fit); the
-  // shared-memory rounds above that
-  if constexpr (MR <= 48) return jacobi_warp_reg<MR, HW>(m, tol, tol_stop, sw);
-  else return jacobi_warp<MR, HW>(m, tol, tol_stop, sw);
+  // the columns in registers (three MR-float arrays a lane)
+  return jacobi_warp_reg<MR, HW>(m, tol, tol_stop, sw);
 }
 
 }  // namespace seedk

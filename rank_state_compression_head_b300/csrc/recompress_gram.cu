@@ -29,9 +29,10 @@
 // keep the QR route.
 //
 //   gram_phase     one CTA per head: both factors into shared memory (cp.async),
-//                  G_w on mma.sync, Cholesky by one warp, B = U diag(c) R_b^T on
-//                  mma.sync (KDA: rows times D), M = B^T B in fp32 4 x 4 blocks;
-//                  M and R_b to the workspace
+//                  G_w on mma.sync, Cholesky by one warp in registers,
+//                  B = U diag(c) R_b^T on mma.sync (KDA: rows times D), stored
+//                  over the tiles, M = B^T B in fp32 4 x 4 blocks; M and R_b to
+//                  the workspace
 //   evd_phase      one lane group per head: eigenvectors of M (evd_warp.cuh),
 //                  truncation error, the kept Y to the workspace
 //   gram_rebuild   one CTA per (head, factor): Z = diag(c) R_b^T Y_r (U) or
@@ -40,7 +41,10 @@
 //                  KDA's row scale applied to U', lazy scales reset
 //
 // Workspace per head (fp32): M [m][m], R_b [m][m] (upper, row-major), Y [r][m4]
-// (m4 = m rounded up to 4), each region on 16 bytes, the whole on 256 bytes.
+// (m4 = m rounded up to 4), eight words of class lists, each region on 16 bytes,
+// the whole on 256 bytes.  With ragged ranks a chunk's heads are first listed by
+// 16-column class (gram_classify), and each class's three launches run over its
+// list, so that every lane group of an evd_phase CTA has a head of the class.
 #include "evd_warp.cuh"
 
 #include <type_traits>
@@ -52,8 +56,11 @@ namespace seedk {
 constexpr float kCholFloor = 1e-6f;
 constexpr int kGramThreads = 128;
 
+// Per-head slot (floats): M, R_b, Y, then eight words of the class lists: word c
+// of slot i names the i-th head (slot) of column class c in this chunk, and words
+// 4..7 of slot 0 hold the four class counts.
 struct GramLayout {
-  int64_t mq, rb, y, per_head;  // offsets and stride in floats
+  int64_t mq, rb, y, lst, per_head;  // offsets and stride in floats
   int m4;
   __host__ __device__ GramLayout(int m, int r) {
     m4 = (m + 3) & ~3;
@@ -61,8 +68,8 @@ struct GramLayout {
     mq = 0;
     rb = mq + mm4;
     y = rb + mm4;
-    per_head = (y + (int64_t)r * m4 + 63) & ~(int64_t)63;
-    if (per_head == 0) per_head = 64;
+    lst = y + (int64_t)r * m4;
+    per_head = (lst + 8 + 63) & ~(int64_t)63;
   }
 };
 
@@ -76,6 +83,7 @@ struct GramArgs {
   int layout_m, r_max;
   float *trunc_err;
   int32_t *sweeps;
+  int cls;          // column class of this launch (its heads from the class list), or -1: every slot
 };
 
 __device__ inline bool gram_head(const GramArgs &p, int h, int &r, int &m) {
@@ -84,6 +92,63 @@ __device__ inline bool gram_head(const GramArgs &p, int h, int &r, int &m) {
   return r >= 0 && r <= p.r_max && m <= p.layout_m;
 }
 __device__ inline bool gram_in_class(const GramArgs &p, int m) { return m > p.m_lo && m <= p.m_max; }
+
+// The workspace slot (= head - head0) that item i of this launch serves, from the
+// class list when the launch has one.  False past the end.
+__device__ inline bool gram_slot(const GramArgs &p, int i, int &b) {
+  if (p.cls < 0) {
+    b = i;
+    return i < p.n_group;
+  }
+  const GramLayout L(p.layout_m, p.r_max);
+  if (i >= reinterpret_cast<const int *>(p.ws + L.lst)[4 + p.cls]) return false;
+  b = reinterpret_cast<const int *>(p.ws + (int64_t)i * L.per_head + L.lst)[p.cls];
+  return true;
+}
+
+// Class lists of one chunk, in slot order: column class c holds the heads with
+// 16c < m <= 16c + 16 (class 0 also those with no columns).  One CTA: per pass of
+// 1024 slots a ballot per class, warp offsets scanned in shared memory.  A head
+// whose rank disagrees with the state's r_max goes in no list and is reported.
+__global__ void __launch_bounds__(1024) gram_classify(const GramArgs p, int n_cls) {
+  __shared__ int woff[32][4];
+  __shared__ int base[4];
+  const GramLayout L(p.layout_m, p.r_max);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid < 4) base[tid] = 0;
+  for (int i0 = 0; i0 < p.n_group; i0 += 1024) {
+    const int b = i0 + tid;
+    int c = -1;
+    if (b < p.n_group) {
+      int r, m;
+      const int h = p.head0 + b;
+      if (gram_head(p, h, r, m)) c = m <= 16 ? 0 : (m - 1) / 16;
+      else if (p.sv.status) p.sv.status[h] = SEED_ERR_INVALID_ARG;
+      if (c >= n_cls) c = -1;
+    }
+    unsigned bal[4];
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) bal[cc] = __ballot_sync(0xffffffffu, c == cc);
+    if (lane < 4) woff[warp][lane] = __popc(bal[lane]);
+    __syncthreads();
+    if (tid < 4) {
+      int acc = base[tid];
+      for (int w = 0; w < 32; ++w) {
+        const int t = woff[w][tid];
+        woff[w][tid] = acc;
+        acc += t;
+      }
+      base[tid] = acc;
+    }
+    __syncthreads();
+    if (c >= 0) {
+      const int pos = woff[warp][c] + __popc(bal[c] & ((1u << lane) - 1u));
+      reinterpret_cast<int *>(p.ws + (int64_t)pos * L.per_head + L.lst)[c] = b;
+    }
+    __syncthreads();
+  }
+  if (tid < 4) reinterpret_cast<int *>(p.ws + L.lst)[4 + tid] = base[tid];
+}
 
 // ---- tensor-core helpers (mma.sync m16n8k16, bf16/fp16 in, fp32 accumulate) --------------
 __device__ static inline void g_cp_async16(void *dst, const void *src) {
@@ -139,9 +204,9 @@ __device__ inline void scale_z_rows(float *Zt, int zp, int rows, int cols, float
 
 // Shared layout of gram_phase (bytes): both factor tiles (column j of the factor
 // in row j, rows padded by 16 bytes so that ldmatrix hits distinct banks; the W
-// tile's space is reused for Z once G_w is formed), G_w / R_b (row i at i * GP
-// floats; GP odd: row-per-thread access is conflict-free), B = U_eff R_b^T
-// (row i at i * BP floats), the scales, the original diagonal of G_w.
+// tile's space is reused for Z once G_w is formed), B = U_eff R_b^T over both
+// tiles once they have been read (row i at i * BP floats), G_w / R_b (row i at
+// i * GP floats), the scales, the original diagonal of G_w.
 template <int DV, int MR>
 struct GramSmem {
   static constexpr int USTR = kDK * 2 + 16, WSTR = DV * 2 + 16;
@@ -151,14 +216,70 @@ struct GramSmem {
   static constexpr int WZ_BYTES = MR * WSTR > MR * ZP * 4 ? MR * WSTR : MR * ZP * 4;
   static constexpr int U_OFF = 0;
   static constexpr int W_OFF = U_OFF + MR * USTR;  // W tile, then Z
-  static constexpr int G_OFF = W_OFF + WZ_BYTES;
-  static constexpr int B_OFF = G_OFF + ((MR * GP * 4 + 15) & ~15);
-  static constexpr int SC_OFF = B_OFF + kDK * BP * 4;
+  static constexpr int TILE_BYTES = W_OFF + WZ_BYTES;
+  static constexpr int B_OFF = 0;                  // B, over both tiles
+  static constexpr int B_BYTES = kDK * BP * 4;
+  static constexpr int G_OFF = ((TILE_BYTES > B_BYTES ? TILE_BYTES : B_BYTES) + 15) & ~15;
+  static constexpr int SC_OFF = G_OFF + ((MR * GP * 4 + 15) & ~15);
   static constexpr int DG_OFF = SC_OFF + (MR > kDK ? MR : kDK) * 4;
-  static constexpr int RR_OFF = DG_OFF + MR * 4;  // row j of R_b, two buffers
-  static constexpr int ZS_OFF = RR_OFF + 2 * MR * 4;  // per-column unscale of Z (fp16)
+  static constexpr int ZS_OFF = DG_OFF + MR * 4;  // per-column unscale of Z (fp16)
   static constexpr int BYTES = ZS_OFF + MR * 4;
 };
+
+// Cholesky G_w = R_b^T R_b by one warp, the matrix in registers: lane l owns
+// columns l and l + 32 of the upper triangle (column c needs rows 0..c only, so
+// the first column's array stops at 32).  Step j: the pivot's lane hands round
+// the current G[j][j]; every lane forms its entries of row j of R_b (R[j][c] =
+// G[j][c] / r_jj, r_jj on the diagonal) and writes them over G_w's row j in
+// shared memory; then row j is handed round entry by entry and each lane takes
+// R[j][i] R[j][c] off its rows i > j.  A pivot below kCholFloor of its column's
+// squared norm means the column lies in the span of the earlier ones to within
+// the resolution of the Gram matrix: its row of R_b is dropped (zero) and the
+// column is represented by its projections.  G_w in Gw (row i at i * GP); row j
+// of R_b replaces row j of G_w (entries c >= j; below the diagonal untouched),
+// dg gets the original diagonal.
+template <int MR>
+__device__ inline void chol_warp(float *Gw, float *dg, int m) {
+  constexpr int GP = MR + 1;
+  constexpr bool TWO = MR > 32;
+  constexpr int NA = MR < 32 ? MR : 32;
+  const int lane = threadIdx.x & 31;
+  const int c0 = lane, c1 = lane + 32;
+  float gA[NA], gB[TWO ? MR : 1];
+#pragma unroll
+  for (int i = 0; i < NA; ++i) gA[i] = c0 < MR ? Gw[i * GP + c0] : 0.f;
+  if constexpr (TWO) {
+#pragma unroll
+    for (int i = 0; i < MR; ++i) gB[i] = c1 < MR ? Gw[i * GP + c1] : 0.f;
+  }
+  if (c0 < m) dg[c0] = Gw[c0 * GP + c0];
+  if (TWO && c1 < m) dg[c1] = Gw[c1 * GP + c1];
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < MR; ++j) {
+    if (j < m) {
+      float own;  // my column's entry in row j (pivot lane: the diagonal)
+      if constexpr (TWO) own = j < 32 ? gA[j < NA ? j : 0] : gB[j];
+      else own = gA[j < NA ? j : 0];
+      const float d = __shfl_sync(0xffffffffu, own, j & 31);
+      const float rjj = d > kCholFloor * dg[j] ? sqrtf(d) : 0.f;
+      const float inv = rjj > 0.f ? 1.f / rjj : 0.f;
+      const float rA = j < NA && c0 > j ? gA[j < NA ? j : 0] * inv : (c0 == j ? rjj : 0.f);
+      float rB = 0.f;
+      if constexpr (TWO) rB = c1 > j ? gB[j] * inv : (c1 == j ? rjj : 0.f);
+      if (c0 >= j && c0 < m) Gw[j * GP + c0] = rA;
+      if (TWO && c1 >= j && c1 < m) Gw[j * GP + c1] = rB;
+#pragma unroll
+      for (int i = j + 1; i < MR; ++i) {
+        if (i < m) {
+          const float ri = __shfl_sync(0xffffffffu, i < 32 ? rA : rB, i & 31);
+          if (i < NA) gA[i < NA ? i : 0] = fmaf(-ri, rA, gA[i < NA ? i : 0]);
+          if constexpr (TWO) gB[i] = fmaf(-ri, rB, gB[i]);
+        }
+      }
+    }
+  }
+}
 
 // G[i0..i0+15][j0..j0+7] += F^T F over `depth` rows of the tiles, F column j in
 // smem row j (stride STR bytes): exact products of the stored 16-bit values,
@@ -201,14 +322,20 @@ __device__ inline void tile_times_z(uint32_t tile, const float *Zt, int i0, int 
 }
 
 // ---- phase 1: G_w, its Cholesky, B = U_eff R_b^T, M = B^T B ---------------------------------
+// Resident CTAs to plan registers for (shared memory allows about this many).
+template <int MR>
+constexpr int gram_min_blocks() { return MR <= 16 ? 8 : MR <= 32 ? 6 : MR <= 48 ? 5 : 4; }
+
 template <typename TF, int VAR, int DV, int MR>
-__global__ void __launch_bounds__(kGramThreads) gram_phase(const GramArgs p) {
+__global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phase(const GramArgs p) {
   constexpr int DK = kDK;
   using L = GramSmem<DV, MR>;
   constexpr int GP = L::GP, ZP = L::ZP, BP = L::BP;
   constexpr bool KDA = VAR == SEED_KDA;
   extern __shared__ __align__(128) unsigned char smem[];
-  const int h = p.head0 + blockIdx.x;
+  int slot;
+  if (!gram_slot(p, blockIdx.x, slot)) return;
+  const int h = p.head0 + slot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const StateView &sv = p.sv;
@@ -221,7 +348,6 @@ __global__ void __launch_bounds__(kGramThreads) gram_phase(const GramArgs p) {
   float *B = reinterpret_cast<float *>(smem + L::B_OFF);
   float *sc = reinterpret_cast<float *>(smem + L::SC_OFF);
   float *dg = reinterpret_cast<float *>(smem + L::DG_OFF);
-  float *rrow = reinterpret_cast<float *>(smem + L::RR_OFF);
   float *zsc = reinterpret_cast<float *>(smem + L::ZS_OFF);
 
   // ---- factors into shared memory, padding columns zero ---------------------------------
@@ -264,49 +390,8 @@ __global__ void __launch_bounds__(kGramThreads) gram_phase(const GramArgs p) {
   }
   __syncthreads();
 
-  // ---- Cholesky G_w = R_b^T R_b (upper, in place) by warps 0-1 (warp 0 up to 32 columns) -----------
-  // Thread l owns column l of the upper triangle (entries at i * GP + l: threads of
-  // one row touch consecutive words).  Step j: every owner of a column l >= j reads
-  // the pivot, forms R_b[j][l] and publishes it in rrow (double-buffered by step
-  // parity); after the barrier each owner of l > j updates its entries i in (j, l].
-  // A pivot below kCholFloor of its column's squared norm means the column lies in
-  // the span of the earlier ones to within the resolution of the Gram matrix: its
-  // row of R_b is dropped (zero), the column is represented by its projections.
-  constexpr int NCH = MR <= 32 ? 32 : 64;  // column owners: one warp or two
-  if (tid < NCH) {
-    const int l = tid;
-    const bool own = l < m;
-    if (own) dg[l] = Gw[l * GP + l];
-    for (int j = 0; j < m; ++j) {
-      team_sync(2, NCH);  // step j-1's updates (and the diagonal) are visible
-      float rl = 0.f;
-      if (own && l >= j) {
-        const float d = Gw[j * GP + j], g0 = dg[j];
-        const float rjj = d > kCholFloor * g0 ? sqrtf(d) : 0.f;
-        const float inv = rjj > 0.f ? 1.f / rjj : 0.f;
-        rl = l == j ? rjj : Gw[j * GP + l] * inv;
-        rrow[(j & 1) * MR + l] = rl;
-      }
-      team_sync(2, NCH);  // row j of R_b is published
-      if (own && l > j) {
-        Gw[j * GP + l] = rl;
-        const float *rr = rrow + (j & 1) * MR;
-        int i = j + 1;
-        for (; i + 3 <= l; i += 4) {
-          const float r0 = rr[i], r1 = rr[i + 1], r2 = rr[i + 2], r3 = rr[i + 3];
-          const float g0 = Gw[i * GP + l], g1 = Gw[(i + 1) * GP + l], g2 = Gw[(i + 2) * GP + l],
-                      g3 = Gw[(i + 3) * GP + l];
-          Gw[i * GP + l] = fmaf(-r0, rl, g0);
-          Gw[(i + 1) * GP + l] = fmaf(-r1, rl, g1);
-          Gw[(i + 2) * GP + l] = fmaf(-r2, rl, g2);
-          Gw[(i + 3) * GP + l] = fmaf(-r3, rl, g3);
-        }
-        for (; i <= l; ++i) Gw[i * GP + l] = fmaf(-rr[i], rl, Gw[i * GP + l]);
-      } else if (own && l == j) {
-        Gw[j * GP + j] = rl;
-      }
-    }
-  }
+  // ---- Cholesky G_w = R_b^T R_b (upper, in place) by warp 0 --------------------------------------
+  if (warp == 0) chol_warp<MR>(Gw, dg, m);
   __syncthreads();
 
   // ---- Z = diag(c) R_b^T (Z[l][j] = c_l R_b[j][l]), stored by rows of Z^T --------------------------
@@ -322,18 +407,34 @@ __global__ void __launch_bounds__(kGramThreads) gram_phase(const GramArgs p) {
   __syncthreads();
 
   // ---- B = U Z (U_eff = U diag(c)), or diag(D) (U R_b^T) for KDA, on the tensor cores -----------
+  // (held in registers until every warp has read both tiles, then stored over them)
   {
+    constexpr int NW = kGramThreads / 32, NT = (DK / 16) * (MR / 8) / NW;
     const int ntile = m16 / 8, per = (DK / 16) * ntile;
     const uint32_t ub = smem_u32(smem + L::U_OFF);
-    for (int task = warp; task < per; task += kGramThreads / 32) {
-      const int i0 = (task / ntile) * 16, n0 = (task % ntile) * 8;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      tile_times_z<TF, L::USTR, ZP>(ub, Zt, i0, n0, m16, d);
+    float bacc[NT][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = i0 + g + (e >> 1) * 8, n = n0 + 2 * t + (e & 1);
-        const float v = d[e] * zsc[n];
-        B[i * BP + n] = KDA ? v * sc[i] : v;
+    for (int q = 0; q < NT; ++q) {
+      const int task = warp + q * NW;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) bacc[q][e] = 0.f;
+      if (task < per) {
+        const int i0 = (task / ntile) * 16, n0 = (task % ntile) * 8;
+        tile_times_z<TF, L::USTR, ZP>(ub, Zt, i0, n0, m16, bacc[q]);
+      }
+    }
+    __syncthreads();  // both tiles are read
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+      const int task = warp + q * NW;
+      if (task < per) {
+        const int i0 = (task / ntile) * 16, n0 = (task % ntile) * 8;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = i0 + g + (e >> 1) * 8, n = n0 + 2 * t + (e & 1);
+          const float v = bacc[q][e] * zsc[n];
+          B[i * BP + n] = KDA ? v * sc[i] : v;
+        }
       }
     }
   }
@@ -341,7 +442,7 @@ __global__ void __launch_bounds__(kGramThreads) gram_phase(const GramArgs p) {
 
   // ---- M = B^T B in fp32 (4 x 4 blocks of the upper triangle), M and R_b to the workspace -----
   const GramLayout W(p.layout_m, p.r_max);
-  float *ws = p.ws + (int64_t)blockIdx.x * W.per_head;
+  float *ws = p.ws + (int64_t)slot * W.per_head;
   {
     const int nb = (m + 3) / 4, nblk = nb * (nb + 1) / 2;
     for (int blk = tid; blk < nblk; blk += kGramThreads) {
@@ -382,10 +483,10 @@ constexpr int evd_group() { return MR <= 32 ? 16 : 32; }
 template <int MR>
 constexpr int evd_heads_per_cta() { return kSvdWarps * (32 / evd_group<MR>()); }
 
-// Resident CTAs to plan registers for: the register Jacobi (MR <= 48) holds four
-// MR-float arrays per lane, so its larger cores get fewer, fatter lanes.
+// Resident CTAs to plan registers for: the register Jacobi holds three MR-float
+// arrays per lane, so the larger cores get fewer, fatter lanes.
 template <int MR>
-constexpr int evd_min_blocks() { return MR <= 16 ? 8 : MR <= 32 ? 6 : MR <= 48 ? 4 : 6; }
+constexpr int evd_min_blocks() { return MR <= 16 ? 8 : MR <= 32 ? 5 : MR <= 48 ? 5 : 4; }
 
 template <int MR>
 __global__ void __launch_bounds__(32 * kSvdWarps, evd_min_blocks<MR>()) evd_phase(const GramArgs p) {
@@ -394,8 +495,8 @@ __global__ void __launch_bounds__(32 * kSvdWarps, evd_min_blocks<MR>()) evd_phas
   extern __shared__ __align__(16) float smem_f[];
   const int grp = threadIdx.x / HW, lane = threadIdx.x & (HW - 1);
   const unsigned gmask = HW == 32 ? 0xffffffffu : 0xffffu << (threadIdx.x & 16);
-  const int b = blockIdx.x * evd_heads_per_cta<MR>() + grp;
-  if (b >= p.n_group) return;
+  int b;
+  if (!gram_slot(p, blockIdx.x * evd_heads_per_cta<MR>() + grp, b)) return;
   const int h = p.head0 + b;
   const StateView &sv = p.sv;
   int r, m;
@@ -460,11 +561,12 @@ struct RebuildSmem {
   static constexpr int YP = MR + 4;             // Y^T row pitch: row j holds y_n[j] for every n
   static constexpr int ZP = MR + 2;             // Z row pitch (floats): row n = column n of Z;
                                                 // 2 mod 4 keeps both access patterns at 2-way
-  static constexpr int T_OFF = 0;               // factor tile, then the output tile
-  static constexpr int O_OFF = T_OFF + MR * STR;
-  static constexpr int R_OFF = O_OFF + MR * STR;
+  static constexpr int T_OFF = 0;               // factor tile
+  static constexpr int R_OFF = T_OFF + MR * STR;
   static constexpr int Y_OFF = R_OFF + MR * RP * 4;
-  static constexpr int Z_OFF = Y_OFF + MR * YP * 4;
+  static constexpr int O_OFF = R_OFF;           // the output tile, over R_b and Y once Z is formed
+  static constexpr int RY_BYTES = MR * STR > MR * (RP + YP) * 4 ? MR * STR : MR * (RP + YP) * 4;
+  static constexpr int Z_OFF = R_OFF + RY_BYTES;
   static constexpr int S_OFF = Z_OFF + MR * ZP * 4;  // scales c [MR] or D [DK]
   static constexpr int ZS_OFF = S_OFF + (MR > kDK ? MR : kDK) * 4;  // per-column unscale of Z
   static constexpr int BYTES = ZS_OFF + MR * 4;
@@ -477,7 +579,9 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
   constexpr int RP = L::RP, YP = L::YP, ZP = L::ZP;
   constexpr bool KDA = VAR == SEED_KDA;
   extern __shared__ __align__(128) unsigned char smem[];
-  const int h = p.head0 + blockIdx.x;
+  int slot;
+  if (!gram_slot(p, blockIdx.x, slot)) return;
+  const int h = p.head0 + slot;
   const bool isU = blockIdx.y == 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const StateView &sv = p.sv;
@@ -494,7 +598,7 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
   const int m16 = (m + 15) & ~15, rk8 = (rk + 7) & ~7;
   const int64_t c0 = sv.col0(h);
   const GramLayout W(p.layout_m, p.r_max);
-  const float *ws = p.ws + (int64_t)blockIdx.x * W.per_head;
+  const float *ws = p.ws + (int64_t)slot * W.per_head;
   float *Rb = reinterpret_cast<float *>(smem + L::R_OFF);
   float *Yt = reinterpret_cast<float *>(smem + L::Y_OFF);   // y_n[j] at j * YP + n
   float *Z = reinterpret_cast<float *>(smem + L::Z_OFF);    // [rk8][ZP]: z_n[j] at n * ZP + j
@@ -629,7 +733,7 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
 }
 
 template <typename TF, int VAR, int DV, int MR>
-static cudaError_t launch_gram_t(GramArgs a, int n_heads, int64_t chunk, cudaStream_t s) {
+static cudaError_t launch_gram_t(const GramArgs &a, cudaStream_t s) {
   using L1 = GramSmem<DV, MR>;
   using L3 = RebuildSmem<DV, MR>;
   const int evd_bytes = evd_heads_per_cta<MR>() * SvdWarpSmem<MR>::FLOATS * 4;
@@ -640,53 +744,59 @@ static cudaError_t launch_gram_t(GramArgs a, int n_heads, int64_t chunk, cudaStr
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, evd_bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, L3::BYTES);
   if (e != cudaSuccess) return e;
-  for (int64_t h0 = 0; h0 < n_heads; h0 += chunk) {
-    const int n = (int)(n_heads - h0 < chunk ? n_heads - h0 : chunk);
-    a.head0 = (int)h0;
-    a.n_group = n;
-    k1<<<n, kGramThreads, L1::BYTES, s>>>(a);
-    k2<<<(n + evd_heads_per_cta<MR>() - 1) / evd_heads_per_cta<MR>(), 32 * kSvdWarps, evd_bytes, s>>>(a);
-    k3<<<dim3(n, 2), kGramThreads, L3::BYTES, s>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  const int n = a.n_group;  // the class's heads are a prefix of its list; the rest leave at once
+  k1<<<n, kGramThreads, L1::BYTES, s>>>(a);
+  k2<<<(n + evd_heads_per_cta<MR>() - 1) / evd_heads_per_cta<MR>(), 32 * kSvdWarps, evd_bytes, s>>>(a);
+  k3<<<dim3(n, 2), kGramThreads, L3::BYTES, s>>>(a);
+  return cudaGetLastError();
 }
 
 template <typename TF, int VAR, int DV>
-static cudaError_t launch_gram_m(const GramArgs &a, int n, int64_t chunk, cudaStream_t s) {
-  if (a.m_max <= 16) return launch_gram_t<TF, VAR, DV, 16>(a, n, chunk, s);
-  if (a.m_max <= 32) return launch_gram_t<TF, VAR, DV, 32>(a, n, chunk, s);
-  if (a.m_max <= 48) return launch_gram_t<TF, VAR, DV, 48>(a, n, chunk, s);
-  return launch_gram_t<TF, VAR, DV, 64>(a, n, chunk, s);
+static cudaError_t launch_gram_m(const GramArgs &a, cudaStream_t s) {
+  if (a.m_max <= 16) return launch_gram_t<TF, VAR, DV, 16>(a, s);
+  if (a.m_max <= 32) return launch_gram_t<TF, VAR, DV, 32>(a, s);
+  if (a.m_max <= 48) return launch_gram_t<TF, VAR, DV, 48>(a, s);
+  return launch_gram_t<TF, VAR, DV, 64>(a, s);
 }
 
 template <typename TF, int DV>
-static cudaError_t launch_gram_v(const GramArgs &a, int n, int64_t chunk, cudaStream_t s) {
+static cudaError_t launch_gram_v(const GramArgs &a, cudaStream_t s) {
   // Only the scale layout differs between variants here.
-  if (a.sv.variant == SEED_KDA) return launch_gram_m<TF, SEED_KDA, DV>(a, n, chunk, s);
-  return launch_gram_m<TF, SEED_GDN, DV>(a, n, chunk, s);
+  if (a.sv.variant == SEED_KDA) return launch_gram_m<TF, SEED_KDA, DV>(a, s);
+  return launch_gram_m<TF, SEED_GDN, DV>(a, s);
 }
 
 cudaError_t launch_recompress_gram(const StateView &sv, int factor_dtype, float *trunc_err, int32_t *sweeps,
                                    int m_max, int r_max, float *ws, int64_t chunk, cudaStream_t s) {
-  GramArgs a{sv, ws, 0, 0, m_max, -1, m_max, r_max, trunc_err, sweeps};
+  GramArgs a{sv, ws, 0, 0, m_max, -1, m_max, r_max, trunc_err, sweeps, -1};
   const int n = sv.n_heads;
   auto one = [&](const GramArgs &x) {
     if (factor_dtype == SEED_F16)
-      return sv.d_v == 64 ? launch_gram_v<__half, 64>(x, n, chunk, s) : launch_gram_v<__half, 128>(x, n, chunk, s);
-    return sv.d_v == 64 ? launch_gram_v<__nv_bfloat16, 64>(x, n, chunk, s)
-                        : launch_gram_v<__nv_bfloat16, 128>(x, n, chunk, s);
+      return sv.d_v == 64 ? launch_gram_v<__half, 64>(x, s) : launch_gram_v<__half, 128>(x, s);
+    return sv.d_v == 64 ? launch_gram_v<__nv_bfloat16, 64>(x, s) : launch_gram_v<__nv_bfloat16, 128>(x, s);
   };
-  if (!sv.rank || m_max <= 16) return one(a);
-  // Ragged ranks: one launch per 16-column class, each sized for its class; heads of
-  // other classes leave at once.
-  for (int hi = 16; hi - 16 < m_max; hi += 16) {
-    GramArgs c = a;
-    c.m_max = hi < m_max ? hi : m_max;
-    c.m_lo = hi == 16 ? -1 : hi - 16;  // the first class also takes heads with no columns
-    const cudaError_t e = one(c);
-    if (e != cudaSuccess) return e;
+  // Ragged ranks: per chunk, the heads are listed by 16-column class, and each
+  // class gets its own launches, sized for it, over its list.
+  const bool ragged = sv.rank && m_max > 16;
+  const int n_cls = ragged ? (m_max + 15) / 16 : 1;
+  for (int64_t h0 = 0; h0 < n; h0 += chunk) {
+    a.head0 = (int)h0;
+    a.n_group = (int)(n - h0 < chunk ? n - h0 : chunk);
+    if (ragged) {
+      gram_classify<<<1, 1024, 0, s>>>(a, n_cls);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    for (int c = 0; c < n_cls; ++c) {
+      GramArgs x = a;
+      if (ragged) {
+        x.cls = c;
+        x.m_max = 16 * (c + 1) < m_max ? 16 * (c + 1) : m_max;
+        x.m_lo = c == 0 ? -1 : 16 * c;  // the first class also takes heads with no columns
+      }
+      const cudaError_t e = one(x);
+      if (e != cudaSuccess) return e;
+    }
   }
   return cudaSuccess;
 }

@@ -406,7 +406,7 @@ __device__ int jacobi_warp(int m, float tol, float tol_stop, float *sw) {
 }
 
 // ---------------------------------------------------------------------------------------
-// One-sided Jacobi with the columns in registers (cores of at most 48 columns).
+// One-sided Jacobi with the columns in registers.
 //
 // Same rotation rule, tolerance, stopping rule, scaled columns and carried norms as
 // jacobi_warp; only the pair order and where the columns live differ.  Lane i
@@ -416,10 +416,9 @@ __device__ int jacobi_warp(int m, float tol, float tol_stop, float *sw) {
 // positions (2i, 2i+1), both held by lane i; odd rounds pair (2i+1, 2i+2), one
 // column of lane i with one of lane i+1.  An exchange within a lane is only a
 // relabelling (which register holds the left position flips every even round),
-// so columns move between lanes only in odd rounds: each lane receives its two
-// partners' columns by neighbour shuffles, computes both rotations (both lanes of a
-// pair compute the same one, bit for bit, from the same values) and keeps the
-// rotated partner column that lands on its own position.
+// so columns move between lanes only in odd rounds, where the left lane of a
+// pair decides the rotation and both build the rotated column that lands on
+// their own position (jac_round_pair).
 // ---------------------------------------------------------------------------------------
 
 struct JacCol {     // metadata of a column held in registers
@@ -466,12 +465,20 @@ __device__ inline float jac_dot(const float (&x)[MR], const float (&y)[MR]) {
 }
 
 // One even round (the lane's own pair) and one odd round (pairs with the
-// neighbours).  RIGHT_A: after the even round the right-facing column is A.  Both
-// pairs of the odd round are decided before either is applied, so that their
-// dependent chains overlap; a rotation not taken has identity coefficients.
+// neighbours).  RIGHT_A: after the even round the right-facing column is A.
+//
+// Odd round, pair (x = my right-facing column, y = the right neighbour's
+// left-facing one): I receive y into Y and decide the rotation; the neighbour
+// receives my decision (ta, c, tg, whether it rotated) and x's metadata by
+// shuffles instead of deciding it again, then each side builds the rotated column
+// that lands on its own position from the other's old column (y' = y + tb x stays
+// on my right, x' = x - ta y goes to the neighbour's left), which needs the old
+// columns to cross once more.  So a lane holds three columns, and the pair's dot
+// product and coefficients are formed once.
 template <int MR, int HW, bool RIGHT_A>
-__device__ inline void jac_round_pair(float (&A)[MR], float (&B)[MR], JacCol &ca, JacCol &cb, bool has_left,
-                                      bool has_right, unsigned full, float tol2, float stop2, int &far) {
+__device__ inline void jac_round_pair(float (&A)[MR], float (&B)[MR], float (&Y)[MR], JacCol &ca, JacCol &cb,
+                                      bool has_left, bool has_right, unsigned full, float tol2, float stop2,
+                                      int &far) {
   // ---- even round ----
   {
     float ta, tb, c, tg;
@@ -493,36 +500,40 @@ __device__ inline void jac_round_pair(float (&A)[MR], float (&B)[MR], JacCol &ca
   float (&Xl)[MR] = RIGHT_A ? B : A;   // my left-facing column
   JacCol &cxr = RIGHT_A ? ca : cb;
   JacCol &cxl = RIGHT_A ? cb : ca;
-  float R[MR], Lf[MR];
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int k = 0; k < MR; ++k) {
-    R[k] = __shfl_down_sync(full, Xl[k], 1, HW);   // right neighbour's left-facing column
-    Lf[k] = __shfl_up_sync(full, Xr[k], 1, HW);    // left neighbour's right-facing column
+    Y[k] = __shfl_down_sync(full, Xl[k], 1, HW);   // right neighbour's left-facing column
+    s[k & 3] = fmaf(Xr[k], Y[k], s[k & 3]);
   }
-  JacCol cr, cl;
+  JacCol cr;
   cr.d = __shfl_down_sync(full, cxl.d, 1, HW);
   cr.n2 = __shfl_down_sync(full, cxl.n2, 1, HW);
+  float ta1, tb1, c1, tg1;
+  int far1 = 0;
+  const bool rot1 = jac_rotation((s[0] + s[1]) + (s[2] + s[3]), cxr, cr, tol2, stop2, ta1, tb1, c1, tg1, far1);
+  far |= has_right && far1;
+  // the left neighbour's decision on the pair (its x, my left-facing y), and its x's metadata
+  const float ta2 = __shfl_up_sync(full, ta1, 1, HW);
+  const float c2 = __shfl_up_sync(full, c1, 1, HW);
+  const float tg2 = __shfl_up_sync(full, tg1, 1, HW);
+  const bool rot2 = __shfl_up_sync(full, (int)rot1, 1, HW) != 0;
+  JacCol cl;
   cl.d = __shfl_up_sync(full, cxr.d, 1, HW);
   cl.n2 = __shfl_up_sync(full, cxr.n2, 1, HW);
-  // pair (my right-facing x, right neighbour's y): I keep y' on my right position;
-  // pair (left neighbour's x, my left-facing y): I keep x' on my left position
-  float ta1, tb1, c1, tg1, ta2, tb2, c2, tg2;
-  int far1 = 0, far2 = 0;
-  const float d1 = jac_dot<MR>(Xr, R), d2 = jac_dot<MR>(Lf, Xl);
-  const bool rot1 = jac_rotation(d1, cxr, cr, tol2, stop2, ta1, tb1, c1, tg1, far1);
-  const bool rot2 = jac_rotation(d2, cl, cxl, tol2, stop2, ta2, tb2, c2, tg2, far2);
-  far |= (has_right && far1) || (has_left && far2);
+#pragma unroll
+  for (int k = 0; k < MR; ++k) {
+    const float lw = __shfl_up_sync(full, Xr[k], 1, HW);   // left neighbour's old right-facing column
+    if (has_right) Xr[k] = fmaf(tb1, Xr[k], Y[k]);
+    if (has_left) Xl[k] = fmaf(-ta2, Xl[k], lw);
+  }
   if (has_right) {
     const float ny = cr.n2 + tg1;
-#pragma unroll
-    for (int k = 0; k < MR; ++k) Xr[k] = fmaf(tb1, Xr[k], R[k]);
     cxr.d = cr.d * c1;
     cxr.n2 = (rot1 && ny < 0.25f * cr.n2) ? jac_norm2<MR>(Xr, cxr.d) : ny;
   }
   if (has_left) {
     const float nx = cl.n2 - tg2;
-#pragma unroll
-    for (int k = 0; k < MR; ++k) Xl[k] = fmaf(-ta2, Xl[k], Lf[k]);
     cxl.d = cl.d * c2;
     cxl.n2 = (rot2 && nx < 0.25f * cl.n2) ? jac_norm2<MR>(Xl, cxl.d) : nx;
   }
@@ -535,7 +546,7 @@ template <int MR, int HW>
 __device__ int jacobi_warp_reg(int m, float tol, float tol_stop, float *sw) {
   using L = SvdWarpSmem<MR>;
   constexpr int TP = L::TP;
-  static_assert(MR % 4 == 0 && MR <= 48, "columns in registers");
+  static_assert(MR % 4 == 0 && MR <= 2 * HW, "two columns a lane, in registers");
   const int lane = threadIdx.x & (HW - 1);
   const unsigned full = HW == 32 ? 0xffffffffu : 0xffffu << (threadIdx.x & 16);
   float *T = sw + L::T_OFF, *sig2 = sw + L::S_OFF, *inv = sw + L::I_OFF;
@@ -545,7 +556,7 @@ __device__ int jacobi_warp_reg(int m, float tol, float tol_stop, float *sw) {
   const bool has_right = lane + 1 < P, has_left = lane > 0 && active;
   const float tol2 = tol * tol, stop2 = tol_stop * tol_stop;
 
-  float A[MR], B[MR];
+  float A[MR], B[MR], Y[MR];
   {
     const float4 *a4 = reinterpret_cast<const float4 *>(T + (2 * lane) * TP);
     const float4 *b4 = reinterpret_cast<const float4 *>(T + (2 * lane + 1) * TP);
@@ -568,8 +579,8 @@ __device__ int jacobi_warp_reg(int m, float tol, float tol_stop, float *sw) {
       // rounds in pairs (even, odd); after an even round at parity 0 the right-facing
       // register is A, at parity 1 it is B: two copies of the pair, fixed at compile time
       for (int rr = 0; rr < P; ++rr) {
-        if ((rr & 1) == 0) jac_round_pair<MR, HW, true>(A, B, ca, cb, has_left, has_right, full, tol2, stop2, far);
-        else jac_round_pair<MR, HW, false>(A, B, ca, cb, has_left, has_right, full, tol2, stop2, far);
+        if ((rr & 1) == 0) jac_round_pair<MR, HW, true>(A, B, Y, ca, cb, has_left, has_right, full, tol2, stop2, far);
+        else jac_round_pair<MR, HW, false>(A, B, Y, ca, cb, has_left, has_right, full, tol2, stop2, far);
       }
       const bool conv = !__any_sync(full, far);
       // fold the scales into the columns: at the end, or once one has shrunk below 2^-20

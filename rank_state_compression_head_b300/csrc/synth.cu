@@ -482,30 +482,43 @@ __global__ void __launch_bounds__(256, 2) prefill_chunk_kernel(const seed_synth_
       for (int t = 0; t < C; ++t) Pp[(q * C + t) * DV + j] = KDA ? acc[t] : acc[t] * Gi[t];
       __syncthreads();
       if (q == 0) {
+        // the triangular solve, one column j per thread, with the chunk's solution in
+        // registers (fully unrolled: row t's sum runs as soon as its terms are ready)
         if (KDA) {
           // x_t = -beta_t (P_t + sum_{r<t} E[t][r] y_r + sum_{r<t} Cm[t][r] x_r), y_r = beta_r v_r;
           // x_t goes into slice 0 of P, y_t into V
+          float x[C], y[C];
+#pragma unroll
           for (int t = 0; t < C; ++t) {
             float p = 0.f;
 #pragma unroll
             for (int qq = 0; qq < NQ; ++qq) p += Pp[(qq * C + t) * DV + j];
-            for (int r = 0; r < t; ++r)
-              p = fmaf(Em[t * (C + 1) + r], Vc[r * DV + j], fmaf(Am[t * (C + 1) + r], Pp[r * DV + j], p));
-            Pp[t * DV + j] = -Bc[t] * p;
-            Vc[t * DV + j] *= Bc[t];
+            y[t] = Bc[t] * Vc[t * DV + j];
+#pragma unroll
+            for (int r = 0; r < t; ++r) p = fmaf(Em[t * (C + 1) + r], y[r], fmaf(Am[t * (C + 1) + r], x[r], p));
+            x[t] = -Bc[t] * p;
+          }
+#pragma unroll
+          for (int t = 0; t < C; ++t) {
+            Pp[t * DV + j] = x[t];
+            Vc[t * DV + j] = y[t];
           }
         } else {
           // u_t = beta_t (v_t - P_t) - sum_{r<t} A[t][r] u_r, then the weight gamma_C / gamma_t
+          float u[C];
+#pragma unroll
           for (int t = 0; t < C; ++t) {
             float p = 0.f;
 #pragma unroll
             for (int qq = 0; qq < NQ; ++qq) p += Pp[(qq * C + t) * DV + j];
-            float u = Bc[t] * (Vc[t * DV + j] - p);
-            for (int r = 0; r < t; ++r) u = fmaf(-Am[t * (C + 1) + r], Vc[r * DV + j], u);
-            Vc[t * DV + j] = u;
+            float acc = Bc[t] * (Vc[t * DV + j] - p);
+#pragma unroll
+            for (int r = 0; r < t; ++r) acc = fmaf(-Am[t * (C + 1) + r], u[r], acc);
+            u[t] = acc;
           }
           const float gC = Gi[C - 1];
-          for (int t = 0; t < C; ++t) Vc[t * DV + j] *= gC / Gi[t];
+#pragma unroll
+          for (int t = 0; t < C; ++t) Vc[t * DV + j] = u[t] * (gC / Gi[t]);
         }
       } else if (KDA) {
         // meanwhile the update weights: gamma_C / gm_r * k_r (into G) and gamma_C / gamma_r * k_r (into K)

@@ -121,8 +121,12 @@ class DeviceRun:
         st = self.state
         m_max = st.r_max + st.growth * self.w.T
         groups = -(-self.H // min(self.H, self.ws_heads))
-        classes = 1 if st.ranks is None or m_max <= 16 else -(-m_max // 16)
-        return 3 * groups * classes
+        if st.ranks is None or m_max <= 16:
+            return 3 * groups
+        classes = -(-m_max // 16)
+        if self.w.factor_dtype == 'f32':
+            return 3 * groups * classes
+        return groups * (1 + 3 * classes)  # a class-list pass, then three launches per class
 
     def step(self, t: int, slot: int = 0, stream=None) -> bool:
         """Decode step t (1-based) with inputs already in ``slot``; recompress when T divides t."""
