@@ -299,25 +299,38 @@ __device__ inline void gram_tile(uint32_t base, int i0, int j0, int depth, float
   }
 }
 
-// D[i0..i0+15][n0..n0+7] = sum_j F[i][j] Z[j][n] for j < depth16, F column j in smem
-// row j of the tile at `tile` (stride STR bytes), Z row n at Zt + n * ZP (fp32, split
-// into three bf16 terms: 24 significant bits, products exact, fp32 accumulation).
-template <typename TF, int STR, int ZP>
-__device__ inline void tile_times_z(uint32_t tile, const float *Zt, int i0, int n0, int depth16,
-                                    float (&d)[4]) {
+// D[r][i][n] += sum_j F[i][j] Z[j][n] for the rows i of tile r (i0 + 16 r .. + 15), the
+// columns n0..n0+7 and j < depth16: F column j in smem row j of the tile at `tile`
+// (stride STR bytes), Z row n at Zt + n * ZP (fp32, split once into three 16-bit terms:
+// 24 significant bits, products exact, fp32 accumulation).
+template <typename TF, int STR, int ZP, int NR, int KMAX>
+__device__ inline void tiles_times_z(uint32_t tile, const float *Zt, int i0, int n0, int depth16,
+                                     float (&d)[NR][4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int rsel = (lane & 7) + ((lane >> 4) << 3);
-  const int csel = i0 + ((lane >> 3) & 1) * 8;
-  for (int j0 = 0; j0 < depth16; j0 += 16) {
-    uint32_t a[4];
-    g_ldsm_x4_t(tile + (uint32_t)((j0 + rsel) * STR + csel * 2), a);
-    const float2 z0 = *reinterpret_cast<const float2 *>(Zt + (n0 + g) * ZP + j0 + 2 * t);
-    const float2 z1 = *reinterpret_cast<const float2 *>(Zt + (n0 + g) * ZP + j0 + 8 + 2 * t);
-    uint32_t b0[3], b1[3];
-    g_split3<TF>(z0.x, z0.y, b0);
-    g_split3<TF>(z1.x, z1.y, b1);
+  const int cofs = ((lane >> 3) & 1) * 8;
+  constexpr int NK = KMAX / 16;
+  uint32_t bz[NK][2][3];
 #pragma unroll
-    for (int q = 0; q < 3; ++q) g_mma<TF>(d, a, b0[q], b1[q]);
+  for (int kk = 0; kk < NK; ++kk) {
+    if (16 * kk < depth16) {
+      const float2 z0 = *reinterpret_cast<const float2 *>(Zt + (n0 + g) * ZP + 16 * kk + 2 * t);
+      const float2 z1 = *reinterpret_cast<const float2 *>(Zt + (n0 + g) * ZP + 16 * kk + 8 + 2 * t);
+      g_split3<TF>(z0.x, z0.y, bz[kk][0]);
+      g_split3<TF>(z1.x, z1.y, bz[kk][1]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+#pragma unroll
+    for (int kk = 0; kk < NK; ++kk) {
+      if (16 * kk < depth16) {
+        uint32_t a[4];
+        g_ldsm_x4_t(tile + (uint32_t)((16 * kk + rsel) * STR + (i0 + 16 * r + cofs) * 2), a);
+#pragma unroll
+        for (int q = 0; q < 3; ++q) g_mma<TF>(d[r], a, bz[kk][0][q], bz[kk][1][q]);
+      }
+    }
   }
 }
 
@@ -407,34 +420,38 @@ __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phas
   __syncthreads();
 
   // ---- B = U Z (U_eff = U diag(c)), or diag(D) (U R_b^T) for KDA, on the tensor cores -----------
-  // (held in registers until every warp has read both tiles, then stored over them)
+  // A task is one column tile of B over half of its rows (four row tiles), Z's columns
+  // split once per task; the results are held in registers until every warp has read
+  // both tiles, then stored over them.
   {
-    constexpr int NW = kGramThreads / 32, NT = (DK / 16) * (MR / 8) / NW;
-    const int ntile = m16 / 8, per = (DK / 16) * ntile;
+    constexpr int NW = kGramThreads / 32, NTK = 2 * (MR / 8) / NW;  // tasks per warp at most
+    const int ntile = m16 / 8, per = 2 * ntile;
     const uint32_t ub = smem_u32(smem + L::U_OFF);
-    float bacc[NT][4];
+    float bacc[NTK][4][4];
 #pragma unroll
-    for (int q = 0; q < NT; ++q) {
+    for (int q = 0; q < NTK; ++q) {
       const int task = warp + q * NW;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) bacc[q][e] = 0.f;
-      if (task < per) {
-        const int i0 = (task / ntile) * 16, n0 = (task % ntile) * 8;
-        tile_times_z<TF, L::USTR, ZP>(ub, Zt, i0, n0, m16, bacc[q]);
-      }
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) bacc[q][r][e] = 0.f;
+      if (task < per)
+        tiles_times_z<TF, L::USTR, ZP, 4, MR>(ub, Zt, (task / ntile) * 64, (task % ntile) * 8, m16, bacc[q]);
     }
     __syncthreads();  // both tiles are read
 #pragma unroll
-    for (int q = 0; q < NT; ++q) {
+    for (int q = 0; q < NTK; ++q) {
       const int task = warp + q * NW;
       if (task < per) {
-        const int i0 = (task / ntile) * 16, n0 = (task % ntile) * 8;
+        const int ib = (task / ntile) * 64, n0 = (task % ntile) * 8;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = i0 + g + (e >> 1) * 8, n = n0 + 2 * t + (e & 1);
-          const float v = bacc[q][e] * zsc[n];
-          B[i * BP + n] = KDA ? v * sc[i] : v;
-        }
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = ib + 16 * r + g + (e >> 1) * 8, n = n0 + 2 * t + (e & 1);
+            const float v = bacc[q][r][e] * zsc[n];
+            B[i * BP + n] = KDA ? v * sc[i] : v;
+          }
       }
     }
   }
@@ -565,7 +582,7 @@ struct RebuildSmem {
   static constexpr int R_OFF = T_OFF + MR * STR;
   static constexpr int Y_OFF = R_OFF + MR * RP * 4;
   static constexpr int O_OFF = R_OFF;           // the output tile, over R_b and Y once Z is formed
-  static constexpr int RY_BYTES = MR * STR > MR * (RP + YP) * 4 ? MR * STR : MR * (RP + YP) * 4;
+  static constexpr int RY_BYTES = MR * STR > (MR * (RP + YP) + MR) * 4 ? MR * STR : (MR * (RP + YP) + MR) * 4;
   static constexpr int Z_OFF = R_OFF + RY_BYTES;
   static constexpr int S_OFF = Z_OFF + MR * ZP * 4;  // scales c [MR] or D [DK]
   static constexpr int ZS_OFF = S_OFF + (MR > kDK ? MR : kDK) * 4;  // per-column unscale of Z
@@ -621,9 +638,12 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
     const int i = idx / RP, l = idx % RP;
     Rb[idx] = (i < m && l < m) ? ws[W.rb + i * m + l] : 0.f;
   }
-  for (int idx = tid; idx < m16 * YP; idx += kGramThreads) {
-    const int j = idx / YP, n = idx % YP;
-    Yt[idx] = (j < m && n < rk) ? ws[W.y + n * W.m4 + j] : 0.f;
+  {  // Y^T: consecutive threads read consecutive entries of one kept vector
+    const int rk4 = (rk + 3) & ~3;
+    for (int idx = tid; idx < rk4 * m16; idx += kGramThreads) {
+      const int n = idx / m16, j = idx % m16;
+      Yt[j * YP + n] = (j < m && n < rk) ? ws[W.y + n * W.m4 + j] : 0.f;
+    }
   }
   if (isU) {
     if (KDA) for (int i = tid; i < DK; i += kGramThreads) sc[i] = sv.scale[(int64_t)h * DK + i];
@@ -658,23 +678,41 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
     }
   } else {
     // R_b Z = Y by back substitution in row panels of 16 from the bottom: a thread per
-    // column n solves the panel's triangle, then all threads take the panel's
-    // contribution off the rows above.  A zero pivot (dropped row) gives a zero entry.
+    // column n solves the panel's triangle in registers (each row's sum taken over the
+    // earliest-solved entries first, so that consecutive rows overlap), then all
+    // threads take the panel's contribution off the rows above.  A zero pivot
+    // (dropped row) gives a zero entry.
+    float *rinv = Yt + m16 * YP;  // 1 / R_b[i][i] (0 for a dropped row), after Y^T
     for (int idx = tid; idx < rk * m; idx += kGramThreads) {
       const int n = idx / m, i = idx % m;
       Z[n * ZP + i] = Yt[i * YP + n];
+    }
+    for (int i = tid; i < m; i += kGramThreads) {
+      const float piv = Rb[i * RP + i];
+      rinv[i] = piv != 0.f ? 1.f / piv : 0.f;
     }
     __syncthreads();
     for (int b1 = m; b1 > 0; b1 -= 16) {
       const int b0 = b1 > 16 ? b1 - 16 : 0;
       for (int n = tid; n < rk; n += kGramThreads) {
         float *z = Z + n * ZP;
-        for (int i = b1 - 1; i >= b0; --i) {
-          float s = z[i];
-          for (int l = i + 1; l < b1; ++l) s = fmaf(-Rb[i * RP + l], z[l], s);
-          const float piv = Rb[i * RP + i];
-          z[i] = piv != 0.f ? s / piv : 0.f;
+        float zp[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) zp[q] = b0 + q < b1 ? z[b0 + q] : 0.f;
+#pragma unroll
+        for (int q = 15; q >= 0; --q) {
+          const int i = b0 + q;
+          if (i < b1) {
+            float s = zp[q];
+#pragma unroll
+            for (int u = 15; u > q; --u)
+              if (b0 + u < b1) s = fmaf(-Rb[i * RP + b0 + u], zp[u], s);
+            zp[q] = s * rinv[i];
+          }
         }
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          if (b0 + q < b1) z[b0 + q] = zp[q];
       }
       __syncthreads();
       for (int idx = tid; idx < rk * b0; idx += kGramThreads) {
@@ -695,25 +733,31 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
   // ---- F' = F Z on the tensor cores (Z in three 16-bit terms) -----------------------------------
   {
     const int g = lane >> 2, t = lane & 3;
-    const int ntile = rk8 / 8, per = (rows / 16) * ntile;
+    // a task is one column tile over four row tiles (all of a 64-row factor, half of a
+    // 128-row one), Z's columns split once per task
+    const int ntile = rk8 / 8, per = (rows / 64) * ntile;
     const uint32_t tb = smem_u32(smem + L::T_OFF);
     TF *out = reinterpret_cast<TF *>(smem + L::O_OFF);
     for (int task = warp; task < per; task += kGramThreads / 32) {
-      const int i0 = (task / ntile) * 16, n0 = (task % ntile) * 8;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      tile_times_z<TF, L::STR, ZP>(tb, Z, i0, n0, m16, d);
-      // d[e]: row i (element of the column), output column n; stochastic rounding:
-      // one Philox block for the lane's four elements (counter: its even column, row)
-      uint4 rb = make_uint4(0u, 0u, 0u, 0u);
-      if (sv.rounding == kRoundStochastic)
-        rb = sr_bits(sv.sr_seed, c0 + n0 + 2 * t, (uint32_t)(i0 + g), isU ? kSrRebuildU : kSrRebuildW);
-      const uint32_t words[4] = {rb.x, rb.y, rb.z, rb.w};
+      const int ib = (task / ntile) * 64, n0 = (task % ntile) * 8;
+      float d[4][4] = {};
+      tiles_times_z<TF, L::STR, ZP, 4, MR>(tb, Z, ib, n0, m16, d);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = i0 + g + (e >> 1) * 8, n = n0 + 2 * t + (e & 1);
-        float v = d[e] * zsc[n];
-        if (isU && KDA) v *= sc[i];
-        out[n * (L::STR / 2) + i] = Mma16<TF>::cvt(store_value<TF>(v, sv.rounding, words[e]));
+      for (int r = 0; r < 4; ++r) {
+        const int i0 = ib + 16 * r;
+        // d[r][e]: row i (element of the column), output column n; stochastic rounding:
+        // one Philox block for the lane's four elements (counter: its even column, row)
+        uint4 rb = make_uint4(0u, 0u, 0u, 0u);
+        if (sv.rounding == kRoundStochastic)
+          rb = sr_bits(sv.sr_seed, c0 + n0 + 2 * t, (uint32_t)(i0 + g), isU ? kSrRebuildU : kSrRebuildW);
+        const uint32_t words[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = i0 + g + (e >> 1) * 8, n = n0 + 2 * t + (e & 1);
+          float v = d[r][e] * zsc[n];
+          if (isU && KDA) v *= sc[i];
+          out[n * (L::STR / 2) + i] = Mma16<TF>::cvt(store_value<TF>(v, sv.rounding, words[e]));
+        }
       }
     }
   }
