@@ -50,6 +50,9 @@ def parse():
     ap.add_argument('--no-cpu', action='store_true')
     ap.add_argument('--recompress', default='phases', choices=['phases', 'single'],
                     help='three-phase recompression over a workspace, or the single kernel')
+    ap.add_argument('--requests', type=int, default=0,
+                    help='run the workload with this many requests instead of its own count '
+                         '(the same shapes on a smaller batch, for profiling captures)')
     return ap.parse_args()
 
 
@@ -217,8 +220,11 @@ def measured_peaks():
 # counts only while the hash of these files is the one it records.
 PROFILE_SOURCES = {
     'decode': ['decode_mma.cu', 'common.cuh'],
-    'recompress': ['recompress_split.cu', 'qr_registers.cuh', 'svd_warp.cuh', 'recompress_core.cuh',
-                   'common.cuh'],
+    # 16-bit factors: Cholesky of the value-side Gram matrix (gram_phase, evd_phase, gram_rebuild)
+    'recompress': ['recompress_gram.cu', 'evd_warp.cuh', 'svd_warp.cuh', 'recompress_core.cuh', 'common.cuh'],
+    # 32-bit factors: QR of both factors (qr_phase, svd_phase, rebuild_phase)
+    'recompress_f32': ['recompress_split.cu', 'qr_registers.cuh', 'svd_warp.cuh', 'recompress_core.cuh',
+                       'common.cuh'],
 }
 
 
@@ -409,7 +415,7 @@ def run_gpu(args, w):
                             / float(prof['algorithmic_bytes_per_launch']))
         except (KeyError, ValueError, ZeroDivisionError):
             traffic = None
-    prof = profiled_record('recompress', w.name)
+    prof = profiled_record('recompress' if w.factor_dtype != 'f32' else 'recompress_f32', w.name)
     if prof is not None and run.ws is not None:
         try:
             rec_traffic = round(float(prof['traffic_bytes_per_launch']))
@@ -421,7 +427,13 @@ def run_gpu(args, w):
                     traffic=traffic, peak_src=peaks['src'],
                     algorithmic_bytes_per_launch=round(bytes_decode / K),
                     avg_launch_us=round(dec_avg_ms * 1e3, 3))
-    rec_kernels = 'qr_phase + svd_phase + rebuild_phase' if run.ws is not None else 'recompress_kernel'
+    if run.ws is None:
+        rec_kernels = 'recompress_kernel'
+    elif w.factor_dtype == 'f32':
+        rec_kernels = 'qr_phase + svd_phase + rebuild_phase'
+    else:
+        rec_kernels = ('gram_classify + ' if run.state.ranks is not None else '') + \
+            'gram_phase + evd_phase + gram_rebuild'
     roof_rec = dict(kernel=f'{rec_kernels} (recompress)', bound='alu', achieved=rec_tflops and round(rec_tflops, 3),
                     peak=round(fp32_peak, 1), unit='TFLOP/s',
                     frac=rec_tflops and round(rec_tflops / fp32_peak, 4), traffic=rec_traffic,
@@ -604,6 +616,8 @@ def main():
     if args.workload not in synth.WORKLOADS:
         raise SystemExit(f'unknown workload {args.workload}; one of {sorted(synth.WORKLOADS)}')
     w = synth.WORKLOADS[args.workload]
+    if args.requests > 0:
+        w = w.with_(n_req=args.requests)
     if args.impl == 'reference':
         run_reference(args, w)
     else:
