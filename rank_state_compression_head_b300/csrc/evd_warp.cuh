@@ -57,8 +57,7 @@ __device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw) {
     }
     const int p = bi;
     const float d = fmaxf(best, 0.f);
-    const float rjj = sqrtf(d);
-    const float inv = d > 0.f ? 1.f / rjj : 0.f;
+    const float inv = d > 0.f ? rsqrtf(d) : 0.f;  // 1 / r_jj (a couple of ulp)
     float *cp = T + p * TP;
     if (lane == (p & (HW - 1))) {
       if (p >= HW) done1 = true;

@@ -157,6 +157,12 @@ __device__ static inline void g_cp_async16(void *dst, const void *src) {
 __device__ static inline void g_cp_commit_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
+__device__ static inline void g_cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ static inline void g_cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// all but the most recently committed group have landed
+__device__ static inline void g_cp_wait_but_last() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ static inline void g_ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -223,23 +229,25 @@ struct GramSmem {
   static constexpr int SC_OFF = G_OFF + ((MR * GP * 4 + 15) & ~15);
   static constexpr int DG_OFF = SC_OFF + (MR > kDK ? MR : kDK) * 4;
   static constexpr int ZS_OFF = DG_OFF + MR * 4;  // per-column unscale of Z (fp16)
-  static constexpr int BYTES = ZS_OFF + MR * 4;
+  static constexpr int RR_OFF = ZS_OFF + MR * 4;  // the Cholesky's current row of R_b, two buffers
+  static constexpr int BYTES = RR_OFF + 2 * MR * 4;
 };
 
 // Cholesky G_w = R_b^T R_b by one warp, the matrix in registers: lane l owns
 // columns l and l + 32 of the upper triangle (column c needs rows 0..c only, so
 // the first column's array stops at 32).  Step j: the pivot's lane hands round
 // the current G[j][j]; every lane forms its entries of row j of R_b (R[j][c] =
-// G[j][c] / r_jj, r_jj on the diagonal) and writes them over G_w's row j in
-// shared memory; then row j is handed round entry by entry and each lane takes
-// R[j][i] R[j][c] off its rows i > j.  A pivot below kCholFloor of its column's
-// squared norm means the column lies in the span of the earlier ones to within
-// the resolution of the Gram matrix: its row of R_b is dropped (zero) and the
-// column is represented by its projections.  G_w in Gw (row i at i * GP); row j
-// of R_b replaces row j of G_w (entries c >= j; below the diagonal untouched),
-// dg gets the original diagonal.
+// G[j][c] / r_jj, r_jj on the diagonal), writes them over G_w's row j and into a
+// row buffer in shared memory; after a warp barrier every lane reads row j back
+// with 16-byte broadcast loads and takes R[j][i] R[j][c] off its rows i > j.  A
+// pivot below kCholFloor of its column's squared norm means the column lies in
+// the span of the earlier ones to within the resolution of the Gram matrix: its
+// row of R_b is dropped (zero) and the column is represented by its projections.
+// G_w in Gw (row i at i * GP); row j of R_b replaces row j of G_w (entries c >= j;
+// below the diagonal untouched), dg gets the original diagonal; rr holds 2 * MR
+// floats (the row buffer, double-buffered by step parity).
 template <int MR>
-__device__ inline void chol_warp(float *Gw, float *dg, int m) {
+__device__ inline void chol_warp(float *Gw, float *dg, float *rr, int m) {
   constexpr int GP = MR + 1;
   constexpr bool TWO = MR > 32;
   constexpr int NA = MR < 32 ? MR : 32;
@@ -262,19 +270,31 @@ __device__ inline void chol_warp(float *Gw, float *dg, int m) {
       if constexpr (TWO) own = j < 32 ? gA[j < NA ? j : 0] : gB[j];
       else own = gA[j < NA ? j : 0];
       const float d = __shfl_sync(0xffffffffu, own, j & 31);
-      const float rjj = d > kCholFloor * dg[j] ? sqrtf(d) : 0.f;
-      const float inv = rjj > 0.f ? 1.f / rjj : 0.f;
+      // 1 / r_jj and r_jj from one reciprocal square root (a couple of ulp)
+      const bool keep = d > kCholFloor * dg[j];
+      const float inv = keep ? rsqrtf(d) : 0.f;
+      const float rjj = d * inv;
       const float rA = j < NA && c0 > j ? gA[j < NA ? j : 0] * inv : (c0 == j ? rjj : 0.f);
       float rB = 0.f;
       if constexpr (TWO) rB = c1 > j ? gB[j] * inv : (c1 == j ? rjj : 0.f);
+      float *row = rr + (j & 1) * MR;
+      if (c0 < MR) row[c0] = rA;
+      if (TWO && c1 < MR) row[c1] = rB;
       if (c0 >= j && c0 < m) Gw[j * GP + c0] = rA;
       if (TWO && c1 >= j && c1 < m) Gw[j * GP + c1] = rB;
+      __syncwarp();
+      const float4 *row4 = reinterpret_cast<const float4 *>(row);
 #pragma unroll
-      for (int i = j + 1; i < MR; ++i) {
-        if (i < m) {
-          const float ri = __shfl_sync(0xffffffffu, i < 32 ? rA : rB, i & 31);
-          if (i < NA) gA[i < NA ? i : 0] = fmaf(-ri, rA, gA[i < NA ? i : 0]);
-          if constexpr (TWO) gB[i] = fmaf(-ri, rB, gB[i]);
+      for (int q = (j + 1) / 4; q < MR / 4; ++q) {
+        const float4 v = row4[q];
+        const float rv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 4 * q + e;
+          if (i > j && i < m) {
+            if (i < NA) gA[i < NA ? i : 0] = fmaf(-rv[e], rA, gA[i < NA ? i : 0]);
+            if constexpr (TWO) gB[i] = fmaf(-rv[e], rB, gB[i]);
+          }
         }
       }
     }
@@ -404,7 +424,7 @@ __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phas
   __syncthreads();
 
   // ---- Cholesky G_w = R_b^T R_b (upper, in place) by warp 0 --------------------------------------
-  if (warp == 0) chol_warp<MR>(Gw, dg, m);
+  if (warp == 0) chol_warp<MR>(Gw, dg, reinterpret_cast<float *>(smem + L::RR_OFF), m);
   __syncthreads();
 
   // ---- Z = diag(c) R_b^T (Z[l][j] = c_l R_b[j][l]), stored by rows of Z^T --------------------------
@@ -622,7 +642,27 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
   float *sc = reinterpret_cast<float *>(smem + L::S_OFF);
   TF *pool = reinterpret_cast<TF *>(isU ? sv.U : sv.W) + c0 * rows;
 
-  // ---- the factor tile (cp.async), R_b, Y, the scales --------------------------------------
+  // ---- R_b, Y, the scales (first copy group), the factor tile (second) -----------------------
+  // R_b upper (zero below the diagonal and beyond m), Y^T (zero beyond m and rk), Z zero;
+  // consecutive threads copy consecutive workspace words
+  for (int idx = tid; idx < m16 * RP; idx += kGramThreads) {
+    const int i = idx / RP, l = idx % RP;
+    if (i < m && l < m) g_cp_async4(Rb + idx, ws + W.rb + i * m + l);
+    else Rb[idx] = 0.f;
+  }
+  {
+    const int rk4 = (rk + 3) & ~3;
+    for (int idx = tid; idx < rk4 * m16; idx += kGramThreads) {
+      const int n = idx / m16, j = idx % m16;
+      if (j < m && n < rk) g_cp_async4(Yt + j * YP + n, ws + W.y + n * W.m4 + j);
+      else Yt[j * YP + n] = 0.f;
+    }
+  }
+  if (isU) {
+    if (KDA) for (int i = tid; i < DK; i += kGramThreads) g_cp_async4(sc + i, sv.scale + (int64_t)h * DK + i);
+    else for (int j = tid; j < m; j += kGramThreads) g_cp_async4(sc + j, sv.scale + c0 + j);
+  }
+  g_cp_commit();
   {
     const int CH = rows / 8;
     for (int idx = tid; idx < m16 * CH; idx += kGramThreads) {
@@ -632,24 +672,9 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
       else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
     }
   }
-  // R_b (upper, zero below the diagonal and beyond m), Y^T (zero beyond m and rk),
-  // the scales, Z zero
-  for (int idx = tid; idx < m16 * RP; idx += kGramThreads) {
-    const int i = idx / RP, l = idx % RP;
-    Rb[idx] = (i < m && l < m) ? ws[W.rb + i * m + l] : 0.f;
-  }
-  {  // Y^T: consecutive threads read consecutive entries of one kept vector
-    const int rk4 = (rk + 3) & ~3;
-    for (int idx = tid; idx < rk4 * m16; idx += kGramThreads) {
-      const int n = idx / m16, j = idx % m16;
-      Yt[j * YP + n] = (j < m && n < rk) ? ws[W.y + n * W.m4 + j] : 0.f;
-    }
-  }
-  if (isU) {
-    if (KDA) for (int i = tid; i < DK; i += kGramThreads) sc[i] = sv.scale[(int64_t)h * DK + i];
-    else for (int j = tid; j < m; j += kGramThreads) sc[j] = sv.scale[c0 + j];
-  }
+  g_cp_commit();
   for (int idx = tid; idx < rk8 * ZP; idx += kGramThreads) Z[idx] = 0.f;
+  g_cp_wait_but_last();  // R_b, Y and the scales are in; the tile may still be on its way
   __syncthreads();
 
   // ---- Z ------------------------------------------------------------------------------------
