@@ -43,19 +43,22 @@ __device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw) {
   bool done0 = c0 >= m, done1 = !TWO || c1 >= m;
   float dg0 = done0 ? 0.f : T[c0 * TP + c0];
   float dg1 = done1 ? 0.f : T[c1 * TP + c1];
+  // order-preserving integer key of a finite float (larger float, larger key; 0 = none)
+  auto okey = [](float f) {
+    const unsigned u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  };
+  const int gbase = threadIdx.x & (32 - HW);  // first lane of my group in the warp
   for (int j = 0; j < m; ++j) {
-    // the remaining index of largest diagonal (ties to the lower index)
-    float best = -FLT_MAX;
-    int bi = 1 << 20;
-    if (!done0) { best = dg0; bi = c0; }
-    if (!done1 && dg1 > best) { best = dg1; bi = c1; }
-#pragma unroll
-    for (int o = HW / 2; o > 0; o >>= 1) {
-      const float ob = __shfl_xor_sync(full, best, o);
-      const int oi = __shfl_xor_sync(full, bi, o);
-      if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
-    }
-    const int p = bi;
+    // the remaining index of largest diagonal (ties to the lower index): one warp
+    // reduction of the keys, then the lowest lane holding the maximum, first among the
+    // lower indices l, then among l + HW
+    const unsigned k0 = done0 ? 0u : okey(dg0), k1 = done1 ? 0u : okey(dg1);
+    const unsigned kmax = __reduce_max_sync(full, k0 > k1 ? k0 : k1);
+    const unsigned b0 = (__ballot_sync(full, !done0 && k0 == kmax) >> gbase) & (HW == 32 ? 0xffffffffu : 0xffffu);
+    const unsigned b1 = (__ballot_sync(full, !done1 && k1 == kmax) >> gbase) & (HW == 32 ? 0xffffffffu : 0xffffu);
+    const int p = b0 ? __ffs(b0) - 1 : HW + __ffs(b1) - 1;
+    const float best = __uint_as_float((kmax & 0x80000000u) ? (kmax ^ 0x80000000u) : ~kmax);
     const float d = fmaxf(best, 0.f);
     const float inv = d > 0.f ? rsqrtf(d) : 0.f;  // 1 / r_jj (a couple of ulp)
     float *cp = T + p * TP;
