@@ -50,6 +50,8 @@ def parse():
     ap.add_argument('--no-cpu', action='store_true')
     ap.add_argument('--recompress', default='phases', choices=['phases', 'single'],
                     help='three-phase recompression over a workspace, or the single kernel')
+    ap.add_argument('--ws-heads', type=int, default=0,
+                    help='heads per recompression workspace chunk (default: the library default)')
     ap.add_argument('--requests', type=int, default=0,
                     help='run the workload with this many requests instead of its own count '
                          '(the same shapes on a smaller batch, for profiling captures)')
@@ -272,7 +274,7 @@ def run_gpu(args, w):
     total_steps = K + W_
 
     # ---- setup: constants, prefill, compression, inputs of every step -----------------
-    ws_heads = DEFAULT_WS_HEADS if args.recompress == 'phases' else 0
+    ws_heads = (args.ws_heads or DEFAULT_WS_HEADS) if args.recompress == 'phases' else 0
     run = DeviceRun(w, device=dev, steps_buffered=total_steps, ws_heads=ws_heads)
     rec_launches = run.recompress_launches()
     # setup, timed once (not part of the decode metric): dense prefill and compression
@@ -449,7 +451,8 @@ def run_gpu(args, w):
                            T=w.T, factor_dtype=w.factor_dtype, variant=w.variant,
                            l2='flushed before every timed step (256 MiB write then 256 MiB read, untimed)',
                            parallelism=f'heads sharded over {ws} rank(s), one batch of requests each'),
-               roofline=dominant, gpu_launches=K + rec_launches * len(rec_ms), clocks=clocks)
+               roofline=dominant, gpu_launches=K * run.decode_launches() + rec_launches * len(rec_ms),
+               clocks=clocks)
     out['config']['recompression'] = (f'after every {T}th step, amortised: ms_per_step = mean decode + '
                                       f'mean recompression / {T} ({len(rec_ms)} recompression(s) timed)')
     out['decode'] = dict(head_steps_per_s=round(heads_all * K / (dec_total / 1e3)),

@@ -127,7 +127,25 @@ typedef struct {
   uint64_t sr_seed;              /* key of the stochastic-rounding bits: change it from call
                                     to call (e.g. the global step number) for fresh bits; the
                                     same seed and inputs give the same bits                */
+  const int32_t *head_order;     /* [n_heads] every head once, grouped by column class, or
+                                    NULL (see below)                                       */
+  int32_t class_end[4];          /* with head_order: where each column class ends in it    */
 } seed_state;
+
+/*
+ * Column classes (optional, for ragged ranks).  Head h belongs to class c when
+ * its capacity r(h) + growth * T lies in (16c, 16c + 16] (class 0 also takes 0).
+ * With head_order != NULL, positions [class_end[c-1], class_end[c]) of
+ * head_order (class_end[-1] = 0) list the heads of class c, and class_end[3] =
+ * n_heads.  seed_decode_step and the 16-bit paths of seed_recompress_ws /
+ * seed_recompress_noalloc then launch once per class, each launch sized for its
+ * class (shared-memory stages of 16(c+1) columns) and covering exactly its heads;
+ * the results are the same as without the order, head for head.  The host checks
+ * that class_end is nondecreasing and ends at n_heads; head_order must list every
+ * head once (not checked).  A listed head whose columns exceed its class's size
+ * is left untouched by the call that finds it so, with status
+ * SEED_ERR_INVALID_ARG.  32-bit factors ignore the order.
+ */
 
 /* Columns one head needs: r + growth * T. */
 int32_t seed_columns_per_head(int32_t variant, int32_t r, int32_t T);

@@ -59,6 +59,7 @@ class seed_state(ctypes.Structure):
         ('T', _i32), ('r', _i32), ('r_max', _i32), ('steps_since_compress', _i32), ('rounding', _i32),
         ('rank', _vp), ('col_offset', _vp), ('a', _vp), ('U', _vp), ('W', _vp), ('scale', _vp),
         ('vbar', _vp), ('vbar_index', _vp), ('status', _vp), ('sr_seed', ctypes.c_uint64),
+        ('head_order', _vp), ('class_end', _i32 * 4),
     ]
 
 

@@ -38,6 +38,14 @@ int check_state(const seed_state *st) {
   if (misaligned(st->a) || misaligned(st->U) || misaligned(st->W) || misaligned(st->vbar) ||
       misaligned(st->scale))
     return SEED_ERR_ALIGNMENT;
+  if (st->head_order) {
+    int prev = 0;
+    for (int c = 0; c < 4; ++c) {
+      if (st->class_end[c] < prev) return SEED_ERR_INVALID_ARG;
+      prev = st->class_end[c];
+    }
+    if (prev != st->n_heads) return SEED_ERR_INVALID_ARG;
+  }
   return SEED_OK;
 }
 
@@ -63,6 +71,9 @@ StateView view_of(const seed_state *st) {
   v.vbar = st->vbar;
   v.vbar_index = st->vbar_index;
   v.status = st->status;
+  // the class order serves 16-bit factors with per-head ranks
+  v.order = st->head_order && st->rank && st->factor_dtype != SEED_F32 ? st->head_order : nullptr;
+  for (int c = 0; c < 4; ++c) v.class_end[c] = v.order ? st->class_end[c] : 0;
   return v;
 }
 

@@ -273,6 +273,8 @@ struct StateView {
   const float *vbar;
   const int32_t *vbar_index;
   int32_t *status;
+  const int32_t *order;           // heads grouped by column class, or NULL
+  int32_t class_end[4];           // with order: where each class ends in it
 
   __device__ inline int rank_of(int h) const { return rank ? rank[h] : r; }
   __device__ inline int64_t col0(int h) const {
@@ -296,6 +298,9 @@ struct DecodeArgs {
   StateView sv;
   const float *q, *k, *v, *gate, *beta, *A;
   float *o;
+  // heads of this launch: sv.order[pos0 .. pos0 + count) when sv.order is set (one
+  // column class), else all n_heads heads in index order
+  int32_t pos0, count;
 };
 
 // Sum of eight per-lane values over the warp: after 9 shuffles lane l holds

@@ -466,10 +466,25 @@ static cudaError_t launch_decode_v(const DecodeArgs &a, int cols_max, cudaStream
 cudaError_t launch_decode(const StateView &sv, int factor_dtype, const float *q, const float *k,
                           const float *v, const float *gate, const float *beta, const float *A,
                           float *o, int cols_max, cudaStream_t s) {
-  DecodeArgs a{sv, q, k, v, gate, beta, A, o};
-  // 16-bit factors: the two contractions run on the tensor cores (decode_mma.cu)
-  if (factor_dtype != SEED_F32) return launch_decode_mma(a, factor_dtype, cols_max, s);
-  return launch_decode_v<float>(a, cols_max, s);
+  DecodeArgs a{sv, q, k, v, gate, beta, A, o, 0, sv.n_heads};
+  if (factor_dtype == SEED_F32) {
+    a.sv.order = nullptr;
+    return launch_decode_v<float>(a, cols_max, s);
+  }
+  // 16-bit factors: the two contractions run on the tensor cores (decode_mma.cu);
+  // with a class order, one launch per column class, sized for it
+  if (!sv.order) return launch_decode_mma(a, factor_dtype, cols_max, s);
+  const int cols16 = (cols_max + 15) & ~15;
+  for (int c = 0, begin = 0; c < 4; begin = sv.class_end[c], ++c) {
+    const int end = sv.class_end[c];
+    if (end <= begin) continue;
+    a.pos0 = begin;
+    a.count = end - begin;
+    const int cls_cols = 16 * (c + 1) < cols16 ? 16 * (c + 1) : cols16;
+    const cudaError_t e = launch_decode_mma(a, factor_dtype, cls_cols, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace seedk

@@ -90,7 +90,7 @@ __device__ static inline void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr));
 }
 template <typename TF, int VAR, int DV, int MAXC, int NS>
-__global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const DecodeArgs p) {
+__global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_kernel(const DecodeArgs p) {
   constexpr int DK = kDK;
   constexpr int NT = kMmaThreads;
   using S = MmaStage<VAR, DV, MAXC>;
@@ -113,13 +113,15 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
   const int growth = sv.growth;
   const int G = gridDim.x;
   const int first = blockIdx.x;
-  const int nmine = first < sv.n_heads ? (sv.n_heads - first + G - 1) / G : 0;
+  const int nmine = first < p.count ? (p.count - first + G - 1) / G : 0;
+  // head of launch item i: through the class order when the launch has one
+  auto head_at = [&](int i) { return sv.order ? sv.order[p.pos0 + i] : i; };
 
   // Copy head number i of this CTA into stage i % NS (one commit group per head,
   // empty when i is past the end, so that group counting stays uniform).
   auto issue = [&](int i) {
     if (i < nmine) {
-      const int h = first + i * G;
+      const int h = head_at(first + i * G);
       const int r_h = sv.rank_of(h);
       const int m = r_h + growth * sv.steps;
       if (r_h >= 0 && m <= MAXC) {
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(kMmaThreads, 7) decode_mma_kernel(const Decode
     issue(i + NS - 1);
     cp_async_wait<NS - 1>();  // this thread's copies of head i have landed
 
-    const int h = first + i * G;
+    const int h = head_at(first + i * G);
     const int r_h = sv.rank_of(h);
     const int m = r_h + growth * sv.steps;
     const bool bad_rank = r_h < 0 || m > MAXC;
@@ -451,7 +453,7 @@ static cudaError_t launch_mma_t(const DecodeArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     ready.fetch_or(bit, std::memory_order_acq_rel);
   }
-  kern<<<a.sv.n_heads, kMmaThreads, L::BYTES, s>>>(a);
+  kern<<<a.count, kMmaThreads, L::BYTES, s>>>(a);
   return cudaGetLastError();
 }
 

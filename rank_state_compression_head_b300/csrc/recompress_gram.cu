@@ -84,6 +84,7 @@ struct GramArgs {
   float *trunc_err;
   int32_t *sweeps;
   int cls;          // column class of this launch (its heads from the class list), or -1: every slot
+  int pos_lo, pos_hi;  // with the state's class order: this launch's positions in it
 };
 
 __device__ inline bool gram_head(const GramArgs &p, int h, int &r, int &m) {
@@ -93,16 +94,27 @@ __device__ inline bool gram_head(const GramArgs &p, int h, int &r, int &m) {
 }
 __device__ inline bool gram_in_class(const GramArgs &p, int m) { return m > p.m_lo && m <= p.m_max; }
 
-// The workspace slot (= head - head0) that item i of this launch serves, from the
-// class list when the launch has one.  False past the end.
-__device__ inline bool gram_slot(const GramArgs &p, int i, int &b) {
+// The workspace slot and the head that item i of this launch serves: position
+// pos_lo + i of the state's class order (slot = position - head0, the chunk's first
+// position), an entry of this chunk's class list, or slot i (head head0 + i).
+// False past the end.
+__device__ inline bool gram_item(const GramArgs &p, int i, int &b, int &h) {
+  if (p.sv.order) {
+    const int pos = p.pos_lo + i;
+    if (pos >= p.pos_hi) return false;
+    b = pos - p.head0;
+    h = p.sv.order[pos];
+    return true;
+  }
   if (p.cls < 0) {
     b = i;
+    h = p.head0 + i;
     return i < p.n_group;
   }
   const GramLayout L(p.layout_m, p.r_max);
   if (i >= reinterpret_cast<const int *>(p.ws + L.lst)[4 + p.cls]) return false;
   b = reinterpret_cast<const int *>(p.ws + (int64_t)i * L.per_head + L.lst)[p.cls];
+  h = p.head0 + b;
   return true;
 }
 
@@ -366,9 +378,8 @@ __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phas
   constexpr int GP = L::GP, ZP = L::ZP, BP = L::BP;
   constexpr bool KDA = VAR == SEED_KDA;
   extern __shared__ __align__(128) unsigned char smem[];
-  int slot;
-  if (!gram_slot(p, blockIdx.x, slot)) return;
-  const int h = p.head0 + slot;
+  int slot, h;
+  if (!gram_item(p, blockIdx.x, slot, h)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const StateView &sv = p.sv;
@@ -532,16 +543,18 @@ __global__ void __launch_bounds__(32 * kSvdWarps, evd_min_blocks<MR>()) evd_phas
   extern __shared__ __align__(16) float smem_f[];
   const int grp = threadIdx.x / HW, lane = threadIdx.x & (HW - 1);
   const unsigned gmask = HW == 32 ? 0xffffffffu : 0xffffu << (threadIdx.x & 16);
-  int b;
-  if (!gram_slot(p, blockIdx.x * evd_heads_per_cta<MR>() + grp, b)) return;
-  const int h = p.head0 + b;
+  int b, h;
+  if (!gram_item(p, blockIdx.x * evd_heads_per_cta<MR>() + grp, b, h)) return;
   const StateView &sv = p.sv;
   int r, m;
   if (!gram_head(p, h, r, m)) {  // rank table disagrees with r_max: touch nothing
     if (lane == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
     return;
   }
-  if (!gram_in_class(p, m)) return;
+  if (!gram_in_class(p, m)) {  // a head listed in a class too small for it: touch nothing
+    if (p.sv.order && lane == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
+    return;
+  }
   float *sw = smem_f + grp * SW::FLOATS;
   float *T = sw + SW::T_OFF;
   const GramLayout W(p.layout_m, p.r_max);
@@ -616,9 +629,8 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
   constexpr int RP = L::RP, YP = L::YP, ZP = L::ZP;
   constexpr bool KDA = VAR == SEED_KDA;
   extern __shared__ __align__(128) unsigned char smem[];
-  int slot;
-  if (!gram_slot(p, blockIdx.x, slot)) return;
-  const int h = p.head0 + slot;
+  int slot, h;
+  if (!gram_item(p, blockIdx.x, slot, h)) return;
   const bool isU = blockIdx.y == 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const StateView &sv = p.sv;
@@ -837,13 +849,35 @@ static cudaError_t launch_gram_v(const GramArgs &a, cudaStream_t s) {
 
 cudaError_t launch_recompress_gram(const StateView &sv, int factor_dtype, float *trunc_err, int32_t *sweeps,
                                    int m_max, int r_max, float *ws, int64_t chunk, cudaStream_t s) {
-  GramArgs a{sv, ws, 0, 0, m_max, -1, m_max, r_max, trunc_err, sweeps, -1};
+  GramArgs a{sv, ws, 0, 0, m_max, -1, m_max, r_max, trunc_err, sweeps, -1, 0, 0};
   const int n = sv.n_heads;
   auto one = [&](const GramArgs &x) {
     if (factor_dtype == SEED_F16)
       return sv.d_v == 64 ? launch_gram_v<__half, 64>(x, s) : launch_gram_v<__half, 128>(x, s);
     return sv.d_v == 64 ? launch_gram_v<__nv_bfloat16, 64>(x, s) : launch_gram_v<__nv_bfloat16, 128>(x, s);
   };
+  // With the state's class order: chunks of consecutive positions, and in each one
+  // launch triple per class present, sized for the class and covering exactly its
+  // heads (a head's columns need only fit its class, so any m up to the class size).
+  if (sv.order) {
+    for (int64_t p0 = 0; p0 < n; p0 += chunk) {
+      const int p1 = (int)(n - p0 < chunk ? n : p0 + chunk);
+      for (int c = 0, begin = 0; c < 4; begin = sv.class_end[c], ++c) {
+        const int lo = begin > p0 ? begin : (int)p0, hi = sv.class_end[c] < p1 ? sv.class_end[c] : p1;
+        if (hi <= lo) continue;
+        GramArgs x = a;
+        x.head0 = (int)p0;
+        x.n_group = hi - lo;
+        x.pos_lo = lo;
+        x.pos_hi = hi;
+        x.m_max = 16 * (c + 1) < m_max ? 16 * (c + 1) : m_max;
+        x.m_lo = -1;
+        const cudaError_t e = one(x);
+        if (e != cudaSuccess) return e;
+      }
+    }
+    return cudaSuccess;
+  }
   // Ragged ranks: per chunk, the heads are listed by 16-column class, and each
   // class gets its own launches, sized for it, over its list.
   const bool ragged = sv.rank && m_max > 16;

@@ -24,13 +24,16 @@ class FactoredStateBuffers:
     ``h * (r + growth*T)``.  Ragged ranks: ``ranks`` [n_heads] int32 and
     per-head column offsets (an exclusive prefix sum of ``rank + growth*T``).
     ``vbar`` is the [n_dir, d_v] table of unit sink directions and
-    ``vbar_index`` (optional) the direction of each head.
+    ``vbar_index`` (optional) the direction of each head.  With ragged ranks and
+    ``class_order`` (the default), the heads are also listed by column class
+    (capacity ``rank + growth*T`` in (16c, 16c + 16]) for the per-class launches
+    that ``seed.h`` describes.
     """
 
     def __init__(self, variant: str, factor_dtype: str, n_heads: int, d_k: int, d_v: int, T: int,
                  vbar: torch.Tensor, r: int = 0, ranks: Optional[torch.Tensor] = None,
                  vbar_index: Optional[torch.Tensor] = None, device='cuda', rounding: str = 'nearest',
-                 sr_seed: int = 0):
+                 sr_seed: int = 0, class_order: bool = True):
         self.variant = variant
         self.factor_dtype = factor_dtype
         self.n_heads, self.d_k, self.d_v, self.T = n_heads, d_k, d_v, T
@@ -42,6 +45,7 @@ class FactoredStateBuffers:
             self.cap = r + self.growth * T
             self.ranks = None
             self.col_offset = None
+            self.head_order, self.class_end = None, [0, 0, 0, 0]
             n_cols = n_heads * self.cap
         else:
             self.ranks = ranks.to(device=dev, dtype=torch.int32).contiguous()
@@ -55,6 +59,11 @@ class FactoredStateBuffers:
             self.cap = None
             n_cols = int(caps.sum())
             r = self.r_max
+            self.head_order, self.class_end = None, [0, 0, 0, 0]
+            if class_order and n_heads:
+                cls = torch.where(caps <= 16, torch.zeros_like(caps), (caps - 1) // 16).clamp(max=3)
+                self.head_order = torch.argsort(cls, stable=True).to(device=dev, dtype=torch.int32)
+                self.class_end = torch.cumsum(torch.bincount(cls, minlength=4), 0).tolist()
         self.r = r
         self.n_cols = n_cols
         self.a = torch.zeros(n_heads, d_k, device=dev)
@@ -72,7 +81,9 @@ class FactoredStateBuffers:
             d_v=d_v, T=T, r=r, r_max=self.r_max, steps_since_compress=0, rounding=ROUNDINGS[rounding],
             rank=_p(self.ranks), col_offset=_p(self.col_offset), a=_p(self.a), U=_p(self.U),
             W=_p(self.W), scale=_p(self.scale), vbar=_p(self.vbar), vbar_index=_p(self.vbar_index),
-            status=_p(self.status), sr_seed=sr_seed)
+            status=_p(self.status), sr_seed=sr_seed, head_order=_p(self.head_order))
+        for c in range(4):
+            self.st.class_end[c] = int(self.class_end[c])
 
     @property
     def steps_since_compress(self) -> int:

@@ -113,6 +113,15 @@ class DeviceRun:
         else:
             seed_recompress_ex(self.state.st, trunc_err, sweeps, stream)
 
+    def decode_launches(self) -> int:
+        """Kernels one decode step launches: one per column class present when the state
+        carries a class order (16-bit factors), else one (mirrors decode.cu)."""
+        st = self.state
+        if st.head_order is None or self.w.factor_dtype == 'f32':
+            return 1
+        ends = [0] + list(st.class_end)
+        return sum(1 for c in range(4) if ends[c + 1] > ends[c])
+
     def recompress_launches(self) -> int:
         """Kernels one recompression after T steps launches (bookkeeping of the count
         a benchmark reports; mirrors the launcher in recompress_split.cu)."""
@@ -126,6 +135,12 @@ class DeviceRun:
         classes = -(-m_max // 16)
         if self.w.factor_dtype == 'f32':
             return 3 * groups * classes
+        if st.head_order is not None:  # three launches per class present in each chunk
+            chunk, n, ends = min(self.H, self.ws_heads), 0, [0] + list(st.class_end)
+            for p0 in range(0, self.H, chunk):
+                p1 = min(self.H, p0 + chunk)
+                n += 3 * sum(1 for c in range(4) if min(ends[c + 1], p1) > max(ends[c], p0))
+            return n
         return groups * (1 + 3 * classes)  # a class-list pass, then three launches per class
 
     def step(self, t: int, slot: int = 0, stream=None) -> bool:

@@ -43,10 +43,12 @@ def random_states(seed, H, d_k, d_v, ranks, s, T, variant, dtype):
     return states, raw['vbar']
 
 
-def make_buffers(variant, dtype, H, d_k, d_v, T, vbar, ranks, ragged=True, rounding='nearest', sr_seed=0):
+def make_buffers(variant, dtype, H, d_k, d_v, T, vbar, ranks, ragged=True, rounding='nearest', sr_seed=0,
+                 class_order=True):
     vb = torch.tensor(np.asarray(vbar), dtype=torch.float32)
     kw = dict(rounding=rounding, sr_seed=sr_seed)
     if ragged:
+        kw['class_order'] = class_order
         return R.FactoredStateBuffers(variant, dtype, H, d_k, d_v, T, vb,
                                       ranks=torch.tensor(np.asarray(ranks), dtype=torch.int32), **kw)
     return R.FactoredStateBuffers(variant, dtype, H, d_k, d_v, T, vb, r=int(ranks[0]), **kw)

@@ -36,8 +36,9 @@ def test_library_exports_every_declared_function():
 
 
 def test_struct_layout_matches_header(tmp_path):
-    # 10 int32 fields, 9 pointers, the 64-bit stochastic-rounding seed
-    assert ctypes.sizeof(R.seed_state) == 10 * 4 + 9 * 8 + 8
+    # 10 int32 fields, 9 pointers, the 64-bit stochastic-rounding seed, the class
+    # order pointer and its four class ends
+    assert ctypes.sizeof(R.seed_state) == 10 * 4 + 9 * 8 + 8 + 8 + 4 * 4
     assert R.seed_state.a.offset == 56
     # the C compiler's view of seed.h agrees field by field with the ctypes mirror
     gcc = shutil.which('gcc')
@@ -118,6 +119,21 @@ def test_decode_rejects_missing_inputs():
     m2 = make_state(variant=R.SEED_MAMBA2, d_v=64, r=16, r_max=16)
     assert decode(m2, A=None, beta=None) == R.SEED_ERR_INVALID_ARG
     assert R._lib.seed_decode_step(None, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None) == R.SEED_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize('ends', [(1, 0, 2, 4), (0, 1, 2, 3), (0, 0, 0, 5), (-1, 0, 0, 4)])
+def test_class_order_rejected_on_host(ends):
+    # class ends must not decrease and must end at n_heads; checked before any launch
+    st = make_state(rank=FAKE, r_max=32, head_order=FAKE)
+    for c in range(4):
+        st.class_end[c] = ends[c]
+    before = st.steps_since_compress
+    assert decode(st) == R.SEED_ERR_INVALID_ARG
+    assert st.steps_since_compress == before
+    f = R._lib.seed_recompress_ws
+    st.steps_since_compress = 16
+    assert f(ctypes.byref(st), None, None, FAKE, 1 << 30, None) == R.SEED_ERR_INVALID_ARG
+    assert st.steps_since_compress == 16
 
 
 def test_zero_heads_is_a_no_op_that_advances_the_counter():

@@ -27,6 +27,7 @@ def head_view(buf, h: int) -> R.seed_state:
     v = R.seed_state()
     ctypes.memmove(ctypes.byref(v), ctypes.byref(st), ctypes.sizeof(st))
     v.n_heads = 1
+    v.head_order = None  # the class order lists all heads; a one-head view has none
     v.a = st.a + h * buf.d_k * 4
     v.status = st.status + h * 4
     if st.vbar_index:
