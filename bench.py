@@ -434,8 +434,8 @@ def run_gpu(args, w):
     elif w.factor_dtype == 'f32':
         rec_kernels = 'qr_phase + svd_phase + rebuild_phase'
     else:
-        rec_kernels = ('gram_classify + ' if run.state.ranks is not None else '') + \
-            'gram_phase + evd_phase + gram_rebuild'
+        listed = run.state.ranks is not None and run.state.head_order is None  # class lists on the device
+        rec_kernels = ('gram_classify + ' if listed else '') + 'gram_phase + evd_phase + gram_rebuild'
     roof_rec = dict(kernel=f'{rec_kernels} (recompress)', bound='alu', achieved=rec_tflops and round(rec_tflops, 3),
                     peak=round(fp32_peak, 1), unit='TFLOP/s',
                     frac=rec_tflops and round(rec_tflops / fp32_peak, 4), traffic=rec_traffic,
