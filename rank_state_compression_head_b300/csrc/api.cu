@@ -6,6 +6,8 @@
 // lives in the caller's seed_state and device buffers.  The one exception is
 // the fixed device scratch of seed_recompress_noalloc (recompress_split.cu),
 // a file-scope __device__ array that every device loading the library holds.
+// Besides that, the decode launchers remember per device which of their kernels
+// already had their shared-memory attributes set.
 #include "common.cuh"
 
 #include <stdint.h>

@@ -338,7 +338,6 @@ namespace seedk {
 cudaError_t launch_decode(const StateView &sv, int factor_dtype, const float *q, const float *k,
                           const float *v, const float *gate, const float *beta, const float *A,
                           float *o, int cols_max, cudaStream_t s);
-int sm_count();
 cudaError_t launch_decode_mma(const DecodeArgs &a, int factor_dtype, int cols_max, cudaStream_t s);
 cudaError_t launch_recompress(const StateView &sv, int factor_dtype, float *trunc_err,
                               int32_t *sweeps, int m_max, cudaStream_t s);

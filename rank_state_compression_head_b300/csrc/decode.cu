@@ -22,6 +22,8 @@
 // stored bf16 column is rounded exactly once.
 #include "common.cuh"
 
+#include <atomic>
+
 namespace seedk {
 
 constexpr int kConsumerWarps = 8;
@@ -413,29 +415,25 @@ decode_kernel(const DecodeArgs p) {
   }
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 template <int VAR, typename TF, int DV, int MAXC>
 static cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
   using L = DecodeSmem<VAR, TF, DV, MAXC>;
   auto kern = decode_kernel<VAR, TF, DV, MAXC>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+  // attributes belong to (kernel, device): set them the first time this kernel runs on
+  // each device of the process; the SM count is the current device's
+  static std::atomic<uint64_t> ready{0};
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+  if (!bit || !(ready.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
     if (e != cudaSuccess) return e;
-    configured = true;
+    ready.fetch_or(bit, std::memory_order_acq_rel);
   }
   const int per_sm = (227 * 1024) / (L::BYTES + 1024) >= 2 ? 2 : 1;
-  int grid = sm_count() * per_sm;
+  int grid = (sms > 0 ? sms : 1) * per_sm;
   if (grid > a.sv.n_heads) grid = a.sv.n_heads;
   kern<<<grid, (kConsumerWarps + 1) * 32, L::BYTES, s>>>(a);
   return cudaGetLastError();

@@ -117,9 +117,13 @@ __global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_ke
   // head of launch item i: through the class order when the launch has one
   auto head_at = [&](int i) { return sv.order ? sv.order[p.pos0 + i] : i; };
 
-  // Copy head number i of this CTA into stage i % NS (one commit group per head,
-  // empty when i is past the end, so that group counting stays uniform).
+  // Copy head number i of this CTA into stage i % NS in two commit groups, U and the
+  // per-head vectors first, W second (empty when i is past the end, so that group
+  // counting stays uniform): the U pass needs only the first.
   auto issue = [&](int i) {
+    const TF *wsrc = nullptr;
+    unsigned char *wst = nullptr;
+    int wm = 0;
     if (i < nmine) {
       const int h = head_at(first + i * G);
       const int r_h = sv.rank_of(h);
@@ -132,19 +136,13 @@ __global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_ke
         const TF *Wg = reinterpret_cast<const TF *>(sv.W) + c0 * DV;
         // 16-byte chunk c of column j: a thread keeps its chunk and walks the
         // columns NT / chunks-per-column apart (pointer increments only)
-        constexpr int UCH = DK * 2 / 16, WCH = DV * 2 / 16;  // 16-byte chunks per column
-        constexpr int UJS = NT / UCH, WJS = NT / WCH;         // column step of a thread
+        constexpr int UCH = DK * 2 / 16;  // 16-byte chunks per column
+        constexpr int UJS = NT / UCH;     // column step of a thread
         {
           const int c = tid % UCH;
           unsigned char *d = st + S::U_OFF + (tid / UCH) * S::USTR + c * 16;
           const TF *src = Ug + (int64_t)(tid / UCH) * DK + c * 8;
           for (int j = tid / UCH; j < m; j += UJS, d += UJS * S::USTR, src += UJS * DK) cp_async16(d, src);
-        }
-        {
-          const int c = tid % WCH;
-          unsigned char *d = st + S::W_OFF + (tid / WCH) * S::WSTR + c * 16;
-          const TF *src = Wg + (int64_t)(tid / WCH) * DV + c * 8;
-          for (int j = tid / WCH; j < m; j += WJS, d += WJS * S::WSTR, src += WJS * DV) cp_async16(d, src);
         }
         if (tid < DK / 4) {
           cp_async16(st + S::Q_OFF + tid * 16, p.q + (int64_t)h * DK + tid * 4);
@@ -168,7 +166,18 @@ __global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_ke
           for (int cc = c; cc * 4 < m; cc += NT - DK / 4 - DV / 4 - 1)
             cp_async16(st + S::SC_OFF + cc * 16, sv.scale + c0 + cc * 4);
         }
+        wsrc = Wg;
+        wm = m;
+        wst = st;
       }
+    }
+    cp_async_commit();  // first group: U and the per-head vectors
+    if (wsrc) {         // second group: W, on its way while the U pass runs
+      constexpr int WCH = DV * 2 / 16, WJS = NT / WCH;
+      const int c = tid % WCH;
+      unsigned char *d = wst + S::W_OFF + (tid / WCH) * S::WSTR + c * 16;
+      const TF *src = wsrc + (int64_t)(tid / WCH) * DV + c * 8;
+      for (int j = tid / WCH; j < wm; j += WJS, d += WJS * S::WSTR, src += WJS * DV) cp_async16(d, src);
     }
     cp_async_commit();
   };
@@ -178,7 +187,7 @@ __global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_ke
   for (int i = 0; i < nmine; ++i) {
     // The stage of head i-1 is free: its last readers passed barrier C of that head.
     issue(i + NS - 1);
-    cp_async_wait<NS - 1>();  // this thread's copies of head i have landed
+    cp_async_wait<2 * NS - 1>();  // this thread's copies of head i's U and vectors have landed
 
     const int h = head_at(first + i * G);
     const int r_h = sv.rank_of(h);
@@ -326,7 +335,8 @@ __global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_ke
       const float r = warp_reduce8(S_loc, lane);
       if ((lane & 3) == 0) scal[warp * 8 + reduce8_index(lane)] = r;
     }
-    __syncthreads();  // barrier B: x, the padding and the scalar partials are visible
+    cp_async_wait<2 * NS - 2>();  // and its copies of head i's W
+    __syncthreads();  // barrier B: x, W, the padding and the scalar partials are visible
     float Sg[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
