@@ -493,10 +493,52 @@ __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phas
   float *ws = p.ws + (int64_t)slot * W.per_head;
   {
     const int nb = (m + 3) / 4, nblk = nb * (nb + 1) / 2;
-    for (int blk = tid; blk < nblk; blk += kGramThreads) {
-      int jb = 0, rem = blk;  // blk -> (jb <= lb)
-      while (rem >= nb - jb) { rem -= nb - jb; ++jb; }
-      const int lb = jb + rem;
+    // More blocks than threads (64 columns: 136): the off-diagonal blocks one a thread and
+    // the diagonal ones two a thread, their upper triangles only (10 entries each), so
+    // that no thread takes a second round while the others wait (same sums, same order)
+    const int noff = nb * (nb - 1) / 2;
+    const bool pair_diag = nblk > kGramThreads;
+    for (int d = tid - noff; pair_diag && d >= 0 && 2 * d < nb; d += kGramThreads) {
+      float acc2[2][10] = {};
+      const int jb0 = 2 * d, nd = 2 * d + 1 < nb ? 2 : 1;
+      for (int i = 0; i < DK; ++i) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          if (q < nd) {
+            const float4 x = *reinterpret_cast<const float4 *>(B + i * BP + 4 * (jb0 + q));
+            const float xs[4] = {x.x, x.y, x.z, x.w};
+            int e = 0;
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+              for (int c = a; c < 4; ++c, ++e) acc2[q][e] = fmaf(xs[a], xs[c], acc2[q][e]);
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        int e = 0;
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int c = a; c < 4; ++c, ++e) {
+            const int j = 4 * (jb0 + q) + a, l = 4 * (jb0 + q) + c;
+            if (q < nd && j < m && l < m) {
+              ws[W.mq + j * m + l] = acc2[q][e];
+              ws[W.mq + l * m + j] = acc2[q][e];
+            }
+          }
+      }
+    }
+    for (int blk = tid; blk < (pair_diag ? noff : nblk); blk += kGramThreads) {
+      int jb = 0, lb = 0, rem = blk;
+      if (pair_diag) {  // blk -> (jb < lb)
+        while (rem >= nb - 1 - jb) { rem -= nb - 1 - jb; ++jb; }
+        lb = jb + 1 + rem;
+      } else {          // blk -> (jb <= lb)
+        while (rem >= nb - jb) { rem -= nb - jb; ++jb; }
+        lb = jb + rem;
+      }
       float acc[4][4] = {};
       for (int i = 0; i < DK; ++i) {
         const float4 x = *reinterpret_cast<const float4 *>(B + i * BP + 4 * jb);
