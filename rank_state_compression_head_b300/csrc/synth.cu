@@ -302,8 +302,10 @@ __global__ void __launch_bounds__(256) prefill_kernel(const seed_synth_workload 
 //     S_C = diag(gamma_C) S_0 + sum_r (gamma_C / gm_r * k_r) x_r^T + (gamma_C / gamma_r * k_r) y_r^T.
 //   Mamba-2 (no erase): S_C = gamma_C S_0 + sum_t (gamma_C / gamma_t) dt_t B_t x_t^T.
 // All arithmetic is fp32 FMA.  One CTA of 256 threads per head; thread
-// (q, j) holds column j of the state for a quarter or half of its rows in
-// registers; the chunk's tokens are generated in parallel (one warp a token).
+// (q, jp) holds columns 2jp and 2jp + 1 of the state for a quarter (d_v = 128) or
+// an eighth (d_v = 64) of its rows in registers, so that each key value it reads
+// from shared memory serves two columns; the chunk's tokens are generated in
+// parallel (one warp a token); the triangular solve takes one column a thread.
 // ---------------------------------------------------------------------------
 
 // One warp generates every input of one prefill token (the values of gen_token).
@@ -359,7 +361,7 @@ constexpr int chunk_len() { return VAR == SEED_KDA ? 16 : 32; }
 template <int VAR, int DV>
 struct ChunkSmem {
   static constexpr int DK = kDK, C = chunk_len<VAR>();
-  static constexpr int NQ = 256 / DV;                         // row groups of the state
+  static constexpr int NQ = 512 / DV;                         // row groups of the state (two columns a thread)
   static constexpr bool KDA = VAR == SEED_KDA;
   static constexpr int K_OFF = 0;                             // [C][DK] keys, later update weights
   static constexpr int V_OFF = K_OFF + C * DK;                // [C][DV] values, later U (or y)
@@ -387,7 +389,10 @@ __global__ void __launch_bounds__(256, 2) prefill_chunk_kernel(const seed_synth_
 
   const int64_t h = head0 + blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int j = tid % DV, q = tid / DV, i0 = q * RPT;
+  // state mapping: thread (q, jp) holds columns j2, j2 + 1 of rows i0 .. i0 + RPT - 1, so that
+  // every key value read from shared memory serves two columns
+  const int jp = tid % (DV / 2), q = tid / (DV / 2), i0 = q * RPT, j2 = 2 * jp;
+  const int j = tid;  // the triangular solve: one column per thread (tid < DV)
   const int n_dir = w.n_layers * w.n_head;
   const int dir = (int)(h % n_dir);
   const int L_tok = plen[h / n_dir];
@@ -395,9 +400,9 @@ __global__ void __launch_bounds__(256, 2) prefill_chunk_kernel(const seed_synth_
   const float sd = sink[dir];
   const float Ad = M2 ? A[dir] : 0.f;
 
-  float st[RPT];
+  float st[RPT][2];
 #pragma unroll
-  for (int r = 0; r < RPT; ++r) st[r] = 0.f;
+  for (int r = 0; r < RPT; ++r) st[r][0] = st[r][1] = 0.f;
 
   for (int t0 = 0; t0 < L_tok; t0 += C) {
     // ---- the chunk's tokens (past the prompt: identity steps) ----------------------------------
@@ -463,25 +468,35 @@ __global__ void __launch_bounds__(256, 2) prefill_chunk_kernel(const seed_synth_
       }
       // ---- partial P over my rows: P[q][t][j] = sum_i k_t[i] w_t[i] S_0[i][j] ----------------------
       // (w_t = gamma_t for the scalar gate, applied after; gm_t per channel)
-      float acc[C];
+      // (tokens in halves of 16 to bound the accumulators)
 #pragma unroll
-      for (int t = 0; t < C; ++t) acc[t] = 0.f;
+      for (int th = 0; th < C; th += 16) {
+        float acc[16][2];
 #pragma unroll
-      for (int r4 = 0; r4 < RPT / 4; ++r4) {
+        for (int t = 0; t < 16; ++t) acc[t][0] = acc[t][1] = 0.f;
 #pragma unroll
-        for (int t = 0; t < C; ++t) {
-          float4 kk = *reinterpret_cast<const float4 *>(Kc + t * DK + i0 + 4 * r4);
-          if (KDA && t > 0) {
-            const float4 g = *reinterpret_cast<const float4 *>(Gc + (t - 1) * DK + i0 + 4 * r4);
-            kk = make_float4(kk.x * g.x, kk.y * g.y, kk.z * g.z, kk.w * g.w);
+        for (int r4 = 0; r4 < RPT / 4; ++r4) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            float4 kk = *reinterpret_cast<const float4 *>(Kc + (th + t) * DK + i0 + 4 * r4);
+            if (KDA && th + t > 0) {
+              const float4 g = *reinterpret_cast<const float4 *>(Gc + (th + t - 1) * DK + i0 + 4 * r4);
+              kk = make_float4(kk.x * g.x, kk.y * g.y, kk.z * g.z, kk.w * g.w);
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              acc[t][c] = fmaf(kk.x, st[4 * r4][c], fmaf(kk.y, st[4 * r4 + 1][c],
+                               fmaf(kk.z, st[4 * r4 + 2][c], fmaf(kk.w, st[4 * r4 + 3][c], acc[t][c]))));
           }
-          acc[t] = fmaf(kk.x, st[4 * r4], fmaf(kk.y, st[4 * r4 + 1], fmaf(kk.z, st[4 * r4 + 2], fmaf(kk.w, st[4 * r4 + 3], acc[t]))));
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float sc = KDA ? 1.f : Gi[th + t];
+          *reinterpret_cast<float2 *>(Pp + (q * C + th + t) * DV + j2) = make_float2(acc[t][0] * sc, acc[t][1] * sc);
         }
       }
-#pragma unroll
-      for (int t = 0; t < C; ++t) Pp[(q * C + t) * DV + j] = KDA ? acc[t] : acc[t] * Gi[t];
       __syncthreads();
-      if (q == 0) {
+      if (tid < DV) {
         // the triangular solve, one column j per thread, with the chunk's solution in
         // registers (fully unrolled: row t's sum runs as soon as its terms are ready)
         if (KDA) {
@@ -541,23 +556,31 @@ __global__ void __launch_bounds__(256, 2) prefill_chunk_kernel(const seed_synth_
     // ---- S_C = Gamma_C S_0 + sum_t (weights_t) (x) (U or x, y)_t over my rows ---------------------
     {
 #pragma unroll
-      for (int r = 0; r < RPT; ++r) st[r] *= KDA ? gCr[i0 + r] : (M2 ? expf(Gi[C - 1]) : Gi[C - 1]);
+      for (int r = 0; r < RPT; ++r) {
+        const float g = KDA ? gCr[i0 + r] : (M2 ? expf(Gi[C - 1]) : Gi[C - 1]);
+        st[r][0] *= g;
+        st[r][1] *= g;
+      }
       for (int t = 0; t < C; ++t) {
-        const float u = Vc[t * DV + j];
-        const float x = KDA ? Pp[t * DV + j] : 0.f;
+        const float2 u = *reinterpret_cast<const float2 *>(Vc + t * DV + j2);
+        const float2 x = KDA ? *reinterpret_cast<const float2 *>(Pp + t * DV + j2) : make_float2(0.f, 0.f);
 #pragma unroll
         for (int r4 = 0; r4 < RPT / 4; ++r4) {
           const float4 kk = *reinterpret_cast<const float4 *>(Kc + t * DK + i0 + 4 * r4);
-          st[4 * r4] = fmaf(kk.x, u, st[4 * r4]);
-          st[4 * r4 + 1] = fmaf(kk.y, u, st[4 * r4 + 1]);
-          st[4 * r4 + 2] = fmaf(kk.z, u, st[4 * r4 + 2]);
-          st[4 * r4 + 3] = fmaf(kk.w, u, st[4 * r4 + 3]);
+          const float ks[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            st[4 * r4 + e][0] = fmaf(ks[e], u.x, st[4 * r4 + e][0]);
+            st[4 * r4 + e][1] = fmaf(ks[e], u.y, st[4 * r4 + e][1]);
+          }
           if (KDA) {
             const float4 k1 = *reinterpret_cast<const float4 *>(Gc + t * DK + i0 + 4 * r4);
-            st[4 * r4] = fmaf(k1.x, x, st[4 * r4]);
-            st[4 * r4 + 1] = fmaf(k1.y, x, st[4 * r4 + 1]);
-            st[4 * r4 + 2] = fmaf(k1.z, x, st[4 * r4 + 2]);
-            st[4 * r4 + 3] = fmaf(k1.w, x, st[4 * r4 + 3]);
+            const float k1s[4] = {k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              st[4 * r4 + e][0] = fmaf(k1s[e], x.x, st[4 * r4 + e][0]);
+              st[4 * r4 + e][1] = fmaf(k1s[e], x.y, st[4 * r4 + e][1]);
+            }
           }
         }
       }
@@ -566,7 +589,8 @@ __global__ void __launch_bounds__(256, 2) prefill_chunk_kernel(const seed_synth_
   }
   float *out = S_out + (int64_t)blockIdx.x * DK * DV;
 #pragma unroll
-  for (int r = 0; r < RPT; ++r) out[(int64_t)(i0 + r) * DV + j] = st[r];
+  for (int r = 0; r < RPT; ++r)
+    *reinterpret_cast<float2 *>(out + (int64_t)(i0 + r) * DV + j2) = make_float2(st[r][0], st[r][1]);
 }
 
 static int check_workload(const seed_synth_workload *w) {
