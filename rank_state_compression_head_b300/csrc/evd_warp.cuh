@@ -10,15 +10,16 @@
 // rows needs about half the sweeps that it needs on K itself.
 //
 // Layout: M sits in the warp's shared square (SvdWarpSmem), column c at
-// T[c * TP], rows and columns m..MR-1 zero; lane l looks after indices l and
-// l + HW.  The Schur complement stays in the original index order, nothing is
-// swapped: step j picks the remaining index p of largest diagonal, forms row j
-// of Rt (Rt[j][x] = S[x][p] / sqrt(S[p][p]) for the remaining x, zero for the
-// pivoted ones), updates the remaining columns S[.][c] -= Rt[j][.] Rt[j][c], and
-// then stores row j of Rt in column p, which is no longer needed.  So Rt's rows
-// are kept in the original column order, and the Jacobi's columns give the
-// eigenvectors directly in that order (no permutation back).  A diagonal that
-// has fallen to zero or below (rounding) gives a zero row.
+// T[c * TP], rows and columns m..MR-1 zero; lane l takes columns l and l + HW
+// into registers.  The Schur complement stays in the original index order,
+// nothing is swapped: step j picks the remaining index p of largest diagonal;
+// the pivot's lane forms row j of Rt (Rt[j][x] = S[x][p] / sqrt(S[p][p]) for the
+// remaining x, zero for the pivoted ones) and stores it where column p was, and
+// every lane reads it back and updates its remaining columns S[.][c] -=
+// Rt[j][.] Rt[j][c].  So Rt's rows are kept in the original column order, and
+// the Jacobi's columns give the eigenvectors directly in that order (no
+// permutation back).  A diagonal that has fallen to zero or below (rounding)
+// gives a zero row.
 #pragma once
 
 #include "svd_warp.cuh"
@@ -40,9 +41,27 @@ __device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw) {
   int *piv = reinterpret_cast<int *>(sw + L::P_OFF);
   const int c0 = lane, c1 = lane + HW;
 
+  // My columns in registers (rows 0..MR-1; rows and columns from m on are zero).
+  float colA[MR], colB[TWO ? MR : 1];
+  {
+    const float4 *a4 = reinterpret_cast<const float4 *>(T + c0 * TP);
+    const float4 *b4 = reinterpret_cast<const float4 *>(T + (TWO && c1 < MR ? c1 : 0) * TP);
+#pragma unroll
+    for (int q = 0; q < MR / 4; ++q) {
+      const float4 x = c0 < MR ? a4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+      colA[4 * q] = x.x; colA[4 * q + 1] = x.y; colA[4 * q + 2] = x.z; colA[4 * q + 3] = x.w;
+      if constexpr (TWO) {
+        const float4 y = c1 < MR ? b4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        colB[4 * q] = y.x; colB[4 * q + 1] = y.y; colB[4 * q + 2] = y.z; colB[4 * q + 3] = y.w;
+      }
+    }
+  }
   bool done0 = c0 >= m, done1 = !TWO || c1 >= m;
   float dg0 = done0 ? 0.f : T[c0 * TP + c0];
   float dg1 = done1 ? 0.f : T[c1 * TP + c1];
+  // rows already pivoted (and rows from m on), the same in every lane
+  uint64_t gone = m >= 64 ? 0ull : ~0ull << m;
+  __syncwarp(full);  // every lane has read its columns; the square now takes the rows of Rt
   // order-preserving integer key of a finite float (larger float, larger key; 0 = none)
   auto okey = [](float f) {
     const unsigned u = __float_as_uint(f);
@@ -61,42 +80,45 @@ __device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw) {
     const float best = __uint_as_float((kmax & 0x80000000u) ? (kmax ^ 0x80000000u) : ~kmax);
     const float d = fmaxf(best, 0.f);
     const float inv = d > 0.f ? rsqrtf(d) : 0.f;  // 1 / r_jj (a couple of ulp)
-    float *cp = T + p * TP;
+    float *row = T + p * TP;  // row j of Rt goes where column p was
+    // The pivot's lane writes row j of Rt: Rt[j][x] = S[x][p] / r_jj for the rows not yet
+    // pivoted (r_jj at x = p), zero for the others.
     if (lane == (p & (HW - 1))) {
-      if (p >= HW) done1 = true;
-      else done0 = true;
-    }
-    // Schur update of my remaining columns: S[.][c] -= (S[.][p] / rjj) (S[c][p] / rjj)
-    const float4 *p4 = reinterpret_cast<const float4 *>(cp);
-#pragma unroll
-    for (int e = 0; e < (TWO ? 2 : 1); ++e) {
-      if (e == 0 ? done0 : done1) continue;
-      const int c = e == 0 ? c0 : c1;
-      const float t = cp[c] * inv * inv;
-      float4 *x4 = reinterpret_cast<float4 *>(T + c * TP);
+      const bool hi = p >= HW;
 #pragma unroll
       for (int q = 0; q < MR / 4; ++q) {
-        const float4 v = p4[q];
-        float4 x = x4[q];
-        x.x = fmaf(-t, v.x, x.x); x.y = fmaf(-t, v.y, x.y); x.z = fmaf(-t, v.z, x.z); x.w = fmaf(-t, v.w, x.w);
-        x4[q] = x;
-      }
-      if (e == 0) dg0 = T[c * TP + c];
-      else dg1 = T[c * TP + c];
-    }
-    __syncwarp(full);  // column p has been read by every lane
-    // column p becomes row j of Rt: my two entries of it (zero where already pivoted,
-    // including p itself before this step's flag; Rt[j][p] = S[p][p] / rjj = rjj)
+        float v[4];
 #pragma unroll
-    for (int e = 0; e < (TWO ? 2 : 1); ++e) {
-      const int x = e == 0 ? c0 : c1;
-      if (x < MR) {
-        const bool was_done = x == p ? false : (e == 0 ? done0 : done1);
-        cp[x] = was_done ? 0.f : cp[x] * inv;
+        for (int e = 0; e < 4; ++e) {
+          const int x = 4 * q + e;
+          const float sx = (TWO && hi) ? colB[TWO ? x : 0] : colA[x];
+          v[e] = (gone >> x) & 1ull ? 0.f : sx * inv;
+        }
+        reinterpret_cast<float4 *>(row)[q] = make_float4(v[0], v[1], v[2], v[3]);
+      }
+      if (hi) done1 = true;
+      else done0 = true;
+    }
+    gone |= 1ull << p;
+    __syncwarp(full);
+    // Schur update of my remaining columns: S[x][c] -= Rt[j][x] Rt[j][c]
+    const float4 *r4 = reinterpret_cast<const float4 *>(row);
+    const float t0 = done0 ? 0.f : row[c0];
+    const float t1 = done1 ? 0.f : row[TWO ? c1 : 0];
+#pragma unroll
+    for (int q = 0; q < MR / 4; ++q) {
+      const float4 v = r4[q];
+      const float vs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        colA[4 * q + e] = fmaf(-vs[e], t0, colA[4 * q + e]);
+        if constexpr (TWO) colB[4 * q + e] = fmaf(-vs[e], t1, colB[4 * q + e]);
       }
     }
+    dg0 = fmaf(-t0, t0, dg0);
+    if (TWO) dg1 = fmaf(-t1, t1, dg1);
     if (lane == 0) piv[j] = p;
-    __syncwarp(full);
+    __syncwarp(full);  // row j has been read by every lane
   }
 
   // ---- rows of Rt to the Jacobi seats: seat s = column piv[s] -----------------------------
