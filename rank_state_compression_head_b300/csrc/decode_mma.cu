@@ -8,8 +8,11 @@
 // CTAs of 128 threads walk the heads blockIdx.x, blockIdx.x + gridDim.x, ...
 // through a ring of NS shared-memory stages (NS - 1 heads in flight while one
 // is computed); launched with one stage and one head per CTA, as many CTAs per
-// SM as fit keep several heads' loads in flight.  The threads copy the factor
-// columns (contiguous in HBM) with asynchronous 16-byte copies into rows padded
+// SM as fit keep several heads' loads in flight.  With the state's class order
+// there is one launch per column class, each with stages sized for its class
+// (seed.h).  A head's copies form two groups, U and the per-head vectors first
+// and W second, so that the U pass starts while W is on its way.  The threads
+// copy the factor columns (contiguous in HBM) with asynchronous 16-byte copies into rows padded
 // to 272 bytes, so that the ldmatrix reads below hit 32 distinct banks.  Per
 // head the CTA does
 //

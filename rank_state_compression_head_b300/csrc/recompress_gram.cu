@@ -42,9 +42,11 @@
 //
 // Workspace per head (fp32): M [m][m], R_b [m][m] (upper, row-major), Y [r][m4]
 // (m4 = m rounded up to 4), eight words of class lists, each region on 16 bytes,
-// the whole on 256 bytes.  With ragged ranks a chunk's heads are first listed by
-// 16-column class (gram_classify), and each class's three launches run over its
-// list, so that every lane group of an evd_phase CTA has a head of the class.
+// the whole on 256 bytes.  With ragged ranks each 16-column class gets its own
+// three launches, sized for it: with the state's class order (seed.h) over
+// exactly the class's positions in it, chunk by chunk; without it, over a list
+// of the chunk's heads of the class that gram_classify builds first.  Either way
+// every lane group of an evd_phase CTA has a head of the class.
 #include "evd_warp.cuh"
 
 #include <type_traits>
