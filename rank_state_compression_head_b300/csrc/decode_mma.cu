@@ -5,16 +5,17 @@
 // Exact Update (Lemma 2); thelatestinai.com list view, Table 1 (decode
 // column: read-out and update of each recurrent state).
 //
-// CTAs of 128 threads walk the heads blockIdx.x, blockIdx.x + gridDim.x, ...
-// through a ring of NS shared-memory stages (NS - 1 heads in flight while one
-// is computed); launched with one stage and one head per CTA, as many CTAs per
-// SM as fit keep several heads' loads in flight.  With the state's class order
-// there is one launch per column class, each with stages sized for its class
-// (seed.h).  A head's copies form two groups, U and the per-head vectors first
-// and W second, so that the U pass starts while W is on its way.  The threads
-// copy the factor columns (contiguous in HBM) with asynchronous 16-byte copies into rows padded
-// to 272 bytes, so that the ldmatrix reads below hit 32 distinct banks.  Per
-// head the CTA does
+// A persistent grid of CTAs of 128 threads (as many as fit on the device) walks
+// the heads blockIdx.x, blockIdx.x + gridDim.x, ... with one shared-memory stage
+// a CTA.  A head's copies form two groups, U and the per-head vectors first and
+// W second, and each half of the stage is refilled with the next head's data as
+// soon as the current head has read it: the next U during this head's W pass,
+// the next W during its update and the next head's U pass.  So every CTA keeps
+// copies in flight while it computes.  With the state's class order there is one
+// launch per column class, each with a stage sized for its class (seed.h).  The
+// threads copy the factor columns (contiguous in HBM) with asynchronous 16-byte
+// copies into rows padded to 272 bytes, so that the ldmatrix reads below hit 32
+// distinct banks.  Per head the CTA does
 //
 //   split    rows [k_hi; k_lo; q_hi; q_lo] of the U-pass operand, once (smem)
 //   U pass   X[4][m] = [k_hi; k_lo; q_hi; q_lo] U_stored          (mma m16n8k16)
@@ -58,12 +59,12 @@ struct MmaStage {
                 "16-byte copies");
 };
 
-template <int VAR, int DV, int MAXC, int NS>
+template <int VAR, int DV, int MAXC>
 struct MmaSmem {
   using S = MmaStage<VAR, DV, MAXC>;
   static constexpr int NX = VAR == SEED_MAMBA2 ? 1 : 2;
   static constexpr int XLD = MAXC + 16;                                    // bf16 per x row
-  static constexpr int XS_OFF = NS * S::BYTES;                             // bf16 [2 NX][XLD]
+  static constexpr int XS_OFF = S::BYTES;                                  // bf16 [2 NX][XLD]
   static constexpr int WX_OFF = XS_OFF + ((2 * NX * XLD * 2 + 15) & ~15);  // f32 [NX][DV]
   static constexpr int SCAL_OFF = WX_OFF + NX * DV * 4;                    // f32 [NW][8]
   static constexpr int ALD = kDK + 8;                                      // 16-bit per operand row
@@ -92,12 +93,17 @@ __device__ static inline void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
-template <typename TF, int VAR, int DV, int MAXC, int NS>
-__global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_kernel(const DecodeArgs p) {
+// CTAs an SM should hold: as many as the stage's shared memory allows for the
+// larger classes (5 of 40.5 KB, 7 of 32 KB), 8 for the smaller ones
+template <int MAXC>
+constexpr int mma_min_blocks() { return MAXC > 48 ? 5 : MAXC > 32 ? 7 : 8; }
+
+template <typename TF, int VAR, int DV, int MAXC>
+__global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MAXC>()) decode_mma_kernel(const DecodeArgs p) {
   constexpr int DK = kDK;
   constexpr int NT = kMmaThreads;
   using S = MmaStage<VAR, DV, MAXC>;
-  using L = MmaSmem<VAR, DV, MAXC, NS>;
+  using L = MmaSmem<VAR, DV, MAXC>;
   constexpr int NX = L::NX;
   constexpr int NA = 2 * NX;  // rows of the U-pass operand: hi/lo of k (and q)
   constexpr bool KDA = VAR == SEED_KDA;
@@ -106,6 +112,7 @@ __global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_ke
   static_assert(MAXC % 16 == 0 && MAXC <= 64, "column tiles");
 
   extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char *const st = smem;  // the stage: U, W and the per-head vectors
   TF *xs = reinterpret_cast<TF *>(smem + L::XS_OFF);
   float *wxs = reinterpret_cast<float *>(smem + L::WX_OFF);
   float *scal = reinterpret_cast<float *>(smem + L::SCAL_OFF);
@@ -120,93 +127,107 @@ __global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_ke
   // head of launch item i: through the class order when the launch has one
   auto head_at = [&](int i) { return sv.order ? sv.order[p.pos0 + i] : i; };
 
-  // Copy head number i of this CTA into stage i % NS in two commit groups, U and the
-  // per-head vectors first, W second (empty when i is past the end, so that group
-  // counting stays uniform): the U pass needs only the first.
-  auto issue = [&](int i) {
-    const TF *wsrc = nullptr;
-    unsigned char *wst = nullptr;
-    int wm = 0;
-    if (i < nmine) {
-      const int h = head_at(first + i * G);
-      const int r_h = sv.rank_of(h);
-      const int m = r_h + growth * sv.steps;
-      if (r_h >= 0 && m <= MAXC) {
-        unsigned char *st = smem + (i % NS) * S::BYTES;
-        const int64_t c0 = sv.col0(h);
-        const int dir = sv.dir_of(h);
-        const TF *Ug = reinterpret_cast<const TF *>(sv.U) + c0 * DK;
-        const TF *Wg = reinterpret_cast<const TF *>(sv.W) + c0 * DV;
-        // 16-byte chunk c of column j: a thread keeps its chunk and walks the
-        // columns NT / chunks-per-column apart (pointer increments only)
-        constexpr int UCH = DK * 2 / 16;  // 16-byte chunks per column
-        constexpr int UJS = NT / UCH;     // column step of a thread
-        {
-          const int c = tid % UCH;
-          unsigned char *d = st + S::U_OFF + (tid / UCH) * S::USTR + c * 16;
-          const TF *src = Ug + (int64_t)(tid / UCH) * DK + c * 8;
-          for (int j = tid / UCH; j < m; j += UJS, d += UJS * S::USTR, src += UJS * DK) cp_async16(d, src);
+  // What the copies of an item need: its head, rank, columns and sink direction.
+  // The head index is read one item ahead and the rest during the U pass, so that
+  // the chain of dependent reads is off the path of the copies.
+  struct Item {
+    int h, r, m, dir;
+    int64_t c0;
+  };
+  auto describe = [&](int h, Item &it) {
+    it.h = h;
+    it.r = h >= 0 ? sv.rank_of(h) : -1;
+    it.m = it.r + growth * sv.steps;
+    const bool ok = it.r >= 0 && it.m <= MAXC;
+    it.c0 = ok ? sv.col0(h) : 0;
+    it.dir = ok ? sv.dir_of(h) : 0;
+  };
+  auto valid = [&](const Item &it) { return it.r >= 0 && it.m <= MAXC; };
+
+  // The copies of an item form two commit groups (empty for no item, so that the
+  // group counting stays uniform): U and the per-head vectors, then W.
+  auto issue_u = [&](const Item &it) {
+    if (valid(it)) {
+      const int h = it.h, m = it.m;
+      const int64_t c0 = it.c0;
+      const TF *Ug = reinterpret_cast<const TF *>(sv.U) + c0 * DK;
+      // 16-byte chunk c of column j: a thread keeps its chunk and walks the
+      // columns NT / chunks-per-column apart (pointer increments only)
+      constexpr int UCH = DK * 2 / 16;  // 16-byte chunks per column
+      constexpr int UJS = NT / UCH;     // column step of a thread
+      {
+        const int c = tid % UCH;
+        unsigned char *d = st + S::U_OFF + (tid / UCH) * S::USTR + c * 16;
+        const TF *src = Ug + (int64_t)(tid / UCH) * DK + c * 8;
+        for (int j = tid / UCH; j < m; j += UJS, d += UJS * S::USTR, src += UJS * DK) cp_async16(d, src);
+      }
+      if (tid < DK / 4) {
+        cp_async16(st + S::Q_OFF + tid * 16, p.q + (int64_t)h * DK + tid * 4);
+        cp_async16(st + S::K_OFF + tid * 16, p.k + (int64_t)h * DK + tid * 4);
+        cp_async16(st + S::A_OFF + tid * 16, sv.a + (int64_t)h * DK + tid * 4);
+        if (KDA) {
+          cp_async16(st + S::SC_OFF + tid * 16, sv.scale + (int64_t)h * DK + tid * 4);
+          cp_async16(st + S::AL_OFF + tid * 16, p.gate + (int64_t)h * DK + tid * 4);
         }
-        if (tid < DK / 4) {
-          cp_async16(st + S::Q_OFF + tid * 16, p.q + (int64_t)h * DK + tid * 4);
-          cp_async16(st + S::K_OFF + tid * 16, p.k + (int64_t)h * DK + tid * 4);
-          cp_async16(st + S::A_OFF + tid * 16, sv.a + (int64_t)h * DK + tid * 4);
-          if (KDA) {
-            cp_async16(st + S::SC_OFF + tid * 16, sv.scale + (int64_t)h * DK + tid * 4);
-            cp_async16(st + S::AL_OFF + tid * 16, p.gate + (int64_t)h * DK + tid * 4);
-          }
-        } else if (tid < DK / 4 + DV / 4) {
-          const int c = tid - DK / 4;
-          cp_async16(st + S::V_OFF + c * 16, p.v + (int64_t)h * DV + c * 4);
-          cp_async16(st + S::VB_OFF + c * 16, sv.vbar + (int64_t)dir * DV + c * 4);
-        } else if (tid == DK / 4 + DV / 4) {
-          float *gates = reinterpret_cast<float *>(st + S::G_OFF);
-          if (!KDA) cp_async4(gates + 0, p.gate + h);
-          if (!M2) cp_async4(gates + 1, p.beta + h);
-          if (M2) cp_async4(gates + 2, p.A + dir);
-        } else if (!KDA && scales_in_stage(c0, r_h + growth * sv.T)) {
-          const int c = tid - DK / 4 - DV / 4 - 1;
-          for (int cc = c; cc * 4 < m; cc += NT - DK / 4 - DV / 4 - 1)
-            cp_async16(st + S::SC_OFF + cc * 16, sv.scale + c0 + cc * 4);
-        }
-        wsrc = Wg;
-        wm = m;
-        wst = st;
+      } else if (tid < DK / 4 + DV / 4) {
+        const int c = tid - DK / 4;
+        cp_async16(st + S::V_OFF + c * 16, p.v + (int64_t)h * DV + c * 4);
+        cp_async16(st + S::VB_OFF + c * 16, sv.vbar + (int64_t)it.dir * DV + c * 4);
+      } else if (tid == DK / 4 + DV / 4) {
+        float *gates = reinterpret_cast<float *>(st + S::G_OFF);
+        if (!KDA) cp_async4(gates + 0, p.gate + h);
+        if (!M2) cp_async4(gates + 1, p.beta + h);
+        if (M2) cp_async4(gates + 2, p.A + it.dir);
+      } else if (!KDA && scales_in_stage(c0, it.r + growth * sv.T)) {
+        const int c = tid - DK / 4 - DV / 4 - 1;
+        for (int cc = c; cc * 4 < m; cc += NT - DK / 4 - DV / 4 - 1)
+          cp_async16(st + S::SC_OFF + cc * 16, sv.scale + c0 + cc * 4);
       }
     }
-    cp_async_commit();  // first group: U and the per-head vectors
-    if (wsrc) {         // second group: W, on its way while the U pass runs
+    cp_async_commit();
+  };
+  auto issue_w = [&](const Item &it) {
+    if (valid(it)) {
       constexpr int WCH = DV * 2 / 16, WJS = NT / WCH;
       const int c = tid % WCH;
-      unsigned char *d = wst + S::W_OFF + (tid / WCH) * S::WSTR + c * 16;
-      const TF *src = wsrc + (int64_t)(tid / WCH) * DV + c * 8;
-      for (int j = tid / WCH; j < wm; j += WJS, d += WJS * S::WSTR, src += WJS * DV) cp_async16(d, src);
+      unsigned char *d = st + S::W_OFF + (tid / WCH) * S::WSTR + c * 16;
+      const TF *src = reinterpret_cast<const TF *>(sv.W) + it.c0 * DV + (int64_t)(tid / WCH) * DV + c * 8;
+      for (int j = tid / WCH; j < it.m; j += WJS, d += WJS * S::WSTR, src += WJS * DV) cp_async16(d, src);
     }
     cp_async_commit();
   };
 
-  for (int i = 0; i < NS - 1; ++i) issue(i);
+  // One stage, refilled in two halves as soon as each is free: item i+1's U and
+  // vectors are copied in during item i's W pass and update (its U pass and scalars
+  // have read them into registers by barrier B), and its W during item i's update
+  // and item i+1's U pass (item i's W pass is done at barrier C).  So a CTA always
+  // has copies in flight, and several CTAs per SM share the SM's bandwidth.
+  Item cur, nxt;
+  describe(nmine > 0 ? head_at(first) : -1, cur);
+  issue_u(cur);
+  issue_w(cur);
 
   for (int i = 0; i < nmine; ++i) {
-    // The stage of head i-1 is free: its last readers passed barrier C of that head.
-    issue(i + NS - 1);
-    cp_async_wait<2 * NS - 1>();  // this thread's copies of head i's U and vectors have landed
+    const int hn = i + 1 < nmine ? head_at(first + (i + 1) * G) : -1;
+    cp_async_wait<1>();  // this thread's copies of item i's U and vectors have landed
 
-    const int h = head_at(first + i * G);
-    const int r_h = sv.rank_of(h);
-    const int m = r_h + growth * sv.steps;
-    const bool bad_rank = r_h < 0 || m > MAXC;
-    const int64_t c0 = bad_rank ? 0 : sv.col0(h);
-    unsigned char *st = smem + (i % NS) * S::BYTES;
+    const int h = cur.h;
+    const int r_h = cur.r;
+    const int m = cur.m;
+    const bool bad_rank = !valid(cur);
+    const int64_t c0 = cur.c0;
     float *scw = reinterpret_cast<float *>(st + S::SC_OFF);
     if (!bad_rank && !KDA && !scales_in_stage(c0, r_h + growth * sv.T))
       for (int j = tid; j < m; j += NT) scw[j] = sv.scale[c0 + j];  // unaligned column scales
-    __syncthreads();  // barrier A: head i is in shared memory
-    if (bad_rank) {
-      if (tid == 0 && sv.status) sv.status[h] = SEED_ERR_INVALID_ARG;
+    __syncthreads();  // barrier A: item i's U and vectors are in shared memory
+    if (tid == 0 && sv.status) sv.status[h] = bad_rank ? SEED_ERR_INVALID_ARG : SEED_OK;
+    if (bad_rank) {  // nothing was copied for it; the stage is free
+      describe(hn, nxt);
+      issue_u(nxt);
+      issue_w(nxt);
+      cur = nxt;
       continue;
     }
-    if (tid == 0 && sv.status) sv.status[h] = SEED_OK;
 
     const uint32_t u_base = smem_u32(st + S::U_OFF), w_base = smem_u32(st + S::W_OFF);
     const float *qs = reinterpret_cast<const float *>(st + S::Q_OFF);
@@ -301,6 +322,8 @@ __global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_ke
       }
     }
 
+    describe(hn, nxt);  // the next item's rank and columns, while this one computes
+
     // ---- block scalars: thread t owns row t (< DK) and value column t (< DV) ----------
     // stochastic rounding of the appended elements: one Philox block a thread, words
     // x, y for U and W of column m, z, w for column m + 1 (KDA)
@@ -338,8 +361,9 @@ __global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_ke
       const float r = warp_reduce8(S_loc, lane);
       if ((lane & 3) == 0) scal[warp * 8 + reduce8_index(lane)] = r;
     }
-    cp_async_wait<2 * NS - 2>();  // and its copies of head i's W
+    cp_async_wait<0>();  // and its copies of item i's W
     __syncthreads();  // barrier B: x, W, the padding and the scalar partials are visible
+    issue_u(nxt);     // U and the vectors have been read: the next item's go in
     float Sg[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -370,6 +394,7 @@ __global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_ke
       }
     }
     __syncthreads();  // barrier C: W x complete; the stage is no longer read
+    issue_w(nxt);
 
     // ---- update and read-out (registers, scal, wxs only) -------------------------------
     const float omega = Sg[4] / Sg[5];
@@ -439,34 +464,39 @@ __global__ void __launch_bounds__(kMmaThreads, MAXC <= 32 ? 8 : 7) decode_mma_ke
     }
     // thread 0 wrote OK before barriers B and C, so this write lands after it
     if (bad && sv.status) sv.status[h] = SEED_ERR_NONFINITE;
+    cur = nxt;
   }
   cp_async_wait<0>();
 }
 
-// One stage and one head per CTA (grid = heads): several CTAs per SM keep
-// several heads' loads in flight.  (The same kernel can run persistently over a
-// ring of NS > 1 stages; with two 64-column stages only two CTAs fit per SM and
-// the serving-scale decode ran at 0.32 of the copy bandwidth against 0.55 here.)
+// A persistent grid: as many CTAs as fit on the device at once (or one per head
+// when there are fewer heads), each walking its heads with the two-half refill.
 template <typename TF, int VAR, int DV, int MAXC>
 static cudaError_t launch_mma_t(const DecodeArgs &a, cudaStream_t s) {
-  constexpr int NS = 1;
-  using L = MmaSmem<VAR, DV, MAXC, NS>;
-  auto kern = decode_mma_kernel<TF, VAR, DV, MAXC, NS>;
-  // attributes belong to (kernel, device): set them the first time this kernel
-  // runs on each device of the process
-  static std::atomic<uint64_t> ready{0};
+  using L = MmaSmem<VAR, DV, MAXC>;
+  auto kern = decode_mma_kernel<TF, VAR, DV, MAXC>;
+  // attributes and the resident grid belong to (kernel, device): set and measure
+  // them the first time this kernel runs on each device of the process
+  constexpr int kDevs = 64;
+  static std::atomic<int> resident[kDevs];  // CTAs resident on the device, 0 = not yet known
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
-  if (!bit || !(ready.load(std::memory_order_acquire) & bit)) {
+  int grid = dev < kDevs ? resident[dev].load(std::memory_order_acquire) : 0;
+  if (grid == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
     if (e == cudaSuccess)  // all of the unified L1/shared capacity as shared memory: more heads per SM
       e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    int per_sm = 0, sms = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMmaThreads, L::BYTES);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    ready.fetch_or(bit, std::memory_order_acq_rel);
+    grid = per_sm * sms;
+    if (grid < 1) return cudaErrorInvalidConfiguration;
+    if (dev < kDevs) resident[dev].store(grid, std::memory_order_release);
   }
-  kern<<<a.count, kMmaThreads, L::BYTES, s>>>(a);
+  if (a.count <= 0) return cudaSuccess;
+  kern<<<a.count < grid ? a.count : grid, kMmaThreads, L::BYTES, s>>>(a);
   return cudaGetLastError();
 }
 
