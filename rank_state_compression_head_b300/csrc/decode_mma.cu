@@ -88,6 +88,9 @@ __device__ static inline void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
+__device__ static inline void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
 __device__ static inline void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -206,9 +209,14 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MAXC>()) decode_mm
   describe(nmine > 0 ? head_at(first) : -1, cur);
   issue_u(cur);
   issue_w(cur);
+  // The next item's head index is read an iteration ahead and its rank and columns
+  // at the top of the iteration before its copies are issued: after the step's
+  // first items these reads have a whole iteration to arrive.
+  int h_next = nmine > 1 ? head_at(first + G) : -1;
 
   for (int i = 0; i < nmine; ++i) {
-    const int hn = i + 1 < nmine ? head_at(first + (i + 1) * G) : -1;
+    describe(h_next, nxt);
+    h_next = i + 2 < nmine ? head_at(first + (i + 2) * G) : -1;
     cp_async_wait<1>();  // this thread's copies of item i's U and vectors have landed
 
     const int h = cur.h;
@@ -222,7 +230,6 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MAXC>()) decode_mm
     __syncthreads();  // barrier A: item i's U and vectors are in shared memory
     if (tid == 0 && sv.status) sv.status[h] = bad_rank ? SEED_ERR_INVALID_ARG : SEED_OK;
     if (bad_rank) {  // nothing was copied for it; the stage is free
-      describe(hn, nxt);
       issue_u(nxt);
       issue_w(nxt);
       cur = nxt;
@@ -245,12 +252,12 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MAXC>()) decode_mm
     const int m16 = (m + 15) & ~15;
 
     // padding: x rows and W columns [m, m16) must be zero for the W pass
-    for (int idx = tid; idx < NA * (L::XLD - m); idx += NT) {
-      const int row = idx / (L::XLD - m), j = m + idx % (L::XLD - m);
-      xs[row * L::XLD + j] = Mma16<TF>::cvt(0.f);
+    if (tid < NA * 16) {
+      const int j = m + (tid & 15);
+      if (j < m16) xs[(tid >> 4) * L::XLD + j] = Mma16<TF>::cvt(0.f);
     }
     {
-      constexpr int CH = S::WSTR / 16;
+      constexpr int CH = DV * 2 / 16;  // 16-byte chunks of a W column read by the W pass
       for (int idx = tid; idx < (m16 - m) * CH; idx += NT) {
         const int j = m + idx / CH, c = idx % CH;
         *reinterpret_cast<uint4 *>(st + S::W_OFF + j * S::WSTR + c * 16) = make_uint4(0, 0, 0, 0);
@@ -281,14 +288,20 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MAXC>()) decode_mm
 
     // ---- U pass: column tiles of 8, round robin over the warps -----------------------
     if (warp * 8 < m) {
+      // A fragments (rows 0..7; rows from NA on repeat row 0 and their products are
+      // not used): one ldmatrix of four 8x8 matrices covers two k-steps
       uint32_t a0[8], a2[8];
       {
-        const TF *row = reinterpret_cast<const TF *>(smem + L::AS_OFF) + (gq < NA ? gq : 0) * L::ALD;
+        const int rr = lane & 7;
+        const uint32_t arow = smem_u32(smem + L::AS_OFF) + (uint32_t)((rr < NA ? rr : 0) * L::ALD * 2 + (lane >> 3) * 16);
 #pragma unroll
-        for (int ks_ = 0; ks_ < 8; ++ks_) {
-          const int k0 = ks_ * 16 + 2 * tq;
-          a0[ks_] = gq < NA ? *reinterpret_cast<const uint32_t *>(row + k0) : 0u;
-          a2[ks_] = gq < NA ? *reinterpret_cast<const uint32_t *>(row + k0 + 8) : 0u;
+        for (int pp = 0; pp < 4; ++pp) {
+          uint32_t r[4];
+          ldsm_x4(arow + pp * 64, r);
+          a0[2 * pp] = r[0];
+          a2[2 * pp] = r[1];
+          a0[2 * pp + 1] = r[2];
+          a2[2 * pp + 1] = r[3];
         }
       }
       for (int n0 = warp * 8; n0 < m; n0 += NT / 4) {
@@ -321,8 +334,6 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MAXC>()) decode_mm
       }
       }
     }
-
-    describe(hn, nxt);  // the next item's rank and columns, while this one computes
 
     // ---- block scalars: thread t owns row t (< DK) and value column t (< DV) ----------
     // stochastic rounding of the appended elements: one Philox block a thread, words
@@ -364,29 +375,46 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MAXC>()) decode_mm
     cp_async_wait<0>();  // and its copies of item i's W
     __syncthreads();  // barrier B: x, W, the padding and the scalar partials are visible
     issue_u(nxt);     // U and the vectors have been read: the next item's go in
-    float Sg[8];
+    float Sg[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float a = 0.f;
-#pragma unroll
-      for (int w = 0; w < NSW; ++w) a += scal[w * 8 + j];
-      Sg[j] = a;
+    for (int w = 0; w < NSW; ++w) {
+      const float4 lo = reinterpret_cast<const float4 *>(scal + w * 8)[0];
+      const float4 hi = reinterpret_cast<const float4 *>(scal + w * 8)[1];
+      Sg[0] += lo.x; Sg[1] += lo.y; Sg[2] += lo.z; Sg[3] += lo.w;
+      Sg[4] += hi.x; Sg[5] += hi.y; Sg[6] += hi.z; Sg[7] += hi.w;
     }
 
     // ---- W pass: row tiles of 16 of W x, round robin over the warps -------------------
+    // B fragments (the x rows, the same for every row tile), loaded once: columns n
+    // from NA on repeat row 0 and their products are not used; k-steps past m16 are
+    // loaded (inside the x rows) but not used
+    constexpr int KS = MAXC / 16;
+    uint32_t bx0[KS], bx1[KS];
+    {
+      const int rr = lane & 7;
+      const uint32_t xrow = smem_u32(xs) + (uint32_t)(((rr < NA ? rr : 0) * L::XLD + (lane >> 3) * 8) * 2);
+#pragma unroll
+      for (int kk = 0; kk < KS; kk += 2) {
+        if (kk + 1 < KS) {
+          uint32_t r[4];
+          ldsm_x4(xrow + kk * 32, r);
+          bx0[kk] = r[0]; bx1[kk] = r[1]; bx0[kk + 1] = r[2]; bx1[kk + 1] = r[3];
+        } else {
+          ldsm_x2(xrow + kk * 32, bx0[kk], bx1[kk]);
+        }
+      }
+    }
     for (int i0 = warp * 16; i0 < DV; i0 += NT / 2) {
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       const int rsel = (lane & 7) + ((lane >> 4) << 3);
       const int csel = i0 + ((lane >> 3) & 1) * 8;
-      for (int j0 = 0; j0 < m16; j0 += 16) {
-        uint32_t a[4];
-        ldsm_x4_t(w_base + (uint32_t)((j0 + rsel) * S::WSTR + csel * 2), a);
-        uint32_t b0 = 0u, b1 = 0u;
-        if (gq < NA) {
-          b0 = *reinterpret_cast<const uint32_t *>(xs + gq * L::XLD + j0 + 2 * tq);
-          b1 = *reinterpret_cast<const uint32_t *>(xs + gq * L::XLD + j0 + 2 * tq + 8);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        if (kk * 16 < m16) {
+          uint32_t a[4];
+          ldsm_x4_t(w_base + (uint32_t)((kk * 16 + rsel) * S::WSTR + csel * 2), a);
+          Mma16<TF>::mma(d, a[0], a[1], a[2], a[3], bx0[kk], bx1[kk]);
         }
-        Mma16<TF>::mma(d, a[0], a[1], a[2], a[3], b0, b1);
       }
       if (tq < NX) {
         wxs[tq * DV + i0 + gq] = d[0] + d[1];
@@ -397,7 +425,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MAXC>()) decode_mm
     issue_w(nxt);
 
     // ---- update and read-out (registers, scal, wxs only) -------------------------------
-    const float omega = Sg[4] / Sg[5];
+    const float omega = __fdividef(Sg[4], Sg[5]);  // Sg[5] = |vbar|^2, about 1
     int bad = 0;
     TF *Uo = reinterpret_cast<TF *>(sv.U) + (c0 + m) * DK;
     TF *Wo = reinterpret_cast<TF *>(sv.W) + (c0 + m) * DV;
