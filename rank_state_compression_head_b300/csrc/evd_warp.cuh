@@ -41,18 +41,19 @@ __device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw) {
   int *piv = reinterpret_cast<int *>(sw + L::P_OFF);
   const int c0 = lane, c1 = lane + HW;
 
-  // My columns in registers (rows 0..MR-1; rows and columns from m on are zero).
-  float colA[MR], colB[TWO ? MR : 1];
+  // My columns in registers (rows 0..MR-1; rows and columns from m on are zero), as
+  // pairs of consecutive rows for the packed fp32 instructions (svd_warp.cuh)
+  float2 colA[MR / 2], colB[TWO ? MR / 2 : 1];
   {
     const float4 *a4 = reinterpret_cast<const float4 *>(T + c0 * TP);
     const float4 *b4 = reinterpret_cast<const float4 *>(T + (TWO && c1 < MR ? c1 : 0) * TP);
 #pragma unroll
     for (int q = 0; q < MR / 4; ++q) {
       const float4 x = c0 < MR ? a4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-      colA[4 * q] = x.x; colA[4 * q + 1] = x.y; colA[4 * q + 2] = x.z; colA[4 * q + 3] = x.w;
+      colA[2 * q] = make_float2(x.x, x.y); colA[2 * q + 1] = make_float2(x.z, x.w);
       if constexpr (TWO) {
         const float4 y = c1 < MR ? b4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-        colB[4 * q] = y.x; colB[4 * q + 1] = y.y; colB[4 * q + 2] = y.z; colB[4 * q + 3] = y.w;
+        colB[2 * q] = make_float2(y.x, y.y); colB[2 * q + 1] = make_float2(y.z, y.w);
       }
     }
   }
@@ -91,7 +92,8 @@ __device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int x = 4 * q + e;
-          const float sx = (TWO && hi) ? colB[TWO ? x : 0] : colA[x];
+          const float2 pa = colA[x >> 1], pb = colB[TWO ? x >> 1 : 0];
+          const float sx = (TWO && hi) ? ((x & 1) ? pb.y : pb.x) : ((x & 1) ? pa.y : pa.x);
           v[e] = (gone >> x) & 1ull ? 0.f : sx * inv;
         }
         reinterpret_cast<float4 *>(row)[q] = make_float4(v[0], v[1], v[2], v[3]);
@@ -105,14 +107,17 @@ __device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw) {
     const float4 *r4 = reinterpret_cast<const float4 *>(row);
     const float t0 = done0 ? 0.f : row[c0];
     const float t1 = done1 ? 0.f : row[TWO ? c1 : 0];
+    // (v (-t) rounds as (-v) t: the sign is exact)
+    const float2 mt0 = make_float2(-t0, -t0), mt1 = make_float2(-t1, -t1);
 #pragma unroll
     for (int q = 0; q < MR / 4; ++q) {
       const float4 v = r4[q];
-      const float vs[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        colA[4 * q + e] = fmaf(-vs[e], t0, colA[4 * q + e]);
-        if constexpr (TWO) colB[4 * q + e] = fmaf(-vs[e], t1, colB[4 * q + e]);
+      const float2 v01 = make_float2(v.x, v.y), v23 = make_float2(v.z, v.w);
+      colA[2 * q] = __ffma2_rn(v01, mt0, colA[2 * q]);
+      colA[2 * q + 1] = __ffma2_rn(v23, mt0, colA[2 * q + 1]);
+      if constexpr (TWO) {
+        colB[2 * q] = __ffma2_rn(v01, mt1, colB[2 * q]);
+        colB[2 * q + 1] = __ffma2_rn(v23, mt1, colB[2 * q + 1]);
       }
     }
     dg0 = fmaf(-t0, t0, dg0);

@@ -452,21 +452,34 @@ __device__ inline bool jac_rotation(float dot_xy, const JacCol &x, const JacCol 
   return rot;
 }
 
+// The register arrays hold a column as MR / 2 pairs of consecutive elements, so that
+// the element loops run on the packed two-lane fp32 instructions of sm_100 and later
+// (each lane rounds as its scalar counterpart: the same results in half the issue
+// slots).  Elements 4j, 4j+1 sit in pair 2j and 4j+2, 4j+3 in pair 2j+1, so two
+// packed accumulators are the four chains of element k % 4.
+__device__ inline float2 f2(float v) { return make_float2(v, v); }
+
 template <int MR>
-__device__ inline float jac_norm2(const float (&x)[MR], float d) {
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
+__device__ inline float jac_norm2(const float2 (&x)[MR / 2], float d) {
+  float2 s0 = f2(0.f), s1 = f2(0.f);
 #pragma unroll
-  for (int k = 0; k < MR; ++k) s[k & 3] = fmaf(x[k], x[k], s[k & 3]);
-  return ((s[0] + s[1]) + (s[2] + s[3])) * (d * d);
+  for (int k = 0; k < MR / 2; ++k) {
+    if (k & 1) s1 = __ffma2_rn(x[k], x[k], s1);
+    else s0 = __ffma2_rn(x[k], x[k], s0);
+  }
+  return ((s0.x + s0.y) + (s1.x + s1.y)) * (d * d);
 }
 
 // dot product with four accumulation chains (a shorter dependent chain)
 template <int MR>
-__device__ inline float jac_dot(const float (&x)[MR], const float (&y)[MR]) {
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
+__device__ inline float jac_dot(const float2 (&x)[MR / 2], const float2 (&y)[MR / 2]) {
+  float2 s0 = f2(0.f), s1 = f2(0.f);
 #pragma unroll
-  for (int k = 0; k < MR; ++k) s[k & 3] = fmaf(x[k], y[k], s[k & 3]);
-  return (s[0] + s[1]) + (s[2] + s[3]);
+  for (int k = 0; k < MR / 2; ++k) {
+    if (k & 1) s1 = __ffma2_rn(x[k], y[k], s1);
+    else s0 = __ffma2_rn(x[k], y[k], s0);
+  }
+  return (s0.x + s0.y) + (s1.x + s1.y);
 }
 
 // One even round (the lane's own pair) and one odd round (pairs with the
@@ -481,18 +494,20 @@ __device__ inline float jac_dot(const float (&x)[MR], const float (&y)[MR]) {
 // columns to cross once more.  So a lane holds three columns, and the pair's dot
 // product and coefficients are formed once.
 template <int MR, int HW, bool RIGHT_A>
-__device__ inline void jac_round_pair(float (&A)[MR], float (&B)[MR], float (&Y)[MR], JacCol &ca, JacCol &cb,
-                                      bool has_left, bool has_right, unsigned full, float tol2, float stop2,
-                                      int &far) {
+__device__ inline void jac_round_pair(float2 (&A)[MR / 2], float2 (&B)[MR / 2], float2 (&Y)[MR / 2], JacCol &ca,
+                                      JacCol &cb, bool has_left, bool has_right, unsigned full, float tol2,
+                                      float stop2, int &far) {
+  constexpr int NP = MR / 2;
   // ---- even round ----
   {
     float ta, tb, c, tg;
     const bool rot = jac_rotation(jac_dot<MR>(A, B), ca, cb, tol2, stop2, ta, tb, c, tg, far);
+    const float2 mta = f2(-ta), ptb = f2(tb);
 #pragma unroll
-    for (int k = 0; k < MR; ++k) {
-      const float a = A[k], b = B[k];
-      A[k] = fmaf(-ta, b, a);
-      B[k] = fmaf(tb, a, b);
+    for (int k = 0; k < NP; ++k) {
+      const float2 a = A[k], b = B[k];
+      A[k] = __ffma2_rn(mta, b, a);
+      B[k] = __ffma2_rn(ptb, a, b);
     }
     const float na = ca.n2 - tg, nb = cb.n2 + tg;
     ca.d *= c;
@@ -501,22 +516,24 @@ __device__ inline void jac_round_pair(float (&A)[MR], float (&B)[MR], float (&Y)
     if (rot && nb < 0.25f * cb.n2) cb.n2 = jac_norm2<MR>(B, cb.d); else cb.n2 = nb;
   }
   // ---- odd round ----
-  float (&Xr)[MR] = RIGHT_A ? A : B;   // my right-facing column
-  float (&Xl)[MR] = RIGHT_A ? B : A;   // my left-facing column
+  float2 (&Xr)[NP] = RIGHT_A ? A : B;   // my right-facing column
+  float2 (&Xl)[NP] = RIGHT_A ? B : A;   // my left-facing column
   JacCol &cxr = RIGHT_A ? ca : cb;
   JacCol &cxl = RIGHT_A ? cb : ca;
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  float2 s0 = f2(0.f), s1 = f2(0.f);
 #pragma unroll
-  for (int k = 0; k < MR; ++k) {
-    Y[k] = __shfl_down_sync(full, Xl[k], 1, HW);   // right neighbour's left-facing column
-    s[k & 3] = fmaf(Xr[k], Y[k], s[k & 3]);
+  for (int k = 0; k < NP; ++k) {
+    Y[k].x = __shfl_down_sync(full, Xl[k].x, 1, HW);   // right neighbour's left-facing column
+    Y[k].y = __shfl_down_sync(full, Xl[k].y, 1, HW);
+    if (k & 1) s1 = __ffma2_rn(Xr[k], Y[k], s1);
+    else s0 = __ffma2_rn(Xr[k], Y[k], s0);
   }
   JacCol cr;
   cr.d = __shfl_down_sync(full, cxl.d, 1, HW);
   cr.n2 = __shfl_down_sync(full, cxl.n2, 1, HW);
   float ta1, tb1, c1, tg1;
   int far1 = 0;
-  const bool rot1 = jac_rotation((s[0] + s[1]) + (s[2] + s[3]), cxr, cr, tol2, stop2, ta1, tb1, c1, tg1, far1);
+  const bool rot1 = jac_rotation((s0.x + s0.y) + (s1.x + s1.y), cxr, cr, tol2, stop2, ta1, tb1, c1, tg1, far1);
   far |= has_right && far1;
   // the left neighbour's decision on the pair (its x, my left-facing y), and its x's metadata
   const float ta2 = __shfl_up_sync(full, ta1, 1, HW);
@@ -526,11 +543,21 @@ __device__ inline void jac_round_pair(float (&A)[MR], float (&B)[MR], float (&Y)
   JacCol cl;
   cl.d = __shfl_up_sync(full, cxr.d, 1, HW);
   cl.n2 = __shfl_up_sync(full, cxr.n2, 1, HW);
+  // (lane-predicated, so element by element: a packed update under a per-lane
+  // condition costs more registers than it saves)
 #pragma unroll
-  for (int k = 0; k < MR; ++k) {
-    const float lw = __shfl_up_sync(full, Xr[k], 1, HW);   // left neighbour's old right-facing column
-    if (has_right) Xr[k] = fmaf(tb1, Xr[k], Y[k]);
-    if (has_left) Xl[k] = fmaf(-ta2, Xl[k], lw);
+  for (int k = 0; k < NP; ++k) {
+    float2 lw;  // left neighbour's old right-facing column
+    lw.x = __shfl_up_sync(full, Xr[k].x, 1, HW);
+    lw.y = __shfl_up_sync(full, Xr[k].y, 1, HW);
+    if (has_right) {
+      Xr[k].x = fmaf(tb1, Xr[k].x, Y[k].x);
+      Xr[k].y = fmaf(tb1, Xr[k].y, Y[k].y);
+    }
+    if (has_left) {
+      Xl[k].x = fmaf(-ta2, Xl[k].x, lw.x);
+      Xl[k].y = fmaf(-ta2, Xl[k].y, lw.y);
+    }
   }
   if (has_right) {
     const float ny = cr.n2 + tg1;
@@ -561,7 +588,7 @@ __device__ int jacobi_warp_reg(int m, float tol, float tol_stop, float *sw) {
   const bool has_right = lane + 1 < P, has_left = lane > 0 && active;
   const float tol2 = tol * tol, stop2 = tol_stop * tol_stop;
 
-  float A[MR], B[MR], Y[MR];
+  float2 A[MR / 2], B[MR / 2], Y[MR / 2];
   {
     const float4 *a4 = reinterpret_cast<const float4 *>(T + (2 * lane) * TP);
     const float4 *b4 = reinterpret_cast<const float4 *>(T + (2 * lane + 1) * TP);
@@ -569,8 +596,8 @@ __device__ int jacobi_warp_reg(int m, float tol, float tol_stop, float *sw) {
     for (int q = 0; q < MR / 4; ++q) {
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
       const float4 a = active ? a4[q] : z, b = active ? b4[q] : z;
-      A[4 * q] = a.x; A[4 * q + 1] = a.y; A[4 * q + 2] = a.z; A[4 * q + 3] = a.w;
-      B[4 * q] = b.x; B[4 * q + 1] = b.y; B[4 * q + 2] = b.z; B[4 * q + 3] = b.w;
+      A[2 * q] = make_float2(a.x, a.y); A[2 * q + 1] = make_float2(a.z, a.w);
+      B[2 * q] = make_float2(b.x, b.y); B[2 * q + 1] = make_float2(b.z, b.w);
     }
   }
   JacCol ca{1.f, 0.f}, cb{1.f, 0.f};
@@ -591,12 +618,12 @@ __device__ int jacobi_warp_reg(int m, float tol, float tol_stop, float *sw) {
       // fold the scales into the columns: at the end, or once one has shrunk below 2^-20
       if (conv || sweep + 1 == kMaxSweeps || ca.d < 9.5367e-7f) {
 #pragma unroll
-        for (int k = 0; k < MR; ++k) A[k] *= ca.d;
+        for (int k = 0; k < MR / 2; ++k) A[k] = __fmul2_rn(A[k], f2(ca.d));
         ca.d = 1.f;
       }
       if (conv || sweep + 1 == kMaxSweeps || cb.d < 9.5367e-7f) {
 #pragma unroll
-        for (int k = 0; k < MR; ++k) B[k] *= cb.d;
+        for (int k = 0; k < MR / 2; ++k) B[k] = __fmul2_rn(B[k], f2(cb.d));
         cb.d = 1.f;
       }
       if (conv) {
@@ -609,8 +636,8 @@ __device__ int jacobi_warp_reg(int m, float tol, float tol_stop, float *sw) {
   if (active) {
 #pragma unroll
     for (int q = 0; q < MR / 4; ++q) {
-      reinterpret_cast<float4 *>(T + (2 * lane) * TP)[q] = make_float4(A[4 * q], A[4 * q + 1], A[4 * q + 2], A[4 * q + 3]);
-      reinterpret_cast<float4 *>(T + (2 * lane + 1) * TP)[q] = make_float4(B[4 * q], B[4 * q + 1], B[4 * q + 2], B[4 * q + 3]);
+      reinterpret_cast<float4 *>(T + (2 * lane) * TP)[q] = make_float4(A[2 * q].x, A[2 * q].y, A[2 * q + 1].x, A[2 * q + 1].y);
+      reinterpret_cast<float4 *>(T + (2 * lane + 1) * TP)[q] = make_float4(B[2 * q].x, B[2 * q].y, B[2 * q + 1].x, B[2 * q + 1].y);
     }
     const float a2 = jac_norm2<MR>(A, 1.f), b2 = jac_norm2<MR>(B, 1.f);
     sig2[2 * lane] = a2;
