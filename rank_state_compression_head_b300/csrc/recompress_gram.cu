@@ -267,13 +267,20 @@ __device__ inline void chol_warp(float *Gw, float *dg, float *rr, int m) {
   constexpr int NA = MR < 32 ? MR : 32;
   const int lane = threadIdx.x & 31;
   const int c0 = lane, c1 = lane + 32;
-  float gA[NA], gB[TWO ? MR : 1];
+  // the columns as pairs of consecutive rows, updated on the packed fp32
+  // instructions; every row past the step is updated, those from m on included (their
+  // multipliers are entries of columns that are never written back), so the unrolled
+  // steps carry no per-row conditions
+  float2 gA[NA / 2], gB[TWO ? MR / 2 : 1];
 #pragma unroll
-  for (int i = 0; i < NA; ++i) gA[i] = c0 < MR ? Gw[i * GP + c0] : 0.f;
+  for (int i = 0; i < NA / 2; ++i)
+    gA[i] = c0 < MR ? make_float2(Gw[2 * i * GP + c0], Gw[(2 * i + 1) * GP + c0]) : make_float2(0.f, 0.f);
   if constexpr (TWO) {
 #pragma unroll
-    for (int i = 0; i < MR; ++i) gB[i] = c1 < MR ? Gw[i * GP + c1] : 0.f;
+    for (int i = 0; i < MR / 2; ++i)
+      gB[i] = c1 < MR ? make_float2(Gw[2 * i * GP + c1], Gw[(2 * i + 1) * GP + c1]) : make_float2(0.f, 0.f);
   }
+  auto el = [](const float2 &v, int odd) { return odd ? v.y : v.x; };
   if (c0 < m) dg[c0] = Gw[c0 * GP + c0];
   if (TWO && c1 < m) dg[c1] = Gw[c1 * GP + c1];
   __syncwarp();
@@ -281,34 +288,36 @@ __device__ inline void chol_warp(float *Gw, float *dg, float *rr, int m) {
   for (int j = 0; j < MR; ++j) {
     if (j < m) {
       float own;  // my column's entry in row j (pivot lane: the diagonal)
-      if constexpr (TWO) own = j < 32 ? gA[j < NA ? j : 0] : gB[j];
-      else own = gA[j < NA ? j : 0];
+      if constexpr (TWO) own = j < 32 ? el(gA[j < NA ? j / 2 : 0], j & 1) : el(gB[j / 2], j & 1);
+      else own = el(gA[j < NA ? j / 2 : 0], j & 1);
       const float d = __shfl_sync(0xffffffffu, own, j & 31);
       // 1 / r_jj and r_jj from one reciprocal square root (a couple of ulp)
       const bool keep = d > kCholFloor * dg[j];
       const float inv = keep ? rsqrtf(d) : 0.f;
       const float rjj = d * inv;
-      const float rA = j < NA && c0 > j ? gA[j < NA ? j : 0] * inv : (c0 == j ? rjj : 0.f);
+      const float rA = j < NA && c0 > j ? el(gA[j < NA ? j / 2 : 0], j & 1) * inv : (c0 == j ? rjj : 0.f);
       float rB = 0.f;
-      if constexpr (TWO) rB = c1 > j ? gB[j] * inv : (c1 == j ? rjj : 0.f);
+      if constexpr (TWO) rB = c1 > j ? el(gB[j / 2], j & 1) * inv : (c1 == j ? rjj : 0.f);
       float *row = rr + (j & 1) * MR;
       if (c0 < MR) row[c0] = rA;
       if (TWO && c1 < MR) row[c1] = rB;
       if (c0 >= j && c0 < m) Gw[j * GP + c0] = rA;
       if (TWO && c1 >= j && c1 < m) Gw[j * GP + c1] = rB;
       __syncwarp();
+      // S[i][c] -= R[j][i] R[j][c] for the pairs holding a row past j ((-r) v rounds as r (-v))
       const float4 *row4 = reinterpret_cast<const float4 *>(row);
+      const float2 mA = make_float2(-rA, -rA), mB = make_float2(-rB, -rB);
 #pragma unroll
       for (int q = (j + 1) / 4; q < MR / 4; ++q) {
         const float4 v = row4[q];
-        const float rv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 4 * q + e;
-          if (i > j && i < m) {
-            if (i < NA) gA[i < NA ? i : 0] = fmaf(-rv[e], rA, gA[i < NA ? i : 0]);
-            if constexpr (TWO) gB[i] = fmaf(-rv[e], rB, gB[i]);
-          }
+        const float2 v01 = make_float2(v.x, v.y), v23 = make_float2(v.z, v.w);
+        if (4 * q + 1 > j) {
+          if (4 * q < NA) gA[4 * q < NA ? 2 * q : 0] = __ffma2_rn(v01, mA, gA[4 * q < NA ? 2 * q : 0]);
+          if constexpr (TWO) gB[2 * q] = __ffma2_rn(v01, mB, gB[2 * q]);
+        }
+        if (4 * q + 3 > j) {
+          if (4 * q + 2 < NA) gA[4 * q + 2 < NA ? 2 * q + 1 : 0] = __ffma2_rn(v23, mA, gA[4 * q + 2 < NA ? 2 * q + 1 : 0]);
+          if constexpr (TWO) gB[2 * q + 1] = __ffma2_rn(v23, mB, gB[2 * q + 1]);
         }
       }
     }
