@@ -40,7 +40,7 @@
 //                  with Z split into three bf16 terms (24 significant bits),
 //                  KDA's row scale applied to U', lazy scales reset
 //
-// Workspace per head (fp32): M [m][m], R_b [m][m] (upper, row-major), Y [r][m4]
+// Workspace per head (fp32): M [m][m], R_b [m][m4] (upper, row-major), Y [r][m4]
 // (m4 = m rounded up to 4), eight words of class lists, each region on 16 bytes,
 // the whole on 256 bytes.  With ragged ranks each 16-column class gets its own
 // three launches, sized for it: with the state's class order (seed.h) over
@@ -68,8 +68,8 @@ struct GramLayout {
     m4 = (m + 3) & ~3;
     const int64_t mm4 = ((int64_t)m * m + 3) & ~(int64_t)3;
     mq = 0;
-    rb = mq + mm4;
-    y = rb + mm4;
+    rb = mq + mm4;                 // R_b: m rows of m4 floats (16-byte rows)
+    y = rb + (int64_t)m * m4;
     lst = y + (int64_t)r * m4;
     per_head = (lst + 8 + 63) & ~(int64_t)63;
   }
@@ -572,10 +572,8 @@ __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phas
         }
     }
   }
-  for (int idx = tid; idx < m * m; idx += kGramThreads) {
-    const int i = idx / m, l = idx % m;
-    ws[W.rb + idx] = l >= i ? Gw[i * GP + l] : 0.f;
-  }
+  for (int i = warp; i < m; i += kGramThreads / 32)  // R_b by rows of W.m4, zero beyond m
+    for (int l = lane; l < W.m4; l += 32) ws[W.rb + (int64_t)i * W.m4 + l] = (l >= i && l < m) ? Gw[i * GP + l] : 0.f;
 }
 
 // ---- phase 2: eigenvectors of M, one lane group per head -------------------------------------
@@ -661,7 +659,7 @@ template <int DV, int MR>
 struct RebuildSmem {
   static constexpr int STR = kDK * 2 + 16;      // tile row stride (bytes), the larger factor
   static constexpr int RP = MR + 4;             // R_b row pitch (floats; 16-byte rows)
-  static constexpr int YP = MR + 4;             // Y^T row pitch: row j holds y_n[j] for every n
+  static constexpr int YP = MR + 4;             // Y row pitch: row n holds y_n[j] for every j
   static constexpr int ZP = MR + 2;             // Z row pitch (floats): row n = column n of Z;
                                                 // 2 mod 4 keeps both access patterns at 2-way
   static constexpr int T_OFF = 0;               // factor tile
@@ -702,25 +700,29 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
   const GramLayout W(p.layout_m, p.r_max);
   const float *ws = p.ws + (int64_t)slot * W.per_head;
   float *Rb = reinterpret_cast<float *>(smem + L::R_OFF);
-  float *Yt = reinterpret_cast<float *>(smem + L::Y_OFF);   // y_n[j] at j * YP + n
+  float *Ys = reinterpret_cast<float *>(smem + L::Y_OFF);   // y_n[j] at n * YP + j
   float *Z = reinterpret_cast<float *>(smem + L::Z_OFF);    // [rk8][ZP]: z_n[j] at n * ZP + j
   float *sc = reinterpret_cast<float *>(smem + L::S_OFF);
   TF *pool = reinterpret_cast<TF *>(isU ? sv.U : sv.W) + c0 * rows;
 
   // ---- R_b, Y, the scales (first copy group), the factor tile (second) -----------------------
-  // R_b upper (zero below the diagonal and beyond m), Y^T (zero beyond m and rk), Z zero;
-  // consecutive threads copy consecutive workspace words
-  for (int idx = tid; idx < m16 * RP; idx += kGramThreads) {
-    const int i = idx / RP, l = idx % RP;
-    if (i < m && l < m) g_cp_async4(Rb + idx, ws + W.rb + i * m + l);
-    else Rb[idx] = 0.f;
-  }
+  // R_b upper (zero below the diagonal and beyond m) and Y (zero beyond m and rk) by
+  // 16-byte copies of their rows, both stored by rows of W.m4 floats; Z zero
   {
-    const int rk4 = (rk + 3) & ~3;
-    for (int idx = tid; idx < rk4 * m16; idx += kGramThreads) {
-      const int n = idx / m16, j = idx % m16;
-      if (j < m && n < rk) g_cp_async4(Yt + j * YP + n, ws + W.y + n * W.m4 + j);
-      else Yt[j * YP + n] = 0.f;
+    constexpr int RC = RP / 4;  // 16-byte chunks of a row of R_b in shared memory
+    const int m4c = W.m4 / 4 < RC ? W.m4 / 4 : RC;
+    for (int idx = tid; idx < m16 * RC; idx += kGramThreads) {
+      const int i = idx / RC, c = idx % RC;
+      float *dst = Rb + i * RP + 4 * c;
+      if (i < m && c < m4c) g_cp_async16(dst, ws + W.rb + (int64_t)i * W.m4 + 4 * c);
+      else *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int rk8r = (rk + 7) & ~7;
+    for (int idx = tid; idx < rk8r * RC; idx += kGramThreads) {
+      const int n = idx / RC, c = idx % RC;
+      float *dst = Ys + n * YP + 4 * c;
+      if (n < rk && c < m4c) g_cp_async16(dst, ws + W.y + (int64_t)n * W.m4 + 4 * c);
+      else *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
   if (isU) {
@@ -744,19 +746,30 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
 
   // ---- Z ------------------------------------------------------------------------------------
   if (isU) {
-    // z_n[l] = c_l sum_{j <= l} y_n[j] R_b[j][l], 4 x 4 blocks of (n, l) a thread
+    // z_n[l] = c_l sum_{j <= l} y_n[j] R_b[j][l], 4 x 4 blocks of (n, l) a thread, four
+    // j at a time (rows of Y and R_b are zero from m on)
     const int nbn = (rk + 3) / 4, nbl = (m + 3) / 4;
     for (int blk = tid; blk < nbn * nbl; blk += kGramThreads) {
       const int nb = blk / nbl, lb = blk % nbl;
       float acc[4][4] = {};
-      for (int j = 0; j < 4 * lb + 4 && j < m; ++j) {
-        const float4 y = *reinterpret_cast<const float4 *>(Yt + j * YP + 4 * nb);
-        const float4 rv = *reinterpret_cast<const float4 *>(Rb + j * RP + 4 * lb);
-        const float ys[4] = {y.x, y.y, y.z, y.w}, rs[4] = {rv.x, rv.y, rv.z, rv.w};
+      for (int j4 = 0; j4 <= lb; ++j4) {
+        float ys[4][4], rs[4][4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < 4; ++a) {
+          const float4 y = *reinterpret_cast<const float4 *>(Ys + (4 * nb + a) * YP + 4 * j4);
+          ys[a][0] = y.x; ys[a][1] = y.y; ys[a][2] = y.z; ys[a][3] = y.w;
+        }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(ys[a], rs[c], acc[a][c]);
+        for (int u = 0; u < 4; ++u) {
+          const float4 rv = *reinterpret_cast<const float4 *>(Rb + (4 * j4 + u) * RP + 4 * lb);
+          rs[u][0] = rv.x; rs[u][1] = rv.y; rs[u][2] = rv.z; rs[u][3] = rv.w;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(ys[a][u], rs[u][c], acc[a][c]);
       }
 #pragma unroll
       for (int a = 0; a < 4; ++a)
@@ -772,10 +785,10 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
     // earliest-solved entries first, so that consecutive rows overlap), then all
     // threads take the panel's contribution off the rows above.  A zero pivot
     // (dropped row) gives a zero entry.
-    float *rinv = Yt + m16 * YP;  // 1 / R_b[i][i] (0 for a dropped row), after Y^T
+    float *rinv = Ys + MR * YP;  // 1 / R_b[i][i] (0 for a dropped row), after Y
     for (int idx = tid; idx < rk * m; idx += kGramThreads) {
       const int n = idx / m, i = idx % m;
-      Z[n * ZP + i] = Yt[i * YP + n];
+      Z[n * ZP + i] = Ys[n * YP + i];
     }
     for (int i = tid; i < m; i += kGramThreads) {
       const float piv = Rb[i * RP + i];
@@ -805,11 +818,40 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
           if (b0 + q < b1) z[b0 + q] = zp[q];
       }
       __syncthreads();
-      for (int idx = tid; idx < rk * b0; idx += kGramThreads) {
-        const int n = idx / b0, i = idx % b0;
-        float s = Z[n * ZP + i];
-        for (int l = b0; l < b1; ++l) s = fmaf(-Rb[i * RP + l], Z[n * ZP + l], s);
-        Z[n * ZP + i] = s;
+      // z_n[i] -= sum_{b0 <= l < b1} R_b[i][l] z_n[l] for the rows i < b0, in the same
+      // order as one element at a time, by 4 x 4 blocks of (n, i) a thread: columns
+      // nb + nbn a (neighbouring threads read neighbouring rows of Z) and rows
+      // 4 ib .. 4 ib + 3 (shared by neighbouring threads: broadcast reads of R_b);
+      // rows of Z from rk on are zero and stay unwritten
+      const int nbn = (rk + 3) / 4, nib = (b0 + 3) / 4;
+      for (int blk = tid; blk < nbn * nib; blk += kGramThreads) {
+        const int ib = blk / nbn, nb = blk % nbn;
+        float acc[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int i = 4 * ib + c;
+            acc[a][c] = i < b0 ? Z[(nb + nbn * a) * ZP + i] : 0.f;
+          }
+        for (int l = b0; l < b1; ++l) {
+          float zl[4], rl[4];
+#pragma unroll
+          for (int a = 0; a < 4; ++a) zl[a] = Z[(nb + nbn * a) * ZP + l];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) rl[c] = Rb[(4 * ib + c) * RP + l];
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(-rl[c], zl[a], acc[a][c]);
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int n = nb + nbn * a, i = 4 * ib + c;
+            if (n < rk && i < b0) Z[n * ZP + i] = acc[a][c];
+          }
       }
       __syncthreads();
     }

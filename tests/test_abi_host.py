@@ -173,15 +173,16 @@ def test_synth_calls_reject_on_host():
 
 
 def _ws_floats(m, r, dk, dv, dtype='bf16'):
-    # 16-bit factors (Cholesky of the value-side Gram matrix): M, R_b, Y and eight
-    # words of class lists; 32-bit factors (QR of both factors): W's reflectors,
-    # their tau, R_b^T, K, Y; each region on 16 bytes, the whole on 256 bytes
+    # 16-bit factors (Cholesky of the value-side Gram matrix): M, R_b (rows of m4
+    # floats), Y and eight words of class lists; 32-bit factors (QR of both factors):
+    # W's reflectors, their tau, R_b^T, K, Y; each region on 16 bytes, the whole on
+    # 256 bytes
     m4 = (m + 3) // 4 * 4
     mm4 = (m * m + 3) // 4 * 4
     if dtype == 'f32':
         n = m * dv + m4 + 2 * mm4 + r * m4
     else:
-        n = 2 * mm4 + r * m4 + 8
+        n = mm4 + m * m4 + r * m4 + 8
     n = (n + 63) // 64 * 64
     return max(n, 64)
 
