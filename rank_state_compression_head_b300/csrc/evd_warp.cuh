@@ -82,25 +82,26 @@ __device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw) {
     const float d = fmaxf(best, 0.f);
     const float inv = d > 0.f ? rsqrtf(d) : 0.f;  // 1 / r_jj (a couple of ulp)
     float *row = T + p * TP;  // row j of Rt goes where column p was
-    // The pivot's lane writes row j of Rt: Rt[j][x] = S[x][p] / r_jj for the rows not yet
-    // pivoted (r_jj at x = p), zero for the others.
+    // The pivot's lane stores its column as it stands; then every lane turns its own
+    // two entries into those of row j of Rt: Rt[j][x] = S[x][p] / r_jj for the rows not
+    // yet pivoted (r_jj at x = p), zero for the others.
     if (lane == (p & (HW - 1))) {
-      const bool hi = p >= HW;
+      if (TWO && p >= HW) {
 #pragma unroll
-      for (int q = 0; q < MR / 4; ++q) {
-        float v[4];
+        for (int q = 0; q < MR / 4; ++q)
+          reinterpret_cast<float4 *>(row)[q] =
+              make_float4(colB[TWO ? 2 * q : 0].x, colB[TWO ? 2 * q : 0].y, colB[TWO ? 2 * q + 1 : 0].x, colB[TWO ? 2 * q + 1 : 0].y);
+        done1 = true;
+      } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int x = 4 * q + e;
-          const float2 pa = colA[x >> 1], pb = colB[TWO ? x >> 1 : 0];
-          const float sx = (TWO && hi) ? ((x & 1) ? pb.y : pb.x) : ((x & 1) ? pa.y : pa.x);
-          v[e] = (gone >> x) & 1ull ? 0.f : sx * inv;
-        }
-        reinterpret_cast<float4 *>(row)[q] = make_float4(v[0], v[1], v[2], v[3]);
+        for (int q = 0; q < MR / 4; ++q)
+          reinterpret_cast<float4 *>(row)[q] = make_float4(colA[2 * q].x, colA[2 * q].y, colA[2 * q + 1].x, colA[2 * q + 1].y);
+        done0 = true;
       }
-      if (hi) done1 = true;
-      else done0 = true;
     }
+    __syncwarp(full);
+    if (c0 < MR) row[c0] = (gone >> c0) & 1ull ? 0.f : row[c0] * inv;
+    if (TWO && c1 < MR) row[c1] = (gone >> c1) & 1ull ? 0.f : row[c1] * inv;
     gone |= 1ull << p;
     __syncwarp(full);
     // Schur update of my remaining columns: S[x][c] -= Rt[j][x] Rt[j][c]
