@@ -9,9 +9,10 @@
 // if M = K^T K, then P^T M P = R^T R is the R of K P, and the Jacobi on its graded
 // rows needs about half the sweeps that it needs on K itself.
 //
-// Layout: M sits in the warp's shared square (SvdWarpSmem), column c at
-// T[c * TP], rows and columns m..MR-1 zero; lane l takes columns l and l + HW
-// into registers.  The Schur complement stays in the original index order,
+// Layout: M (symmetric) comes from global memory, row c at Mg + c * mp (16-byte
+// rows): lane l loads rows l and l + HW, which are its columns, straight into
+// registers with 16-byte loads, scaled by mscale, zero from m on; the warp's
+// shared square (SvdWarpSmem) takes the rows of Rt.  The Schur complement stays in the original index order,
 // nothing is swapped: step j picks the remaining index p of largest diagonal;
 // the pivot's lane forms row j of Rt (Rt[j][x] = S[x][p] / sqrt(S[p][p]) for the
 // remaining x, zero for the pivoted ones) and stores it where column p was, and
@@ -29,7 +30,7 @@ namespace seedk {
 // Returns the Jacobi sweeps (or -1); leaves what jacobi_warp leaves, with the
 // eigenvector of seat s in T[s * TP + x], x in the original order, and piv.
 template <int MR, int HW>
-__device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw) {
+__device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw, const float *Mg, int mp, float mscale) {
   using L = SvdWarpSmem<MR>;
   static_assert(HW == 16 || HW == 32, "a lane group is a half warp or a warp");
   static_assert(MR <= 2 * HW, "two indices per lane at most");
@@ -42,27 +43,36 @@ __device__ int evd_warp_core(int m, float tol, float tol_stop, float *sw) {
   const int c0 = lane, c1 = lane + HW;
 
   // My columns in registers (rows 0..MR-1; rows and columns from m on are zero), as
-  // pairs of consecutive rows for the packed fp32 instructions (svd_warp.cuh)
+  // pairs of consecutive rows for the packed fp32 instructions (svd_warp.cuh); all
+  // the loads are issued before any is used
   float2 colA[MR / 2], colB[TWO ? MR / 2 : 1];
+  bool done0 = c0 >= m, done1 = !TWO || c1 >= m;
   {
-    const float4 *a4 = reinterpret_cast<const float4 *>(T + c0 * TP);
-    const float4 *b4 = reinterpret_cast<const float4 *>(T + (TWO && c1 < MR ? c1 : 0) * TP);
+    const float4 *a4 = reinterpret_cast<const float4 *>(Mg + (int64_t)(done0 ? 0 : c0) * mp);
+    const float4 *b4 = reinterpret_cast<const float4 *>(Mg + (int64_t)(done1 ? 0 : c1) * mp);
+    float4 xa[MR / 4], xb[TWO ? MR / 4 : 1];
 #pragma unroll
     for (int q = 0; q < MR / 4; ++q) {
-      const float4 x = c0 < MR ? a4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-      colA[2 * q] = make_float2(x.x, x.y); colA[2 * q + 1] = make_float2(x.z, x.w);
+      const bool in = 4 * q < mp;
+      xa[q] = !done0 && in ? a4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (TWO) xb[q] = !done1 && in ? b4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    auto keep = [&](float v, int x) { return x < m ? v * mscale : 0.f; };
+#pragma unroll
+    for (int q = 0; q < MR / 4; ++q) {
+      colA[2 * q] = make_float2(keep(xa[q].x, 4 * q), keep(xa[q].y, 4 * q + 1));
+      colA[2 * q + 1] = make_float2(keep(xa[q].z, 4 * q + 2), keep(xa[q].w, 4 * q + 3));
       if constexpr (TWO) {
-        const float4 y = c1 < MR ? b4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-        colB[2 * q] = make_float2(y.x, y.y); colB[2 * q + 1] = make_float2(y.z, y.w);
+        colB[2 * q] = make_float2(keep(xb[q].x, 4 * q), keep(xb[q].y, 4 * q + 1));
+        colB[2 * q + 1] = make_float2(keep(xb[q].z, 4 * q + 2), keep(xb[q].w, 4 * q + 3));
       }
     }
   }
-  bool done0 = c0 >= m, done1 = !TWO || c1 >= m;
-  float dg0 = done0 ? 0.f : T[c0 * TP + c0];
-  float dg1 = done1 ? 0.f : T[c1 * TP + c1];
+  float dg0 = done0 ? 0.f : Mg[(int64_t)c0 * mp + c0] * mscale;
+  float dg1 = done1 ? 0.f : Mg[(int64_t)(TWO ? c1 : 0) * mp + (TWO ? c1 : 0)] * mscale;
   // rows already pivoted (and rows from m on), the same in every lane
   uint64_t gone = m >= 64 ? 0ull : ~0ull << m;
-  __syncwarp(full);  // every lane has read its columns; the square now takes the rows of Rt
+  __syncwarp(full);
   // order-preserving integer key of a finite float (larger float, larger key; 0 = none)
   auto okey = [](float f) {
     const unsigned u = __float_as_uint(f);

@@ -40,7 +40,7 @@
 //                  with Z split into three bf16 terms (24 significant bits),
 //                  KDA's row scale applied to U', lazy scales reset
 //
-// Workspace per head (fp32): M [m][m], R_b [m][m4] (upper, row-major), Y [r][m4]
+// Workspace per head (fp32): M [m][m4], R_b [m][m4] (upper, row-major), Y [r][m4]
 // (m4 = m rounded up to 4), eight words of class lists, each region on 16 bytes,
 // the whole on 256 bytes.  With ragged ranks each 16-column class gets its own
 // three launches, sized for it: with the state's class order (seed.h) over
@@ -67,8 +67,8 @@ struct GramLayout {
   __host__ __device__ GramLayout(int m, int r) {
     m4 = (m + 3) & ~3;
     const int64_t mm4 = ((int64_t)m * m + 3) & ~(int64_t)3;
-    mq = 0;
-    rb = mq + mm4;                 // R_b: m rows of m4 floats (16-byte rows)
+    mq = 0;                        // M: m rows of m4 floats (16-byte rows)
+    rb = mq + (int64_t)m * m4;     // R_b: the same
     y = rb + (int64_t)m * m4;
     lst = y + (int64_t)r * m4;
     per_head = (lst + 8 + 63) & ~(int64_t)63;
@@ -535,8 +535,8 @@ __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phas
           for (int c = a; c < 4; ++c, ++e) {
             const int j = 4 * (jb0 + q) + a, l = 4 * (jb0 + q) + c;
             if (q < nd && j < m && l < m) {
-              ws[W.mq + j * m + l] = acc2[q][e];
-              ws[W.mq + l * m + j] = acc2[q][e];
+              ws[W.mq + j * W.m4 + l] = acc2[q][e];
+              ws[W.mq + l * W.m4 + j] = acc2[q][e];
             }
           }
       }
@@ -566,8 +566,8 @@ __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phas
         for (int c = 0; c < 4; ++c) {
           const int j = 4 * jb + a, l = 4 * lb + c;
           if (j < m && l < m) {
-            ws[W.mq + j * m + l] = acc[a][c];
-            ws[W.mq + l * m + j] = acc[a][c];
+            ws[W.mq + j * W.m4 + l] = acc[a][c];
+            ws[W.mq + l * W.m4 + j] = acc[a][c];
           }
         }
     }
@@ -612,26 +612,18 @@ __global__ void __launch_bounds__(32 * kSvdWarps, evd_min_blocks<MR>()) evd_phas
   float *ws = p.ws + (int64_t)b * W.per_head;
   const float *Mw = ws + W.mq;
 
-  // M into the square (column c at T[c * TP], zero beyond m), scaled by a power of
-  // four to a largest diagonal below one (its square root, sigma, by a power of two)
+  // M is scaled by a power of four to a largest diagonal below one (its square root,
+  // sigma, by a power of two); the core loads it straight into registers
   float dmax = 0.f;
-  for (int idx = lane; idx < MR * MR; idx += HW) {
-    const int c = idx / MR, x = idx % MR;
-    const float v = (c < m && x < m) ? Mw[c * m + x] : 0.f;
-    T[c * SW::TP + x] = v;
-    if (c == x) dmax = fmaxf(dmax, v);
-  }
+  for (int c = lane; c < m; c += HW) dmax = fmaxf(dmax, Mw[(int64_t)c * W.m4 + c]);
 #pragma unroll
   for (int o = HW / 2; o > 0; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(gmask, dmax, o));
   int e = 0;
   if (dmax > 0.f) frexpf(dmax, &e);
   const int e2 = e >= 0 ? (e + 1) / 2 : -((-e) / 2);  // ceil(e / 2)
   const float mscale = ldexpf(1.f, -2 * e2), sunscale = ldexpf(1.f, e2);
-  __syncwarp(gmask);
-  for (int idx = lane; idx < m * MR; idx += HW) T[(idx / MR) * SW::TP + idx % MR] *= mscale;
-  __syncwarp(gmask);
   const float tol = 1e-4f;  // 16-bit factors: their own rounding is 2^-9
-  const int sweeps = evd_warp_core<MR, HW>(m, tol, sqrtf(tol), sw);
+  const int sweeps = evd_warp_core<MR, HW>(m, tol, sqrtf(tol), sw, Mw, W.m4, mscale);
   const float *sig2 = sw + SW::S_OFF, *inv = sw + SW::I_OFF;
   const int *order = reinterpret_cast<const int *>(sw + SW::O_OFF);
   if (lane == 0) {

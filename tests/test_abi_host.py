@@ -173,7 +173,7 @@ def test_synth_calls_reject_on_host():
 
 
 def _ws_floats(m, r, dk, dv, dtype='bf16'):
-    # 16-bit factors (Cholesky of the value-side Gram matrix): M, R_b (rows of m4
+    # 16-bit factors (Cholesky of the value-side Gram matrix): M and R_b (rows of m4
     # floats), Y and eight words of class lists; 32-bit factors (QR of both factors):
     # W's reflectors, their tau, R_b^T, K, Y; each region on 16 bytes, the whole on
     # 256 bytes
@@ -182,7 +182,7 @@ def _ws_floats(m, r, dk, dv, dtype='bf16'):
     if dtype == 'f32':
         n = m * dv + m4 + 2 * mm4 + r * m4
     else:
-        n = mm4 + m * m4 + r * m4 + 8
+        n = 2 * m * m4 + r * m4 + 8
     n = (n + 63) // 64 * 64
     return max(n, 64)
 
