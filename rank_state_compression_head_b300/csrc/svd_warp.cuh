@@ -454,32 +454,31 @@ __device__ inline bool jac_rotation(float dot_xy, const JacCol &x, const JacCol 
 
 // The register arrays hold a column as MR / 2 pairs of consecutive elements, so that
 // the element loops run on the packed two-lane fp32 instructions of sm_100 and later
-// (each lane rounds as its scalar counterpart: the same results in half the issue
-// slots).  Elements 4j, 4j+1 sit in pair 2j and 4j+2, 4j+3 in pair 2j+1, so two
-// packed accumulators are the four chains of element k % 4.
+// (each lane of a packed FMA rounds as a scalar FMA does, in half the issue slots).
+// Elements 2k, 2k+1 sit in pair k.
 __device__ inline float2 f2(float v) { return make_float2(v, v); }
+
+// Sums of products over a column in four packed accumulators (pair k into k % 4:
+// eight chains of element k % 8), so that the dependent chains are short.
+template <int MR>
+__device__ inline float jac_sum8(float2 (&s)[4]) {
+  return ((s[0].x + s[0].y) + (s[1].x + s[1].y)) + ((s[2].x + s[2].y) + (s[3].x + s[3].y));
+}
 
 template <int MR>
 __device__ inline float jac_norm2(const float2 (&x)[MR / 2], float d) {
-  float2 s0 = f2(0.f), s1 = f2(0.f);
+  float2 s[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
 #pragma unroll
-  for (int k = 0; k < MR / 2; ++k) {
-    if (k & 1) s1 = __ffma2_rn(x[k], x[k], s1);
-    else s0 = __ffma2_rn(x[k], x[k], s0);
-  }
-  return ((s0.x + s0.y) + (s1.x + s1.y)) * (d * d);
+  for (int k = 0; k < MR / 2; ++k) s[k & 3] = __ffma2_rn(x[k], x[k], s[k & 3]);
+  return jac_sum8<MR>(s) * (d * d);
 }
 
-// dot product with four accumulation chains (a shorter dependent chain)
 template <int MR>
 __device__ inline float jac_dot(const float2 (&x)[MR / 2], const float2 (&y)[MR / 2]) {
-  float2 s0 = f2(0.f), s1 = f2(0.f);
+  float2 s[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
 #pragma unroll
-  for (int k = 0; k < MR / 2; ++k) {
-    if (k & 1) s1 = __ffma2_rn(x[k], y[k], s1);
-    else s0 = __ffma2_rn(x[k], y[k], s0);
-  }
-  return (s0.x + s0.y) + (s1.x + s1.y);
+  for (int k = 0; k < MR / 2; ++k) s[k & 3] = __ffma2_rn(x[k], y[k], s[k & 3]);
+  return jac_sum8<MR>(s);
 }
 
 // One even round (the lane's own pair) and one odd round (pairs with the
@@ -520,20 +519,19 @@ __device__ inline void jac_round_pair(float2 (&A)[MR / 2], float2 (&B)[MR / 2], 
   float2 (&Xl)[NP] = RIGHT_A ? B : A;   // my left-facing column
   JacCol &cxr = RIGHT_A ? ca : cb;
   JacCol &cxl = RIGHT_A ? cb : ca;
-  float2 s0 = f2(0.f), s1 = f2(0.f);
+  float2 s[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
     Y[k].x = __shfl_down_sync(full, Xl[k].x, 1, HW);   // right neighbour's left-facing column
     Y[k].y = __shfl_down_sync(full, Xl[k].y, 1, HW);
-    if (k & 1) s1 = __ffma2_rn(Xr[k], Y[k], s1);
-    else s0 = __ffma2_rn(Xr[k], Y[k], s0);
+    s[k & 3] = __ffma2_rn(Xr[k], Y[k], s[k & 3]);
   }
   JacCol cr;
   cr.d = __shfl_down_sync(full, cxl.d, 1, HW);
   cr.n2 = __shfl_down_sync(full, cxl.n2, 1, HW);
   float ta1, tb1, c1, tg1;
   int far1 = 0;
-  const bool rot1 = jac_rotation((s0.x + s0.y) + (s1.x + s1.y), cxr, cr, tol2, stop2, ta1, tb1, c1, tg1, far1);
+  const bool rot1 = jac_rotation(jac_sum8<MR>(s), cxr, cr, tol2, stop2, ta1, tb1, c1, tg1, far1);
   far |= has_right && far1;
   // the left neighbour's decision on the pair (its x, my left-facing y), and its x's metadata
   const float ta2 = __shfl_up_sync(full, ta1, 1, HW);
