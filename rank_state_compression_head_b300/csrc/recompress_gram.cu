@@ -37,7 +37,8 @@
 //                  truncation error, the kept Y to the workspace
 //   gram_rebuild   one CTA per (head, factor): Z = diag(c) R_b^T Y_r (U) or
 //                  R_b^{-1} Y_r (W, back substitution), F' = F Z on mma.sync
-//                  with Z split into three bf16 terms (24 significant bits),
+//                  with Z split into two 16-bit terms (16 or 22 significant
+//                  bits, far finer than the factor's own rounding),
 //                  KDA's row scale applied to U', lazy scales reset
 //
 // Workspace per head (fp32): M [m][m4], R_b [m][m4] (upper, row-major), Y [r][m4]
@@ -191,16 +192,19 @@ template <typename TF>
 __device__ static inline void g_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   Mma16<TF>::mma(d, a[0], a[1], a[2], a[3], b0, b1);
 }
-// (x, y) as three packed 16-bit terms t0 + t1 + t2 (24 significant bits while the
-// terms stay in the type's normal range: fp16 callers scale Z by a power of two)
-template <typename TF>
-__device__ static inline void g_split3(float x, float y, uint32_t (&t)[3]) {
+// (x, y) as NTERM packed 16-bit terms t0 + t1 (+ t2): 16 (bf16) or 22 (fp16)
+// significant bits with two terms, 24 with three, while the terms stay in the type's
+// normal range (fp16 callers scale Z by a power of two)
+template <typename TF, int NTERM>
+__device__ static inline void g_split(float x, float y, uint32_t (&t)[3]) {
   t[0] = Mma16<TF>::pack(x, y);
   float2 h = Mma16<TF>::unpack(t[0]);
   x -= h.x; y -= h.y;
   t[1] = Mma16<TF>::pack(x, y);
-  h = Mma16<TF>::unpack(t[1]);
-  t[2] = Mma16<TF>::pack(x - h.x, y - h.y);
+  if constexpr (NTERM == 3) {
+    h = Mma16<TF>::unpack(t[1]);
+    t[2] = Mma16<TF>::pack(x - h.x, y - h.y);
+  }
 }
 
 // fp16 operands of F Z: each row n of Z^T (a column of Z) scaled by a power of two so
@@ -344,9 +348,9 @@ __device__ inline void gram_tile(uint32_t base, int i0, int j0, int depth, float
 
 // D[r][i][n] += sum_j F[i][j] Z[j][n] for the rows i of tile r (i0 + 16 r .. + 15), the
 // columns n0..n0+7 and j < depth16: F column j in smem row j of the tile at `tile`
-// (stride STR bytes), Z row n at Zt + n * ZP (fp32, split once into three 16-bit terms:
-// 24 significant bits, products exact, fp32 accumulation).
-template <typename TF, int STR, int ZP, int NR, int KMAX>
+// (stride STR bytes), Z row n at Zt + n * ZP (fp32, split once into NTERM 16-bit terms,
+// g_split; products exact, fp32 accumulation).
+template <typename TF, int STR, int ZP, int NR, int KMAX, int NTERM>
 __device__ inline void tiles_times_z(uint32_t tile, const float *Zt, int i0, int n0, int depth16,
                                      float (&d)[NR][4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -359,8 +363,8 @@ __device__ inline void tiles_times_z(uint32_t tile, const float *Zt, int i0, int
     if (16 * kk < depth16) {
       const float2 z0 = *reinterpret_cast<const float2 *>(Zt + (n0 + g) * ZP + 16 * kk + 2 * t);
       const float2 z1 = *reinterpret_cast<const float2 *>(Zt + (n0 + g) * ZP + 16 * kk + 8 + 2 * t);
-      g_split3<TF>(z0.x, z0.y, bz[kk][0]);
-      g_split3<TF>(z1.x, z1.y, bz[kk][1]);
+      g_split<TF, NTERM>(z0.x, z0.y, bz[kk][0]);
+      g_split<TF, NTERM>(z1.x, z1.y, bz[kk][1]);
     }
   }
 #pragma unroll
@@ -371,7 +375,7 @@ __device__ inline void tiles_times_z(uint32_t tile, const float *Zt, int i0, int
         uint32_t a[4];
         g_ldsm_x4_t(tile + (uint32_t)((16 * kk + rsel) * STR + (i0 + 16 * r + cofs) * 2), a);
 #pragma unroll
-        for (int q = 0; q < 3; ++q) g_mma<TF>(d[r], a, bz[kk][0][q], bz[kk][1][q]);
+        for (int q = 0; q < NTERM; ++q) g_mma<TF>(d[r], a, bz[kk][0][q], bz[kk][1][q]);
       }
     }
   }
@@ -478,7 +482,7 @@ __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phas
 #pragma unroll
         for (int e = 0; e < 4; ++e) bacc[q][r][e] = 0.f;
       if (task < per)
-        tiles_times_z<TF, L::USTR, ZP, 4, MR>(ub, Zt, (task / ntile) * 64, (task % ntile) * 8, m16, bacc[q]);
+        tiles_times_z<TF, L::USTR, ZP, 4, MR, 3>(ub, Zt, (task / ntile) * 64, (task % ntile) * 8, m16, bacc[q]);
     }
     __syncthreads();  // both tiles are read
 #pragma unroll
@@ -854,7 +858,7 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
   g_cp_commit_wait_all();
   __syncthreads();
 
-  // ---- F' = F Z on the tensor cores (Z in three 16-bit terms) -----------------------------------
+  // ---- F' = F Z on the tensor cores (Z in two 16-bit terms) -------------------------------------
   {
     const int g = lane >> 2, t = lane & 3;
     // a task is one column tile over four row tiles (all of a 64-row factor, half of a
@@ -865,7 +869,9 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
     for (int task = warp; task < per; task += kGramThreads / 32) {
       const int ib = (task / ntile) * 64, n0 = (task % ntile) * 8;
       float d[4][4] = {};
-      tiles_times_z<TF, L::STR, ZP, 4, MR>(tb, Z, ib, n0, m16, d);
+      // two terms of Z: their 2^-17 (bf16) or 2^-23 (fp16) is far below the rounding
+      // of the stored factor that the product becomes
+      tiles_times_z<TF, L::STR, ZP, 4, MR, 2>(tb, Z, ib, n0, m16, d);
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int i0 = ib + 16 * r;

@@ -114,3 +114,50 @@ def test_head_in_too_small_a_class_is_reported_and_untouched():
         c, r, _ = good.head_cols(h)
         assert torch.equal(good.U[c:c + r + T], bad.U[c:c + r + T]), h
         assert torch.equal(good.a[h], bad.a[h]), h
+
+
+def test_misfiled_heads_in_a_persistent_launch():
+    """More heads than one launch keeps resident: each CTA walks several heads and
+    refills its stage from one to the next; the misfiled ones among them are reported
+    and left untouched, and every other head comes out as in a correct order."""
+    variant, dtype, H, T = 'gdn', 'bf16', 2600, 8
+    ranks = np.where(np.arange(H) % 50 == 7, 40, 16).astype(np.int32)  # capacity 24 (class 1), 48 (class 2)
+    states, vbar = random_states(79, H, 128, 128, ranks, 0, T, variant, dtype)
+    good = make_buffers(variant, dtype, H, 128, 128, T, vbar, ranks)
+    bad = make_buffers(variant, dtype, H, 128, 128, T, vbar, ranks)
+    upload(good, states, 0)
+    upload(bad, states, 0)
+    order = bad.head_order.cpu().numpy().tolist()
+    ends = list(bad.class_end)
+    misfiled = [h for h in range(H) if ranks[h] == 40][::3]
+    for h in misfiled:
+        order.remove(h)
+    span = ends[1] - ends[0]
+    for i, h in enumerate(misfiled):  # spread through the class-1 positions
+        order.insert(ends[0] + (i * span) // len(misfiled) + i, h)
+    ends[1] += len(misfiled)
+    bad.head_order.copy_(torch.tensor(order, dtype=torch.int32))
+    for c in range(4):
+        bad.st.class_end[c] = ends[c]
+    steps, A = _inputs(variant, H, T, 5)
+    U0, a0 = bad.U.clone(), bad.a.clone()
+    outs = []
+    for buf in (good, bad):
+        o = torch.empty(2, H, 128, device='cuda')
+        for t, (q, k, v, gate, beta) in enumerate(steps[:2]):
+            R.seed_decode_step(buf.st, q, k, v, gate, beta, None, o[t])
+        outs.append(o)
+    torch.cuda.synchronize()
+    st = bad.status.cpu().numpy()
+    assert (st[misfiled] == R.SEED_ERR_INVALID_ARG).all()
+    assert (np.delete(st, misfiled) == 0).all() and int(good.status.abs().sum()) == 0
+    bad_set = set(misfiled)
+    for h in range(H):
+        c, r, _ = good.head_cols(h)
+        if h in bad_set:
+            assert torch.equal(bad.U[c:c + r + T], U0[c:c + r + T]) and torch.equal(bad.a[h], a0[h]), h
+            continue
+        assert torch.equal(outs[0][:, h], outs[1][:, h]), h
+        assert torch.equal(good.U[c:c + r + T], bad.U[c:c + r + T]), h
+        assert torch.equal(good.W[c:c + r + T], bad.W[c:c + r + T]), h
+        assert torch.equal(good.a[h], bad.a[h]), h
