@@ -1,8 +1,8 @@
 """Data-parallel layout of the decode path over several GPUs.
 
-Every head is independent in every call (one head per CTA or warp, no
-cross-head data), so the path shards by head with no collective on the data
-path: each rank holds its own batch of requests, with the shapes of the
+Every head is independent in every call (a CTA or a warp works on one head at
+a time, with no cross-head data), so the path shards by head with no collective
+on the data path: each rank holds its own batch of requests, with the shapes of the
 workload and its own seed, and runs the whole decode + recompression schedule
 on them.  The only communication is for measurement: a barrier around the
 timed region and the maximum of the ranks' times (weak scaling: the job's
