@@ -518,8 +518,12 @@ def run_gpu(args, w):
         for j, src in enumerate((run.q, run.k, run.v, run.gate, run.beta)):
             hin[:, offs[j]:offs[j + 1]].copy_(src[:n_host].reshape(n_host, -1))
         hout = torch.empty(n_host, *run.o.shape, pin_memory=True)
-        din = [torch.empty(n_in, device=dev) for _ in range(2)]
-        dout = [torch.empty_like(run.o) for _ in range(2)]
+        # device slots for the steps' inputs and outputs: the uploads run up to
+        # n_dev - 1 steps ahead of the compute, so the host link keeps streaming while
+        # a recompression runs
+        n_dev = 4
+        din = [torch.empty(n_in, device=dev) for _ in range(n_dev)]
+        dout = [torch.empty_like(run.o) for _ in range(n_dev)]
         up, down = torch.cuda.Stream(), torch.cuda.Stream()
         # Raw runtime calls keep the host's issue cost per step to a few microseconds,
         # well under the copy time, so the host runs ahead of the GPU.
@@ -554,22 +558,24 @@ def run_gpu(args, w):
         def e2e_loop(n):
             """n steps from a compression boundary; the last ends on one when T | n."""
             def upload(i):
-                if i >= 2:
-                    rt.cudaStreamWaitEvent(s_up, comp_done[i - 2], 0)  # slot i % 2 consumed by step i-2
-                rc_ = rt.cudaMemcpyAsync(din_p[i % 2], hin_p[i % n_host], h2d, 1, s_up)
+                if i >= n_dev:
+                    rt.cudaStreamWaitEvent(s_up, comp_done[i - n_dev], 0)  # slot consumed by step i - n_dev
+                rc_ = rt.cudaMemcpyAsync(din_p[i % n_dev], hin_p[i % n_host], h2d, 1, s_up)
                 rt.cudaEventRecord(h2d_done[i], s_up)
                 return rc_
 
             up.wait_stream(stream)
             down.wait_stream(stream)
-            rc = upload(0)
+            rc = 0
+            for i in range(min(n_dev - 1, n)):
+                rc |= upload(i)
             for i in range(n):
-                slot = i % 2
-                if i + 1 < n:
-                    rc |= upload(i + 1)
+                slot = i % n_dev
+                if i + n_dev - 1 < n:
+                    rc |= upload(i + n_dev - 1)
                 rt.cudaStreamWaitEvent(s_comp, h2d_done[i], 0)
-                if i >= 2:
-                    rt.cudaStreamWaitEvent(s_comp, d2h_done[i - 2], 0)  # output slot read back
+                if i >= n_dev:
+                    rt.cudaStreamWaitEvent(s_comp, d2h_done[i - n_dev], 0)  # output slot read back
                 a_ = in_args[slot]
                 rc |= dec_fn(st_ref, a_[0], a_[1], a_[2], a_[3], a_[4], A_ptr, dout_p[slot], sptr)
                 if run.state.steps_since_compress == T:
