@@ -9,7 +9,8 @@
 //   G_w = W^T W = R_b^T R_b    (tensor cores; Cholesky, so Q_b = W R_b^{-1} has
 //                               orthonormal columns and U_eff W^T = B Q_b^T)
 //   B   = U_eff R_b^T          (tensor cores, R_b in three bf16 terms)
-//   M   = B^T B = Y Sigma^2 Y^T (fp32; pivoted Cholesky + one-sided Jacobi, evd_warp.cuh)
+//   M   = B^T B = Y Sigma^2 Y^T (tensor cores, B in three bf16 terms; pivoted Cholesky +
+//                               one-sided Jacobi, evd_warp.cuh)
 //   U'  = U_eff R_b^T Y_r = B Y_r,   W' = W R_b^{-1} Y_r = Q_b Y_r  (tensor cores)
 //
 // With Q_b orthonormal the singular values of U_eff W^T are those of B, Y holds
@@ -30,9 +31,9 @@
 //
 //   gram_phase     one CTA per head: both factors into shared memory (cp.async),
 //                  G_w on mma.sync, Cholesky by one warp in registers,
-//                  B = U diag(c) R_b^T on mma.sync (KDA: rows times D), stored
-//                  over the tiles, M = B^T B in fp32 4 x 4 blocks; M and R_b to
-//                  the workspace
+//                  B = U diag(c) R_b^T on mma.sync (KDA: rows times D), then
+//                  M = B^T B on mma.sync from B's three bf16 terms stored over the
+//                  tiles, half its rows at a time; M and R_b to the workspace
 //   evd_phase      one lane group per head: eigenvectors of M (evd_warp.cuh),
 //                  truncation error, the kept Y to the workspace
 //   gram_rebuild   one CTA per (head, factor): Z = diag(c) R_b^T Y_r (U) or
@@ -67,7 +68,6 @@ struct GramLayout {
   int m4;
   __host__ __device__ GramLayout(int m, int r) {
     m4 = (m + 3) & ~3;
-    const int64_t mm4 = ((int64_t)m * m + 3) & ~(int64_t)3;
     mq = 0;                        // M: m rows of m4 floats (16-byte rows)
     rb = mq + (int64_t)m * m4;     // R_b: the same
     y = rb + (int64_t)m * m4;
@@ -228,22 +228,21 @@ __device__ inline void scale_z_rows(float *Zt, int zp, int rows, int cols, float
 
 // Shared layout of gram_phase (bytes): both factor tiles (column j of the factor
 // in row j, rows padded by 16 bytes so that ldmatrix hits distinct banks; the W
-// tile's space is reused for Z once G_w is formed), B = U_eff R_b^T over both
-// tiles once they have been read (row i at i * BP floats), G_w / R_b (row i at
-// i * GP floats), the scales, the original diagonal of G_w.
+// tile's space is reused for Z once G_w is formed), the three bf16 terms of half of
+// B = U_eff R_b^T over both tiles once they have been read (S_BYTES), G_w / R_b
+// (row i at i * GP floats), the scales, the original diagonal of G_w.
 template <int DV, int MR>
 struct GramSmem {
   static constexpr int USTR = kDK * 2 + 16, WSTR = DV * 2 + 16;
   static constexpr int GP = MR + 1;
   static constexpr int ZP = MR + 8;  // Z row pitch (floats): row n = column n of Z
-  static constexpr int BP = MR + 4;
   static constexpr int WZ_BYTES = MR * WSTR > MR * ZP * 4 ? MR * WSTR : MR * ZP * 4;
   static constexpr int U_OFF = 0;
   static constexpr int W_OFF = U_OFF + MR * USTR;  // W tile, then Z
   static constexpr int TILE_BYTES = W_OFF + WZ_BYTES;
-  static constexpr int B_OFF = 0;                  // B, over both tiles
-  static constexpr int B_BYTES = kDK * BP * 4;
-  static constexpr int G_OFF = ((TILE_BYTES > B_BYTES ? TILE_BYTES : B_BYTES) + 15) & ~15;
+  static constexpr int KP = 64 + 8;                // bf16 a row of a term of half of B
+  static constexpr int S_BYTES = 3 * MR * KP * 2;  // the three terms, over the tiles
+  static constexpr int G_OFF = ((TILE_BYTES > S_BYTES ? TILE_BYTES : S_BYTES) + 15) & ~15;
   static constexpr int SC_OFF = G_OFF + ((MR * GP * 4 + 15) & ~15);
   static constexpr int DG_OFF = SC_OFF + (MR > kDK ? MR : kDK) * 4;
   static constexpr int ZS_OFF = DG_OFF + MR * 4;  // per-column unscale of Z (fp16)
@@ -390,7 +389,7 @@ template <typename TF, int VAR, int DV, int MR>
 __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phase(const GramArgs p) {
   constexpr int DK = kDK;
   using L = GramSmem<DV, MR>;
-  constexpr int GP = L::GP, ZP = L::ZP, BP = L::BP;
+  constexpr int GP = L::GP, ZP = L::ZP;
   constexpr bool KDA = VAR == SEED_KDA;
   extern __shared__ __align__(128) unsigned char smem[];
   int slot, h;
@@ -404,7 +403,6 @@ __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phas
   const int64_t c0 = sv.col0(h);
   float *Gw = reinterpret_cast<float *>(smem + L::G_OFF);
   float *Zt = reinterpret_cast<float *>(smem + L::W_OFF);
-  float *B = reinterpret_cast<float *>(smem + L::B_OFF);
   float *sc = reinterpret_cast<float *>(smem + L::SC_OFF);
   float *dg = reinterpret_cast<float *>(smem + L::DG_OFF);
   float *zsc = reinterpret_cast<float *>(smem + L::ZS_OFF);
@@ -484,98 +482,104 @@ __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phas
       if (task < per)
         tiles_times_z<TF, L::USTR, ZP, 4, MR, 3>(ub, Zt, (task / ntile) * 64, (task % ntile) * 8, m16, bacc[q]);
     }
-    __syncthreads();  // both tiles are read
+    __syncthreads();  // both tiles are read: they take B, in three bf16 terms, half its rows at a time
+
+    // ---- M = B^T B on the tensor cores ------------------------------------------------------
+    // B = B0 + B1 + B2 (bf16 terms of the fp32 values: 24 significant bits, whatever the
+    // factor type) and M = sum of Bp^T Bq over p + q <= 2, the six products that carry
+    // it to fp32 accuracy (those left out are below 2^-24 of it), with fp32 accumulation.
+    // Term p of rows 64h .. 64h + 63 lies at Sp[n * KP + i] (column n of B as a row, so
+    // that both operands load by ldmatrix).  A warp keeps its tiles of the upper triangle
+    // (16 x 8, j-tile J and l-tile L with L >= 2J) in registers over both halves.
+    constexpr int KP = L::KP;                           // bf16 a row of a term: 144 bytes
+    constexpr int NUT = (MR / 16) * (MR / 8) - (MR / 16) * (MR / 16 - 1);  // upper tiles
+    constexpr int TPW = (NUT + NW - 1) / NW;            // tiles a warp, at most
+    static_assert(L::S_BYTES <= L::G_OFF, "the three terms of half of B lie before G_w");
+    __nv_bfloat16 *S0 = reinterpret_cast<__nv_bfloat16 *>(smem + L::U_OFF);
+    const uint32_t s_base = smem_u32(S0);
+    constexpr uint32_t TERM = MR * KP * 2;              // bytes a term
+    int tJ[TPW], tL[TPW];
+    float dm[TPW][4];
 #pragma unroll
-    for (int q = 0; q < NTK; ++q) {
-      const int task = warp + q * NW;
-      if (task < per) {
-        const int ib = (task / ntile) * 64, n0 = (task % ntile) * 8;
+    for (int s_ = 0; s_ < TPW; ++s_) {
+      int k = warp + NW * s_, J = 0;
+      while (J < MR / 16 && k >= MR / 8 - 2 * J) { k -= MR / 8 - 2 * J; ++J; }
+      tJ[s_] = J < MR / 16 && 16 * J < m16 ? J : -1;
+      tL[s_] = 2 * J + k;
+      if (tJ[s_] >= 0 && 8 * tL[s_] >= m16) tJ[s_] = -1;
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+      for (int e = 0; e < 4; ++e) dm[s_][e] = 0.f;
+    }
+    for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = ib + 16 * r + g + (e >> 1) * 8, n = n0 + 2 * t + (e & 1);
-            const float v = bacc[q][r][e] * zsc[n];
-            B[i * BP + n] = KDA ? v * sc[i] : v;
+      for (int q = 0; q < NTK; ++q) {
+        const int task = warp + q * NW;
+        if (task < per && task / ntile == h) {
+          const int n0 = (task % ntile) * 8;
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = 16 * r + g + (e >> 1) * 8, n = n0 + 2 * t + (e & 1);
+              float v = bacc[q][r][e] * zsc[n];
+              if (KDA) v *= sc[64 * h + i];
+              const __nv_bfloat16 b0 = __float2bfloat16_rn(v);
+              const float r1 = v - __bfloat162float(b0);
+              const __nv_bfloat16 b1 = __float2bfloat16_rn(r1);
+              const __nv_bfloat16 b2 = __float2bfloat16_rn(r1 - __bfloat162float(b1));
+              S0[n * KP + i] = b0;
+              S0[MR * KP + n * KP + i] = b1;
+              S0[2 * MR * KP + n * KP + i] = b2;
+            }
+        }
+      }
+      __syncthreads();  // this half's terms are in place
+#pragma unroll
+      for (int s_ = 0; s_ < TPW; ++s_) {
+        if (tJ[s_] < 0) continue;
+        // A: rows 16J .. of each term (ldmatrix x4); B: rows 8L .. (x2)
+        const uint32_t a_row = s_base + (uint32_t)(((16 * tJ[s_] + (lane & 7) + ((lane >> 3) & 1) * 8) * KP + (lane >> 4) * 8) * 2);
+        const uint32_t b_row = s_base + (uint32_t)(((8 * tL[s_] + (lane & 7)) * KP + ((lane >> 3) & 1) * 8) * 2);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t A[3][4], Bq[3][2];
+#pragma unroll
+          for (int p_ = 0; p_ < 3; ++p_) {
+            g_ldsm_x4(a_row + p_ * TERM + kk * 32, A[p_]);
+            asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                         : "=r"(Bq[p_][0]), "=r"(Bq[p_][1]) : "r"(b_row + p_ * TERM + kk * 32));
           }
+          g_mma<__nv_bfloat16>(dm[s_], A[0], Bq[0][0], Bq[0][1]);
+          g_mma<__nv_bfloat16>(dm[s_], A[0], Bq[1][0], Bq[1][1]);
+          g_mma<__nv_bfloat16>(dm[s_], A[1], Bq[0][0], Bq[0][1]);
+          g_mma<__nv_bfloat16>(dm[s_], A[0], Bq[2][0], Bq[2][1]);
+          g_mma<__nv_bfloat16>(dm[s_], A[2], Bq[0][0], Bq[0][1]);
+          g_mma<__nv_bfloat16>(dm[s_], A[1], Bq[1][0], Bq[1][1]);
+        }
+      }
+      __syncthreads();  // the terms have been read
+    }
+
+    // ---- M to the workspace: each entry with j <= l once, and its mirror ---------------------
+    const GramLayout W(p.layout_m, p.r_max);
+    float *ws = p.ws + (int64_t)slot * W.per_head;
+#pragma unroll
+    for (int s_ = 0; s_ < TPW; ++s_) {
+      if (tJ[s_] < 0) continue;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 16 * tJ[s_] + g + (e >> 1) * 8, l = 8 * tL[s_] + 2 * t + (e & 1);
+        if (j <= l && l < m) {
+          ws[W.mq + (int64_t)j * W.m4 + l] = dm[s_][e];
+          if (j != l) ws[W.mq + (int64_t)l * W.m4 + j] = dm[s_][e];
+        }
       }
     }
   }
-  __syncthreads();
 
-  // ---- M = B^T B in fp32 (4 x 4 blocks of the upper triangle), M and R_b to the workspace -----
+  // ---- R_b to the workspace ---------------------------------------------------------------------
   const GramLayout W(p.layout_m, p.r_max);
   float *ws = p.ws + (int64_t)slot * W.per_head;
-  {
-    const int nb = (m + 3) / 4, nblk = nb * (nb + 1) / 2;
-    // More blocks than threads (64 columns: 136): the off-diagonal blocks one a thread and
-    // the diagonal ones two a thread, their upper triangles only (10 entries each), so
-    // that no thread takes a second round while the others wait (same sums, same order)
-    const int noff = nb * (nb - 1) / 2;
-    const bool pair_diag = nblk > kGramThreads;
-    for (int d = tid - noff; pair_diag && d >= 0 && 2 * d < nb; d += kGramThreads) {
-      float acc2[2][10] = {};
-      const int jb0 = 2 * d, nd = 2 * d + 1 < nb ? 2 : 1;
-      for (int i = 0; i < DK; ++i) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          if (q < nd) {
-            const float4 x = *reinterpret_cast<const float4 *>(B + i * BP + 4 * (jb0 + q));
-            const float xs[4] = {x.x, x.y, x.z, x.w};
-            int e = 0;
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-              for (int c = a; c < 4; ++c, ++e) acc2[q][e] = fmaf(xs[a], xs[c], acc2[q][e]);
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        int e = 0;
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int c = a; c < 4; ++c, ++e) {
-            const int j = 4 * (jb0 + q) + a, l = 4 * (jb0 + q) + c;
-            if (q < nd && j < m && l < m) {
-              ws[W.mq + j * W.m4 + l] = acc2[q][e];
-              ws[W.mq + l * W.m4 + j] = acc2[q][e];
-            }
-          }
-      }
-    }
-    for (int blk = tid; blk < (pair_diag ? noff : nblk); blk += kGramThreads) {
-      int jb = 0, lb = 0, rem = blk;
-      if (pair_diag) {  // blk -> (jb < lb)
-        while (rem >= nb - 1 - jb) { rem -= nb - 1 - jb; ++jb; }
-        lb = jb + 1 + rem;
-      } else {          // blk -> (jb <= lb)
-        while (rem >= nb - jb) { rem -= nb - jb; ++jb; }
-        lb = jb + rem;
-      }
-      float acc[4][4] = {};
-      for (int i = 0; i < DK; ++i) {
-        const float4 x = *reinterpret_cast<const float4 *>(B + i * BP + 4 * jb);
-        const float4 y = *reinterpret_cast<const float4 *>(B + i * BP + 4 * lb);
-        const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(xs[a], ys[c], acc[a][c]);
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int j = 4 * jb + a, l = 4 * lb + c;
-          if (j < m && l < m) {
-            ws[W.mq + j * W.m4 + l] = acc[a][c];
-            ws[W.mq + l * W.m4 + j] = acc[a][c];
-          }
-        }
-    }
-  }
   for (int i = warp; i < m; i += kGramThreads / 32)  // R_b by rows of W.m4, zero beyond m
     for (int l = lane; l < W.m4; l += 32) ws[W.rb + (int64_t)i * W.m4 + l] = (l >= i && l < m) ? Gw[i * GP + l] : 0.f;
 }
