@@ -439,6 +439,9 @@ __global__ void __launch_bounds__(kGramThreads, gram_min_blocks<MR>()) gram_phas
     const uint32_t wb = smem_u32(smem + L::W_OFF);
     for (int task = warp; task < per; task += kGramThreads / 32) {
       const int i0 = (task / ncol) * 16, j0 = (task % ncol) * 8;
+      // only tiles that reach the upper triangle: the Cholesky reads nothing below the
+      // diagonal into its results (those registers are updated but never read back)
+      if (j0 + 8 <= i0) continue;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       gram_tile<TF, L::WSTR>(wb, i0, j0, DV, d);
 #pragma unroll
