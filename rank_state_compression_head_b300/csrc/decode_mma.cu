@@ -130,9 +130,9 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MAXC>()) decode_mm
   // head of launch item i: through the class order when the launch has one
   auto head_at = [&](int i) { return sv.order ? sv.order[p.pos0 + i] : i; };
 
-  // What the copies of an item need: its head, rank, columns and sink direction.
-  // The head index is read one item ahead and the rest during the U pass, so that
-  // the chain of dependent reads is off the path of the copies.
+  // What the copies of an item need: its head, rank, columns and sink direction,
+  // read ahead of the copies (below), so that the chain of dependent reads is off
+  // their path.
   struct Item {
     int h, r, m, dir;
     int64_t c0;
