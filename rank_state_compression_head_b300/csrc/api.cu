@@ -7,7 +7,8 @@
 // the fixed device scratch of seed_recompress_noalloc (recompress_split.cu),
 // a file-scope __device__ array that every device loading the library holds.
 // Besides that, the decode launchers remember per device which of their kernels
-// already had their shared-memory attributes set.
+// already had their shared-memory attributes set, and the 16-bit one how many
+// CTAs of each kernel the device holds at once (the size of its persistent grid).
 #include "common.cuh"
 
 #include <stdint.h>
