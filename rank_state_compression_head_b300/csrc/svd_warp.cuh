@@ -439,11 +439,13 @@ __device__ inline bool jac_rotation(float dot_xy, const JacCol &x, const JacCol 
   // error of that size in t makes each rotation orthogonal to about 2^-22; over the
   // few hundred rotations a column takes part in, that stays near 1e-6, far below
   // the convergence tolerance.
-  const float gs = rot ? ga : 1.f;
-  const float zeta = __fdividef(be - al, 2.f * gs);
-  const float az = fabsf(zeta);
-  const float root = az < 1e18f ? az + fmaf(az, az, 1.f) * rsqrtf(fmaf(az, az, 1.f)) : 2.f * az;
-  const float t = rot ? copysignf(__fdividef(1.f, root), zeta) : 0.f;
+  // t = sign(zeta) / (|zeta| + sqrt(1 + zeta^2)) with zeta = (be - al) / (2 ga), written
+  // as 2 ga sign(be - al) / (|be - al| + sqrt((be - al)^2 + 4 ga^2)): the same root with
+  // one quotient fewer on the chain (ga^2 > 0 when the pair rotates; the other branch
+  // is discarded by the select)
+  const float dba = be - al, dd = fabsf(dba), g2 = 2.f * ga;
+  const float r2 = fmaf(dd, dd, g2 * g2);
+  const float t = rot ? __fdividef(copysignf(1.f, dba) * g2, dd + r2 * rsqrtf(r2)) : 0.f;
   c = rsqrtf(fmaf(t, t, 1.f));
   ta = t * __fdividef(y.d, x.d);
   tb = t * __fdividef(x.d, y.d);
