@@ -783,12 +783,15 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
         }
     }
   } else {
-    // R_b Z = Y by back substitution in row panels of 16 from the bottom: a thread per
-    // column n solves the panel's triangle in registers (each row's sum taken over the
-    // earliest-solved entries first, so that consecutive rows overlap), then all
-    // threads take the panel's contribution off the rows above.  A zero pivot
-    // (dropped row) gives a zero entry.
+    // R_b Z = Y by back substitution in row panels of 16 from the bottom.  The inverses
+    // of the panels' diagonal 16 x 16 blocks are formed first, a thread per column of a
+    // block (back substitution of a unit vector; a zero pivot, a dropped row, gives a
+    // zero row), in Y's space once Y has been copied into Z.  Each panel then takes its
+    // triangle as a product with its block's inverse (two threads a column of Z, each
+    // warp on the same half of the rows), and the rows above lose the panel's
+    // contribution.  In exact arithmetic this is the back substitution itself.
     float *rinv = Ys + MR * YP;  // 1 / R_b[i][i] (0 for a dropped row), after Y
+    float *Dv = Ys;              // the block inverses, 256 floats each, once Y is in Z
     for (int idx = tid; idx < rk * m; idx += kGramThreads) {
       const int n = idx / m, i = idx % m;
       Z[n * ZP + i] = Ys[n * YP + i];
@@ -798,27 +801,55 @@ __global__ void __launch_bounds__(kGramThreads) gram_rebuild(const GramArgs p) {
       rinv[i] = piv != 0.f ? 1.f / piv : 0.f;
     }
     __syncthreads();
+    const int np = (m + 15) / 16;
+    for (int tsk = tid; tsk < 16 * np; tsk += kGramThreads) {
+      const int kb = tsk >> 4, c = tsk & 15;
+      const int bb1 = m - 16 * kb, bb0 = bb1 > 16 ? bb1 - 16 : 0, w = bb1 - bb0;
+      float x[16];
+#pragma unroll
+      for (int q = 15; q >= 0; --q) {
+        float s_ = q == c ? 1.f : 0.f;
+#pragma unroll
+        for (int u = 15; u > q; --u)
+          if (u < w) s_ = fmaf(-Rb[(bb0 + q) * RP + bb0 + u], x[u], s_);
+        x[q] = q < w ? s_ * rinv[bb0 + q] : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) Dv[kb * 256 + q * 16 + c] = x[q];
+    }
+    __syncthreads();
+    static_assert((MR / 16) * 256 <= MR * YP, "the block inverses fit Y's space");
     for (int b1 = m; b1 > 0; b1 -= 16) {
-      const int b0 = b1 > 16 ? b1 - 16 : 0;
-      for (int n = tid; n < rk; n += kGramThreads) {
-        float *z = Z + n * ZP;
-        float zp[16];
+      const int b0 = b1 > 16 ? b1 - 16 : 0, kb = (m - b1) / 16;
+      // z_n[b0 + q] = sum_u Dinv[q][u] z_n[b0 + u], Dinv upper triangular (zero past the
+      // block); thread t: column n = t % 64, rows 8h .. 8h + 7 with h = t / 64
+      const int n = tid & 63, h = tid >> 6;
+      const bool act = n < rk;
+      float zp[16];
+      if (act) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) zp[q] = b0 + q < b1 ? z[b0 + q] : 0.f;
+        for (int u = 0; u < 16; ++u) zp[u] = Z[n * ZP + b0 + u];
+      }
+      __syncthreads();  // every thread has the panel's old values
+      if (act) {
+        const float *D = Dv + kb * 256;
+        if (h == 0) {
 #pragma unroll
-        for (int q = 15; q >= 0; --q) {
-          const int i = b0 + q;
-          if (i < b1) {
-            float s = zp[q];
+          for (int q = 0; q < 8; ++q) {
+            float s_ = 0.f;
 #pragma unroll
-            for (int u = 15; u > q; --u)
-              if (b0 + u < b1) s = fmaf(-Rb[i * RP + b0 + u], zp[u], s);
-            zp[q] = s * rinv[i];
+            for (int u = q; u < 16; ++u) s_ = fmaf(D[q * 16 + u], zp[u], s_);
+            if (b0 + q < b1) Z[n * ZP + b0 + q] = s_;
+          }
+        } else {
+#pragma unroll
+          for (int q = 8; q < 16; ++q) {
+            float s_ = 0.f;
+#pragma unroll
+            for (int u = q; u < 16; ++u) s_ = fmaf(D[q * 16 + u], zp[u], s_);
+            if (b0 + q < b1) Z[n * ZP + b0 + q] = s_;
           }
         }
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-          if (b0 + q < b1) z[b0 + q] = zp[q];
       }
       __syncthreads();
       // z_n[i] -= sum_{b0 <= l < b1} R_b[i][l] z_n[l] for the rows i < b0, in the same
